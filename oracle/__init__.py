@@ -1,0 +1,177 @@
+"""CPU oracle for the KV-cache write path -- TEST INFRASTRUCTURE ONLY.
+
+This package wraps ``kv_oracle.c`` (a plain C restatement of the write path,
+compiled with gcc) for the tests, the package smoke check and the
+benchmark's CPU-baseline leg. Nothing else may import it; the CUDA library
+neither links nor calls it, and it shares no code with the library.
+
+Functions follow sglang's ``kvcache.cuh`` (kernel ``store_kvcache``: byte copy
+of each token's K and V row into slot ``indices[token]``, with the rule
+``0 <= slot < size_limit``) and ``trtllm_fp8_kv_kernel.py`` (kernels
+``_fused_fp8_set_kv_buffer_kernel`` / ``_process_kv_tensor``: page
+decomposition of the slot, fp32 multiply by the inverse scale, conversion to
+FP8 e4m3fn).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kv_oracle.c")
+_LIBDIR = os.path.join(_HERE, "lib")
+_LIB = os.path.join(_LIBDIR, "libkvoracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc into ``oracle/lib/libkvoracle.so``."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    os.makedirs(_LIBDIR, exist_ok=True)
+    tmp = _LIB + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        lib.kvo_e4m3fn_encode.argtypes = [ctypes.c_float]
+        lib.kvo_e4m3fn_encode.restype = ctypes.c_uint8
+        lib.kvo_e4m3fn_decode.argtypes = [ctypes.c_uint8]
+        lib.kvo_e4m3fn_decode.restype = ctypes.c_double
+        lib.kvo_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.kvo_bf16_to_f32.restype = ctypes.c_float
+        lib.kvo_f16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.kvo_f16_to_f32.restype = ctypes.c_float
+        lib.kvo_scale_f32.argtypes = [ctypes.c_float, ctypes.c_float]
+        lib.kvo_scale_f32.restype = ctypes.c_float
+        lib.kvo_encode_f32_array.argtypes = [P, P, I64]
+        lib.kvo_decode_array.argtypes = [P, P, I64]
+        lib.kvo_store_copy.argtypes = [P, P, P, P, P, I32, I64, I64, I64, I32, I32, I32,
+                                       P, I64, P, P]
+        lib.kvo_store_copy.restype = I32
+        lib.kvo_store_fp8.argtypes = [P, P, P, P, P, I32, I64, I64, I64, I32, I32, I32,
+                                      P, I64, I64, I64, I64, ctypes.c_float, ctypes.c_float,
+                                      I32, P, P]
+        lib.kvo_store_fp8.restype = I32
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+# -- number formats ---------------------------------------------------------
+
+def e4m3fn_encode(x) -> np.ndarray:
+    """e4m3fn codes (uint8) of float32 values: nearest, ties even, saturating."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().kvo_encode_f32_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def e4m3fn_decode(codes) -> np.ndarray:
+    """Exact float64 values of e4m3fn codes (NaN for 0x7F / 0xFF)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().kvo_decode_array(_ptr(c), _ptr(out), c.size)
+    return out
+
+
+def bf16_to_f32(bits: int) -> float:
+    return _load().kvo_bf16_to_f32(bits)
+
+
+def f16_to_f32(bits: int) -> float:
+    return _load().kvo_f16_to_f32(bits)
+
+
+def scale_f32(x: float, inv: float) -> float:
+    return _load().kvo_scale_f32(x, inv)
+
+
+# -- the write path ---------------------------------------------------------
+
+class Strides:
+    """Byte strides of K, V and the two caches, in the library's order."""
+
+    FIELDS = ("k_token", "k_head", "k_dim", "v_token", "v_head", "v_dim",
+              "kc_slot", "kc_head", "kc_dim", "vc_slot", "vc_head", "vc_dim")
+
+    def __init__(self, **kw):
+        self.values = np.array([int(kw[f]) for f in self.FIELDS], dtype=np.int64)
+
+
+def _check_buf(a: np.ndarray, name: str):
+    if not (isinstance(a, np.ndarray) and a.flags.c_contiguous):
+        raise TypeError(f"{name} must be a C-contiguous numpy array")
+
+
+def store_copy(k, v, k_cache, v_cache, indices, strides: Strides, num_heads, head_dim,
+               elem_bytes, size_limit, k_off=0, v_off=0, kc_off=0, vc_off=0,
+               index_stride=1, t_begin=0, t_end=None):
+    """Plain copy scatter into host caches (in place). Returns (bad_count, first_bad).
+
+    ``k``/``v``/``k_cache``/``v_cache`` are host arrays; ``*_off`` are byte
+    offsets of the first element inside them (views such as a fused QKV).
+    """
+    for a, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_buf(a, n)
+    idx = np.ascontiguousarray(indices)
+    if idx.dtype not in (np.int32, np.int64):
+        raise TypeError("indices must be int32 or int64")
+    T = idx.size // index_stride if t_end is None else t_end
+    bad = np.zeros(1, np.int64)
+    first = np.zeros(1, np.int64)
+    rc = _load().kvo_store_copy(_ptr(k) + k_off, _ptr(v) + v_off, _ptr(k_cache) + kc_off,
+                                _ptr(v_cache) + vc_off, _ptr(idx), int(idx.dtype == np.int64),
+                                index_stride, t_begin, T, num_heads, head_dim, elem_bytes,
+                                _ptr(strides.values), size_limit, _ptr(bad), _ptr(first))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return int(bad[0]), int(first[0])
+
+
+def store_fp8(k, v, k_cache, v_cache, indices, strides: Strides, num_heads, head_dim,
+              src_dtype, page_size, kc_page_stride, vc_page_stride, size_limit,
+              inv_k=1.0, inv_v=1.0, use_scale=0, k_off=0, v_off=0, index_stride=1,
+              t_begin=0, t_end=None):
+    """Fused scale + e4m3fn scatter into host uint8 caches (in place).
+
+    Returns (bad_count, first_bad)."""
+    for a, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_buf(a, n)
+    idx = np.ascontiguousarray(indices)
+    if idx.dtype not in (np.int32, np.int64):
+        raise TypeError("indices must be int32 or int64")
+    if src_dtype not in ("bf16", "f16"):
+        raise ValueError(src_dtype)
+    T = idx.size // index_stride if t_end is None else t_end
+    bad = np.zeros(1, np.int64)
+    first = np.zeros(1, np.int64)
+    rc = _load().kvo_store_fp8(_ptr(k) + k_off, _ptr(v) + v_off, _ptr(k_cache), _ptr(v_cache),
+                               _ptr(idx), int(idx.dtype == np.int64), index_stride, t_begin, T,
+                               num_heads, head_dim, int(src_dtype == "bf16"),
+                               _ptr(strides.values), page_size, kc_page_stride,
+                               vc_page_stride, size_limit, float(np.float32(inv_k)),
+                               float(np.float32(inv_v)), int(use_scale), _ptr(bad), _ptr(first))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return int(bad[0]), int(first[0])

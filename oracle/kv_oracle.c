@@ -1,0 +1,248 @@
+/*
+ * CPU oracle for the KV-cache write path -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously correct restatement of what the write path
+ * computes, used to check the CUDA library.  Only the tests, the package's
+ * smoke check and the benchmark's CPU-baseline leg may load it.  It shares no
+ * code, header, table or constant with the CUDA library, and the library never
+ * calls it.
+ *
+ * Sources restated here (sglang):
+ *   - kvcache.cuh, kernel `store_kvcache` and helper `copy_kv_warp`: each new
+ *     token's K row and V row are copied byte for byte into the cache row
+ *     named by `indices[token]`; the slot must satisfy 0 <= slot < size_limit.
+ *   - trtllm_fp8_kv_kernel.py, kernels `_fused_fp8_set_kv_buffer_kernel` and
+ *     `_process_kv_tensor`: slot -> (page_id = slot / page_size,
+ *     page_offset = slot % page_size); each element is multiplied by the fp32
+ *     inverse scale (when a scale is provided), converted to FP8 e4m3fn, and
+ *     stored at page_id*stride_page + page_offset*stride_offset
+ *     + head*stride_head + dim*stride_dim.
+ *
+ * Readings taken where the pages are silent (all stated again in the design
+ * notes): out-of-range slots are skipped and counted instead of trapping; the
+ * FP8 conversion rounds to nearest, ties to even, saturates to +-448 (+-Inf
+ * included) and maps every NaN to 0x7F; a bf16/fp16 input widens exactly to
+ * fp32 and the scale multiply is a single fp32 rounding.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define KVO_OK 0
+#define KVO_ERR_ARG 1
+
+/* ------------------------------------------------------------------------ */
+/* Number formats.                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* bf16 is the top half of an IEEE binary32: widening is exact. */
+float kvo_bf16_to_f32(uint16_t bits)
+{
+    uint32_t w = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return f;
+}
+
+/* IEEE binary16: 1 sign, 5 exponent bits (bias 15), 10 fraction bits.
+ * Value = (-1)^s * 2^(e-15) * (1 + f/1024) for 1 <= e <= 30,
+ *         (-1)^s * 2^-14 * (f/1024) for e == 0, Inf/NaN for e == 31. */
+float kvo_f16_to_f32(uint16_t bits)
+{
+    int s = (bits >> 15) & 1;
+    int e = (bits >> 10) & 0x1F;
+    int f = bits & 0x3FF;
+    double mag;
+    if (e == 0x1F) {
+        mag = f ? NAN : INFINITY;
+    } else if (e == 0) {
+        mag = ldexp((double)f, -24);
+    } else {
+        mag = ldexp(1024.0 + (double)f, e - 25);
+    }
+    return (float)(s ? -mag : mag);
+}
+
+/* FP8 e4m3fn (OCP 8-bit floating point, E4M3): 1 sign, 4 exponent bits
+ * (bias 7), 3 mantissa bits; no infinities; S.1111.111 is NaN, so the
+ * largest finite magnitude is S.1111.110 = 1.75 * 2^8 = 448.
+ * Value = (-1)^s * 2^(E-7) * (1 + m/8) for E >= 1, (-1)^s * 2^-6 * (m/8)
+ * for E == 0.  Returns the exact value (NaN for the two NaN codes). */
+double kvo_e4m3fn_decode(uint8_t code)
+{
+    int s = code >> 7;
+    int E = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double mag;
+    if (E == 0xF && m == 0x7)
+        return NAN;
+    if (E == 0)
+        mag = ldexp((double)m, -9);
+    else
+        mag = ldexp(8.0 + (double)m, E - 10);
+    return s ? -mag : mag;
+}
+
+#define KVO_E4M3_NAN 0x7F       /* every NaN input maps to this code */
+#define KVO_E4M3_MAXFIN 0x7E    /* 448 */
+
+/* Round y to the nearest e4m3fn value, ties to the even mantissa, saturating
+ * finite overflow and infinities to +-448.  Works in float64, where every
+ * fp32 input and every e4m3fn value is exact, so the only rounding is the
+ * explicit nearest-even step below. */
+uint8_t kvo_e4m3fn_encode(float y)
+{
+    double a = fabs((double)y);
+    uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    if (isnan(y))
+        return KVO_E4M3_NAN;
+    if (a >= 448.0)
+        return sign | KVO_E4M3_MAXFIN;
+    if (a < 0x1p-6) {
+        /* Subnormal range: multiples of 2^-9.  q = a / 2^-9 is exact. */
+        double q = a * 0x1p9;
+        double m = nearbyint(q);       /* default mode: nearest, ties even */
+        /* m == 8 is the smallest normal, 2^-6, whose code is also 8. */
+        return sign | (uint8_t)m;
+    }
+    int ex;
+    (void)frexp(a, &ex);               /* a = f * 2^ex, f in [0.5, 1) */
+    int e = ex - 1;                    /* a in [2^e, 2^(e+1)), e in [-6, 8] */
+    double q = ldexp(a, 3 - e);        /* in [8, 16), exact */
+    double m = nearbyint(q);           /* in [8, 16] */
+    if (m == 16.0) {                   /* mantissa carry into the exponent */
+        m = 8.0;
+        e += 1;
+    }
+    int code = ((e + 7) << 3) | ((int)m - 8);
+    if (code > KVO_E4M3_MAXFIN)        /* cannot happen for a < 448 */
+        code = KVO_E4M3_MAXFIN;
+    return sign | (uint8_t)code;
+}
+
+/* fp32 product of the widened input and the fp32 inverse scale: the exact
+ * float64 product of two floats rounded once to float. */
+float kvo_scale_f32(float x, float inv)
+{
+    return (float)((double)x * (double)inv);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Index read and bounds rule.                                              */
+/* ------------------------------------------------------------------------ */
+
+static int64_t read_index(const void *indices, int index_is_i64, int64_t index_stride, int64_t t)
+{
+    if (index_is_i64)
+        return ((const int64_t *)indices)[t * index_stride];
+    return (int64_t)((const int32_t *)indices)[t * index_stride];
+}
+
+static void note_bad(int64_t t, int64_t *bad_count, int64_t *first_bad)
+{
+    if (*bad_count == 0 || t < *first_bad)
+        *first_bad = t;
+    *bad_count += 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Plain copy: kvcache.cuh `store_kvcache`.                                 */
+/* strides[12], all in bytes:                                               */
+/*   k_token, k_head, k_dim, v_token, v_head, v_dim,                        */
+/*   kc_slot, kc_head, kc_dim, vc_slot, vc_head, vc_dim.                    */
+/* Tokens [t_begin, t_end) are processed.  Returns KVO_OK or KVO_ERR_ARG;   */
+/* *bad_count / *first_bad report tokens whose slot is out of range.        */
+/* ------------------------------------------------------------------------ */
+int kvo_store_copy(const uint8_t *k, const uint8_t *v, uint8_t *k_cache, uint8_t *v_cache,
+                   const void *indices, int index_is_i64, int64_t index_stride,
+                   int64_t t_begin, int64_t t_end, int32_t num_heads, int32_t head_dim,
+                   int32_t elem_bytes, const int64_t *strides, int64_t size_limit,
+                   int64_t *bad_count, int64_t *first_bad)
+{
+    if (elem_bytes <= 0 || num_heads <= 0 || head_dim <= 0 || t_begin > t_end)
+        return KVO_ERR_ARG;
+    *bad_count = 0;
+    *first_bad = -1;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        int64_t slot = read_index(indices, index_is_i64, index_stride, t);
+        if (slot < 0 || slot >= size_limit) {
+            note_bad(t, bad_count, first_bad);
+            continue;
+        }
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint8_t *src = kv ? v : k;
+            uint8_t *dst = kv ? v_cache : k_cache;
+            const int64_t *ss = strides + 3 * kv;       /* token, head, dim */
+            const int64_t *ds = strides + 6 + 3 * kv;   /* slot, head, dim */
+            for (int32_t h = 0; h < num_heads; ++h)
+                for (int32_t d = 0; d < head_dim; ++d)
+                    memcpy(dst + slot * ds[0] + h * ds[1] + d * ds[2],
+                           src + t * ss[0] + h * ss[1] + d * ss[2], (size_t)elem_bytes);
+        }
+    }
+    return KVO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Fused FP8 write: trtllm_fp8_kv_kernel.py `_fused_fp8_set_kv_buffer_kernel`
+ * and `_process_kv_tensor`.  Inputs are bf16 (src_is_bf16 = 1) or fp16.
+ * The cache element is one e4m3fn byte; strides as for kvo_store_copy, plus
+ * the page strides of the two caches.  With use_scale == 0 the value is
+ * converted unscaled. */
+/* ------------------------------------------------------------------------ */
+int kvo_store_fp8(const uint8_t *k, const uint8_t *v, uint8_t *k_cache, uint8_t *v_cache,
+                  const void *indices, int index_is_i64, int64_t index_stride,
+                  int64_t t_begin, int64_t t_end, int32_t num_heads, int32_t head_dim,
+                  int src_is_bf16, const int64_t *strides, int64_t page_size,
+                  int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
+                  float inv_k, float inv_v, int use_scale,
+                  int64_t *bad_count, int64_t *first_bad)
+{
+    if (num_heads <= 0 || head_dim <= 0 || page_size <= 0 || t_begin > t_end)
+        return KVO_ERR_ARG;
+    *bad_count = 0;
+    *first_bad = -1;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        int64_t slot = read_index(indices, index_is_i64, index_stride, t);
+        if (slot < 0 || slot >= size_limit) {
+            note_bad(t, bad_count, first_bad);
+            continue;
+        }
+        int64_t page_id = slot / page_size;
+        int64_t page_offset = slot % page_size;
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint8_t *src = kv ? v : k;
+            uint8_t *dst = kv ? v_cache : k_cache;
+            const int64_t *ss = strides + 3 * kv;
+            const int64_t *ds = strides + 6 + 3 * kv;
+            int64_t page_stride = kv ? vc_page_stride : kc_page_stride;
+            float inv = kv ? inv_v : inv_k;
+            for (int32_t h = 0; h < num_heads; ++h) {
+                for (int32_t d = 0; d < head_dim; ++d) {
+                    uint16_t bits;
+                    memcpy(&bits, src + t * ss[0] + h * ss[1] + d * ss[2], sizeof bits);
+                    float x = src_is_bf16 ? kvo_bf16_to_f32(bits) : kvo_f16_to_f32(bits);
+                    float y = use_scale ? kvo_scale_f32(x, inv) : x;
+                    dst[page_id * page_stride + page_offset * ds[0] + h * ds[1] + d * ds[2]] =
+                        kvo_e4m3fn_encode(y);
+                }
+            }
+        }
+    }
+    return KVO_OK;
+}
+
+/* Element-wise conversion helpers for the tests: n values in, n codes out. */
+void kvo_encode_f32_array(const float *x, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kvo_e4m3fn_encode(x[i]);
+}
+
+void kvo_decode_array(const uint8_t *codes, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kvo_e4m3fn_decode(codes[i]);
+}

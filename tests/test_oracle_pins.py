@@ -1,0 +1,402 @@
+"""Pins for the CPU oracle, each against something other than the oracle.
+
+* The e4m3fn encoder against a brute-force nearest-finite-code search over a
+  decode table taken from a library (torch's float8_e4m3fn), on every bf16 and
+  fp16 bit pattern and on a million random float32 patterns, plus the closed
+  forms in ``golden/e4m3fn_points.txt``.
+* The decoder against the same library table and against closed forms.
+* The bf16/fp16 widening and the fp32 scale multiply against numpy / torch.
+* The copy scatter against the worked example in ``golden/worked_copy.txt``,
+  the untouched-slot invariant, a round-trip gather, and index-dtype,
+  stride and page-layout equivalences.
+* The FP8 scatter element by element against the brute-force encoder of the
+  numpy fp32 product, the +-half-step error bound, and the use_scale=0 / inv=1
+  and page-layout equivalences.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# Independent e4m3fn references
+# ---------------------------------------------------------------------------
+
+def _library_table() -> np.ndarray:
+    """Values of all 256 e4m3fn codes according to torch (float64)."""
+    return (torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn)
+            .to(torch.float64).numpy())
+
+
+LIB = _library_table()
+POS_FINITE = np.arange(0x7F)          # 0x00 .. 0x7E
+
+
+def brute_encode(x32: np.ndarray) -> np.ndarray:
+    """Nearest finite e4m3fn value by exhaustive search; ties to the even code.
+
+    Saturation needs no rule here: above 448 the nearest finite value is 448.
+    """
+    x = np.asarray(x32, dtype=np.float32).ravel()
+    out = np.empty(x.size, dtype=np.uint8)
+    vals = LIB[POS_FINITE]
+    for c0 in range(0, x.size, 1 << 15):
+        with np.errstate(invalid="ignore"):       # signalling NaN patterns
+            xs = x[c0:c0 + (1 << 15)].astype(np.float64)
+        a = np.abs(xs)
+        # beyond 448 every magnitude has the same nearest finite value (448); cap
+        # it so that the float64 distances stay distinguishable
+        a = np.minimum(a, 1024.0)
+        d = np.abs(a[:, None] - vals[None, :])
+        best = d.min(axis=1, keepdims=True)
+        tied = d == best
+        # among the (at most two) nearest codes prefer the even one
+        even = tied & ((POS_FINITE[None, :] & 1) == 0)
+        code = np.where(even.any(axis=1), np.argmax(even, axis=1), np.argmax(tied, axis=1))
+        code = code.astype(np.uint8) | np.where(np.signbit(xs), 0x80, 0).astype(np.uint8)
+        code = np.where(np.isnan(xs), 0x7F, code)
+        out[c0:c0 + xs.size] = code
+    return out
+
+
+def all_bf16_as_f32() -> np.ndarray:
+    return (np.arange(1 << 16, dtype=np.uint32) << 16).view(np.float32)
+
+
+def all_f16_as_f32() -> np.ndarray:
+    return np.arange(1 << 16, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Number formats
+# ---------------------------------------------------------------------------
+
+def test_decode_matches_library_table():
+    got = oracle.e4m3fn_decode(np.arange(256))
+    nan = np.isnan(LIB)
+    assert np.array_equal(np.isnan(got), nan)
+    assert list(np.flatnonzero(nan)) == [0x7F, 0xFF]
+    assert np.array_equal(got[~nan], LIB[~nan])
+
+
+def test_decode_closed_forms():
+    d = oracle.e4m3fn_decode(np.array([0x00, 0x01, 0x07, 0x08, 0x38, 0x7E, 0xFE, 0x80]))
+    assert list(d[:6]) == [0.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 1.0, 448.0]
+    assert d[6] == -448.0 and d[7] == 0.0 and math.copysign(1, d[7]) == -1
+    # strictly increasing over the non-negative finite codes; sign is the top bit
+    pos = oracle.e4m3fn_decode(POS_FINITE)
+    assert np.all(np.diff(pos) > 0)
+    neg = oracle.e4m3fn_decode(POS_FINITE | 0x80)
+    assert np.array_equal(neg[1:], -pos[1:])
+
+
+def _golden_points():
+    rows = []
+    with open(os.path.join(GOLDEN, "e4m3fn_points.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            x, code, why = [s.strip() for s in line.split(";")]
+            rows.append((float(x), int(code, 16), why))
+    return rows
+
+
+def test_encode_golden_points():
+    rows = _golden_points()
+    assert len(rows) >= 25
+    x = np.array([r[0] for r in rows], dtype=np.float32)
+    # every listed input in the finite range is exactly representable in float32
+    assert all(not abs(r[0]) <= 448 or float(np.float32(r[0])) == r[0] for r in rows)
+    got = oracle.e4m3fn_encode(x)
+    want = np.array([r[1] for r in rows], dtype=np.uint8)
+    bad = [(rows[i][0], hex(got[i]), hex(want[i]), rows[i][2])
+           for i in np.flatnonzero(got != want)]
+    assert not bad, bad
+    # and the brute-force search agrees with every hand-derived point
+    assert np.array_equal(brute_encode(x), want)
+
+
+def test_encode_exhaustive_bf16_and_f16():
+    for x in (all_bf16_as_f32(), all_f16_as_f32()):
+        got = oracle.e4m3fn_encode(x)
+        want = brute_encode(x)
+        assert np.array_equal(got, want), np.flatnonzero(got != want)[:10]
+
+
+def test_encode_random_f32_patterns():
+    # random bit patterns (all magnitudes, NaN, Inf, subnormals) ...
+    bits = (wl.splitmix64(0xE4E3, 0, 1 << 19) >> np.uint64(32)).astype(np.uint32)
+    x1 = bits.view(np.float32)
+    # ... and random values concentrated where e4m3fn codes are (products)
+    u = wl.uniform01(0xE4E4, 1 << 19)
+    x2 = (np.sign(u - 0.5) * np.exp2(-12 + 22 * np.abs(2 * u - 1))).astype(np.float32)
+    for x in (x1, x2):
+        assert np.array_equal(oracle.e4m3fn_encode(x), brute_encode(x))
+
+
+def test_encode_library_crosscheck_below_448():
+    # torch's cast rounds to nearest-even too but does not saturate; below 448
+    # the two must agree.
+    x = all_bf16_as_f32()
+    keep = np.isfinite(x) & (np.abs(x) < 448)
+    lib = torch.from_numpy(x[keep]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3fn_encode(x[keep]), lib)
+
+
+def test_encode_error_bound():
+    # |decode(enc(y)) - clamp(y)| <= half the spacing of e4m3fn around y
+    x = wl.normal(77, 1 << 16) * np.float32(60.0)
+    q = oracle.e4m3fn_decode(oracle.e4m3fn_encode(x))
+    y = np.clip(x.astype(np.float64), -448, 448)
+    a = np.abs(y)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+    half_step = 2.0 ** (e - 3) / 2
+    assert np.all(np.abs(q - y) <= half_step)
+
+
+def test_widening_and_scale():
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    lib_bf = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    lib_f16 = bits.view(np.float16).astype(np.float32)
+    for i in range(0, 1 << 16, 97):
+        a, b = oracle.bf16_to_f32(int(bits[i])), lib_bf[i]
+        assert (np.isnan(a) and np.isnan(b)) or a == b
+        c, d = oracle.f16_to_f32(int(bits[i])), lib_f16[i]
+        assert (np.isnan(c) and np.isnan(d)) or c == d
+    # the fp32 multiply equals numpy's IEEE float32 multiply (subnormals kept)
+    x = wl.normal(5, 4096) * np.float32(3)
+    inv = np.float32(448.0) / np.float32(np.abs(x).max())
+    tiny = np.float32(1e-38)
+    for xi in list(x[:512]) + [tiny, -tiny, np.float32(3e-39)]:
+        got = oracle.scale_f32(float(xi), float(inv))
+        assert np.float32(got) == np.float32(xi) * inv
+    assert oracle.scale_f32(1e-38, 0.25) == float(np.float32(1e-38) * np.float32(0.25)) != 0.0
+
+
+# ---------------------------------------------------------------------------
+# Plain copy scatter
+# ---------------------------------------------------------------------------
+
+def _contig_strides(H, D, e, slot_stride=None):
+    R = H * D * e
+    ss = R if slot_stride is None else slot_stride
+    return oracle.Strides(k_token=R, k_head=D * e, k_dim=e, v_token=R, v_head=D * e, v_dim=e,
+                          kc_slot=ss, kc_head=D * e, kc_dim=e, vc_slot=ss, vc_head=D * e,
+                          vc_dim=e)
+
+
+def _read_worked():
+    spec = {}
+    with open(os.path.join(GOLDEN, "worked_copy.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                key, *vals = line.split()
+                spec[key] = vals
+    return spec
+
+
+def test_copy_worked_example():
+    s = _read_worked()
+    T, H, D = int(s["T"][0]), int(s["H"][0]), int(s["D"][0])
+    hexa = lambda key: np.array([int(x, 16) for x in s[key]], dtype=np.uint16)
+    k, v = hexa("k"), hexa("v")
+    idx = np.array([int(x) for x in s["indices"]], dtype=np.int32)
+    limit = int(s["size_limit"][0])
+    kc = np.full(limit * H * D, int(s["sentinel"][0], 16), dtype=np.uint16)
+    vc = kc.copy()
+    bad, first = oracle.store_copy(k, v, kc, vc, idx, _contig_strides(H, D, 2), H, D, 2, limit)
+    assert np.array_equal(kc, hexa("k_cache"))
+    assert np.array_equal(vc, hexa("v_cache"))
+    assert (bad, first) == (int(s["bad_count"][0]), int(s["first_bad"][0]))
+    assert T == k.size // (H * D)
+
+
+def _copy_problem(T, H, D, n_slots, seed, slot_stride=None, idx_dtype=np.int64):
+    R = H * D * 2
+    ss = R if slot_stride is None else slot_stride
+    k = wl._normal_rows(seed, T, H, D, "bf16")
+    v = wl._normal_rows(seed + 1, T, H, D, "bf16")
+    idx = wl.distinct_slots(seed + 2, n_slots, T).astype(idx_dtype)
+    kc = np.full(n_slots * ss // 2, wl.BF16_SENTINEL, dtype=np.uint16)
+    vc = kc.copy()
+    return k, v, idx, kc, vc, ss
+
+
+@pytest.mark.parametrize("slot_stride", [None, 2 * 8 * 64 + 128])
+def test_copy_roundtrip_and_untouched(slot_stride):
+    T, H, D, n = 200, 8, 64, 1000
+    k, v, idx, kc, vc, ss = _copy_problem(T, H, D, n, 11, slot_stride)
+    bad, _ = oracle.store_copy(k, v, kc, vc, idx, _contig_strides(H, D, 2, ss), H, D, 2, n)
+    assert bad == 0
+    R16 = H * D
+    kc2, vc2 = kc.reshape(n, ss // 2), vc.reshape(n, ss // 2)
+    # round trip: gathering the named rows gives back K and V exactly
+    assert np.array_equal(kc2[idx, :R16], k.reshape(T, R16))
+    assert np.array_equal(vc2[idx, :R16], v.reshape(T, R16))
+    # untouched: every other slot, and the padding of named slots, is pre-fill
+    other = np.setdiff1d(np.arange(n), idx)
+    assert np.all(kc2[other] == wl.BF16_SENTINEL) and np.all(vc2[other] == wl.BF16_SENTINEL)
+    assert np.all(kc2[idx, R16:] == wl.BF16_SENTINEL)
+
+
+def test_copy_index_dtype_and_oob():
+    T, H, D, n = 64, 2, 32, 128
+    k, v, idx, kc, vc, ss = _copy_problem(T, H, D, n, 21)
+    idx = idx.copy()
+    idx[5], idx[9], idx[40] = -1, n, np.iinfo(np.int64).max
+    st = _contig_strides(H, D, 2)
+    kc64, vc64 = kc.copy(), vc.copy()
+    b64 = oracle.store_copy(k, v, kc64, vc64, idx, st, H, D, 2, n)
+    assert b64 == (3, 5)
+    idx32 = idx.copy()
+    idx32[40] = np.iinfo(np.int32).min
+    kc32, vc32 = kc.copy(), vc.copy()
+    b32 = oracle.store_copy(k, v, kc32, vc32, idx32.astype(np.int32), st, H, D, 2, n)
+    assert b32 == (3, 5)
+    assert np.array_equal(kc64, kc32) and np.array_equal(vc64, vc32)
+    # the skipped tokens wrote nothing: only 61 slots differ from the pre-fill
+    changed = np.any(kc64.reshape(n, -1) != wl.BF16_SENTINEL, axis=1)
+    assert changed.sum() == T - 3
+
+
+def test_copy_strided_source_and_head_strides():
+    # K/V as column views of a fused QKV row; caches with a head-major padding
+    T, H, D, n, HQ = 50, 4, 16, 80, 6
+    width = (HQ + 2 * H) * D
+    qkv = wl._normal_rows(31, T, HQ + 2 * H, D, "f16").reshape(T, width)
+    idx = wl.distinct_slots(32, n, T)
+    e = 2
+    cache_head = D * e + 32                       # padded head stride in the cache
+    ss = H * cache_head
+    st = oracle.Strides(k_token=width * e, k_head=D * e, k_dim=e, v_token=width * e,
+                        v_head=D * e, v_dim=e, kc_slot=ss, kc_head=cache_head, kc_dim=e,
+                        vc_slot=ss, vc_head=cache_head, vc_dim=e)
+    kc = np.full(n * ss // 2, wl.BF16_SENTINEL, dtype=np.uint16)
+    vc = kc.copy()
+    oracle.store_copy(qkv, qkv, kc, vc, idx, st, H, D, 2, n,
+                      k_off=HQ * D * e, v_off=(HQ + H) * D * e)
+    kc4 = kc.reshape(n, H, cache_head // 2)
+    kq = qkv.reshape(T, HQ + 2 * H, D)
+    assert np.array_equal(kc4[idx, :, :D], kq[:, HQ:HQ + H])
+    assert np.all(kc4[idx, :, D:] == wl.BF16_SENTINEL)
+    vc4 = vc.reshape(n, H, cache_head // 2)
+    assert np.array_equal(vc4[idx, :, :D], kq[:, HQ + H:])
+
+
+def test_copy_duplicate_slots_take_one_candidate():
+    T, H, D, n = 16, 1, 8, 8
+    k, v, _, kc, vc, _ = _copy_problem(T, H, D, 64, 41)
+    kc, vc = kc[:n * H * D].copy(), vc[:n * H * D].copy()
+    idx = (np.array([3, 3, 5, 3] + list(range(12)), dtype=np.int32) % n)[:T]
+    oracle.store_copy(k, v, kc, vc, idx, _contig_strides(H, D, 2), H, D, 2, n)
+    rows = kc.reshape(n, H * D)
+    for s in np.unique(idx):
+        cands = k.reshape(T, -1)[idx == s]
+        assert any(np.array_equal(rows[s], c) for c in cands)
+
+
+# ---------------------------------------------------------------------------
+# FP8 scatter
+# ---------------------------------------------------------------------------
+
+def _widen(bits: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return (bits.astype(np.uint32) << 16).view(np.float32)
+    return bits.view(np.float16).astype(np.float32)
+
+
+def _fp8_strides(H, D, e_src, slot_stride):
+    R = H * D * e_src
+    return oracle.Strides(k_token=R, k_head=D * e_src, k_dim=e_src, v_token=R,
+                          v_head=D * e_src, v_dim=e_src, kc_slot=slot_stride, kc_head=D,
+                          kc_dim=1, vc_slot=slot_stride, vc_head=D, vc_dim=1)
+
+
+@pytest.mark.parametrize("src", ["bf16", "f16"])
+@pytest.mark.parametrize("use_scale", [0, 1])
+def test_fp8_elementwise_against_brute_force(src, use_scale):
+    T, H, D, n, ps = 96, 4, 32, 256, 16
+    w = wl.make_fp8("t", T, H, D, n, seed=91, dtype=src, page_size=ps)
+    kc = np.full(n * H * D, wl.FP8_SENTINEL, dtype=np.uint8)
+    vc = kc.copy()
+    bad, _ = oracle.store_fp8(w.k, w.v, kc, vc, w.indices, _fp8_strides(H, D, 2, H * D), H, D,
+                              src, ps, ps * H * D, ps * H * D, n, w.inv_k, w.inv_v, use_scale)
+    assert bad == 0
+    for bits, cache, inv in ((w.k, kc, w.inv_k), (w.v, vc, w.inv_v)):
+        x = _widen(bits.reshape(T, -1), src)
+        y = x * np.float32(inv) if use_scale else x
+        want = brute_encode(y).reshape(T, -1)
+        got = cache.reshape(n, -1)[w.indices]
+        assert np.array_equal(got, want)
+        other = np.setdiff1d(np.arange(n), w.indices)
+        assert np.all(cache.reshape(n, -1)[other] == wl.FP8_SENTINEL)
+    if not use_scale:
+        # the outliers saturate: some codes are +-448
+        assert np.any((kc & 0x7F) == 0x7E)
+
+
+def test_fp8_use_scale_off_equals_inv_one():
+    T, H, D, n, ps = 64, 2, 64, 128, 8
+    w = wl.make_fp8("t", T, H, D, n, seed=92, page_size=ps)
+    st = _fp8_strides(H, D, 2, H * D)
+    outs = []
+    for use, inv in ((0, 123.0), (1, 1.0)):
+        kc = np.full(n * H * D, wl.FP8_SENTINEL, dtype=np.uint8)
+        vc = kc.copy()
+        oracle.store_fp8(w.k, w.v, kc, vc, w.indices, st, H, D, "bf16", ps, ps * H * D,
+                         ps * H * D, n, inv, inv, use)
+        outs.append((kc, vc))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+
+
+def test_fp8_page_layouts():
+    # A 3-D cache: page decomposition equals direct slot addressing for any page size.
+    T, H, D, n = 40, 2, 16, 96
+    w = wl.make_fp8("t", T, H, D, n, seed=93, page_size=8)
+    st = _fp8_strides(H, D, 2, H * D)
+    ref = None
+    for ps in (1, 8, 32, 96):
+        kc = np.full(n * H * D, wl.FP8_SENTINEL, dtype=np.uint8)
+        vc = kc.copy()
+        oracle.store_fp8(w.k, w.v, kc, vc, w.indices, st, H, D, "bf16", ps, ps * H * D,
+                         ps * H * D, n, w.inv_k, w.inv_v, 1)
+        ref = (kc, vc) if ref is None else ref
+        assert np.array_equal(kc, ref[0]) and np.array_equal(vc, ref[1])
+    # A 4-D cache [pages, page_size, H, D] with a padded page stride: row of slot
+    # s lands at (s // ps) * page_stride + (s % ps) * slot_stride.
+    ps, pad = 8, 64
+    page_stride = ps * H * D + pad
+    n_pages = n // ps
+    kc = np.full(n_pages * page_stride, wl.FP8_SENTINEL, dtype=np.uint8)
+    vc = kc.copy()
+    oracle.store_fp8(w.k, w.v, kc, vc, w.indices, st, H, D, "bf16", ps, page_stride,
+                     page_stride, n, w.inv_k, w.inv_v, 1)
+    pages = kc.reshape(n_pages, page_stride)
+    rows = pages[:, :ps * H * D].reshape(n, H * D)
+    assert np.array_equal(rows, ref[0].reshape(n, H * D))
+    assert np.all(pages[:, ps * H * D:] == wl.FP8_SENTINEL)
+
+
+def test_fp8_oob_skipped():
+    T, H, D, n, ps = 32, 2, 16, 64, 4
+    w = wl.make_fp8("t", T, H, D, n, seed=94, page_size=ps)
+    idx = w.indices.copy()
+    idx[[3, 17]] = [n, -5]
+    kc = np.full(n * H * D, wl.FP8_SENTINEL, dtype=np.uint8)
+    vc = kc.copy()
+    bad = oracle.store_fp8(w.k, w.v, kc, vc, idx, _fp8_strides(H, D, 2, H * D), H, D, "bf16",
+                           ps, ps * H * D, ps * H * D, n, w.inv_k, w.inv_v, 1)
+    assert bad == (2, 3)
+    changed = np.any(kc.reshape(n, -1) != wl.FP8_SENTINEL, axis=1)
+    assert changed.sum() == T - 2

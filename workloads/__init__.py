@@ -1,0 +1,286 @@
+"""Seeded synthetic inputs for the KV-cache write path.
+
+This module is shared by the tests, ``bench.py`` and the smoke check. It draws
+the K/V rows, the slot indices and the cache pre-fill for every workload, and
+nothing else: it holds none of the write path's arithmetic (no scatter, no
+scaling, no FP8 encoding). Both the CUDA path and the CPU oracle receive exactly
+the arrays built here.
+
+Random numbers come from one counter-based generator, SplitMix64 (Steele, Lea
+and Flood, "Fast splittable pseudorandom number generators", OOPSLA 2014): the
+i-th draw of a stream with key ``seed`` is ``mix(seed + (i + 1) * golden)``.
+Normals use the Box-Muller transform in float64, then float32, then
+round-to-nearest-even to bf16 or fp16. Distinct slots are the ``k`` slots with
+the smallest random keys, listed in random order.
+
+Workloads (sizes of the KV-cache write configurations this library is
+measured on; ``T`` tokens, ``H`` KV heads, ``D`` head dim):
+
+* ``tiny``     T=16,    H=2, D=64,  bf16, cache 256 slots, int32 indices.
+* ``decode``   T=256,   H=8, D=128, bf16, cache 1,048,576 slots, int64.
+* ``prefill``  T=32768, H=8, D=128, bf16, cache 4,194,304 slots, page 64,
+               512 whole pages in random page order, int32.
+* ``fp8``      T=8192,  H=8, D=128, bf16 4*N(0,1) with 0.1% outliers
+               +-U(500,2000), e4m3fn cache 1,048,576 slots, page 32, int64.
+* ``strided``  fp16 K/V as column views of a fused QKV [65536, 6144] tensor,
+               cache 2,097,152 slots, int32.
+* ``odd``      fp16 H=1, D=576 (1152-byte rows), 1280-byte slot stride,
+               cache 2,097,152 slots, int32.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+BF16_SENTINEL = 0x7FC0   # cache pre-fill for 2-byte caches (a bf16 NaN pattern)
+FP8_SENTINEL = 0x7F      # cache pre-fill for e4m3fn caches (the e4m3fn NaN code)
+
+
+def splitmix64(seed: int, start: int, n: int) -> np.ndarray:
+    """Draws ``start .. start+n-1`` of the SplitMix64 stream keyed by ``seed``."""
+    with np.errstate(over="ignore"):
+        ctr = np.arange(start + 1, start + n + 1, dtype=np.uint64)
+        z = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + ctr * _GOLDEN
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+        return z ^ (z >> np.uint64(31))
+
+
+def uniform01(seed: int, n: int, start: int = 0) -> np.ndarray:
+    """Float64 uniforms in [0, 1) with 53 random bits each."""
+    return (splitmix64(seed, start, n) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def normal(seed: int, n: int, chunk: int = 1 << 24) -> np.ndarray:
+    """``n`` standard normals (float32), Box-Muller on pairs of uniforms."""
+    out = np.empty(n, dtype=np.float32)
+    half = (n + 1) // 2
+    for p0 in range(0, half, chunk):
+        m = min(chunk, half - p0)
+        u = uniform01(seed, 2 * m, start=2 * p0)
+        u1 = 1.0 - u[0::2]            # (0, 1]: log is finite
+        u2 = u[1::2]
+        r = np.sqrt(-2.0 * np.log(u1))
+        a = 2.0 * math.pi * u2
+        z = np.empty(2 * m, dtype=np.float64)
+        z[0::2] = r * np.cos(a)
+        z[1::2] = r * np.sin(a)
+        lo = 2 * p0
+        hi = min(n, lo + 2 * m)
+        out[lo:hi] = z[: hi - lo]
+    return out
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (nearest, ties to even); returns the uint16 bits."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    nan = (b & 0x7FFFFFFF) > 0x7F800000
+    r = (b + np.uint32(0x7FFF) + ((b >> 16) & 1)) >> 16
+    r = np.where(nan, (b >> 16) | 0x40, r)
+    return r.astype(np.uint16)
+
+
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to fp16 (IEEE, nearest even); returns the uint16 bits."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return f32_to_bf16_bits(x)
+    if dtype == "f16":
+        return f32_to_f16_bits(x)
+    raise ValueError(dtype)
+
+
+def distinct_slots(seed: int, n_slots: int, k: int) -> np.ndarray:
+    """``k`` distinct slots of ``[0, n_slots)``, in random order (int64)."""
+    if k > n_slots:
+        raise ValueError("more tokens than slots")
+    keys = splitmix64(seed, 0, n_slots)
+    pick = np.argpartition(keys, k - 1)[:k] if k < n_slots else np.arange(n_slots)
+    order = np.argsort(splitmix64(seed ^ 0x5A5A5A5A, 0, k), kind="stable")
+    return pick[order].astype(np.int64)
+
+
+def page_run_slots(seed: int, n_pages: int, page_size: int, k_pages: int) -> np.ndarray:
+    """Whole pages in random page order, each filled with offsets 0..page_size-1."""
+    pages = distinct_slots(seed, n_pages, k_pages)
+    return (pages[:, None] * page_size + np.arange(page_size)[None, :]).reshape(-1)
+
+
+@dataclass
+class Workload:
+    """One synthetic write problem, host side.
+
+    ``k``/``v`` are uint16 bit arrays of shape ``src_shape`` (the input tensors);
+    ``k_view``/``v_view`` describe the K and V rows inside them as
+    (byte offset, token stride, head stride, dim stride), all in bytes. The cache
+    is ``n_slots`` slots of ``slot_stride`` bytes, each slot holding ``H`` heads of
+    ``D`` elements (``cache_elem`` bytes each, head stride ``cache_head_stride``).
+    """
+
+    name: str
+    T: int
+    H: int
+    D: int
+    src_dtype: str                  # "bf16" | "f16"
+    kind: str                       # "copy" | "fp8"
+    k: np.ndarray
+    v: np.ndarray
+    k_view: tuple
+    v_view: tuple
+    indices: np.ndarray             # int32 or int64
+    n_slots: int
+    slot_stride: int
+    cache_head_stride: int
+    cache_elem: int                 # 2 (copy) or 1 (fp8)
+    sentinel: int                   # pre-fill byte pattern (uint16 for copy, uint8 for fp8)
+    page_size: int
+    page_stride: int
+    inv_k: float = 1.0              # fp32 inverse scales (fp8 only)
+    inv_v: float = 1.0
+    use_scale: int = 0
+    num_split: int = 0
+    notes: dict = field(default_factory=dict)
+
+    @property
+    def row_bytes(self) -> int:
+        return self.H * self.D * 2
+
+    @property
+    def cache_bytes(self) -> int:
+        return self.n_slots * self.slot_stride
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes a call must move: K and V rows read, cache rows written, indices read."""
+        out_row = self.H * self.D * self.cache_elem
+        return self.T * (2 * self.row_bytes + 2 * out_row + self.indices.itemsize)
+
+
+def _contig_view(H: int, D: int, elem: int = 2):
+    return (0, H * D * elem, D * elem, elem)
+
+
+def _normal_rows(seed: int, T: int, H: int, D: int, dtype: str, scale: float = 1.0) -> np.ndarray:
+    x = normal(seed, T * H * D)
+    if scale != 1.0:
+        x *= np.float32(scale)
+    return to_bits(x, dtype).reshape(T, H, D)
+
+
+def _amax_inv(bits: np.ndarray, dtype: str) -> float:
+    """Per-tensor inverse scale 448/amax in fp32 (the fp8 workload's input recipe)."""
+    if dtype == "bf16":
+        vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    else:
+        vals = bits.view(np.float16).astype(np.float32)
+    amax = np.float32(np.max(np.abs(vals)))
+    return float(np.float32(448.0) / amax)
+
+
+def make_copy(name, T, H, D, n_slots, seed, dtype="bf16", index_dtype=np.int32,
+              slot_stride=None, slots=None, page_size=16, num_split=0) -> Workload:
+    """A contiguous-row plain-copy problem with distinct random slots."""
+    k = _normal_rows(seed * 4 + 1, T, H, D, dtype)
+    v = _normal_rows(seed * 4 + 2, T, H, D, dtype)
+    if slots is None:
+        slots = distinct_slots(seed * 4 + 3, n_slots, T)
+    ss = slot_stride if slot_stride is not None else H * D * 2
+    return Workload(name=name, T=T, H=H, D=D, src_dtype=dtype, kind="copy", k=k, v=v,
+                    k_view=_contig_view(H, D), v_view=_contig_view(H, D),
+                    indices=slots.astype(index_dtype), n_slots=n_slots, slot_stride=ss,
+                    cache_head_stride=D * 2, cache_elem=2, sentinel=BF16_SENTINEL,
+                    page_size=page_size, page_stride=page_size * ss, num_split=num_split)
+
+
+def make_fp8(name, T, H, D, n_slots, seed, dtype="bf16", index_dtype=np.int64,
+             page_size=32, use_scale=1, scale=4.0, outlier_frac=0.001,
+             slot_stride=None, page_stride=None) -> Workload:
+    """An FP8 problem: scale*N(0,1) with a fraction of +-U(500, 2000) outliers."""
+    ks = []
+    for j in (1, 2):
+        x = normal(seed * 8 + j, T * H * D) * np.float32(scale)
+        u = uniform01(seed * 8 + 2 + j, 3 * x.size)
+        hit = u[0::3] < outlier_frac
+        mag = 500.0 + 1500.0 * u[1::3]
+        sgn = np.where(u[2::3] < 0.5, -1.0, 1.0)
+        x = np.where(hit, (sgn * mag).astype(np.float32), x)
+        ks.append(to_bits(x, dtype).reshape(T, H, D))
+    k, v = ks
+    slots = distinct_slots(seed * 8 + 5, n_slots, T)
+    ss = slot_stride if slot_stride is not None else H * D
+    ps = page_stride if page_stride is not None else page_size * ss
+    w = Workload(name=name, T=T, H=H, D=D, src_dtype=dtype, kind="fp8", k=k, v=v,
+                 k_view=_contig_view(H, D), v_view=_contig_view(H, D),
+                 indices=slots.astype(index_dtype), n_slots=n_slots, slot_stride=ss,
+                 cache_head_stride=D, cache_elem=1, sentinel=FP8_SENTINEL,
+                 page_size=page_size, page_stride=ps, use_scale=use_scale)
+    w.inv_k = _amax_inv(k, dtype)
+    w.inv_v = _amax_inv(v, dtype)
+    return w
+
+
+def tiny() -> Workload:
+    return make_copy("tiny", T=16, H=2, D=64, n_slots=256, seed=0x5EED0000, page_size=16)
+
+
+def decode(num_split: int = 0) -> Workload:
+    return make_copy("decode", T=256, H=8, D=128, n_slots=1 << 20, seed=0x5EED0001,
+                     index_dtype=np.int64, num_split=num_split)
+
+
+def prefill() -> Workload:
+    slots = page_run_slots(0x5EED0002 * 4 + 3, n_pages=(1 << 22) // 64, page_size=64, k_pages=512)
+    return make_copy("prefill", T=32768, H=8, D=128, n_slots=1 << 22, seed=0x5EED0002,
+                     slots=slots, page_size=64)
+
+
+def fp8(use_scale: int = 1) -> Workload:
+    return make_fp8("fp8", T=8192, H=8, D=128, n_slots=1 << 20, seed=0x5EED0003,
+                    page_size=32, use_scale=use_scale)
+
+
+def strided() -> Workload:
+    """fp16 K and V as views into a fused QKV tensor [T, (32 + 2*8) * 128].
+
+    Only the K and V columns are ever read; the Q columns are filled with a
+    constant pattern so that generating them costs nothing.
+    """
+    T, H, D, HQ = 65536, 8, 128, 32
+    width = (HQ + 2 * H) * D
+    qkv = np.full((T, width), 0x3C00, dtype=np.uint16)   # fp16 1.0 in the Q columns
+    qkv[:, HQ * D:(HQ + H) * D] = _normal_rows(0x5EED0004 * 4 + 1, T, H, D, "f16").reshape(T, H * D)
+    qkv[:, (HQ + H) * D:] = _normal_rows(0x5EED0004 * 4 + 2, T, H, D, "f16").reshape(T, H * D)
+    slots = distinct_slots(0x5EED0004 * 4 + 3, 1 << 21, T)
+    tok = width * 2
+    w = Workload(name="strided", T=T, H=H, D=D, src_dtype="f16", kind="copy", k=qkv, v=qkv,
+                 k_view=(HQ * D * 2, tok, D * 2, 2), v_view=((HQ + H) * D * 2, tok, D * 2, 2),
+                 indices=slots.astype(np.int32), n_slots=1 << 21, slot_stride=H * D * 2,
+                 cache_head_stride=D * 2, cache_elem=2, sentinel=BF16_SENTINEL,
+                 page_size=16, page_stride=16 * H * D * 2)
+    w.notes["shared_source"] = True
+    return w
+
+
+def odd() -> Workload:
+    """fp16 H=1, D=576 rows (1152 B) into 1280-byte slots."""
+    return make_copy("odd", T=65536, H=1, D=576, n_slots=1 << 21, seed=0x5EED0005,
+                     dtype="f16", slot_stride=1280)
+
+
+WORKLOADS = {
+    "tiny": tiny,
+    "decode": decode,
+    "prefill": prefill,
+    "fp8": fp8,
+    "strided": strided,
+    "odd": odd,
+}
