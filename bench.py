@@ -1,0 +1,660 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 KV-cache write path.
+
+One step = one call of the write path over one batch of the workload (the
+batch's K rows and V rows scattered into the caches at its slot indices).
+Default workload: the decode batch (T=256 tokens, 8 KV heads, head_dim 128,
+bf16, int64 slots into a 1,048,576-slot cache). Other workloads with
+``--workload``: tiny, prefill, fp8, fp8_noscale, strided, odd.
+
+Protocol (``--impl ours``):
+  * inputs already in HBM; every step uses the next batch of a pool of
+    distinct batches (K/V rows and slot sets) whose total size exceeds 4x the
+    L2 cache, so consecutive steps never hit L2 for their inputs;
+  * the steps run back to back from CUDA graphs of recorded calls (calls
+    are launch-bound at decode size, so the graph removes host overhead but
+    not the per-kernel device cost);
+  * W warm-up steps, then exactly K timed steps bracketed by barrier +
+    synchronise, CUDA events on the launching stream, max over ranks;
+  * clocks sampled with nvidia-smi during the timed region;
+  * ``e2e``: the same steps with each step's inputs copied host->device from
+    pinned memory and the error record read back device->host, all inside
+    the timed region;
+  * ``cpu_baseline``: the CPU oracle, single thread, on a bounded sample of
+    the same workload (rank 0, N=1 only).
+
+``--impl reference`` times the CPU oracle as the reference arm on the same
+metric and prints its own JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV write tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+L2_BYTES = 129 * 1000 * 1000
+FALLBACK_HBM_GBS = 6800.0
+
+DESCRIPTIONS = {
+    "tiny": "tiny copy: T=16, H_kv=2, D=64 bf16, cache 256 slots, int32 indices",
+    "decode": "decode copy: T=256, H_kv=8, D=128 bf16 (2048 B rows), cache 1,048,576 slots, "
+              "int64 distinct random slots",
+    "prefill": "prefill copy: T=32768, H_kv=8, D=128 bf16, page_size 64, 512 whole pages in "
+               "random order, cache 4,194,304 slots, int32",
+    "fp8": "fused FP8 write: T=8192, H_kv=8, D=128 bf16 4*N(0,1) with 0.1% outliers, "
+           "inv_scale=448/amax (use_scale=1), e4m3fn cache 1,048,576 slots, page_size 32, int64",
+    "fp8_noscale": "fused FP8 write as fp8 with use_scale=0",
+    "strided": "strided copy: fp16 K/V views into QKV [65536, 6144] (token stride 12,288 B), "
+               "cache 2,097,152 slots, int32",
+    "odd": "odd-size copy: fp16 H_kv=1, D=576 (1152 B rows), 1280 B slot stride, "
+           "cache 2,097,152 slots, int32",
+}
+
+DEFAULT_STEPS = {"tiny": 200000, "decode": 200000, "prefill": 10000, "fp8": 50000,
+                 "fp8_noscale": 50000, "strided": 5000, "odd": 10000}
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (one process per GPU; weak scaling, no data exchange)
+# ---------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float, device=None) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# Peaks, clocks
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs: STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (no measured peak file)"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str, period_ms: int = 50):
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-i", str(gpu_index), "-lms", str(period_ms)]
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.monotonic())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        return self.summary()
+
+    def summary(self):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(t=ts, sm=float(parts[1]), smax=float(parts[2]),
+                                 reasons=parts[4], hw=parts[5], hwt=parts[6], swt=parts[7],
+                                 pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (0, 1e30)
+        inside = [r for r in rows if t0 - 0.06 <= r["t"] <= t1 + 0.06] or rows
+        reasons = set()
+        for r in inside:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+                "sm_max_mhz": max(r["smax"] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# Workload pools on the device
+# ---------------------------------------------------------------------------
+
+class Pool:
+    """Device-resident batches of one workload plus the caches they write.
+
+    Batch 0 is the workload's own seeded data; further batches (used to keep
+    consecutive steps out of L2) hold N(0,1) rows drawn on the device and
+    fresh slot sets with the same structure (distinct random slots, or whole
+    random pages for the prefill workload).
+    """
+
+    def __init__(self, name: str, device, pool_bytes: int, seed: int = 1234):
+        import torch
+        self.name = name
+        w = load_workload(name)
+        self.w = w
+        self.dev = device
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        T, H, D = w.T, w.H, w.D
+        src_dtype = torch.bfloat16 if w.src_dtype == "bf16" else torch.float16
+        self.src_dtype = src_dtype
+        idx_dtype = torch.int64 if w.indices.dtype == np.int64 else torch.int32
+        self.in_bytes_per_batch = 2 * w.row_bytes * T + w.indices.itemsize * T
+        shared = bool(w.notes.get("shared_source"))
+        src_batch_bytes = w.k.nbytes if shared else 2 * w.k.nbytes
+        nb = max(1, min(256, -(-pool_bytes // max(1, src_batch_bytes))))
+        if src_batch_bytes >= 2 * L2_BYTES:
+            nb = 1
+        self.num_batches = nb
+        self.k, self.v, self.idx = [], [], []
+        host_k = torch.from_numpy(w.k.view(np.int16)).to(device).view(src_dtype)
+        host_v = host_k if shared else torch.from_numpy(w.v.view(np.int16)).to(device).view(src_dtype)
+        for b in range(nb):
+            if b == 0:
+                kb, vb = host_k, host_v
+                ib = torch.from_numpy(w.indices).to(device)
+            else:
+                kb = torch.randn(host_k.shape, generator=g, device=device).to(src_dtype)
+                vb = kb if shared else torch.randn(host_v.shape, generator=g, device=device).to(src_dtype)
+                ib = self._slots(g, idx_dtype)
+            self.k.append(kb)
+            self.v.append(vb)
+            self.idx.append(ib)
+        # caches
+        if w.kind == "copy":
+            words = w.n_slots * w.slot_stride // 2
+            self.kc = torch.full((words,), w.sentinel, dtype=torch.int16, device=device)
+            self.vc = torch.full((words,), w.sentinel, dtype=torch.int16, device=device)
+        else:
+            nbytes = w.n_slots * w.slot_stride
+            self.kc = torch.full((nbytes,), w.sentinel, dtype=torch.uint8, device=device)
+            self.vc = torch.full((nbytes,), w.sentinel, dtype=torch.uint8, device=device)
+        self.inv = torch.tensor([w.inv_k, w.inv_v], dtype=torch.float32, device=device)
+        self.err = torch.zeros(2, dtype=torch.int64, device=device)
+        self.i64 = idx_dtype == torch.int64
+
+    def _slots(self, g, idx_dtype):
+        import torch
+        w = self.w
+        if w.name == "prefill":
+            ps = w.page_size
+            pages = torch.randperm(w.n_slots // ps, generator=g, device=self.dev)[: w.T // ps]
+            s = (pages[:, None] * ps + torch.arange(ps, device=self.dev)[None, :]).reshape(-1)
+        else:
+            s = torch.randperm(w.n_slots, generator=g, device=self.dev)[: w.T]
+        return s.to(idx_dtype)
+
+    def algorithmic_bytes(self) -> int:
+        return self.w.algorithmic_bytes()
+
+    def views(self, b):
+        """Device addresses and byte strides of batch b (source views inside QKV)."""
+        w = self.w
+        e = 2
+        kbase = self.k[b].data_ptr() + w.k_view[0]
+        vbase = self.v[b].data_ptr() + w.v_view[0]
+        strides = (w.k_view[1], w.k_view[2], w.k_view[3], w.v_view[1], w.v_view[2], w.v_view[3],
+                   w.slot_stride, w.cache_head_stride, w.cache_elem,
+                   w.slot_stride, w.cache_head_stride, w.cache_elem)
+        return kbase, vbase, strides
+
+    def call(self, b, stream_handle, k_ptr=None, v_ptr=None, idx_ptr=None) -> int:
+        import fp8_quant_gb300 as kv
+        w = self.w
+        kbase, vbase, strides = self.views(b)
+        k_ptr = kbase if k_ptr is None else k_ptr
+        v_ptr = vbase if v_ptr is None else v_ptr
+        idx_ptr = self.idx[b].data_ptr() if idx_ptr is None else idx_ptr
+        idt = 1 if self.i64 else 0
+        if w.kind == "copy":
+            return kv.raw.kv_store(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(), idx_ptr,
+                                   idt, 1, w.T, w.H, w.D, 2, strides, w.n_slots, w.num_split,
+                                   self.err.data_ptr(), stream_handle)
+        return kv.raw.kv_store_fp8(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(), idx_ptr,
+                                   idt, 1, w.T, w.H, w.D, 1 if w.src_dtype == "bf16" else 0,
+                                   strides, w.page_size, w.page_stride, w.page_stride, w.n_slots,
+                                   self.inv.data_ptr() if w.use_scale else None,
+                                   self.inv.data_ptr() + 4 if w.use_scale else None,
+                                   w.use_scale, self.err.data_ptr(), stream_handle)
+
+
+def capture_graphs(torch, fn_step, steps: int, chunk: int):
+    """CUDA graphs that run `steps` steps: (graph, steps_in_graph) list."""
+    graphs = []
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    done = 0
+    sizes = []
+    full, rem = divmod(steps, chunk)
+    if full:
+        sizes.append((chunk, full))
+    if rem:
+        sizes.append((rem, 1))
+    step_ctr = [0]
+    for size, reps in sizes:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(size):
+                fn_step(step_ctr[0])
+                step_ctr[0] += 1
+        graphs.append((g, size, reps))
+        done += size * reps
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return graphs
+
+
+def run_graphs(graphs):
+    for g, _, reps in graphs:
+        for _ in range(reps):
+            g.replay()
+
+
+def time_region(torch, dist, fn, device):
+    dist.barrier()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    fn()
+    e1.record(st)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms = e0.elapsed_time(e1)
+    return dist.max(ms, device=device)
+
+
+def single_call_cold_us(torch, pool, stream_handle, reps=30):
+    """Median latency of one call with L2 flushed before it (informational)."""
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=pool.dev)
+    times = []
+    st = torch.cuda.current_stream()
+    for r in range(reps):
+        flush.fill_(float(r))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        rc = pool.call(r % pool.num_batches, stream_handle)
+        e1.record(st)
+        assert rc == 0
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
+    del flush
+    return statistics.median(times)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+# ---------------------------------------------------------------------------
+
+def oracle_tokens_per_s(name: str, seconds: float):
+    """Time the CPU oracle (as it stands, one thread) on a bounded sample of
+    the workload: its whole batch, repeated until `seconds` elapse (at least
+    three times). Returns (tokens/s, description of the sample)."""
+    w = load_workload(name)
+    oracle_step(name, w, w.T)                   # first touch of the written pages
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle_step(name, w, w.T)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds and n >= 3:
+            break
+    sample = (f"{n} repetitions of the workload's batch of {w.T} tokens "
+              f"({el:.1f} s, one thread, full-size host caches)")
+    return n * w.T / el, sample
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ---------------------------------------------------------------------------
+# Arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args, dist):
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    if dist.rank != 0:
+        return
+    name = args.workload
+    w = load_workload(name)
+    # calibrate on one whole batch (after a first pass that touches the pages),
+    # then size each step's sample so that the whole run takes about two minutes
+    oracle_step(name, w, w.T)
+    t0 = time.perf_counter()
+    oracle_step(name, w, w.T)
+    rate = w.T / (time.perf_counter() - t0)
+    per_step_s = 120.0 / max(1, args.steps + args.warmup)
+    tokens = max(1, min(w.T, int(rate * per_step_s)))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle_step(name, w, tokens)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = args.steps * tokens / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype_of(w), "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[name], "tokens_per_step": tokens,
+                   "achieved_gbs": value * w.algorithmic_bytes() / w.T / 1e9},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: the first {tokens} of the workload's {w.T} "
+                                   f"tokens through the CPU oracle, one thread ({cpu_model()})"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def load_workload(name):
+    import workloads as wl
+    if name.startswith("fp8"):
+        return wl.fp8(use_scale=0 if name == "fp8_noscale" else 1)
+    return wl.WORKLOADS[name]()
+
+
+_ORACLE_CACHE = {}
+
+
+def oracle_step(name, w, tokens):
+    import oracle
+    key = name
+    if key not in _ORACLE_CACHE:
+        cache_bytes = w.n_slots * w.slot_stride
+        _ORACLE_CACHE[key] = (np.empty(cache_bytes, dtype=np.uint8),
+                              np.empty(cache_bytes, dtype=np.uint8),
+                              np.ascontiguousarray(w.k).view(np.uint8).reshape(-1),
+                              np.ascontiguousarray(w.v).view(np.uint8).reshape(-1),
+                              oracle.Strides(k_token=w.k_view[1], k_head=w.k_view[2],
+                                             k_dim=w.k_view[3], v_token=w.v_view[1],
+                                             v_head=w.v_view[2], v_dim=w.v_view[3],
+                                             kc_slot=w.slot_stride, kc_head=w.cache_head_stride,
+                                             kc_dim=w.cache_elem, vc_slot=w.slot_stride,
+                                             vc_head=w.cache_head_stride, vc_dim=w.cache_elem))
+    kc, vc, k, v, st = _ORACLE_CACHE[key]
+    if w.kind == "copy":
+        oracle.store_copy(k, v, kc, vc, w.indices, st, w.H, w.D, 2, w.n_slots,
+                          k_off=w.k_view[0], v_off=w.v_view[0], t_end=tokens)
+    else:
+        oracle.store_fp8(k, v, kc, vc, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
+                         w.page_stride, w.page_stride, w.n_slots, w.inv_k, w.inv_v,
+                         w.use_scale, t_end=tokens)
+
+
+def dtype_of(w):
+    if w.kind == "fp8":
+        return f"f32 ({w.src_dtype} in, e4m3fn out)"
+    return w.src_dtype
+
+
+def run_ours(args, dist):
+    import torch
+    import fp8_quant_gb300 as kv
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
+    torch.cuda.set_device(dist.local_rank)
+    device = torch.device("cuda", dist.local_rank)
+    kv.load_library()
+    name = args.workload
+    pool = Pool(name, device, pool_bytes=args.pool_mb << 20, seed=1234 + dist.rank)
+    w = pool.w
+    T = w.T
+    stream_handle = lambda: torch.cuda.current_stream().cuda_stream
+    nb = pool.num_batches
+
+    # --- device-resident steps -------------------------------------------
+    def step(i):
+        rc = pool.call(i % nb, stream_handle())
+        if rc != 0:
+            raise RuntimeError(f"launch failed: {kv.kv_status_str(rc)}")
+
+    chunk = min(args.steps, args.graph_chunk)
+    graphs = capture_graphs(torch, step, args.steps, chunk)
+    warm = max(args.warmup, 1)
+    warm_graphs = capture_graphs(torch, step, warm, min(warm, args.graph_chunk))
+    run_graphs(warm_graphs)
+    run_graphs(graphs)                      # first replay uploads the graph
+    torch.cuda.synchronize()
+
+    visible = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    clocks = ClockSampler(visible[dist.local_rank] if len(visible) > dist.local_rank
+                          else str(dist.local_rank))
+    clocks.start()
+    time.sleep(0.3)
+    clocks.mark()
+    ms = time_region(torch, dist, lambda: run_graphs(graphs), device)
+    clocks.mark()
+    clock_summary = clocks.stop()
+
+    st, nbad, _ = kv.kv_error_poll(pool.err)
+    if st != kv.KVStatus.OK:
+        raise RuntimeError(f"{nbad} out-of-range slots in the benchmark data")
+
+    bytes_per_step = pool.algorithmic_bytes()
+    sec_per_step = ms / 1e3 / args.steps
+    value = dist.world * T / sec_per_step
+    achieved_gbs = bytes_per_step / sec_per_step / 1e9
+    peak, peak_src = hbm_peak()
+
+    # --- end to end: pinned host -> device inputs, error record back --------
+    e2e = run_e2e(args, dist, torch, kv, pool, device)
+
+    cold_us = single_call_cold_us(torch, pool, stream_handle())
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        rate, sample = oracle_tokens_per_s(name, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": sample + f"; host CPU: {cpu_model()}"}
+
+    traffic = load_traffic(name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": warm + args.steps,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype_of(w), "data": "synthetic",
+        "config": {
+            "workload": DESCRIPTIONS[name], "tokens_per_step": T,
+            "bytes_per_step": bytes_per_step, "parallelism": f"replicas x{dist.world}",
+            "l2": f"inputs rotate over {nb} batches ({nb * pool.in_bytes_per_batch / 1e6:.0f} MB"
+                  f" read per cycle) > L2 (129 MB)" if nb > 1 else
+                  "one batch, inputs and writes each larger than L2",
+            "timing": "CUDA graphs of back-to-back calls, CUDA events on the launching stream",
+            "achieved_gbs": achieved_gbs, "single_call_cold_us": cold_us,
+            "single_call_cold_gbs": bytes_per_step / (cold_us * 1e-6) / 1e9,
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": achieved_gbs / peak, "traffic": traffic,
+                     "peak_source": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clock_summary,
+    }
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def load_traffic(name):
+    """DRAM bytes per launch from the committed ncu summary, if it matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get(name)
+    except Exception:
+        return None
+
+
+def run_e2e(args, dist, torch, kv, pool, device):
+    """Steps whose inputs come from pinned host memory every time."""
+    w = pool.w
+    nb = pool.num_batches
+    shared = bool(w.notes.get("shared_source"))
+    # pinned host copies of every batch; device staging buffers
+    host_k = [pool.k[b].cpu().pin_memory() for b in range(nb)]
+    host_v = host_k if shared else [pool.v[b].cpu().pin_memory() for b in range(nb)]
+    host_i = [pool.idx[b].cpu().pin_memory() for b in range(nb)]
+    dk = torch.empty_like(pool.k[0])
+    dv = dk if shared else torch.empty_like(pool.v[0])
+    di = torch.empty_like(pool.idx[0])
+    err_host = torch.zeros(2, dtype=torch.int64).pin_memory()
+    h2d = (host_k[0].numel() * host_k[0].element_size() * (1 if shared else 2)
+           + host_i[0].numel() * host_i[0].element_size())
+    d2h = err_host.numel() * err_host.element_size()
+
+    def step(i):
+        b = i % nb
+        dk.copy_(host_k[b], non_blocking=True)
+        if not shared:
+            dv.copy_(host_v[b], non_blocking=True)
+        di.copy_(host_i[b], non_blocking=True)
+        kbase = dk.data_ptr() + w.k_view[0]
+        vbase = dv.data_ptr() + w.v_view[0]
+        rc = pool.call(b, torch.cuda.current_stream().cuda_stream, kbase, vbase, di.data_ptr())
+        if rc != 0:
+            raise RuntimeError(kv.kv_status_str(rc))
+        err_host.copy_(pool.err, non_blocking=True)
+
+    steps = max(3, min(args.steps, args.e2e_steps))
+    graphs = capture_graphs(torch, step, steps, min(steps, args.graph_chunk))
+    run_graphs(graphs)
+    torch.cuda.synchronize()
+    ms = time_region(torch, dist, lambda: run_graphs(graphs), device)
+    sec = ms / 1e3 / steps
+    return {"value": dist.world * w.T / sec, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "how": "pinned host -> device copies of K, V and indices, the kv_store call, and "
+                   "a device -> host read of the error record, every step, from CUDA graphs"}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--workload", default="decode", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pool-mb", type=int, default=512)
+    ap.add_argument("--graph-chunk", type=int, default=1000)
+    ap.add_argument("--e2e-steps", type=int, default=20000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args(argv)
+    if a.steps is None:
+        a.steps = DEFAULT_STEPS[a.workload] if a.impl == "ours" else 20
+    if a.warmup is None:
+        a.warmup = max(3, a.steps // 20) if a.impl == "ours" else 3
+    if a.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if a.steps < 1:
+        ap.error("--steps must be positive")
+    return a
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    dist = Dist()
+    if args.impl == "reference":
+        if dist.rank == 0:
+            run_reference(args, dist)
+        return
+    dist.init("nccl")
+    try:
+        run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,833 @@
+// KV-cache write kernels for GB300 (sm_103a) and the C ABI declared in
+// include/kvstore.h.
+//
+// What is computed (sglang kvcache.cuh, `store_kvcache`; sglang
+// trtllm_fp8_kv_kernel.py, `_fused_fp8_set_kv_buffer_kernel` and
+// `_process_kv_tensor`): for each token t with slot s = indices[t], the K row
+// and the V row are written into cache row s -- byte for byte (kv_store) or
+// as FP8 e4m3fn after an fp32 multiply by the inverse scale (kv_store_fp8).
+//
+// Design.  The path is a pure HBM stream (no arithmetic worth a tensor core),
+// so every choice is about bytes in flight and coalescing:
+//  * A row is cut into "segments" (one per head, or one per row when heads
+//    are contiguous on both sides) and optionally into parts; a unit of work
+//    is (token, K|V, segment, part) and one warp moves one unit at a time.
+//  * Lane l of the warp moves chunks l, l+32, l+64, ... of the unit, so every
+//    warp-wide load or store covers 32 consecutive chunks (512 contiguous
+//    bytes at 16 B per chunk): full 32-byte sectors, one request per 4 lines.
+//  * The unit's first batch of loads (up to U chunks per lane) is issued
+//    before the slot id is known, so the index read and the row read overlap;
+//    only the stores depend on the slot.
+//  * Loads are non-coherent and do not allocate in L1 (the rows are read
+//    once); the grid is a whole number of CTAs per SM and loops over units.
+//  * Out-of-range slots are skipped and counted in the caller's error record
+//    with two atomics per bad token; nothing traps and nothing is written
+//    outside [0, size_limit).
+//  * Every kernel waits on the previous grid (griddepcontrol.wait) before its
+//    first global access and is launched with programmatic stream
+//    serialisation, so its launch overlaps the previous kernel's tail.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+
+#include "kvstore.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarpsPerCta = kThreads / 32;
+constexpr int kMaxDevices = 64;
+
+thread_local int g_last_cuda_error = 0;
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Vector of VEC bytes moved by one lane.
+template <int VEC> struct Chunk;
+template <> struct Chunk<16> { uint32_t w[4]; };
+template <> struct Chunk<8> { uint32_t w[2]; };
+template <> struct Chunk<4> { uint32_t w[1]; };
+template <> struct Chunk<2> { uint16_t h; };
+template <> struct Chunk<1> { uint16_t h; };
+
+// Streaming loads: non-coherent path, no L1 allocation (each byte is read once).
+__device__ __forceinline__ void ld_stream(Chunk<16>& c, const void* p) {
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(c.w[0]), "=r"(c.w[1]), "=r"(c.w[2]), "=r"(c.w[3])
+               : "l"(p));
+}
+__device__ __forceinline__ void ld_stream(Chunk<8>& c, const void* p) {
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+               : "=r"(c.w[0]), "=r"(c.w[1])
+               : "l"(p));
+}
+__device__ __forceinline__ void ld_stream(Chunk<4>& c, const void* p) {
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(c.w[0]) : "l"(p));
+}
+__device__ __forceinline__ void ld_stream(Chunk<2>& c, const void* p) {
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(c.h) : "l"(p));
+}
+__device__ __forceinline__ void ld_stream(Chunk<1>& c, const void* p) {
+  asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(c.h) : "l"(p));
+}
+
+__device__ __forceinline__ void st_stream(void* p, const Chunk<16>& c) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(c.w[0]), "r"(c.w[1]),
+               "r"(c.w[2]), "r"(c.w[3])
+               : "memory");
+}
+__device__ __forceinline__ void st_stream(void* p, const Chunk<8>& c) {
+  asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(c.w[0]), "r"(c.w[1]) : "memory");
+}
+__device__ __forceinline__ void st_stream(void* p, const Chunk<4>& c) {
+  asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(c.w[0]) : "memory");
+}
+__device__ __forceinline__ void st_stream(void* p, const Chunk<2>& c) {
+  asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"(c.h) : "memory");
+}
+__device__ __forceinline__ void st_stream(void* p, const Chunk<1>& c) {
+  asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "h"(c.h) : "memory");
+}
+
+template <typename IdxT>
+__device__ __forceinline__ int64_t load_slot(const void* indices, int64_t stride, int64_t t) {
+  return static_cast<int64_t>(__ldg(static_cast<const IdxT*>(indices) + t * stride));
+}
+
+// One record per skipped token: a count and the lowest skipped token (kept as
+// its bitwise NOT so that a zeroed record means "none").
+__device__ __forceinline__ void record_oob(kv_error_record* err, uint64_t t) {
+  atomicAdd(reinterpret_cast<unsigned long long*>(&err->oob_count), 1ull);
+  atomicMax(reinterpret_cast<unsigned long long*>(&err->first_bad_key),
+            static_cast<unsigned long long>(~t));
+}
+
+// Unit u -> (token, K|V, segment, part).
+struct UnitShape {
+  uint64_t num_units;        // num_tokens * units_per_token
+  uint32_t units_per_token;  // 2 * units_per_side
+  uint32_t units_per_side;   // num_segments * parts
+  uint32_t parts;            // parts per segment
+  uint32_t part_chunks;      // chunks per part
+};
+
+struct Unit {
+  int64_t token;
+  uint32_t kv, seg, part, rank;  // rank: position of the unit inside its token
+};
+
+__device__ __forceinline__ Unit decode_unit(const UnitShape& s, uint64_t u) {
+  Unit r;
+  const uint64_t t = u / s.units_per_token;
+  r.token = static_cast<int64_t>(t);
+  r.rank = static_cast<uint32_t>(u - t * s.units_per_token);
+  r.kv = r.rank >= s.units_per_side ? 1u : 0u;
+  const uint32_t q = r.rank - r.kv * s.units_per_side;
+  r.seg = q / s.parts;
+  r.part = q - r.seg * s.parts;
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Plain copy: kvcache.cuh `store_kvcache` / `copy_kv_warp`.
+// ---------------------------------------------------------------------------
+
+struct CopySide {
+  const uint8_t* src;  // element (0, 0, 0) of the input
+  uint8_t* dst;        // element (slot 0, 0, 0) of the cache
+  int64_t src_token, src_seg, dst_slot, dst_seg;
+};
+
+struct CopyParams {
+  CopySide side[2];
+  const void* indices;
+  int64_t index_stride;
+  int64_t size_limit;
+  UnitShape shape;
+  kv_error_record* err;
+};
+
+template <int VEC, int U, typename IdxT>
+__global__ void __launch_bounds__(kThreads) kv_copy_rows(const __grid_constant__ CopyParams p) {
+  grid_dependency_wait();
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  const uint32_t nchunks = p.shape.part_chunks;
+  const int64_t part_bytes = static_cast<int64_t>(nchunks) * VEC;
+
+  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+       u < p.shape.num_units; u += nwarps) {
+    const Unit w = decode_unit(p.shape, u);
+    const CopySide& sd = p.side[w.kv];
+    const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
+    const uint8_t* src = sd.src + w.token * sd.src_token + static_cast<int64_t>(w.seg) * sd.src_seg +
+                         static_cast<int64_t>(w.part) * part_bytes;
+
+    Chunk<VEC> buf[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = lane + 32u * j;
+      if (c < nchunks) ld_stream(buf[j], src + static_cast<size_t>(c) * VEC);
+    }
+    if (slot < 0 || slot >= p.size_limit) {
+      if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
+      continue;
+    }
+    uint8_t* dst = sd.dst + slot * sd.dst_slot + static_cast<int64_t>(w.seg) * sd.dst_seg +
+                   static_cast<int64_t>(w.part) * part_bytes;
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = lane + 32u * j;
+      if (c < nchunks) st_stream(dst + static_cast<size_t>(c) * VEC, buf[j]);
+    }
+    // Rows longer than 32*U chunks: further batches, loads then stores.
+    for (uint32_t c0 = 32u * U; c0 < nchunks; c0 += 32u * U) {
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + lane + 32u * j;
+        if (c < nchunks) ld_stream(buf[j], src + static_cast<size_t>(c) * VEC);
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + lane + 32u * j;
+        if (c < nchunks) st_stream(dst + static_cast<size_t>(c) * VEC, buf[j]);
+      }
+    }
+  }
+  grid_dependents_launch();
+}
+
+// Element-wise copy for rows whose elements are not contiguous (dim stride
+// different from the element size).  One warp per (token, K|V, head).
+struct GenericCopyParams {
+  const uint8_t* src[2];
+  uint8_t* dst[2];
+  int64_t src_token[2], src_head[2], src_dim[2];
+  int64_t dst_slot[2], dst_head[2], dst_dim[2];
+  const void* indices;
+  int64_t index_stride, size_limit;
+  uint64_t num_units;  // num_tokens * 2 * num_heads
+  int32_t num_heads, head_dim, elem_bytes;
+  kv_error_record* err;
+};
+
+template <typename IdxT>
+__global__ void __launch_bounds__(kThreads) kv_copy_elements(const __grid_constant__ GenericCopyParams p) {
+  grid_dependency_wait();
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  const uint64_t per_token = 2ull * static_cast<uint64_t>(p.num_heads);
+  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+       u < p.num_units; u += nwarps) {
+    const int64_t t = static_cast<int64_t>(u / per_token);
+    const uint32_t r = static_cast<uint32_t>(u - static_cast<uint64_t>(t) * per_token);
+    const int kv = r >= static_cast<uint32_t>(p.num_heads) ? 1 : 0;
+    const int64_t h = r - kv * p.num_heads;
+    const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, t);
+    if (slot < 0 || slot >= p.size_limit) {
+      if (r == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(t));
+      continue;
+    }
+    const uint8_t* src = p.src[kv] + t * p.src_token[kv] + h * p.src_head[kv];
+    uint8_t* dst = p.dst[kv] + slot * p.dst_slot[kv] + h * p.dst_head[kv];
+    for (int64_t d = lane; d < p.head_dim; d += 32) {
+      const uint8_t* s = src + d * p.src_dim[kv];
+      uint8_t* o = dst + d * p.dst_dim[kv];
+      for (int b = 0; b < p.elem_bytes; ++b) o[b] = __ldg(s + b);
+    }
+  }
+  grid_dependents_launch();
+}
+
+// ---------------------------------------------------------------------------
+// Fused FP8 write: trtllm_fp8_kv_kernel.py `_fused_fp8_set_kv_buffer_kernel`
+// and `_process_kv_tensor`.
+// ---------------------------------------------------------------------------
+
+// Two fp32 values to two e4m3fn bytes (lo in bits 0-7): round to nearest even,
+// saturate finite overflow and infinities to +-448.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two packed 2-byte inputs -> fp32 (exact).
+template <bool kBF16>
+__device__ __forceinline__ float2 widen2(uint32_t w) {
+  if constexpr (kBF16) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  } else {
+    return make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu))),
+                       __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))));
+  }
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t quant2(uint32_t w, float inv) {
+  const float2 x = widen2<kBF16>(w);
+  return e4m3x2(__fmul_rn(x.x, inv), __fmul_rn(x.y, inv));
+}
+
+// One lane's chunk: OUT output bytes from OUT 2-byte inputs.
+template <int OUT> struct Fp8Chunk { uint32_t in[OUT / 2]; };
+
+template <int OUT>
+__device__ __forceinline__ void ld_in(Fp8Chunk<OUT>& c, const uint8_t* p) {
+  if constexpr (OUT == 16) {
+    ld_stream(*reinterpret_cast<Chunk<16>*>(&c.in[0]), p);
+    ld_stream(*reinterpret_cast<Chunk<16>*>(&c.in[4]), p + 16);
+  } else if constexpr (OUT == 8) {
+    ld_stream(*reinterpret_cast<Chunk<16>*>(&c.in[0]), p);
+  } else if constexpr (OUT == 4) {
+    ld_stream(*reinterpret_cast<Chunk<8>*>(&c.in[0]), p);
+  } else {
+    static_assert(OUT == 2, "OUT");
+    ld_stream(*reinterpret_cast<Chunk<4>*>(&c.in[0]), p);
+  }
+}
+
+template <int OUT, bool kBF16>
+__device__ __forceinline__ void quant_store(uint8_t* p, const Fp8Chunk<OUT>& c, float inv) {
+  if constexpr (OUT >= 4) {
+    Chunk<OUT> o;
+#pragma unroll
+    for (int i = 0; i < OUT / 4; ++i)
+      o.w[i] = quant2<kBF16>(c.in[2 * i], inv) | (quant2<kBF16>(c.in[2 * i + 1], inv) << 16);
+    st_stream(p, o);
+  } else {
+    Chunk<2> o;
+    o.h = static_cast<uint16_t>(quant2<kBF16>(c.in[0], inv));
+    st_stream(p, o);
+  }
+}
+
+struct Fp8Side {
+  const uint8_t* src;
+  uint8_t* dst;
+  int64_t src_token, src_seg;      // input byte strides
+  int64_t dst_slot, dst_seg, dst_page;
+  const float* inv;                // device scalar, or nullptr (scale 1)
+};
+
+struct Fp8Params {
+  Fp8Side side[2];
+  const void* indices;
+  int64_t index_stride, size_limit, page_size;
+  UnitShape shape;
+  kv_error_record* err;
+};
+
+__device__ __forceinline__ int64_t paged_offset(int64_t slot, int64_t page_size, int64_t page_stride,
+                                                int64_t slot_stride) {
+  if (page_size == 1) return slot * page_stride;
+  const int64_t page = slot / page_size;
+  return page * page_stride + (slot - page * page_size) * slot_stride;
+}
+
+template <int OUT, int U, typename IdxT, bool kBF16>
+__global__ void __launch_bounds__(kThreads) kv_fp8_rows(const __grid_constant__ Fp8Params p) {
+  grid_dependency_wait();
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  const uint32_t nchunks = p.shape.part_chunks;
+  const int64_t part_out = static_cast<int64_t>(nchunks) * OUT;  // bytes out per part
+
+  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+       u < p.shape.num_units; u += nwarps) {
+    const Unit w = decode_unit(p.shape, u);
+    const Fp8Side& sd = p.side[w.kv];
+    const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
+    const float inv = sd.inv != nullptr ? __ldg(sd.inv) : 1.0f;
+    const uint8_t* src = sd.src + w.token * sd.src_token + static_cast<int64_t>(w.seg) * sd.src_seg +
+                         static_cast<int64_t>(w.part) * part_out * 2;
+
+    Fp8Chunk<OUT> buf[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = lane + 32u * j;
+      if (c < nchunks) ld_in<OUT>(buf[j], src + static_cast<size_t>(c) * (2 * OUT));
+    }
+    if (slot < 0 || slot >= p.size_limit) {
+      if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
+      continue;
+    }
+    uint8_t* dst = sd.dst + paged_offset(slot, p.page_size, sd.dst_page, sd.dst_slot) +
+                   static_cast<int64_t>(w.seg) * sd.dst_seg + static_cast<int64_t>(w.part) * part_out;
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = lane + 32u * j;
+      if (c < nchunks) quant_store<OUT, kBF16>(dst + static_cast<size_t>(c) * OUT, buf[j], inv);
+    }
+    for (uint32_t c0 = 32u * U; c0 < nchunks; c0 += 32u * U) {
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + lane + 32u * j;
+        if (c < nchunks) ld_in<OUT>(buf[j], src + static_cast<size_t>(c) * (2 * OUT));
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + lane + 32u * j;
+        if (c < nchunks) quant_store<OUT, kBF16>(dst + static_cast<size_t>(c) * OUT, buf[j], inv);
+      }
+    }
+  }
+  grid_dependents_launch();
+}
+
+// Element-wise FP8 write for strided dims or odd sizes.  One warp per
+// (token, K|V, head); lanes over the head's elements.
+struct GenericFp8Params {
+  const uint8_t* src[2];
+  uint8_t* dst[2];
+  int64_t src_token[2], src_head[2], src_dim[2];
+  int64_t dst_slot[2], dst_head[2], dst_dim[2], dst_page[2];
+  const float* inv[2];
+  const void* indices;
+  int64_t index_stride, size_limit, page_size;
+  uint64_t num_units;
+  int32_t num_heads, head_dim;
+  kv_error_record* err;
+};
+
+template <typename IdxT, bool kBF16>
+__global__ void __launch_bounds__(kThreads) kv_fp8_elements(const __grid_constant__ GenericFp8Params p) {
+  grid_dependency_wait();
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  const uint64_t per_token = 2ull * static_cast<uint64_t>(p.num_heads);
+  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+       u < p.num_units; u += nwarps) {
+    const int64_t t = static_cast<int64_t>(u / per_token);
+    const uint32_t r = static_cast<uint32_t>(u - static_cast<uint64_t>(t) * per_token);
+    const int kv = r >= static_cast<uint32_t>(p.num_heads) ? 1 : 0;
+    const int64_t h = r - kv * p.num_heads;
+    const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, t);
+    if (slot < 0 || slot >= p.size_limit) {
+      if (r == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(t));
+      continue;
+    }
+    const float inv = p.inv[kv] != nullptr ? __ldg(p.inv[kv]) : 1.0f;
+    const uint8_t* src = p.src[kv] + t * p.src_token[kv] + h * p.src_head[kv];
+    uint8_t* dst = p.dst[kv] + paged_offset(slot, p.page_size, p.dst_page[kv], p.dst_slot[kv]) +
+                   h * p.dst_head[kv];
+    for (int64_t d = lane; d < p.head_dim; d += 32) {
+      const uint32_t bits = __ldg(reinterpret_cast<const unsigned short*>(src + d * p.src_dim[kv]));
+      dst[d * p.dst_dim[kv]] = static_cast<uint8_t>(quant2<kBF16>(bits, inv) & 0xFFu);
+    }
+  }
+  grid_dependents_launch();
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+kv_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return KV_ERR_CUDA;
+}
+
+// SM count of the current device, cached per device.
+std::atomic<int> g_sm_count[kMaxDevices];
+
+kv_status current_sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev >= 0 && dev < kMaxDevices) {
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n > 0) {
+      *out = n;
+      return KV_OK;
+    }
+  }
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
+  *out = n;
+  return KV_OK;
+}
+
+// Resident CTAs per SM of a kernel, cached per kernel (the answer is the same
+// on every device this library is built for).
+std::mutex g_occ_mutex;
+struct OccEntry {
+  const void* fn;
+  int blocks;
+};
+OccEntry g_occ[128];
+int g_occ_n = 0;
+
+kv_status blocks_per_sm(const void* fn, int* out) {
+  {
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    for (int i = 0; i < g_occ_n; ++i)
+      if (g_occ[i].fn == fn) {
+        *out = g_occ[i].blocks;
+        return KV_OK;
+      }
+  }
+  int b = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, kThreads, 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (b < 1) b = 1;
+  std::lock_guard<std::mutex> lock(g_occ_mutex);
+  if (g_occ_n < 128) g_occ[g_occ_n++] = OccEntry{fn, b};
+  *out = b;
+  return KV_OK;
+}
+
+// Grid: enough CTAs for every unit to have a warp, capped at the resident
+// capacity (a whole number of CTAs per SM); warps loop over the rest.
+template <typename Params>
+kv_status launch(void (*kernel)(Params), uint64_t num_units, const Params& params,
+                 cudaStream_t stream) {
+  int sms = 0, per_sm = 0;
+  kv_status st = current_sm_count(&sms);
+  if (st != KV_OK) return st;
+  st = blocks_per_sm(reinterpret_cast<const void*>(kernel), &per_sm);
+  if (st != KV_OK) return st;
+  const uint64_t want = (num_units + kWarpsPerCta - 1) / kWarpsPerCta;
+  const uint64_t cap = static_cast<uint64_t>(sms) * static_cast<uint64_t>(per_sm);
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, params);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KV_OK;
+}
+
+// Largest power of two <= 16 dividing every value OR-ed into `bits`.
+int pow2_align(uint64_t bits) {
+  int v = 16;
+  while (v > 1 && (bits & static_cast<uint64_t>(v - 1)) != 0) v >>= 1;
+  return v;
+}
+
+uint64_t u64(const void* p) { return static_cast<uint64_t>(reinterpret_cast<uintptr_t>(p)); }
+uint64_t u64(int64_t x) { return static_cast<uint64_t>(x); }
+
+bool common_args_ok(const void* k, const void* v, const void* k_cache, const void* v_cache,
+                    const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
+                    int32_t num_heads, int32_t head_dim, const kv_strides* s, int64_t size_limit,
+                    const kv_error_record* d_err) {
+  if (!k || !v || !k_cache || !v_cache || !indices || !s || !d_err) return false;
+  if (index_dtype != KV_INDEX_I32 && index_dtype != KV_INDEX_I64) return false;
+  if (index_stride < 1 || num_heads < 1 || head_dim < 1 || size_limit < 0) return false;
+  if ((u64(d_err) & 7u) != 0) return false;
+  return true;
+}
+
+// Segments: one per row when heads are contiguous on every side, else one
+// per head.
+struct Segments {
+  uint32_t count;
+  int64_t elems;  // elements per segment
+};
+
+Segments segments(int32_t num_heads, int32_t head_dim, int64_t src_head_bytes,
+                  int64_t dst_head_bytes, const kv_strides* s) {
+  if (num_heads == 1 ||
+      (s->k_head == src_head_bytes && s->v_head == src_head_bytes &&
+       s->kc_head == dst_head_bytes && s->vc_head == dst_head_bytes))
+    return Segments{1u, static_cast<int64_t>(num_heads) * head_dim};
+  return Segments{static_cast<uint32_t>(num_heads), static_cast<int64_t>(head_dim)};
+}
+
+// Automatic split: small batches get more warps per row so that the copy
+// spreads over every SM; a part keeps at least one chunk per lane.
+uint32_t auto_parts(uint64_t units, int64_t seg_chunks, int sms) {
+  uint32_t parts = 1;
+  while (units * parts < static_cast<uint64_t>(sms) * 16u && seg_chunks % (2 * parts) == 0 &&
+         seg_chunks / (2 * parts) >= 32 && parts < 8)
+    parts *= 2;
+  return parts;
+}
+
+template <int VEC, typename IdxT>
+kv_status launch_copy_vec(const CopyParams& p, cudaStream_t stream) {
+  constexpr int U = 4;
+  return launch(kv_copy_rows<VEC, U, IdxT>, p.shape.num_units, p, stream);
+}
+
+template <typename IdxT>
+kv_status launch_copy(int vec, const CopyParams& p, cudaStream_t stream) {
+  switch (vec) {
+    case 16: return launch_copy_vec<16, IdxT>(p, stream);
+    case 8: return launch_copy_vec<8, IdxT>(p, stream);
+    case 4: return launch_copy_vec<4, IdxT>(p, stream);
+    case 2: return launch_copy_vec<2, IdxT>(p, stream);
+    default: return launch_copy_vec<1, IdxT>(p, stream);
+  }
+}
+
+template <int OUT, typename IdxT>
+kv_status launch_fp8_out(bool bf16, const Fp8Params& p, cudaStream_t stream) {
+  constexpr int U = OUT == 16 ? 2 : 4;
+  if (bf16) return launch(kv_fp8_rows<OUT, U, IdxT, true>, p.shape.num_units, p, stream);
+  return launch(kv_fp8_rows<OUT, U, IdxT, false>, p.shape.num_units, p, stream);
+}
+
+template <typename IdxT>
+kv_status launch_fp8(int out, bool bf16, const Fp8Params& p, cudaStream_t stream) {
+  switch (out) {
+    case 16: return launch_fp8_out<16, IdxT>(bf16, p, stream);
+    case 8: return launch_fp8_out<8, IdxT>(bf16, p, stream);
+    case 4: return launch_fp8_out<4, IdxT>(bf16, p, stream);
+    default: return launch_fp8_out<2, IdxT>(bf16, p, stream);
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+
+extern "C" kv_status kv_store(const void* k, const void* v, void* k_cache, void* v_cache,
+                              const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
+                              int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                              int32_t elem_bytes, const kv_strides* s, int64_t size_limit,
+                              int32_t num_split, kv_error_record* d_err, kv_stream_t stream_) {
+  if (num_tokens < 0) return KV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KV_OK;
+  if (!common_args_ok(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_heads,
+                      head_dim, s, size_limit, d_err))
+    return KV_ERR_INVALID_ARG;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+    return KV_ERR_INVALID_ARG;
+  if (num_split != 0 && num_split != 1 && num_split != 2 && num_split != 4) return KV_ERR_INVALID_ARG;
+  const int64_t row_bytes = static_cast<int64_t>(num_heads) * head_dim * elem_bytes;
+  if (num_split > 1 && row_bytes % (static_cast<int64_t>(num_split) * 128) != 0)
+    return KV_ERR_INVALID_ARG;
+  if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const bool i64 = index_dtype == KV_INDEX_I64;
+
+  if (s->k_dim != elem_bytes || s->v_dim != elem_bytes || s->kc_dim != elem_bytes ||
+      s->vc_dim != elem_bytes) {
+    GenericCopyParams g = {};
+    g.src[0] = static_cast<const uint8_t*>(k);
+    g.src[1] = static_cast<const uint8_t*>(v);
+    g.dst[0] = static_cast<uint8_t*>(k_cache);
+    g.dst[1] = static_cast<uint8_t*>(v_cache);
+    g.src_token[0] = s->k_token; g.src_head[0] = s->k_head; g.src_dim[0] = s->k_dim;
+    g.src_token[1] = s->v_token; g.src_head[1] = s->v_head; g.src_dim[1] = s->v_dim;
+    g.dst_slot[0] = s->kc_slot; g.dst_head[0] = s->kc_head; g.dst_dim[0] = s->kc_dim;
+    g.dst_slot[1] = s->vc_slot; g.dst_head[1] = s->vc_head; g.dst_dim[1] = s->vc_dim;
+    g.indices = indices;
+    g.index_stride = index_stride;
+    g.size_limit = size_limit;
+    g.num_units = static_cast<uint64_t>(num_tokens) * 2u * static_cast<uint64_t>(num_heads);
+    g.num_heads = num_heads;
+    g.head_dim = head_dim;
+    g.elem_bytes = elem_bytes;
+    g.err = d_err;
+    return i64 ? launch(kv_copy_elements<int64_t>, g.num_units, g, stream)
+               : launch(kv_copy_elements<int32_t>, g.num_units, g, stream);
+  }
+
+  const int64_t head_bytes = static_cast<int64_t>(head_dim) * elem_bytes;
+  const Segments sg = segments(num_heads, head_dim, head_bytes, head_bytes, s);
+  const int64_t seg_bytes = sg.elems * elem_bytes;
+  uint64_t bits = u64(k) | u64(v) | u64(k_cache) | u64(v_cache) | u64(s->k_token) |
+                  u64(s->v_token) | u64(s->kc_slot) | u64(s->vc_slot) | u64(seg_bytes);
+  if (sg.count > 1) bits |= u64(s->k_head) | u64(s->v_head) | u64(s->kc_head) | u64(s->vc_head);
+
+  int sms = 0;
+  kv_status st = current_sm_count(&sms);
+  if (st != KV_OK) return st;
+  uint32_t parts = 1;
+  const uint64_t rows = static_cast<uint64_t>(num_tokens) * 2u * sg.count;
+  if (num_split == 0) {
+    const int vec0 = pow2_align(bits);
+    parts = auto_parts(rows, seg_bytes / vec0, sms);
+  } else if (num_split > 1 && seg_bytes % (num_split * 16) == 0) {
+    parts = static_cast<uint32_t>(num_split);
+  }
+  const int64_t part_bytes = seg_bytes / parts;
+  const int vec = pow2_align(bits | u64(part_bytes));
+
+  CopyParams p = {};
+  p.side[0] = CopySide{static_cast<const uint8_t*>(k), static_cast<uint8_t*>(k_cache), s->k_token,
+                       s->k_head, s->kc_slot, s->kc_head};
+  p.side[1] = CopySide{static_cast<const uint8_t*>(v), static_cast<uint8_t*>(v_cache), s->v_token,
+                       s->v_head, s->vc_slot, s->vc_head};
+  p.indices = indices;
+  p.index_stride = index_stride;
+  p.size_limit = size_limit;
+  p.shape.parts = parts;
+  p.shape.units_per_side = sg.count * parts;
+  p.shape.units_per_token = 2u * p.shape.units_per_side;
+  p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
+  p.shape.part_chunks = static_cast<uint32_t>(part_bytes / vec);
+  p.err = d_err;
+  return i64 ? launch_copy<int64_t>(vec, p, stream) : launch_copy<int32_t>(vec, p, stream);
+}
+
+extern "C" kv_status kv_store_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                                  const void* indices, kv_index_dtype index_dtype,
+                                  int64_t index_stride, int64_t num_tokens, int32_t num_heads,
+                                  int32_t head_dim, kv_src_dtype src_dtype, const kv_strides* s,
+                                  int64_t page_size, int64_t kc_page_stride, int64_t vc_page_stride,
+                                  int64_t size_limit, const float* inv_k_scale,
+                                  const float* inv_v_scale, int32_t use_scale,
+                                  kv_error_record* d_err, kv_stream_t stream_) {
+  if (num_tokens < 0) return KV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KV_OK;
+  if (!common_args_ok(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_heads,
+                      head_dim, s, size_limit, d_err))
+    return KV_ERR_INVALID_ARG;
+  if (src_dtype != KV_SRC_F16 && src_dtype != KV_SRC_BF16) return KV_ERR_INVALID_ARG;
+  if (page_size < 1) return KV_ERR_INVALID_ARG;
+  if (use_scale && (!inv_k_scale || !inv_v_scale)) return KV_ERR_INVALID_ARG;
+  if (use_scale && ((u64(inv_k_scale) | u64(inv_v_scale)) & 3u) != 0) return KV_ERR_INVALID_ARG;
+  const uint64_t src_bits = u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token) | u64(s->k_head) |
+                            u64(s->v_head) | u64(s->k_dim) | u64(s->v_dim);
+  if ((src_bits & 1u) != 0) return KV_ERR_INVALID_ARG;
+  if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const bool i64 = index_dtype == KV_INDEX_I64;
+  const bool bf16 = src_dtype == KV_SRC_BF16;
+  const float* inv_k = use_scale ? inv_k_scale : nullptr;
+  const float* inv_v = use_scale ? inv_v_scale : nullptr;
+  // A page stride equal to page_size slots is the flat 3-D layout: s * slot_stride.
+  const bool flat = kc_page_stride == page_size * s->kc_slot && vc_page_stride == page_size * s->vc_slot;
+
+  const bool contiguous = s->k_dim == 2 && s->v_dim == 2 && s->kc_dim == 1 && s->vc_dim == 1;
+  Segments sg{0u, 0};
+  int out = 1;
+  if (contiguous) {
+    sg = segments(num_heads, head_dim, 2 * static_cast<int64_t>(head_dim), head_dim, s);
+    uint64_t dst_bits = u64(k_cache) | u64(v_cache) | u64(s->kc_slot) | u64(s->vc_slot) |
+                        u64(sg.elems);
+    uint64_t sbits = u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token);
+    if (sg.count > 1) {
+      dst_bits |= u64(s->kc_head) | u64(s->vc_head);
+      sbits |= u64(s->k_head) | u64(s->v_head);
+    }
+    if (!flat) dst_bits |= u64(kc_page_stride) | u64(vc_page_stride);
+    out = pow2_align(dst_bits);
+    while (out > 1 && (sbits & static_cast<uint64_t>((2 * out > 16 ? 16 : 2 * out) - 1)) != 0) out >>= 1;
+  }
+
+  if (out < 2) {
+    GenericFp8Params g = {};
+    g.src[0] = static_cast<const uint8_t*>(k);
+    g.src[1] = static_cast<const uint8_t*>(v);
+    g.dst[0] = static_cast<uint8_t*>(k_cache);
+    g.dst[1] = static_cast<uint8_t*>(v_cache);
+    g.src_token[0] = s->k_token; g.src_head[0] = s->k_head; g.src_dim[0] = s->k_dim;
+    g.src_token[1] = s->v_token; g.src_head[1] = s->v_head; g.src_dim[1] = s->v_dim;
+    g.dst_slot[0] = s->kc_slot; g.dst_head[0] = s->kc_head; g.dst_dim[0] = s->kc_dim;
+    g.dst_slot[1] = s->vc_slot; g.dst_head[1] = s->vc_head; g.dst_dim[1] = s->vc_dim;
+    g.dst_page[0] = flat ? s->kc_slot : kc_page_stride;
+    g.dst_page[1] = flat ? s->vc_slot : vc_page_stride;
+    g.page_size = flat ? 1 : page_size;
+    g.inv[0] = inv_k;
+    g.inv[1] = inv_v;
+    g.indices = indices;
+    g.index_stride = index_stride;
+    g.size_limit = size_limit;
+    g.num_units = static_cast<uint64_t>(num_tokens) * 2u * static_cast<uint64_t>(num_heads);
+    g.num_heads = num_heads;
+    g.head_dim = head_dim;
+    g.err = d_err;
+    if (i64)
+      return bf16 ? launch(kv_fp8_elements<int64_t, true>, g.num_units, g, stream)
+                  : launch(kv_fp8_elements<int64_t, false>, g.num_units, g, stream);
+    return bf16 ? launch(kv_fp8_elements<int32_t, true>, g.num_units, g, stream)
+                : launch(kv_fp8_elements<int32_t, false>, g.num_units, g, stream);
+  }
+
+  int sms = 0;
+  kv_status st = current_sm_count(&sms);
+  if (st != KV_OK) return st;
+  const uint64_t rows = static_cast<uint64_t>(num_tokens) * 2u * sg.count;
+  uint32_t parts = auto_parts(rows, sg.elems / out, sms);
+  const int64_t part_elems = sg.elems / parts;
+
+  Fp8Params p = {};
+  p.side[0] = Fp8Side{static_cast<const uint8_t*>(k), static_cast<uint8_t*>(k_cache), s->k_token,
+                      s->k_head, s->kc_slot, s->kc_head, flat ? s->kc_slot : kc_page_stride, inv_k};
+  p.side[1] = Fp8Side{static_cast<const uint8_t*>(v), static_cast<uint8_t*>(v_cache), s->v_token,
+                      s->v_head, s->vc_slot, s->vc_head, flat ? s->vc_slot : vc_page_stride, inv_v};
+  p.indices = indices;
+  p.index_stride = index_stride;
+  p.size_limit = size_limit;
+  p.page_size = flat ? 1 : page_size;
+  p.shape.parts = parts;
+  p.shape.units_per_side = sg.count * parts;
+  p.shape.units_per_token = 2u * p.shape.units_per_side;
+  p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
+  p.shape.part_chunks = static_cast<uint32_t>(part_elems / out);
+  p.err = d_err;
+  return i64 ? launch_fp8<int64_t>(out, bf16, p, stream) : launch_fp8<int32_t>(out, bf16, p, stream);
+}
+
+extern "C" kv_status kv_error_poll(kv_error_record* d_err, kv_stream_t stream_, int64_t* oob_count,
+                                   int64_t* first_bad_token) {
+  if (!d_err || (u64(d_err) & 7u) != 0) return KV_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  kv_error_record h = {0, 0};
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemcpyAsync(&h, d_err, sizeof h, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemsetAsync(d_err, 0, sizeof h, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (oob_count) *oob_count = static_cast<int64_t>(h.oob_count);
+  if (first_bad_token)
+    *first_bad_token = h.oob_count ? static_cast<int64_t>(~h.first_bad_key) : int64_t{-1};
+  return h.oob_count ? KV_ERR_INDEX_OOB : KV_OK;
+}
+
+extern "C" kv_status kv_error_reset(kv_error_record* d_err, kv_stream_t stream_) {
+  if (!d_err || (u64(d_err) & 7u) != 0) return KV_ERR_INVALID_ARG;
+  const cudaError_t e =
+      cudaMemsetAsync(d_err, 0, sizeof(kv_error_record), reinterpret_cast<cudaStream_t>(stream_));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KV_OK;
+}
+
+extern "C" const char* kv_status_str(kv_status status) {
+  switch (status) {
+    case KV_OK: return "KV_OK";
+    case KV_ERR_INVALID_ARG: return "KV_ERR_INVALID_ARG";
+    case KV_ERR_UNSUPPORTED: return "KV_ERR_UNSUPPORTED";
+    case KV_ERR_CUDA: return "KV_ERR_CUDA";
+    case KV_ERR_INDEX_OOB: return "KV_ERR_INDEX_OOB";
+  }
+  return "KV_STATUS_UNKNOWN";
+}
+
+extern "C" int kv_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" int kv_abi_version(void) { return KV_ABI_VERSION; }

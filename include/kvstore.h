@@ -1,0 +1,198 @@
+/*
+ * kvstore.h -- C ABI of the GB300 (sm_103a) KV-cache write library.
+ *
+ * For every new token t, the K row and the V row (num_heads x head_dim
+ * elements, arbitrary byte strides) are written into row indices[t] of a
+ * large K cache and V cache:
+ *
+ *   kv_store      plain byte-exact copy of the rows;
+ *   kv_store_fp8  each element is widened to fp32, optionally multiplied by a
+ *                 per-tensor fp32 inverse scale, converted to FP8 e4m3fn and
+ *                 written at the paged cache address of the slot.
+ *
+ * Sources (sglang): kvcache.cuh, kernel `store_kvcache` and host launcher
+ * `StoreKVCacheKernel::run` (plain copy, the row-split option and the slot
+ * bound 0 <= slot < size_limit); trtllm_fp8_kv_kernel.py, kernels
+ * `_fused_fp8_set_kv_buffer_kernel` / `_process_kv_tensor` and the wrapper
+ * `fused_fp8_set_kv_buffer` (page decomposition, strides, fp32 inverse scale
+ * read on the device, e4m3fn conversion).
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are device memory owned by the caller; the library
+ *    never allocates, frees or retains them, and never allocates memory of
+ *    its own during a call.
+ *  - Calls are asynchronous on `stream` and do not synchronise the host,
+ *    except kv_error_poll.  They may be captured in a CUDA graph.
+ *  - Every kernel launched here waits for the work that precedes it on the
+ *    stream before it touches memory (programmatic dependent launch), so the
+ *    stream's ordering is kept.
+ *  - Strides are in BYTES and may be any int64 value; elements of one head
+ *    are contiguous when the dim stride equals the element size, which is the
+ *    fast path.  Bases and strides that are not 16-byte multiples select
+ *    narrower vector widths; this is never an error.
+ *  - An out-of-range slot (outside [0, size_limit)) is not an argument error:
+ *    the kernel skips that token (neither its K nor its V row is written),
+ *    counts it in the caller's error record and continues.  kv_error_poll
+ *    reports it.  No slot value can cause a write outside the rows
+ *    [0, size_limit) of the caches.
+ *  - size_limit is trusted to be at most the number of cache rows.
+ *  - Duplicate slots: each such cache row ends up equal to one of the
+ *    candidate rows; which one is unspecified.
+ *  - num_tokens == 0 returns KV_OK without launching (pointers may be NULL).
+ */
+#ifndef FP8_QUANT_GB300_KVSTORE_H
+#define FP8_QUANT_GB300_KVSTORE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KV_ABI_VERSION 1
+
+/* Same type as cudaStream_t.  NULL selects the legacy default stream. */
+typedef struct CUstream_st *kv_stream_t;
+
+typedef enum kv_status {
+    KV_OK = 0,
+    KV_ERR_INVALID_ARG = 1,  /* bad argument found on the host; nothing was launched */
+    KV_ERR_UNSUPPORTED = 2,  /* legal request this library does not implement; nothing launched */
+    KV_ERR_CUDA = 3,         /* a CUDA runtime call failed; see kv_last_cuda_error() */
+    KV_ERR_INDEX_OOB = 4     /* kv_error_poll: at least one token had an out-of-range slot */
+} kv_status;
+
+typedef enum kv_index_dtype { KV_INDEX_I32 = 0, KV_INDEX_I64 = 1 } kv_index_dtype;
+
+/* Element type of the K/V inputs of kv_store_fp8 (2-byte floats). */
+typedef enum kv_src_dtype { KV_SRC_F16 = 0, KV_SRC_BF16 = 1 } kv_src_dtype;
+
+/* Byte strides.  Element (t, h, d) of K is at k + t*k_token + h*k_head +
+ * d*k_dim; element (h, d) of cache row s is at k_cache + s*kc_slot +
+ * h*kc_head + d*kc_dim (kv_store_fp8 adds the page decomposition, below).
+ * The K cache and the V cache have separate strides. */
+typedef struct kv_strides {
+    int64_t k_token, k_head, k_dim;
+    int64_t v_token, v_head, v_dim;
+    int64_t kc_slot, kc_head, kc_dim;
+    int64_t vc_slot, vc_head, vc_dim;
+} kv_strides;
+
+/* Device-side error record, owned by the caller (16 bytes, 8-byte aligned,
+ * zero-initialised before first use, e.g. with cudaMemsetAsync or
+ * kv_error_reset).  Kernels only add to it; kv_error_poll reads and clears it.
+ * Calls that share one record on different streams share its counts. */
+typedef struct kv_error_record {
+    uint64_t oob_count;      /* tokens skipped because their slot was out of range */
+    uint64_t first_bad_key;  /* bitwise NOT of the lowest skipped token; 0 if none */
+} kv_error_record;
+
+/*
+ * kv_store -- plain copy (sglang kvcache.cuh, `store_kvcache`).
+ *
+ *   k, v           device pointers to element (0, 0, 0) of the K and V inputs.
+ *   k_cache,
+ *   v_cache        device pointers to element (slot 0, 0, 0) of the caches.
+ *   indices        device pointer to num_tokens slot ids (int32 or int64 per
+ *                  index_dtype), read at indices[t * index_stride]
+ *                  (index_stride in ELEMENTS, >= 1).
+ *   num_heads,
+ *   head_dim       row shape, both >= 1.
+ *   elem_bytes     element size: 1, 2, 4 or 8 (the copy is byte-exact, so the
+ *                  element type does not matter; bf16/fp16 rows use 2).
+ *   strides        byte strides (host pointer, read during the call only).
+ *   size_limit     slots must satisfy 0 <= slot < size_limit.
+ *   num_split      how many parts each contiguous row is split into, each
+ *                  part copied by its own warp: 0 = choose automatically,
+ *                  1, 2 or 4.  2 and 4 need the row's bytes (num_heads *
+ *                  head_dim * elem_bytes) to be a multiple of 256 and 512
+ *                  respectively (the split rule of `StoreKVCacheKernel`);
+ *                  otherwise KV_ERR_INVALID_ARG.  The result does not depend
+ *                  on num_split.
+ *   d_err          device error record (required when num_tokens > 0).
+ *   stream         CUDA stream.
+ *
+ * Returns KV_OK once the kernel is enqueued, KV_ERR_INVALID_ARG for a bad
+ * argument (NULL pointer, num_tokens < 0, num_heads/head_dim < 1, bad
+ * elem_bytes, index_dtype, index_stride, num_split or split rule, size_limit
+ * < 0, misaligned d_err), KV_ERR_CUDA if the launch failed.
+ */
+kv_status kv_store(const void *k, const void *v, void *k_cache, void *v_cache,
+                   const void *indices, kv_index_dtype index_dtype, int64_t index_stride,
+                   int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                   int32_t elem_bytes, const kv_strides *strides, int64_t size_limit,
+                   int32_t num_split, kv_error_record *d_err, kv_stream_t stream);
+
+/*
+ * kv_store_fp8 -- fused scale + FP8 e4m3fn conversion + paged write
+ * (sglang trtllm_fp8_kv_kernel.py, `_fused_fp8_set_kv_buffer_kernel`,
+ * `_process_kv_tensor`, wrapper `fused_fp8_set_kv_buffer`).
+ *
+ * Arguments as for kv_store, except:
+ *   k, v           bf16 or fp16 inputs (src_dtype); addresses and the
+ *                  k/v strides must be even.
+ *   k_cache,
+ *   v_cache        caches of e4m3fn bytes (kc_dim / vc_dim are the byte
+ *                  distance between consecutive dims, normally 1).
+ *   page_size      tokens per page, >= 1.  Slot s is written at
+ *                  (s / page_size) * kc_page_stride + (s % page_size) * kc_slot
+ *                  + h * kc_head + d * kc_dim (likewise for V).  A 3-D cache
+ *                  [slots, H, D] passes kc_page_stride = page_size * kc_slot,
+ *                  which makes this s * kc_slot; a 4-D cache
+ *                  [pages, page_size, H, D] passes its page stride.
+ *   inv_k_scale,
+ *   inv_v_scale    DEVICE pointers to one fp32 each (the inverse scales),
+ *                  read by the kernel, so no host synchronisation is needed;
+ *                  both must be non-NULL when use_scale != 0 and are ignored
+ *                  otherwise.
+ *   use_scale      0: convert x unscaled; else convert fl32(x * inv).
+ *
+ * Numerics (per element): x is widened exactly to fp32; y = x * inv in fp32
+ * with round-to-nearest-even (no fused operations, denormals kept); the code
+ * is the e4m3fn value nearest to y, ties to the even mantissa, with finite
+ * overflow and +-Inf saturated to +-448 and every NaN written as 0x7F.
+ * use_scale == 0 gives the same bytes as use_scale != 0 with inv = 1.0f.
+ *
+ * Returns as kv_store; KV_ERR_INVALID_ARG also for a bad src_dtype,
+ * page_size < 1, odd input addresses or strides, or a NULL scale pointer
+ * with use_scale != 0.
+ */
+kv_status kv_store_fp8(const void *k, const void *v, void *k_cache, void *v_cache,
+                       const void *indices, kv_index_dtype index_dtype, int64_t index_stride,
+                       int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                       kv_src_dtype src_dtype, const kv_strides *strides, int64_t page_size,
+                       int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
+                       const float *inv_k_scale, const float *inv_v_scale, int32_t use_scale,
+                       kv_error_record *d_err, kv_stream_t stream);
+
+/*
+ * kv_error_poll -- synchronise `stream`, read the error record, clear it.
+ * (The pages trap inside the kernel on a bad slot; this library reports it
+ * here instead.)  Writes the number of skipped tokens and the lowest skipped
+ * token (-1 if none) to the optional host outputs.  Returns KV_OK when no
+ * token was skipped, KV_ERR_INDEX_OOB when one was, KV_ERR_INVALID_ARG for a
+ * NULL or misaligned record, KV_ERR_CUDA if a CUDA call failed (including an
+ * earlier asynchronous error surfaced by the synchronisation).
+ * Not capturable in a CUDA graph (it synchronises).
+ */
+kv_status kv_error_poll(kv_error_record *d_err, kv_stream_t stream, int64_t *oob_count,
+                        int64_t *first_bad_token);
+
+/* kv_error_reset -- zero the record asynchronously on `stream` (capturable). */
+kv_status kv_error_reset(kv_error_record *d_err, kv_stream_t stream);
+
+/* Static, NUL-terminated name of a status code. */
+const char *kv_status_str(kv_status status);
+
+/* The cudaError_t value of the last failed CUDA call made by this library on
+ * the calling thread (0 if none). */
+int kv_last_cuda_error(void);
+
+/* KV_ABI_VERSION of the library that was loaded. */
+int kv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8_QUANT_GB300_KVSTORE_H */

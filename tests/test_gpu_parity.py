@@ -1,0 +1,283 @@
+"""GPU parity: the CUDA library through its C ABI against the CPU oracle.
+
+Every case compares every byte of both caches (pre-filled with a sentinel, so
+stray writes show) and the out-of-range report. Sizes span many warps and
+CTAs with ragged tails; the cases cover each kernel variant (16/8/4/2/1-byte
+vectors, head-segmented rows, row splits, element-wise strided paths),
+both index types, index strides, padded slots and pages, misaligned views,
+out-of-range slots, empty calls, duplicates, and all 65,536 bf16 and fp16
+input patterns of the FP8 conversion.
+"""
+
+import zlib
+
+import numpy as np
+import pytest
+
+import workloads as wl
+from kvcheck import Problem, View, GpuRun, assert_same, copy_problem, fp8_problem, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.init()
+    yield
+
+
+# ---------------------------------------------------------------------------
+# Plain copy
+# ---------------------------------------------------------------------------
+
+COPY_CASES = {
+    # name: kwargs of copy_problem
+    "tiny_cfg_shape": dict(T=16, H=2, D=64, n_slots=256, idx_dtype=np.int32),
+    "decode_shape": dict(T=777, H=8, D=128, n_slots=4096),
+    "split2": dict(T=301, H=8, D=128, n_slots=1024, num_split=2),
+    "split4": dict(T=301, H=8, D=128, n_slots=1024, num_split=4, idx_dtype=np.int32),
+    "split1": dict(T=301, H=8, D=128, n_slots=1024, num_split=1),
+    "row1152_pad1280": dict(T=1000, H=1, D=576, n_slots=3000, slot_pad=128, idx_dtype=np.int32),
+    "row4096_long": dict(T=90, H=16, D=128, n_slots=200),
+    "row8192_multi_batch": dict(T=33, H=32, D=128, n_slots=100),
+    "small_rows_h1_d8": dict(T=2049, H=1, D=8, n_slots=5000),
+    "vec8_offset": dict(T=500, H=4, D=64, n_slots=1500, src_off=8, dst_off=8),
+    "vec4_offset": dict(T=500, H=4, D=64, n_slots=1500, src_off=4),
+    "vec2_offset": dict(T=500, H=4, D=64, n_slots=1500, dst_off=2),
+    "vec1_bytes_odd": dict(T=300, H=3, D=7, n_slots=900, elem=1, src_off=1),
+    "elem4_fp32": dict(T=400, H=2, D=96, n_slots=800, elem=4),
+    "elem8": dict(T=200, H=2, D=20, n_slots=800, elem=8),
+    "head_segments": dict(T=640, H=8, D=64, n_slots=2000, head_pad_src=32, head_pad_dst=64),
+    "head_segments_odd_d": dict(T=333, H=5, D=80, n_slots=2000, head_pad_dst=16),
+    "qkv_interleaved": dict(T=1024, H=8, D=128, n_slots=4096, qkv_shared=True),
+    "token_pad_odd": dict(T=257, H=2, D=40, n_slots=700, token_pad=6),
+    "dims_strided_generic": dict(T=200, H=4, D=32, n_slots=600, dim_stride_mult=2),
+    "index_stride3_i32": dict(T=513, H=8, D=128, n_slots=2000, index_stride=3,
+                              idx_dtype=np.int32),
+    "single_token": dict(T=1, H=8, D=128, n_slots=8),
+}
+
+
+@pytest.mark.parametrize("name", sorted(COPY_CASES))
+def test_copy_parity(name):
+    kw = dict(COPY_CASES[name])
+    p = copy_problem(seed=zlib.crc32(name.encode()) % 10000, **kw)
+    assert_same(p)
+
+
+@pytest.mark.parametrize("split", [0, 1, 2, 4])
+def test_copy_split_invariance(split):
+    p = copy_problem(T=256, H=8, D=128, n_slots=4096, seed=5, num_split=split)
+    g = assert_same(p)
+    if split:
+        ref = assert_same(copy_problem(T=256, H=8, D=128, n_slots=4096, seed=5, num_split=0))
+        a, b = g.caches(), ref.caches()
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_copy_out_of_range_slots():
+    T, n = 600, 2000
+    slots = wl.distinct_slots(77, n, T)
+    bad_at = [3, 10, 11, 599]
+    for i, val in zip(bad_at, [-1, n, 2 ** 62, -(2 ** 40)]):
+        slots[i] = val
+    p = copy_problem(T=T, H=8, D=128, n_slots=n, seed=78, slots=slots)
+    g = assert_same(p)
+    # the poll cleared the record
+    rc, nbad, first = g.poll()
+    assert (rc, nbad, first) == (0, 0, -1)
+
+
+def test_copy_out_of_range_int32_extremes():
+    T, n = 64, 128
+    slots = wl.distinct_slots(79, n, T)
+    slots[[0, 63]] = [np.iinfo(np.int32).min, np.iinfo(np.int32).max]
+    p = copy_problem(T=T, H=2, D=64, n_slots=n, seed=80, slots=slots, idx_dtype=np.int32)
+    assert_same(p)
+
+
+def test_copy_size_limit_below_cache_rows():
+    # slots in [size_limit, n) are out of range even though the cache has them
+    p = copy_problem(T=300, H=2, D=64, n_slots=1000, seed=81, size_limit=500)
+    assert_same(p)
+
+
+def test_copy_size_limit_zero():
+    p = copy_problem(T=50, H=2, D=64, n_slots=100, seed=82, size_limit=0)
+    g = assert_same(p)
+    kc, _ = g.caches()
+    assert np.all(kc.view(np.uint16) == wl.BF16_SENTINEL)
+
+
+def test_empty_calls_launch_nothing():
+    import torch
+    import fp8_quant_gb300 as kv
+    s = torch.cuda.current_stream().cuda_stream
+    zeros = (0,) * 12
+    assert kv.raw.kv_store(None, None, None, None, None, 0, 1, 0, 8, 128, 2, zeros, 0, 0,
+                           None, s) == 0
+    assert kv.raw.kv_store_fp8(None, None, None, None, None, 0, 1, 0, 8, 128, 1, zeros, 1, 0, 0,
+                               0, None, None, 0, None, s) == 0
+
+
+def test_copy_duplicate_slots_take_a_candidate():
+    T, n = 512, 64
+    slots = (wl.splitmix64(83, 0, T) % np.uint64(n)).astype(np.int64)
+    p = copy_problem(T=T, H=4, D=64, n_slots=n, seed=84, slots=slots)
+    g = GpuRun(p)
+    assert g.call() == 0
+    kc, vc = g.caches()
+    R = 4 * 64 * 2
+    krows = p.k_src[:T * R].reshape(T, R)
+    vrows = p.v_src[:T * R].reshape(T, R)
+    for s in np.unique(slots):
+        toks = np.flatnonzero(slots == s)
+        row = kc[s * R:(s + 1) * R]
+        hit = [t for t in toks if np.array_equal(row, krows[t])]
+        assert hit, f"slot {s}: row is none of the candidates"
+        # K and V of one slot come from the same kind of rows (V of some candidate)
+        assert any(np.array_equal(vc[s * R:(s + 1) * R], vrows[t]) for t in toks)
+
+
+def test_stream_order_with_preceding_kernels():
+    """A torch kernel writes the indices right before the call; a second call
+    overwrites the same slots. Both orderings must hold (programmatic launch
+    waits for the preceding grid)."""
+    import torch
+    import fp8_quant_gb300 as kv
+    T, H, D, n = 4096, 8, 128, 1 << 15
+    dev = torch.device("cuda")
+    k1 = torch.randn(T, H, D, device=dev, dtype=torch.bfloat16)
+    k2 = torch.randn(T, H, D, device=dev, dtype=torch.bfloat16)
+    kc = torch.zeros(n, H, D, device=dev, dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    idx = torch.zeros(T, device=dev, dtype=torch.int64)
+    err = kv.error_record(dev)
+    perm = torch.randperm(n, device=dev)[:T]
+    for _ in range(3):
+        idx.zero_()
+        idx.copy_(perm)                                   # producer kernel on the stream
+        kv.kv_store(k1, k1, kc, vc, idx, err=err)
+        kv.kv_store(k2, k1, kc, vc, idx, err=err)         # same slots, new K
+    st, nbad, _ = kv.kv_error_poll(err)
+    assert st == kv.KVStatus.OK and nbad == 0
+    assert torch.equal(kc[perm], k2) and torch.equal(vc[perm], k1)
+
+
+def test_graph_capture_replay():
+    import torch
+    import fp8_quant_gb300 as kv
+    T, H, D, n = 1000, 8, 128, 8192
+    dev = torch.device("cuda")
+    k = torch.randn(T, H, D, device=dev, dtype=torch.bfloat16)
+    kc = torch.zeros(n, H, D, device=dev, dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    idx = torch.randperm(n, device=dev)[:T].to(torch.int32)
+    err = kv.error_record(dev)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        kv.kv_store(k, k, kc, vc, idx, err=err)           # warm-up outside the graph
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        kv.kv_store(k, k, kc, vc, idx, err=err)
+    kc.zero_()
+    vc.zero_()
+    k.mul_(-1)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(kc[idx.long()], k) and torch.equal(vc[idx.long()], k)
+    assert kv.kv_error_poll(err)[1] == 0
+
+
+def test_tensor_binding_matches_raw():
+    """The tensor-level binding (views, 2-D caches with padded slots) gives the
+    oracle's bytes too."""
+    import torch
+    import fp8_quant_gb300 as kv
+    T, H, D, n = 300, 1, 576, 1000
+    p = copy_problem(T=T, H=H, D=D, n_slots=n, seed=85, slot_pad=128, idx_dtype=np.int32)
+    okc, ovc, _ = run_oracle(p)
+    dev = torch.device("cuda")
+    k = torch.from_numpy(p.k_src[:T * 1152].copy()).to(dev).view(torch.float16).view(T, H, D)
+    v = torch.from_numpy(p.v_src[:T * 1152].copy()).to(dev).view(torch.float16).view(T, H, D)
+    kc_store = torch.from_numpy(np.full(n * 640, wl.BF16_SENTINEL, np.uint16).view(np.int16))
+    kc_store = kc_store.to(dev).view(n, 640)
+    vc_store = kc_store.clone()
+    idx = torch.from_numpy(p.indices).to(dev)
+    kv.kv_store(k, v, kc_store[:, :576].view(torch.float16), vc_store[:, :576].view(torch.float16),
+                idx, num_heads=1, head_dim=576)
+    assert np.array_equal(kc_store.cpu().numpy().view(np.uint8).ravel(), okc)
+    assert np.array_equal(vc_store.cpu().numpy().view(np.uint8).ravel(), ovc)
+
+
+# ---------------------------------------------------------------------------
+# Fused FP8
+# ---------------------------------------------------------------------------
+
+FP8_CASES = {
+    "cfg_shape_scaled": dict(T=1200, H=8, D=128, n_slots=4096, page_size=32),
+    "cfg_shape_unscaled": dict(T=1200, H=8, D=128, n_slots=4096, page_size=32, use_scale=0),
+    "fp16_scaled": dict(T=700, H=8, D=128, n_slots=2048, src_dtype="f16"),
+    "fp16_unscaled": dict(T=700, H=4, D=64, n_slots=2048, src_dtype="f16", use_scale=0),
+    "int32_index_stride2": dict(T=555, H=8, D=128, n_slots=2048, idx_dtype=np.int32,
+                                index_stride=2),
+    "padded_pages_4d": dict(T=900, H=8, D=128, n_slots=4096, page_size=64, page_pad=256),
+    "page_size_one": dict(T=400, H=2, D=64, n_slots=1024, page_size=1),
+    "odd_page_size": dict(T=400, H=2, D=64, n_slots=1000, page_size=7, page_pad=16),
+    "segmented_heads": dict(T=500, H=8, D=64, n_slots=1500, head_pad_src=64, head_pad_dst=32),
+    "out8_d24": dict(T=640, H=3, D=24, n_slots=1500),
+    "out4_d20": dict(T=640, H=1, D=20, n_slots=1500),
+    "out2_d6": dict(T=640, H=1, D=6, n_slots=1500),
+    "misaligned_src": dict(T=300, H=4, D=64, n_slots=900, src_off=2),
+    "slot_pad_8": dict(T=300, H=4, D=64, n_slots=900, slot_pad=8, page_size=4),
+    "generic_odd_d": dict(T=300, H=3, D=45, n_slots=900),
+    "generic_strided_dims": dict(T=300, H=2, D=32, n_slots=900, src_dim_mult=3,
+                                 dst_dim_mult=2),
+    "long_rows_d576": dict(T=200, H=1, D=576, n_slots=600),
+    "many_heads_long": dict(T=64, H=64, D=128, n_slots=128),
+    "single_token": dict(T=1, H=8, D=128, n_slots=16),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FP8_CASES))
+def test_fp8_parity(name):
+    p = fp8_problem(seed=zlib.crc32(name.encode()) % 10000, **FP8_CASES[name])
+    assert_same(p)
+
+
+def test_fp8_out_of_range():
+    p = fp8_problem(T=300, H=8, D=128, n_slots=1000, seed=91, page_size=16)
+    p.indices[[0, 5, 299]] = [-7, 1000, 2 ** 50]
+    assert_same(p)
+
+
+def test_fp8_use_scale_off_equals_inv_one():
+    a = GpuRun(fp8_problem(T=512, H=8, D=128, n_slots=2048, seed=92, use_scale=0))
+    b = GpuRun(fp8_problem(T=512, H=8, D=128, n_slots=2048, seed=92, use_scale=1,
+                           inv=(1.0, 1.0)))
+    assert a.call() == 0 and b.call() == 0
+    ka, va = a.caches()
+    kb, vb = b.caches()
+    assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+
+
+def _all_patterns():
+    bits = np.arange(1 << 16, dtype=np.uint16).reshape(64, 8, 128)
+    return bits, bits[::-1].copy()
+
+
+@pytest.mark.parametrize("src", ["bf16", "f16"])
+@pytest.mark.parametrize("inv", [None, 1.0, 0.5, 3.0, 448.0 / 2.75, 2.0 ** -20, 1e30])
+def test_fp8_exhaustive_input_patterns(src, inv):
+    """All 65,536 input bit patterns (NaNs, infinities, subnormals included)
+    through the conversion, unscaled and with several inverse scales."""
+    kb, vb = _all_patterns()
+    p = fp8_problem(T=64, H=8, D=128, n_slots=256, seed=93, src_dtype=src, src_bits=(kb, vb),
+                    use_scale=0 if inv is None else 1,
+                    inv=None if inv is None else (inv, inv))
+    assert_same(p)
