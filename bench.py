@@ -203,10 +203,10 @@ class Pool:
     random pages for the prefill workload).
     """
 
-    def __init__(self, name: str, device, pool_bytes: int, seed: int = 1234):
+    def __init__(self, name: str, device, pool_bytes: int, seed: int = 1234, n_slots=None):
         import torch
         self.name = name
-        w = load_workload(name)
+        w = load_workload(name, n_slots)
         self.w = w
         self.dev = device
         g = torch.Generator(device=device)
@@ -436,11 +436,12 @@ def run_reference(args, dist):
     print(json.dumps(line), flush=True)
 
 
-def load_workload(name):
+def load_workload(name, n_slots=None):
     import workloads as wl
+    kw = {} if n_slots is None else {"n_slots": n_slots}
     if name.startswith("fp8"):
-        return wl.fp8(use_scale=0 if name == "fp8_noscale" else 1)
-    return wl.WORKLOADS[name]()
+        return wl.fp8(use_scale=0 if name == "fp8_noscale" else 1, **kw)
+    return wl.WORKLOADS[name](**kw)
 
 
 _ORACLE_CACHE = {}
@@ -486,7 +487,8 @@ def run_ours(args, dist):
     device = torch.device("cuda", dist.local_rank)
     kv.load_library()
     name = args.workload
-    pool = Pool(name, device, pool_bytes=args.pool_mb << 20, seed=1234 + dist.rank)
+    pool = Pool(name, device, pool_bytes=args.pool_mb << 20, seed=1234 + dist.rank,
+                n_slots=args.slots)
     w = pool.w
     T = w.T
     stream_handle = lambda: torch.cuda.current_stream().cuda_stream
@@ -544,7 +546,9 @@ def run_ours(args, dist):
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype_of(w), "data": "synthetic",
         "config": {
-            "workload": DESCRIPTIONS[name], "tokens_per_step": T,
+            "workload": DESCRIPTIONS[name] + ("" if args.slots is None
+                                              else f" [cache reduced to {args.slots} slots]"),
+            "tokens_per_step": T,
             "bytes_per_step": bytes_per_step, "parallelism": f"replicas x{dist.world}",
             "l2": f"inputs rotate over {nb} batches ({nb * pool.in_bytes_per_batch / 1e6:.0f} MB"
                   f" read per cycle) > L2 (129 MB)" if nb > 1 else
@@ -630,6 +634,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--slots", type=int, default=None,
+                    help="override the cache size in slots (small profiler captures)")
     a = ap.parse_args(argv)
     if a.steps is None:
         a.steps = DEFAULT_STEPS[a.workload] if a.impl == "ours" else 20

@@ -36,11 +36,35 @@
 
 #include "kvstore.h"
 
+// Tuning constants (defaults chosen by measurement on GB300).
+#ifndef KV_THREADS
+#define KV_THREADS 256          // threads per CTA
+#endif
+#ifndef KV_COPY_UNROLL
+#define KV_COPY_UNROLL 4        // chunks per lane loaded before the first store
+#endif
+#ifndef KV_FP8_UNROLL
+#define KV_FP8_UNROLL 2
+#endif
+#ifndef KV_MAX_VEC
+#define KV_MAX_VEC 32           // widest per-lane vector, bytes (32 = 256-bit ld/st)
+#endif
+#ifndef KV_EARLY_TRIGGER
+#define KV_EARLY_TRIGGER 1      // let the next kernel on the stream launch at our start
+#endif
+#ifndef KV_L2_EVICT_FIRST
+#define KV_L2_EVICT_FIRST 0     // evict-first L2 policy on the streamed loads and stores
+#endif
+#ifndef KV_GRID_WAVES
+#define KV_GRID_WAVES 1         // grid cap in resident-capacity waves (0 = one warp per unit)
+#endif
+
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = KV_THREADS;
 constexpr int kWarpsPerCta = kThreads / 32;
 constexpr int kMaxDevices = 64;
+static_assert(KV_MAX_VEC == 16 || KV_MAX_VEC == 32, "KV_MAX_VEC");
 
 thread_local int g_last_cuda_error = 0;
 
@@ -58,17 +82,40 @@ __device__ __forceinline__ void grid_dependents_launch() {
 
 // Vector of VEC bytes moved by one lane.
 template <int VEC> struct Chunk;
+template <> struct Chunk<32> { uint32_t w[8]; };
 template <> struct Chunk<16> { uint32_t w[4]; };
 template <> struct Chunk<8> { uint32_t w[2]; };
 template <> struct Chunk<4> { uint32_t w[1]; };
 template <> struct Chunk<2> { uint16_t h; };
 template <> struct Chunk<1> { uint16_t h; };
 
+#if KV_L2_EVICT_FIRST
+#define KV_L2_HINT ".L2::cache_hint"
+#define KV_POLICY_ARG , "l"(l2_policy())
+__device__ __forceinline__ uint64_t l2_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+#define KV_POL(n) ", %" #n
+#else
+#define KV_L2_HINT ""
+#define KV_POLICY_ARG
+#define KV_POL(n) ""
+#endif
+
 // Streaming loads: non-coherent path, no L1 allocation (each byte is read once).
+__device__ __forceinline__ void ld_stream(Chunk<32>& c, const void* p) {
+  asm volatile("ld.global.nc.L1::no_allocate" KV_L2_HINT
+               ".v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8]" KV_POL(9) ";"
+               : "=r"(c.w[0]), "=r"(c.w[1]), "=r"(c.w[2]), "=r"(c.w[3]), "=r"(c.w[4]),
+                 "=r"(c.w[5]), "=r"(c.w[6]), "=r"(c.w[7])
+               : "l"(p) KV_POLICY_ARG);
+}
 __device__ __forceinline__ void ld_stream(Chunk<16>& c, const void* p) {
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate" KV_L2_HINT ".v4.u32 {%0, %1, %2, %3}, [%4]" KV_POL(5) ";"
                : "=r"(c.w[0]), "=r"(c.w[1]), "=r"(c.w[2]), "=r"(c.w[3])
-               : "l"(p));
+               : "l"(p) KV_POLICY_ARG);
 }
 __device__ __forceinline__ void ld_stream(Chunk<8>& c, const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
@@ -85,9 +132,15 @@ __device__ __forceinline__ void ld_stream(Chunk<1>& c, const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(c.h) : "l"(p));
 }
 
+__device__ __forceinline__ void st_stream(void* p, const Chunk<32>& c) {
+  asm volatile("st.global" KV_L2_HINT ".v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}" KV_POL(9) ";"
+               ::"l"(p), "r"(c.w[0]), "r"(c.w[1]), "r"(c.w[2]), "r"(c.w[3]), "r"(c.w[4]),
+               "r"(c.w[5]), "r"(c.w[6]), "r"(c.w[7]) KV_POLICY_ARG
+               : "memory");
+}
 __device__ __forceinline__ void st_stream(void* p, const Chunk<16>& c) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(c.w[0]), "r"(c.w[1]),
-               "r"(c.w[2]), "r"(c.w[3])
+  asm volatile("st.global" KV_L2_HINT ".v4.u32 [%0], {%1, %2, %3, %4}" KV_POL(5) ";"
+               ::"l"(p), "r"(c.w[0]), "r"(c.w[1]), "r"(c.w[2]), "r"(c.w[3]) KV_POLICY_ARG
                : "memory");
 }
 __device__ __forceinline__ void st_stream(void* p, const Chunk<8>& c) {
@@ -164,6 +217,7 @@ struct CopyParams {
 template <int VEC, int U, typename IdxT>
 __global__ void __launch_bounds__(kThreads) kv_copy_rows(const __grid_constant__ CopyParams p) {
   grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
   const uint32_t nchunks = p.shape.part_chunks;
@@ -208,7 +262,7 @@ __global__ void __launch_bounds__(kThreads) kv_copy_rows(const __grid_constant__
       }
     }
   }
-  grid_dependents_launch();
+  if (!KV_EARLY_TRIGGER) grid_dependents_launch();
 }
 
 // Element-wise copy for rows whose elements are not contiguous (dim stride
@@ -228,6 +282,7 @@ struct GenericCopyParams {
 template <typename IdxT>
 __global__ void __launch_bounds__(kThreads) kv_copy_elements(const __grid_constant__ GenericCopyParams p) {
   grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
   const uint64_t per_token = 2ull * static_cast<uint64_t>(p.num_heads);
@@ -250,7 +305,7 @@ __global__ void __launch_bounds__(kThreads) kv_copy_elements(const __grid_consta
       for (int b = 0; b < p.elem_bytes; ++b) o[b] = __ldg(s + b);
     }
   }
-  grid_dependents_launch();
+  if (!KV_EARLY_TRIGGER) grid_dependents_launch();
 }
 
 // ---------------------------------------------------------------------------
@@ -288,9 +343,16 @@ template <int OUT> struct Fp8Chunk { uint32_t in[OUT / 2]; };
 
 template <int OUT>
 __device__ __forceinline__ void ld_in(Fp8Chunk<OUT>& c, const uint8_t* p) {
-  if constexpr (OUT == 16) {
-    ld_stream(*reinterpret_cast<Chunk<16>*>(&c.in[0]), p);
-    ld_stream(*reinterpret_cast<Chunk<16>*>(&c.in[4]), p + 16);
+  if constexpr (OUT == 32) {
+    ld_stream(*reinterpret_cast<Chunk<32>*>(&c.in[0]), p);
+    ld_stream(*reinterpret_cast<Chunk<32>*>(&c.in[8]), p + 32);
+  } else if constexpr (OUT == 16) {
+    if constexpr (KV_MAX_VEC >= 32) {
+      ld_stream(*reinterpret_cast<Chunk<32>*>(&c.in[0]), p);
+    } else {
+      ld_stream(*reinterpret_cast<Chunk<16>*>(&c.in[0]), p);
+      ld_stream(*reinterpret_cast<Chunk<16>*>(&c.in[4]), p + 16);
+    }
   } else if constexpr (OUT == 8) {
     ld_stream(*reinterpret_cast<Chunk<16>*>(&c.in[0]), p);
   } else if constexpr (OUT == 4) {
@@ -342,6 +404,7 @@ __device__ __forceinline__ int64_t paged_offset(int64_t slot, int64_t page_size,
 template <int OUT, int U, typename IdxT, bool kBF16>
 __global__ void __launch_bounds__(kThreads) kv_fp8_rows(const __grid_constant__ Fp8Params p) {
   grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
   const uint32_t nchunks = p.shape.part_chunks;
@@ -386,7 +449,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_rows(const __grid_constant__ 
       }
     }
   }
-  grid_dependents_launch();
+  if (!KV_EARLY_TRIGGER) grid_dependents_launch();
 }
 
 // Element-wise FP8 write for strided dims or odd sizes.  One warp per
@@ -407,6 +470,7 @@ struct GenericFp8Params {
 template <typename IdxT, bool kBF16>
 __global__ void __launch_bounds__(kThreads) kv_fp8_elements(const __grid_constant__ GenericFp8Params p) {
   grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
   const uint64_t per_token = 2ull * static_cast<uint64_t>(p.num_heads);
@@ -430,7 +494,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_elements(const __grid_constan
       dst[d * p.dst_dim[kv]] = static_cast<uint8_t>(quant2<kBF16>(bits, inv) & 0xFFu);
     }
   }
-  grid_dependents_launch();
+  if (!KV_EARLY_TRIGGER) grid_dependents_launch();
 }
 
 // ---------------------------------------------------------------------------
@@ -504,7 +568,9 @@ kv_status launch(void (*kernel)(Params), uint64_t num_units, const Params& param
   st = blocks_per_sm(reinterpret_cast<const void*>(kernel), &per_sm);
   if (st != KV_OK) return st;
   const uint64_t want = (num_units + kWarpsPerCta - 1) / kWarpsPerCta;
-  const uint64_t cap = static_cast<uint64_t>(sms) * static_cast<uint64_t>(per_sm);
+  const uint64_t cap = KV_GRID_WAVES > 0
+                           ? static_cast<uint64_t>(sms) * static_cast<uint64_t>(per_sm) * KV_GRID_WAVES
+                           : uint64_t{0x7FFFFFFF};
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
 
   cudaLaunchConfig_t cfg = {};
@@ -522,9 +588,9 @@ kv_status launch(void (*kernel)(Params), uint64_t num_units, const Params& param
   return KV_OK;
 }
 
-// Largest power of two <= 16 dividing every value OR-ed into `bits`.
+// Largest power of two <= KV_MAX_VEC dividing every value OR-ed into `bits`.
 int pow2_align(uint64_t bits) {
-  int v = 16;
+  int v = KV_MAX_VEC;
   while (v > 1 && (bits & static_cast<uint64_t>(v - 1)) != 0) v >>= 1;
   return v;
 }
@@ -571,13 +637,16 @@ uint32_t auto_parts(uint64_t units, int64_t seg_chunks, int sms) {
 
 template <int VEC, typename IdxT>
 kv_status launch_copy_vec(const CopyParams& p, cudaStream_t stream) {
-  constexpr int U = 4;
+  constexpr int U = VEC == 32 ? (KV_COPY_UNROLL + 1) / 2 : KV_COPY_UNROLL;
   return launch(kv_copy_rows<VEC, U, IdxT>, p.shape.num_units, p, stream);
 }
 
 template <typename IdxT>
 kv_status launch_copy(int vec, const CopyParams& p, cudaStream_t stream) {
   switch (vec) {
+#if KV_MAX_VEC >= 32
+    case 32: return launch_copy_vec<32, IdxT>(p, stream);
+#endif
     case 16: return launch_copy_vec<16, IdxT>(p, stream);
     case 8: return launch_copy_vec<8, IdxT>(p, stream);
     case 4: return launch_copy_vec<4, IdxT>(p, stream);
@@ -588,7 +657,7 @@ kv_status launch_copy(int vec, const CopyParams& p, cudaStream_t stream) {
 
 template <int OUT, typename IdxT>
 kv_status launch_fp8_out(bool bf16, const Fp8Params& p, cudaStream_t stream) {
-  constexpr int U = OUT == 16 ? 2 : 4;
+  constexpr int U = OUT == 32 ? 1 : OUT == 16 ? KV_FP8_UNROLL : 4;
   if (bf16) return launch(kv_fp8_rows<OUT, U, IdxT, true>, p.shape.num_units, p, stream);
   return launch(kv_fp8_rows<OUT, U, IdxT, false>, p.shape.num_units, p, stream);
 }
@@ -596,6 +665,9 @@ kv_status launch_fp8_out(bool bf16, const Fp8Params& p, cudaStream_t stream) {
 template <typename IdxT>
 kv_status launch_fp8(int out, bool bf16, const Fp8Params& p, cudaStream_t stream) {
   switch (out) {
+#if KV_MAX_VEC >= 32
+    case 32: return launch_fp8_out<32, IdxT>(bf16, p, stream);
+#endif
     case 16: return launch_fp8_out<16, IdxT>(bf16, p, stream);
     case 8: return launch_fp8_out<8, IdxT>(bf16, p, stream);
     case 4: return launch_fp8_out<4, IdxT>(bf16, p, stream);
@@ -733,7 +805,10 @@ extern "C" kv_status kv_store_fp8(const void* k, const void* v, void* k_cache, v
     }
     if (!flat) dst_bits |= u64(kc_page_stride) | u64(vc_page_stride);
     out = pow2_align(dst_bits);
-    while (out > 1 && (sbits & static_cast<uint64_t>((2 * out > 16 ? 16 : 2 * out) - 1)) != 0) out >>= 1;
+    // an OUT-byte chunk reads 2*OUT input bytes with loads of at most KV_MAX_VEC bytes
+    while (out > 1 &&
+           (sbits & static_cast<uint64_t>((2 * out > KV_MAX_VEC ? KV_MAX_VEC : 2 * out) - 1)) != 0)
+      out >>= 1;
   }
 
   if (out < 2) {

@@ -36,8 +36,11 @@
  *    reports it.  No slot value can cause a write outside the rows
  *    [0, size_limit) of the caches.
  *  - size_limit is trusted to be at most the number of cache rows.
- *  - Duplicate slots: each such cache row ends up equal to one of the
- *    candidate rows; which one is unspecified.
+ *  - Duplicate slots: calls write the candidate rows concurrently, so each
+ *    element of such a cache row equals the same element of one of the
+ *    candidate rows; which candidate is unspecified and may differ from
+ *    element to element (and between the K and the V row).
+ *  - The inputs and the index array must not overlap the caches.
  *  - num_tokens == 0 returns KV_OK without launching (pointers may be NULL).
  */
 #ifndef FP8_QUANT_GB300_KVSTORE_H

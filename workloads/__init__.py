@@ -228,27 +228,30 @@ def make_fp8(name, T, H, D, n_slots, seed, dtype="bf16", index_dtype=np.int64,
     return w
 
 
-def tiny() -> Workload:
-    return make_copy("tiny", T=16, H=2, D=64, n_slots=256, seed=0x5EED0000, page_size=16)
+# ``n_slots`` overrides the cache size (smaller caches for profiler captures;
+# the slot draws then differ from the full-size workload's).
+
+def tiny(n_slots: int = 256) -> Workload:
+    return make_copy("tiny", T=16, H=2, D=64, n_slots=n_slots, seed=0x5EED0000, page_size=16)
 
 
-def decode(num_split: int = 0) -> Workload:
-    return make_copy("decode", T=256, H=8, D=128, n_slots=1 << 20, seed=0x5EED0001,
+def decode(num_split: int = 0, n_slots: int = 1 << 20) -> Workload:
+    return make_copy("decode", T=256, H=8, D=128, n_slots=n_slots, seed=0x5EED0001,
                      index_dtype=np.int64, num_split=num_split)
 
 
-def prefill() -> Workload:
-    slots = page_run_slots(0x5EED0002 * 4 + 3, n_pages=(1 << 22) // 64, page_size=64, k_pages=512)
-    return make_copy("prefill", T=32768, H=8, D=128, n_slots=1 << 22, seed=0x5EED0002,
+def prefill(n_slots: int = 1 << 22) -> Workload:
+    slots = page_run_slots(0x5EED0002 * 4 + 3, n_pages=n_slots // 64, page_size=64, k_pages=512)
+    return make_copy("prefill", T=32768, H=8, D=128, n_slots=n_slots, seed=0x5EED0002,
                      slots=slots, page_size=64)
 
 
-def fp8(use_scale: int = 1) -> Workload:
-    return make_fp8("fp8", T=8192, H=8, D=128, n_slots=1 << 20, seed=0x5EED0003,
+def fp8(use_scale: int = 1, n_slots: int = 1 << 20) -> Workload:
+    return make_fp8("fp8", T=8192, H=8, D=128, n_slots=n_slots, seed=0x5EED0003,
                     page_size=32, use_scale=use_scale)
 
 
-def strided() -> Workload:
+def strided(n_slots: int = 1 << 21) -> Workload:
     """fp16 K and V as views into a fused QKV tensor [T, (32 + 2*8) * 128].
 
     Only the K and V columns are ever read; the Q columns are filled with a
@@ -259,20 +262,20 @@ def strided() -> Workload:
     qkv = np.full((T, width), 0x3C00, dtype=np.uint16)   # fp16 1.0 in the Q columns
     qkv[:, HQ * D:(HQ + H) * D] = _normal_rows(0x5EED0004 * 4 + 1, T, H, D, "f16").reshape(T, H * D)
     qkv[:, (HQ + H) * D:] = _normal_rows(0x5EED0004 * 4 + 2, T, H, D, "f16").reshape(T, H * D)
-    slots = distinct_slots(0x5EED0004 * 4 + 3, 1 << 21, T)
+    slots = distinct_slots(0x5EED0004 * 4 + 3, n_slots, T)
     tok = width * 2
     w = Workload(name="strided", T=T, H=H, D=D, src_dtype="f16", kind="copy", k=qkv, v=qkv,
                  k_view=(HQ * D * 2, tok, D * 2, 2), v_view=((HQ + H) * D * 2, tok, D * 2, 2),
-                 indices=slots.astype(np.int32), n_slots=1 << 21, slot_stride=H * D * 2,
+                 indices=slots.astype(np.int32), n_slots=n_slots, slot_stride=H * D * 2,
                  cache_head_stride=D * 2, cache_elem=2, sentinel=BF16_SENTINEL,
                  page_size=16, page_stride=16 * H * D * 2)
     w.notes["shared_source"] = True
     return w
 
 
-def odd() -> Workload:
+def odd(n_slots: int = 1 << 21) -> Workload:
     """fp16 H=1, D=576 rows (1152 B) into 1280-byte slots."""
-    return make_copy("odd", T=65536, H=1, D=576, n_slots=1 << 21, seed=0x5EED0005,
+    return make_copy("odd", T=65536, H=1, D=576, n_slots=n_slots, seed=0x5EED0005,
                      dtype="f16", slot_stride=1280)
 
 
