@@ -1,0 +1,97 @@
+"""Full-size parity: every benchmark workload at its full size, in exactly the
+launch configuration ``bench.py`` times (its ``Pool.call`` on batch 0, which is
+the workload's own seeded data).
+
+For each call: every written cache row (gathered on the GPU at the batch's
+slots, whole slot stride including padding) is compared byte for byte with
+the CPU oracle run on the same inputs (slots renumbered 0..T-1 into a compact
+host cache, which leaves the row contents unchanged); the number of cache rows
+that differ from the pre-fill must equal T, so nothing else was touched; and
+the error record must be clean.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+
+
+def _rows_changed(torch, cache, n_slots, slot_bytes, sentinel_bytes):
+    """Rows of the cache whose bytes differ from the pre-fill (counted on the GPU)."""
+    words = cache.view(torch.uint8).view(n_slots, slot_bytes)
+    pat = torch.tensor(list(sentinel_bytes) * (slot_bytes // len(sentinel_bytes)),
+                       dtype=torch.uint8, device=cache.device)
+    total = 0
+    step = max(1, (256 << 20) // slot_bytes)
+    for r0 in range(0, n_slots, step):
+        total += int((words[r0:r0 + step] != pat).any(dim=1).sum().item())
+    return total
+
+
+def _oracle_compact(w):
+    """Oracle over all tokens with slots renumbered 0..T-1 (compact caches)."""
+    T = w.T
+    idx = np.arange(T, dtype=w.indices.dtype)
+    sb = w.slot_stride
+    sent = (w.sentinel.to_bytes(2, "little") if w.cache_elem == 2 else bytes([w.sentinel]))
+    kc = np.frombuffer(sent * (T * sb // len(sent)), dtype=np.uint8).copy()
+    vc = kc.copy()
+    st = oracle.Strides(k_token=w.k_view[1], k_head=w.k_view[2], k_dim=w.k_view[3],
+                        v_token=w.v_view[1], v_head=w.v_view[2], v_dim=w.v_view[3],
+                        kc_slot=sb, kc_head=w.cache_head_stride, kc_dim=w.cache_elem,
+                        vc_slot=sb, vc_head=w.cache_head_stride, vc_dim=w.cache_elem)
+    k = np.ascontiguousarray(w.k).view(np.uint8).reshape(-1)
+    v = np.ascontiguousarray(w.v).view(np.uint8).reshape(-1)
+    if w.kind == "copy":
+        bad = oracle.store_copy(k, v, kc, vc, idx, st, w.H, w.D, 2, T,
+                                k_off=w.k_view[0], v_off=w.v_view[0])
+    else:
+        # compact slot j sits at j * slot_stride for any page size when pages are dense
+        assert w.page_stride == w.page_size * sb
+        bad = oracle.store_fp8(k, v, kc, vc, idx, st, w.H, w.D, w.src_dtype, w.page_size,
+                               w.page_stride, w.page_stride, T + (-T) % w.page_size,
+                               w.inv_k, w.inv_v, w.use_scale,
+                               k_off=w.k_view[0], v_off=w.v_view[0])
+    assert bad == (0, -1)
+    return kc.reshape(T, sb), vc.reshape(T, sb), sent
+
+
+@pytest.mark.parametrize("name,split", [
+    ("tiny", 0), ("decode", 0), ("decode", 1), ("decode", 2), ("decode", 4),
+    ("prefill", 0), ("fp8", 0), ("fp8_noscale", 0), ("strided", 0), ("odd", 0),
+])
+def test_full_size_workload(name, split):
+    import torch
+    import bench
+    import fp8_quant_gb300 as kv
+    dev = torch.device("cuda", 0)
+    pool = bench.Pool(name, dev, pool_bytes=0)
+    w = pool.w
+    w.num_split = split
+    assert pool.num_batches == 1
+    assert pool.call(0, torch.cuda.current_stream().cuda_stream) == 0
+    st, nbad, first = kv.kv_error_poll(pool.err)
+    assert (st, nbad, first) == (kv.KVStatus.OK, 0, -1)
+
+    okc, ovc, sent = _oracle_compact(w)
+    sb = w.slot_stride
+    slots = torch.from_numpy(w.indices.astype(np.int64)).to(dev)
+    for cache, want, what in ((pool.kc, okc, "K"), (pool.vc, ovc, "V")):
+        rows = cache.view(torch.uint8).view(w.n_slots, sb).index_select(0, slots).cpu().numpy()
+        if not np.array_equal(rows, want):
+            bad = np.argwhere(rows != want)
+            t, b = bad[0]
+            raise AssertionError(f"{what} cache: {len(bad)} bytes differ; first token {t} "
+                                 f"byte {b}: got {rows[t, b]:#04x} want {want[t, b]:#04x}")
+        assert _rows_changed(torch, cache, w.n_slots, sb, sent) == w.T, f"{what}: stray rows"
+    del pool
+    torch.cuda.empty_cache()
