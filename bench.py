@@ -570,11 +570,18 @@ def run_ours(args, dist):
 
 
 def load_traffic(name):
-    """DRAM bytes per launch from the committed ncu summary, if it matches."""
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source has changed since those counters were taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "fp8_quant_gb300", "csrc", "kvstore.cu")
     try:
         with open(path) as f:
             d = json.load(f)
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if not sha.startswith(d["source_sha256_prefix"]):
+            return None
         return d.get(name)
     except Exception:
         return None
