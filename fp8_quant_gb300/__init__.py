@@ -78,6 +78,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kv_store_fp8.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
                                      ctypes.POINTER(_Strides), I64, I64, I64, I64, P, P, I32, P, P]
         lib.kv_store_fp8.restype = I32
+        lib.kv_store_noalloc.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
+                                         ctypes.POINTER(_Strides), I64, I32,
+                                         ctypes.POINTER(I64), ctypes.POINTER(I64), P]
+        lib.kv_store_noalloc.restype = I32
         lib.kv_error_poll.argtypes = [P, P, ctypes.POINTER(I64), ctypes.POINTER(I64)]
         lib.kv_error_poll.restype = I32
         lib.kv_error_reset.argtypes = [P, P]
@@ -125,6 +129,22 @@ class raw:
                                            src_dtype, ctypes.byref(st), page_size,
                                            kc_page_stride, vc_page_stride, size_limit,
                                            inv_k_scale, inv_v_scale, use_scale, d_err, stream)
+
+    @staticmethod
+    def kv_store_noalloc(k, v, k_cache, v_cache, indices, index_dtype, index_stride,
+                         num_tokens, num_heads, head_dim, elem_bytes, strides: Sequence[int],
+                         size_limit, num_split, stream):
+        """kv_store without a caller-supplied error record (nothing is
+        allocated; the record is a static array of the library). Blocks until
+        the write is done; returns (status, oob_count, first_bad_token)."""
+        st = _Strides(*[int(x) for x in strides])
+        n = ctypes.c_int64(0)
+        first = ctypes.c_int64(0)
+        rc = load_library().kv_store_noalloc(k, v, k_cache, v_cache, indices, index_dtype,
+                                             index_stride, num_tokens, num_heads, head_dim,
+                                             elem_bytes, ctypes.byref(st), size_limit, num_split,
+                                             ctypes.byref(n), ctypes.byref(first), stream)
+        return rc, n.value, first.value
 
     @staticmethod
     def kv_error_poll(d_err, stream):

@@ -949,3 +949,65 @@ extern "C" const char* kv_status_str(kv_status status) {
 extern "C" int kv_last_cuda_error(void) { return g_last_cuda_error; }
 
 extern "C" int kv_abi_version(void) { return KV_ABI_VERSION; }
+
+// ---------------------------------------------------------------------------
+// Entry point for callers that cannot allocate device memory: kv_store with
+// its error record in a static device array of this library.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KV_NOALLOC_SCRATCH_BYTES];
+static_assert(sizeof(kv_error_record) <= KV_NOALLOC_SCRATCH_BYTES, "record must fit the array");
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current.  In host code the array's name is only a host-side stand-in.
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
+
+kv_status noalloc_record(kv_error_record** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return KV_ERR_UNSUPPORTED;
+  void* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_noalloc_addr[dev].store(p, std::memory_order_release);
+  }
+  *out = static_cast<kv_error_record*>(p);
+  return KV_OK;
+}
+
+}  // namespace
+
+extern "C" kv_status kv_store_noalloc(const void* k, const void* v, void* k_cache, void* v_cache,
+                                      const void* indices, kv_index_dtype index_dtype,
+                                      int64_t index_stride, int64_t num_tokens, int32_t num_heads,
+                                      int32_t head_dim, int32_t elem_bytes, const kv_strides* s,
+                                      int64_t size_limit, int32_t num_split, int64_t* oob_count,
+                                      int64_t* first_bad_token, kv_stream_t stream_) {
+  if (oob_count) *oob_count = 0;
+  if (first_bad_token) *first_bad_token = -1;
+  if (sizeof(kv_error_record) > KV_NOALLOC_SCRATCH_BYTES) return KV_ERR_UNSUPPORTED;
+  if (num_tokens < 0) return KV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KV_OK;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  kv_error_record* rec = nullptr;
+  kv_status st = noalloc_record(&rec);
+  if (st != KV_OK) return st;
+  // The array keeps the previous call's counts: clear them first.
+  cudaError_t e = cudaMemsetAsync(rec, 0, sizeof(kv_error_record), stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  st = kv_store(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_tokens, num_heads,
+                head_dim, elem_bytes, s, size_limit, num_split, rec, stream_);
+  if (st != KV_OK) return st;
+  kv_error_record h = {0, 0};
+  e = cudaMemcpyAsync(&h, rec, sizeof h, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (oob_count) *oob_count = static_cast<int64_t>(h.oob_count);
+  if (first_bad_token && h.oob_count) *first_bad_token = static_cast<int64_t>(~h.first_bad_key);
+  return h.oob_count ? KV_ERR_INDEX_OOB : KV_OK;
+}

@@ -169,6 +169,48 @@ kv_status kv_store_fp8(const void *k, const void *v, void *k_cache, void *v_cach
                        kv_error_record *d_err, kv_stream_t stream);
 
 /*
+ * kv_store_noalloc -- kv_store for callers that cannot allocate device memory.
+ * The pages have no counterpart; this entry point exists for this library's
+ * users only.
+ *
+ * Some callers cannot call cudaMalloc at the point where they write the KV
+ * cache: code running inside an allocator hook or a host callback (where
+ * allocating would re-enter the allocator or deadlock), a plugin that is handed
+ * the tensors but owns no memory pool, or a process whose device memory is
+ * entirely reserved by a pool it does not control.  kv_store needs one more
+ * device buffer besides the tensors, its error record, so those callers could
+ * not use it.  kv_store_noalloc takes the same arguments as kv_store except
+ * d_err and allocates nothing: the record lives in a 256-byte static device
+ * array inside this library (KV_NOALLOC_SCRATCH_BYTES), which every GPU that
+ * loads the library holds until the process exits.  The record needs 16 bytes
+ * whatever the batch size, so no batch exceeds the array; a build whose record
+ * did not fit would return KV_ERR_UNSUPPORTED.
+ *
+ * Behaviour:
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture on the device.
+ *  - Each call clears the record on `stream`, runs kv_store with it, then
+ *    synchronises `stream` and copies the record to *oob_count and
+ *    *first_bad_token (host, nullable; -1 when no token was skipped).  It
+ *    therefore blocks the host until the write has finished.
+ *  - Every call shares the one array: calls that overlap on the GPU (from
+ *    other host threads or on other streams) race on it and may report each
+ *    other's counts.  The cache writes themselves are not affected.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Returns KV_OK, KV_ERR_INDEX_OOB when a token was skipped, or the status of
+ * kv_store / of a failed CUDA call.
+ */
+#define KV_NOALLOC_SCRATCH_BYTES 256
+kv_status kv_store_noalloc(const void *k, const void *v, void *k_cache, void *v_cache,
+                           const void *indices, kv_index_dtype index_dtype, int64_t index_stride,
+                           int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                           int32_t elem_bytes, const kv_strides *strides, int64_t size_limit,
+                           int32_t num_split, int64_t *oob_count, int64_t *first_bad_token,
+                           kv_stream_t stream);
+
+/*
  * kv_error_poll -- synchronise `stream`, read the error record, clear it.
  * (The pages trap inside the kernel on a bad slot; this library reports it
  * here instead.)  Writes the number of skipped tokens and the lowest skipped
