@@ -532,6 +532,7 @@ def run_ours(args, dist):
     e2e = run_e2e(args, dist, torch, kv, pool, device)
 
     cold_us = single_call_cold_us(torch, pool, stream_handle())
+    splits = split_timings(torch, kv, pool) if not args.no_split_timings else {}
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -556,6 +557,7 @@ def run_ours(args, dist):
             "timing": "CUDA graphs of back-to-back calls, CUDA events on the launching stream",
             "achieved_gbs": achieved_gbs, "single_call_cold_us": cold_us,
             "single_call_cold_gbs": bytes_per_step / (cold_us * 1e-6) / 1e9,
+            "us_per_call_by_num_split": splits,
         },
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "traffic": traffic,
@@ -588,31 +590,41 @@ def load_traffic(name):
 
 
 def run_e2e(args, dist, torch, kv, pool, device):
-    """Steps whose inputs come from pinned host memory every time."""
+    """Steps whose inputs come from pinned host memory every time.
+
+    Each batch's K rows, V rows and slot ids sit in one pinned host buffer
+    (256-byte aligned segments), so a step is one host->device copy into a
+    device staging buffer, the kv_store/kv_store_fp8 call on the staged
+    inputs, and a device->host read of the error record."""
     w = pool.w
     nb = pool.num_batches
     shared = bool(w.notes.get("shared_source"))
-    # pinned host copies of every batch; device staging buffers
-    host_k = [pool.k[b].cpu().pin_memory() for b in range(nb)]
-    host_v = host_k if shared else [pool.v[b].cpu().pin_memory() for b in range(nb)]
-    host_i = [pool.idx[b].cpu().pin_memory() for b in range(nb)]
-    dk = torch.empty_like(pool.k[0])
-    dv = dk if shared else torch.empty_like(pool.v[0])
-    di = torch.empty_like(pool.idx[0])
+    align = lambda n: (n + 255) // 256 * 256
+    kbytes = pool.k[0].numel() * pool.k[0].element_size()
+    vbytes = 0 if shared else pool.v[0].numel() * pool.v[0].element_size()
+    ibytes = pool.idx[0].numel() * pool.idx[0].element_size()
+    off_v = align(kbytes)
+    off_i = off_v + align(vbytes)
+    total = off_i + ibytes
+    hosts = []
+    for b in range(nb):
+        h = torch.empty(total, dtype=torch.uint8).pin_memory()
+        h[:kbytes].copy_(pool.k[b].reshape(-1).view(torch.uint8).cpu())
+        if not shared:
+            h[off_v:off_v + vbytes].copy_(pool.v[b].reshape(-1).view(torch.uint8).cpu())
+        h[off_i:off_i + ibytes].copy_(pool.idx[b].view(torch.uint8).cpu())
+        hosts.append(h)
+    stage = torch.empty(total, dtype=torch.uint8, device=device)
     err_host = torch.zeros(2, dtype=torch.int64).pin_memory()
-    h2d = (host_k[0].numel() * host_k[0].element_size() * (1 if shared else 2)
-           + host_i[0].numel() * host_i[0].element_size())
     d2h = err_host.numel() * err_host.element_size()
+    base = stage.data_ptr()
 
     def step(i):
         b = i % nb
-        dk.copy_(host_k[b], non_blocking=True)
-        if not shared:
-            dv.copy_(host_v[b], non_blocking=True)
-        di.copy_(host_i[b], non_blocking=True)
-        kbase = dk.data_ptr() + w.k_view[0]
-        vbase = dv.data_ptr() + w.v_view[0]
-        rc = pool.call(b, torch.cuda.current_stream().cuda_stream, kbase, vbase, di.data_ptr())
+        stage.copy_(hosts[b], non_blocking=True)
+        kbase = base + w.k_view[0]
+        vbase = (base if shared else base + off_v) + w.v_view[0]
+        rc = pool.call(b, torch.cuda.current_stream().cuda_stream, kbase, vbase, base + off_i)
         if rc != 0:
             raise RuntimeError(kv.kv_status_str(rc))
         err_host.copy_(pool.err, non_blocking=True)
@@ -623,10 +635,43 @@ def run_e2e(args, dist, torch, kv, pool, device):
     torch.cuda.synchronize()
     ms = time_region(torch, dist, lambda: run_graphs(graphs), device)
     sec = ms / 1e3 / steps
-    return {"value": dist.world * w.T / sec, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    return {"value": dist.world * w.T / sec, "unit": "tokens/s", "h2d_bytes_per_step": total,
             "d2h_bytes_per_step": d2h, "steps": steps,
-            "how": "pinned host -> device copies of K, V and indices, the kv_store call, and "
-                   "a device -> host read of the error record, every step, from CUDA graphs"}
+            "how": "every step: one pinned host -> device copy of the batch (K, V, slot ids "
+                   "packed), the kv_store call on the staged inputs, and a device -> host read "
+                   "of the error record; back-to-back from CUDA graphs"}
+
+
+def split_timings(torch, kv, pool, steps=2000):
+    """Per-call time of the copy workload with each legal row split (1, 2, 4)."""
+    w = pool.w
+    out = {}
+    if w.kind != "copy":
+        return out
+    saved = w.num_split
+    try:
+        for split in (1, 2, 4):
+            if split > 1 and w.row_bytes % (split * 128):
+                continue
+            w.num_split = split
+
+            def step(i):
+                assert pool.call(i % pool.num_batches, torch.cuda.current_stream().cuda_stream) == 0
+
+            n = min(steps, 1000)
+            graphs = capture_graphs(torch, step, steps, n)
+            run_graphs(graphs)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run_graphs(graphs)
+            e1.record()
+            torch.cuda.synchronize()
+            out[str(split)] = e0.elapsed_time(e1) * 1e3 / steps
+    finally:
+        w.num_split = saved
+    return out
 
 
 def parse_args(argv=None):
@@ -641,6 +686,7 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-split-timings", action="store_true")
     ap.add_argument("--slots", type=int, default=None,
                     help="override the cache size in slots (small profiler captures)")
     a = ap.parse_args(argv)

@@ -229,66 +229,81 @@ struct CopyParams {
   UnitShape shape;
   kv_error_record* err;
   int prefetch;  // sources are 16-byte aligned: prefetch them into L2 before the grid wait
+  int vec;       // bytes per chunk (the kernel's VEC / OUT)
 };
+
+// Moves one unit: loads (issued before the slot is known), bounds check,
+// stores.  `src` already points at the unit's first source byte.
+template <int VEC, int U, typename IdxT>
+__device__ __forceinline__ void copy_unit(const CopyParams& p, const Unit& w, const uint8_t* src,
+                                          uint32_t lane) {
+  const uint32_t nchunks = p.shape.part_chunks;
+  const int64_t part_bytes = static_cast<int64_t>(nchunks) * VEC;
+  const CopySide& sd = p.side[w.kv];
+  const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
+  Chunk<VEC> buf[U];
+#pragma unroll
+  for (int j = 0; j < U; ++j) {
+    const uint32_t c = lane + 32u * j;
+    if (c < nchunks) ld_stream(buf[j], src + static_cast<size_t>(c) * VEC);
+  }
+  if (slot < 0 || slot >= p.size_limit) {
+    if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
+    return;
+  }
+  uint8_t* dst = sd.dst + slot * sd.dst_slot + static_cast<int64_t>(w.seg) * sd.dst_seg +
+                 static_cast<int64_t>(w.part) * part_bytes;
+#pragma unroll
+  for (int j = 0; j < U; ++j) {
+    const uint32_t c = lane + 32u * j;
+    if (c < nchunks) st_stream(dst + static_cast<size_t>(c) * VEC, buf[j]);
+  }
+  // Rows longer than 32*U chunks: further batches, loads then stores.
+  for (uint32_t c0 = 32u * U; c0 < nchunks; c0 += 32u * U) {
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = c0 + lane + 32u * j;
+      if (c < nchunks) ld_stream(buf[j], src + static_cast<size_t>(c) * VEC);
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = c0 + lane + 32u * j;
+      if (c < nchunks) st_stream(dst + static_cast<size_t>(c) * VEC, buf[j]);
+    }
+  }
+}
+
+__device__ __forceinline__ const uint8_t* copy_src(const CopyParams& p, const Unit& w) {
+  const CopySide& sd = p.side[w.kv];
+  return sd.src + w.token * sd.src_token + static_cast<int64_t>(w.seg) * sd.src_seg +
+         static_cast<int64_t>(w.part) * p.shape.part_chunks * static_cast<int64_t>(p.vec);
+}
 
 template <int VEC, int U, typename IdxT>
 __global__ void __launch_bounds__(kThreads) kv_copy_rows(const __grid_constant__ CopyParams p) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
-  const uint32_t nchunks = p.shape.part_chunks;
-  const int64_t part_bytes = static_cast<int64_t>(nchunks) * VEC;
   uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const bool active = u < p.shape.num_units;
 
-  if (KV_PREFETCH && p.prefetch && lane == 0 && u < p.shape.num_units) {
-    // The source rows and the slot id do not depend on the previous grid's
-    // completion to be located: start pulling them into L2 now.
-    const Unit w = decode_unit(p.shape, u);
-    const CopySide& sd = p.side[w.kv];
-    prefetch_l2_bulk(sd.src + w.token * sd.src_token + static_cast<int64_t>(w.seg) * sd.src_seg +
-                         static_cast<int64_t>(w.part) * part_bytes,
-                     static_cast<uint32_t>(part_bytes));
+  // Everything that needs no memory written by the previous grid happens
+  // before the wait: the first unit's coordinates and addresses, and an L2
+  // prefetch of its source bytes and slot id.
+  Unit w = decode_unit(p.shape, active ? u : 0);
+  const uint8_t* src = copy_src(p, w);
+  if (KV_PREFETCH && p.prefetch && lane == 0 && active) {
+    prefetch_l2_bulk(src, p.shape.part_chunks * static_cast<uint32_t>(VEC));
     prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
   }
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
 
-  for (; u < p.shape.num_units; u += nwarps) {
-    const Unit w = decode_unit(p.shape, u);
-    const CopySide& sd = p.side[w.kv];
-    const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
-    const uint8_t* src = sd.src + w.token * sd.src_token + static_cast<int64_t>(w.seg) * sd.src_seg +
-                         static_cast<int64_t>(w.part) * part_bytes;
-
-    Chunk<VEC> buf[U];
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const uint32_t c = lane + 32u * j;
-      if (c < nchunks) ld_stream(buf[j], src + static_cast<size_t>(c) * VEC);
-    }
-    if (slot < 0 || slot >= p.size_limit) {
-      if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
-      continue;
-    }
-    uint8_t* dst = sd.dst + slot * sd.dst_slot + static_cast<int64_t>(w.seg) * sd.dst_seg +
-                   static_cast<int64_t>(w.part) * part_bytes;
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const uint32_t c = lane + 32u * j;
-      if (c < nchunks) st_stream(dst + static_cast<size_t>(c) * VEC, buf[j]);
-    }
-    // Rows longer than 32*U chunks: further batches, loads then stores.
-    for (uint32_t c0 = 32u * U; c0 < nchunks; c0 += 32u * U) {
-#pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const uint32_t c = c0 + lane + 32u * j;
-        if (c < nchunks) ld_stream(buf[j], src + static_cast<size_t>(c) * VEC);
-      }
-#pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const uint32_t c = c0 + lane + 32u * j;
-        if (c < nchunks) st_stream(dst + static_cast<size_t>(c) * VEC, buf[j]);
-      }
-    }
+  while (u < p.shape.num_units) {
+    copy_unit<VEC, U, IdxT>(p, w, src, lane);
+    u += nwarps;
+    if (u >= p.shape.num_units) break;
+    w = decode_unit(p.shape, u);
+    src = copy_src(p, w);
   }
   if (!KV_EARLY_TRIGGER) grid_dependents_launch();
 }
@@ -421,6 +436,7 @@ struct Fp8Params {
   UnitShape shape;
   kv_error_record* err;
   int prefetch;  // sources are 16-byte aligned: prefetch them into L2 before the grid wait
+  int vec;       // bytes per chunk (the kernel's VEC / OUT)
 };
 
 __device__ __forceinline__ int64_t paged_offset(int64_t slot, int64_t page_size, int64_t page_stride,
@@ -431,61 +447,72 @@ __device__ __forceinline__ int64_t paged_offset(int64_t slot, int64_t page_size,
 }
 
 template <int OUT, int U, typename IdxT, bool kBF16>
+__device__ __forceinline__ void fp8_unit(const Fp8Params& p, const Unit& w, const uint8_t* src,
+                                         uint32_t lane) {
+  const uint32_t nchunks = p.shape.part_chunks;
+  const int64_t part_out = static_cast<int64_t>(nchunks) * OUT;  // bytes out per part
+  const Fp8Side& sd = p.side[w.kv];
+  const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
+  const float inv = sd.inv != nullptr ? __ldg(sd.inv) : 1.0f;
+  Fp8Chunk<OUT> buf[U];
+#pragma unroll
+  for (int j = 0; j < U; ++j) {
+    const uint32_t c = lane + 32u * j;
+    if (c < nchunks) ld_in<OUT>(buf[j], src + static_cast<size_t>(c) * (2 * OUT));
+  }
+  if (slot < 0 || slot >= p.size_limit) {
+    if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
+    return;
+  }
+  uint8_t* dst = sd.dst + paged_offset(slot, p.page_size, sd.dst_page, sd.dst_slot) +
+                 static_cast<int64_t>(w.seg) * sd.dst_seg + static_cast<int64_t>(w.part) * part_out;
+#pragma unroll
+  for (int j = 0; j < U; ++j) {
+    const uint32_t c = lane + 32u * j;
+    if (c < nchunks) quant_store<OUT, kBF16>(dst + static_cast<size_t>(c) * OUT, buf[j], inv);
+  }
+  for (uint32_t c0 = 32u * U; c0 < nchunks; c0 += 32u * U) {
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = c0 + lane + 32u * j;
+      if (c < nchunks) ld_in<OUT>(buf[j], src + static_cast<size_t>(c) * (2 * OUT));
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = c0 + lane + 32u * j;
+      if (c < nchunks) quant_store<OUT, kBF16>(dst + static_cast<size_t>(c) * OUT, buf[j], inv);
+    }
+  }
+}
+
+__device__ __forceinline__ const uint8_t* fp8_src(const Fp8Params& p, const Unit& w) {
+  const Fp8Side& sd = p.side[w.kv];
+  return sd.src + w.token * sd.src_token + static_cast<int64_t>(w.seg) * sd.src_seg +
+         static_cast<int64_t>(w.part) * p.shape.part_chunks * 2 * static_cast<int64_t>(p.vec);
+}
+
+template <int OUT, int U, typename IdxT, bool kBF16>
 __global__ void __launch_bounds__(kThreads) kv_fp8_rows(const __grid_constant__ Fp8Params p) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
-  const uint32_t nchunks = p.shape.part_chunks;
-  const int64_t part_out = static_cast<int64_t>(nchunks) * OUT;  // bytes out per part
   uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const bool active = u < p.shape.num_units;
 
-  if (KV_PREFETCH && p.prefetch && lane == 0 && u < p.shape.num_units) {
-    const Unit w = decode_unit(p.shape, u);
-    const Fp8Side& sd = p.side[w.kv];
-    prefetch_l2_bulk(sd.src + w.token * sd.src_token + static_cast<int64_t>(w.seg) * sd.src_seg +
-                         static_cast<int64_t>(w.part) * part_out * 2,
-                     static_cast<uint32_t>(part_out * 2));
+  Unit w = decode_unit(p.shape, active ? u : 0);
+  const uint8_t* src = fp8_src(p, w);
+  if (KV_PREFETCH && p.prefetch && lane == 0 && active) {
+    prefetch_l2_bulk(src, p.shape.part_chunks * 2u * static_cast<uint32_t>(OUT));
     prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
   }
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
 
-  for (; u < p.shape.num_units; u += nwarps) {
-    const Unit w = decode_unit(p.shape, u);
-    const Fp8Side& sd = p.side[w.kv];
-    const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
-    const float inv = sd.inv != nullptr ? __ldg(sd.inv) : 1.0f;
-    const uint8_t* src = sd.src + w.token * sd.src_token + static_cast<int64_t>(w.seg) * sd.src_seg +
-                         static_cast<int64_t>(w.part) * part_out * 2;
-
-    Fp8Chunk<OUT> buf[U];
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const uint32_t c = lane + 32u * j;
-      if (c < nchunks) ld_in<OUT>(buf[j], src + static_cast<size_t>(c) * (2 * OUT));
-    }
-    if (slot < 0 || slot >= p.size_limit) {
-      if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
-      continue;
-    }
-    uint8_t* dst = sd.dst + paged_offset(slot, p.page_size, sd.dst_page, sd.dst_slot) +
-                   static_cast<int64_t>(w.seg) * sd.dst_seg + static_cast<int64_t>(w.part) * part_out;
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const uint32_t c = lane + 32u * j;
-      if (c < nchunks) quant_store<OUT, kBF16>(dst + static_cast<size_t>(c) * OUT, buf[j], inv);
-    }
-    for (uint32_t c0 = 32u * U; c0 < nchunks; c0 += 32u * U) {
-#pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const uint32_t c = c0 + lane + 32u * j;
-        if (c < nchunks) ld_in<OUT>(buf[j], src + static_cast<size_t>(c) * (2 * OUT));
-      }
-#pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const uint32_t c = c0 + lane + 32u * j;
-        if (c < nchunks) quant_store<OUT, kBF16>(dst + static_cast<size_t>(c) * OUT, buf[j], inv);
-      }
-    }
+  while (u < p.shape.num_units) {
+    fp8_unit<OUT, U, IdxT, kBF16>(p, w, src, lane);
+    u += nwarps;
+    if (u >= p.shape.num_units) break;
+    w = decode_unit(p.shape, u);
+    src = fp8_src(p, w);
   }
   if (!KV_EARLY_TRIGGER) grid_dependents_launch();
 }
@@ -801,6 +828,7 @@ extern "C" kv_status kv_store(const void* k, const void* v, void* k_cache, void*
   p.shape.part_chunks = static_cast<uint32_t>(part_bytes / vec);
   p.err = d_err;
   p.prefetch = vec >= 16 ? 1 : 0;
+  p.vec = vec;
   return i64 ? launch_copy<int64_t>(vec, p, stream) : launch_copy<int32_t>(vec, p, stream);
 }
 
@@ -905,6 +933,7 @@ extern "C" kv_status kv_store_fp8(const void* k, const void* v, void* k_cache, v
   p.shape.part_chunks = static_cast<uint32_t>(part_elems / out);
   p.err = d_err;
   p.prefetch = out >= 8 ? 1 : 0;  // 2*OUT input bytes per chunk, 16-byte aligned
+  p.vec = out;
   return i64 ? launch_fp8<int64_t>(out, bf16, p, stream) : launch_fp8<int32_t>(out, bf16, p, stream);
 }
 
