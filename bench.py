@@ -61,10 +61,15 @@ DESCRIPTIONS = {
                "cache 2,097,152 slots, int32",
     "odd": "odd-size copy: fp16 H_kv=1, D=576 (1152 B rows), 1280 B slot stride, "
            "cache 2,097,152 slots, int32",
+    "gather_decode": "gather (inverse of decode): T=256 rows of H_kv=8, D=128 bf16 from a "
+                     "1,048,576-slot cache, int64",
+    "gather_fp8": "dequantising gather (inverse of fp8): T=8192 e4m3fn rows x (1/inv) -> bf16, "
+                  "1,048,576-slot cache, page_size 32, int64",
 }
 
 DEFAULT_STEPS = {"tiny": 200000, "decode": 200000, "prefill": 10000, "fp8": 50000,
-                 "fp8_noscale": 50000, "strided": 5000, "odd": 10000}
+                 "fp8_noscale": 50000, "strided": 5000, "odd": 10000, "gather_decode": 200000,
+                 "gather_fp8": 50000}
 
 
 # ---------------------------------------------------------------------------
@@ -236,8 +241,18 @@ class Pool:
             self.k.append(kb)
             self.v.append(vb)
             self.idx.append(ib)
-        # caches
-        if w.kind == "copy":
+        # caches (for the gather workloads: seeded random content to read back)
+        if w.kind == "gather":
+            words = w.n_slots * w.slot_stride // 2
+            self.kc = torch.randint(-32768, 32767, (words,), generator=g, dtype=torch.int16,
+                                    device=device)
+            self.vc = torch.randint(-32768, 32767, (words,), generator=g, dtype=torch.int16,
+                                    device=device)
+        elif w.kind == "gather_fp8":
+            nbytes = w.n_slots * w.slot_stride
+            self.kc = torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8, device=device)
+            self.vc = torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8, device=device)
+        elif w.kind == "copy":
             words = w.n_slots * w.slot_stride // 2
             self.kc = torch.full((words,), w.sentinel, dtype=torch.int16, device=device)
             self.vc = torch.full((words,), w.sentinel, dtype=torch.int16, device=device)
@@ -246,6 +261,7 @@ class Pool:
             self.kc = torch.full((nbytes,), w.sentinel, dtype=torch.uint8, device=device)
             self.vc = torch.full((nbytes,), w.sentinel, dtype=torch.uint8, device=device)
         self.inv = torch.tensor([w.inv_k, w.inv_v], dtype=torch.float32, device=device)
+        self.scale = torch.ones(2, dtype=torch.float32, device=device) / self.inv
         self.err = torch.zeros(2, dtype=torch.int64, device=device)
         self.i64 = idx_dtype == torch.int64
 
@@ -286,6 +302,17 @@ class Pool:
             return kv.raw.kv_store(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(), idx_ptr,
                                    idt, 1, w.T, w.H, w.D, 2, strides, w.n_slots, w.num_split,
                                    self.err.data_ptr(), stream_handle)
+        if w.kind == "gather":
+            return kv.raw.kv_gather(self.kc.data_ptr(), self.vc.data_ptr(), k_ptr, v_ptr, idx_ptr,
+                                    idt, 1, w.T, w.H, w.D, 2, strides, w.n_slots,
+                                    self.err.data_ptr(), stream_handle)
+        if w.kind == "gather_fp8":
+            return kv.raw.kv_gather_fp8(self.kc.data_ptr(), self.vc.data_ptr(), k_ptr, v_ptr,
+                                        idx_ptr, idt, 1, w.T, w.H, w.D,
+                                        1 if w.src_dtype == "bf16" else 0, strides, w.page_size,
+                                        w.page_stride, w.page_stride, w.n_slots,
+                                        self.scale.data_ptr(), self.scale.data_ptr() + 4, 1,
+                                        self.err.data_ptr(), stream_handle)
         return kv.raw.kv_store_fp8(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(), idx_ptr,
                                    idt, 1, w.T, w.H, w.D, 1 if w.src_dtype == "bf16" else 0,
                                    strides, w.page_size, w.page_stride, w.page_stride, w.n_slots,
@@ -454,8 +481,8 @@ def oracle_step(name, w, tokens):
         cache_bytes = w.n_slots * w.slot_stride
         _ORACLE_CACHE[key] = (np.empty(cache_bytes, dtype=np.uint8),
                               np.empty(cache_bytes, dtype=np.uint8),
-                              np.ascontiguousarray(w.k).view(np.uint8).reshape(-1),
-                              np.ascontiguousarray(w.v).view(np.uint8).reshape(-1),
+                              np.ascontiguousarray(w.k).view(np.uint8).reshape(-1).copy(),
+                              np.ascontiguousarray(w.v).view(np.uint8).reshape(-1).copy(),
                               oracle.Strides(k_token=w.k_view[1], k_head=w.k_view[2],
                                              k_dim=w.k_view[3], v_token=w.v_view[1],
                                              v_head=w.v_view[2], v_dim=w.v_view[3],
@@ -463,7 +490,13 @@ def oracle_step(name, w, tokens):
                                              kc_dim=w.cache_elem, vc_slot=w.slot_stride,
                                              vc_head=w.cache_head_stride, vc_dim=w.cache_elem))
     kc, vc, k, v, st = _ORACLE_CACHE[key]
-    if w.kind == "copy":
+    if w.kind == "gather":
+        oracle.gather_copy(kc, vc, k, v, w.indices, st, w.H, w.D, 2, w.n_slots, t_end=tokens)
+    elif w.kind == "gather_fp8":
+        oracle.gather_fp8(kc, vc, k, v, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
+                          w.page_stride, w.page_stride, w.n_slots, 1.0 / w.inv_k, 1.0 / w.inv_v,
+                          1, t_end=tokens)
+    elif w.kind == "copy":
         oracle.store_copy(k, v, kc, vc, w.indices, st, w.H, w.D, 2, w.n_slots,
                           k_off=w.k_view[0], v_off=w.v_view[0], t_end=tokens)
     else:
@@ -475,6 +508,8 @@ def oracle_step(name, w, tokens):
 def dtype_of(w):
     if w.kind == "fp8":
         return f"f32 ({w.src_dtype} in, e4m3fn out)"
+    if w.kind == "gather_fp8":
+        return f"f32 (e4m3fn in, {w.src_dtype} out)"
     return w.src_dtype
 
 
@@ -598,6 +633,8 @@ def run_e2e(args, dist, torch, kv, pool, device):
     inputs, and a device->host read of the error record."""
     w = pool.w
     nb = pool.num_batches
+    if w.kind.startswith("gather"):
+        return run_e2e_gather(args, dist, torch, kv, pool, device)
     shared = bool(w.notes.get("shared_source"))
     align = lambda n: (n + 255) // 256 * 256
     kbytes = pool.k[0].numel() * pool.k[0].element_size()
@@ -640,6 +677,44 @@ def run_e2e(args, dist, torch, kv, pool, device):
             "how": "every step: one pinned host -> device copy of the batch (K, V, slot ids "
                    "packed), the kv_store call on the staged inputs, and a device -> host read "
                    "of the error record; back-to-back from CUDA graphs"}
+
+
+def run_e2e_gather(args, dist, torch, kv, pool, device):
+    """Gather steps as a KV offload: the slot ids go host -> device, the
+    gathered K and V rows and the error record come back device -> host."""
+    w = pool.w
+    nb = pool.num_batches
+    host_i = [pool.idx[b].cpu().pin_memory() for b in range(nb)]
+    di = torch.empty_like(pool.idx[0])
+    out_k = torch.empty_like(pool.k[0])
+    out_v = torch.empty_like(pool.v[0])
+    host_k = torch.empty(out_k.shape, dtype=out_k.dtype).pin_memory()
+    host_v = torch.empty(out_v.shape, dtype=out_v.dtype).pin_memory()
+    err_host = torch.zeros(2, dtype=torch.int64).pin_memory()
+    h2d = host_i[0].numel() * host_i[0].element_size()
+    d2h = 2 * out_k.numel() * out_k.element_size() + err_host.numel() * 8
+
+    def step(i):
+        b = i % nb
+        di.copy_(host_i[b], non_blocking=True)
+        rc = pool.call(b, torch.cuda.current_stream().cuda_stream, out_k.data_ptr(),
+                       out_v.data_ptr(), di.data_ptr())
+        if rc != 0:
+            raise RuntimeError(kv.kv_status_str(rc))
+        host_k.copy_(out_k, non_blocking=True)
+        host_v.copy_(out_v, non_blocking=True)
+        err_host.copy_(pool.err, non_blocking=True)
+
+    steps = max(3, min(args.steps, args.e2e_steps))
+    graphs = capture_graphs(torch, step, steps, min(steps, args.graph_chunk))
+    run_graphs(graphs)
+    torch.cuda.synchronize()
+    ms = time_region(torch, dist, lambda: run_graphs(graphs), device)
+    sec = ms / 1e3 / steps
+    return {"value": dist.world * w.T / sec, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "how": "every step: slot ids pinned host -> device, the gather, and the gathered K/V "
+                   "rows plus the error record device -> pinned host; from CUDA graphs"}
 
 
 def split_timings(torch, kv, pool, steps=2000):

@@ -78,6 +78,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kv_store_fp8.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
                                      ctypes.POINTER(_Strides), I64, I64, I64, I64, P, P, I32, P, P]
         lib.kv_store_fp8.restype = I32
+        lib.kv_gather.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
+                                  ctypes.POINTER(_Strides), I64, P, P]
+        lib.kv_gather.restype = I32
+        lib.kv_gather_fp8.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
+                                      ctypes.POINTER(_Strides), I64, I64, I64, I64, P, P, I32, P,
+                                      P]
+        lib.kv_gather_fp8.restype = I32
         lib.kv_store_noalloc.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
                                          ctypes.POINTER(_Strides), I64, I32,
                                          ctypes.POINTER(I64), ctypes.POINTER(I64), P]
@@ -129,6 +136,27 @@ class raw:
                                            src_dtype, ctypes.byref(st), page_size,
                                            kc_page_stride, vc_page_stride, size_limit,
                                            inv_k_scale, inv_v_scale, use_scale, d_err, stream)
+
+    @staticmethod
+    def kv_gather(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride, num_tokens,
+                  num_heads, head_dim, elem_bytes, strides: Sequence[int], size_limit, d_err,
+                  stream) -> int:
+        st = _Strides(*[int(x) for x in strides])
+        return load_library().kv_gather(k_cache, v_cache, k_out, v_out, indices, index_dtype,
+                                        index_stride, num_tokens, num_heads, head_dim, elem_bytes,
+                                        ctypes.byref(st), size_limit, d_err, stream)
+
+    @staticmethod
+    def kv_gather_fp8(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
+                      num_tokens, num_heads, head_dim, out_dtype, strides: Sequence[int],
+                      page_size, kc_page_stride, vc_page_stride, size_limit, k_scale, v_scale,
+                      use_scale, d_err, stream) -> int:
+        st = _Strides(*[int(x) for x in strides])
+        return load_library().kv_gather_fp8(k_cache, v_cache, k_out, v_out, indices, index_dtype,
+                                            index_stride, num_tokens, num_heads, head_dim,
+                                            out_dtype, ctypes.byref(st), page_size,
+                                            kc_page_stride, vc_page_stride, size_limit, k_scale,
+                                            v_scale, use_scale, d_err, stream)
 
     @staticmethod
     def kv_store_noalloc(k, v, k_cache, v_cache, indices, index_dtype, index_stride,

@@ -1,0 +1,517 @@
+// The inverse of the KV-cache write: gather cache rows back into token-major
+// rows (kv_gather), optionally dequantising FP8 e4m3fn rows to bf16/fp16
+// (kv_gather_fp8).  Row t of the outputs takes the cache row of slot
+// indices[t].  This is the single-GPU counterpart of the materialise step of
+// vLLM dcp_direct_kv_gather.cu (`materialize_kv_gather_kernel`, a vectorised
+// copy of received KV into the caller's contiguous workspace); the
+// cross-GPU multicast part of that page needs more than one GPU and is not
+// here.
+//
+// Same decomposition as the write kernels: one warp per (token, K|V, segment,
+// part) unit, lane l moving chunks l, l+32, ...  Here the source address
+// depends on the slot, so only the slot id can be prefetched into L2 before
+// the programmatic-launch wait; the row loads follow the slot load.
+#include "kv_host.h"
+
+namespace kvimpl {
+namespace {
+
+struct GatherSide {
+  const uint8_t* cache;  // element (slot 0, 0, 0) of the cache
+  uint8_t* out;          // element (0, 0, 0) of the token-major output
+  int64_t cache_slot, cache_seg, cache_page;
+  int64_t out_token, out_seg;
+  const float* scale;    // fp8 only: device scalar, or nullptr (scale 1)
+};
+
+struct GatherParams {
+  GatherSide side[2];
+  const void* indices;
+  int64_t index_stride, size_limit, page_size;
+  UnitShape shape;
+  kv_error_record* err;
+  int vec;       // cache bytes per chunk
+  int prefetch;  // cache rows are 16-byte aligned: speculative L2 prefetch allowed
+};
+
+
+// Slot id read before the programmatic-launch wait, at L2 only (no L1 line
+// is filled, so the authoritative load after the wait cannot hit a stale
+// copy).  The previous grid may still be writing it: the value is used only
+// to aim an L2 prefetch, never to address a load or a store.
+template <typename IdxT>
+__device__ __forceinline__ int64_t speculative_slot(const void* indices, int64_t stride, int64_t t) {
+  const IdxT* p = static_cast<const IdxT*>(indices) + t * stride;
+  if constexpr (sizeof(IdxT) == 8) {
+    long long v;
+    asm volatile("ld.global.cg.s64 %0, [%1];" : "=l"(v) : "l"(p));
+    return static_cast<int64_t>(v);
+  } else {
+    int v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return static_cast<int64_t>(v);
+  }
+}
+
+__device__ __forceinline__ int64_t gather_slot_offset(const GatherParams& p, const GatherSide& sd,
+                                                      int64_t slot) {
+  if (p.page_size == 1) return slot * sd.cache_page;
+  const int64_t page = slot / p.page_size;
+  return page * sd.cache_page + (slot - page * p.page_size) * sd.cache_slot;
+}
+
+// Before the wait: guess the unit's slot and prefetch that cache row part into
+// L2 when the guess is in range.
+template <typename IdxT>
+__device__ __forceinline__ void gather_prefetch(const GatherParams& p, const Unit& w) {
+  const int64_t s = speculative_slot<IdxT>(p.indices, p.index_stride, w.token);
+  if (s < 0 || s >= p.size_limit) return;
+  const GatherSide& sd = p.side[w.kv];
+  const int64_t part_bytes = static_cast<int64_t>(p.shape.part_chunks) * p.vec;
+  const int64_t off = (p.page_size == 1)
+                          ? s * sd.cache_page
+                          : (s / p.page_size) * sd.cache_page + (s % p.page_size) * sd.cache_slot;
+  prefetch_l2_bulk(sd.cache + off + static_cast<int64_t>(w.seg) * sd.cache_seg +
+                       static_cast<int64_t>(w.part) * part_bytes,
+                   static_cast<uint32_t>(part_bytes));
+}
+
+template <int VEC, int U, typename IdxT>
+__device__ __forceinline__ void gather_unit(const GatherParams& p, const Unit& w, uint32_t lane) {
+  const uint32_t nchunks = p.shape.part_chunks;
+  const int64_t part_bytes = static_cast<int64_t>(nchunks) * VEC;
+  const GatherSide& sd = p.side[w.kv];
+  const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
+  if (slot < 0 || slot >= p.size_limit) {
+    if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
+    return;
+  }
+  const uint8_t* src = sd.cache + gather_slot_offset(p, sd, slot) +
+                       static_cast<int64_t>(w.seg) * sd.cache_seg +
+                       static_cast<int64_t>(w.part) * part_bytes;
+  uint8_t* dst = sd.out + w.token * sd.out_token + static_cast<int64_t>(w.seg) * sd.out_seg +
+                 static_cast<int64_t>(w.part) * part_bytes;
+  Chunk<VEC> buf[U];
+  for (uint32_t c0 = 0; c0 < nchunks; c0 += 32u * U) {
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = c0 + lane + 32u * j;
+      if (c < nchunks) ld_stream(buf[j], src + static_cast<size_t>(c) * VEC);
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = c0 + lane + 32u * j;
+      if (c < nchunks) st_stream(dst + static_cast<size_t>(c) * VEC, buf[j]);
+    }
+  }
+}
+
+template <int VEC, int U, typename IdxT>
+__global__ void __launch_bounds__(kThreads) kv_gather_rows(const __grid_constant__ GatherParams p) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const bool active = u < p.shape.num_units;
+  Unit w = decode_unit(p.shape, active ? u : 0);
+  if (KV_PREFETCH && lane == 0 && active) {
+    if (p.prefetch) gather_prefetch<IdxT>(p, w);
+    else prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
+  }
+  grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  while (u < p.shape.num_units) {
+    gather_unit<VEC, U, IdxT>(p, w, lane);
+    u += nwarps;
+    if (u >= p.shape.num_units) break;
+    w = decode_unit(p.shape, u);
+  }
+  if (!KV_EARLY_TRIGGER) grid_dependents_launch();
+}
+
+// ---------------------------------------------------------------------------
+// FP8 dequantising gather
+// ---------------------------------------------------------------------------
+
+// Two e4m3fn codes (lo in bits 0-7) to two fp32 values, exactly: every e4m3fn
+// value is an fp16 value, and fp16 widens exactly to fp32.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t codes16) {
+  uint32_t h2;
+  const uint16_t c = static_cast<uint16_t>(codes16);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  return make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu))),
+                     __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16))));
+}
+
+// Two fp32 values to two bf16 / fp16 (lo in bits 0-15), nearest even.
+template <bool kBF16>
+__device__ __forceinline__ uint32_t narrow2(float lo, float hi) {
+  uint32_t r;
+  if constexpr (kBF16) {
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  } else {
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  }
+  return r;
+}
+
+// Four codes (one 32-bit word) to four 2-byte outputs (two words).
+template <bool kBF16>
+__device__ __forceinline__ void dequant4(uint32_t codes, float scale, uint32_t& o0, uint32_t& o1) {
+  const float2 a = e4m3x2_to_f32x2(codes & 0xFFFFu);
+  const float2 b = e4m3x2_to_f32x2(codes >> 16);
+  o0 = narrow2<kBF16>(__fmul_rn(a.x, scale), __fmul_rn(a.y, scale));
+  o1 = narrow2<kBF16>(__fmul_rn(b.x, scale), __fmul_rn(b.y, scale));
+}
+
+// IN cache bytes (codes) per lane chunk -> 2*IN output bytes.
+template <int IN, int U, typename IdxT, bool kBF16>
+__device__ __forceinline__ void gather_fp8_unit(const GatherParams& p, const Unit& w,
+                                                uint32_t lane) {
+  const uint32_t nchunks = p.shape.part_chunks;
+  const int64_t part_in = static_cast<int64_t>(nchunks) * IN;
+  const GatherSide& sd = p.side[w.kv];
+  const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
+  const float scale = sd.scale != nullptr ? __ldg(sd.scale) : 1.0f;
+  if (slot < 0 || slot >= p.size_limit) {
+    if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
+    return;
+  }
+  const uint8_t* src = sd.cache + gather_slot_offset(p, sd, slot) +
+                       static_cast<int64_t>(w.seg) * sd.cache_seg +
+                       static_cast<int64_t>(w.part) * part_in;
+  uint8_t* dst = sd.out + w.token * sd.out_token + static_cast<int64_t>(w.seg) * sd.out_seg +
+                 static_cast<int64_t>(w.part) * part_in * 2;
+  constexpr int kWords = IN >= 4 ? IN / 4 : 1;
+  Chunk<IN> buf[U];
+  for (uint32_t c0 = 0; c0 < nchunks; c0 += 32u * U) {
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = c0 + lane + 32u * j;
+      if (c < nchunks) ld_stream(buf[j], src + static_cast<size_t>(c) * IN);
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = c0 + lane + 32u * j;
+      if (c >= nchunks) continue;
+      uint8_t* o = dst + static_cast<size_t>(c) * (2 * IN);
+      if constexpr (IN >= 4) {
+        Chunk<2 * IN> out;
+#pragma unroll
+        for (int i = 0; i < kWords; ++i) dequant4<kBF16>(buf[j].w[i], scale, out.w[2 * i], out.w[2 * i + 1]);
+        st_stream(o, out);
+      } else {
+        static_assert(IN == 2, "IN");
+        const float2 a = e4m3x2_to_f32x2(buf[j].h);
+        Chunk<4> out;
+        out.w[0] = narrow2<kBF16>(__fmul_rn(a.x, scale), __fmul_rn(a.y, scale));
+        st_stream(o, out);
+      }
+    }
+  }
+}
+
+template <int IN, int U, typename IdxT, bool kBF16>
+__global__ void __launch_bounds__(kThreads) kv_gather_fp8_rows(const __grid_constant__ GatherParams p) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const bool active = u < p.shape.num_units;
+  Unit w = decode_unit(p.shape, active ? u : 0);
+  if (KV_PREFETCH && lane == 0 && active) {
+    if (p.prefetch) gather_prefetch<IdxT>(p, w);
+    else prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
+  }
+  grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  while (u < p.shape.num_units) {
+    gather_fp8_unit<IN, U, IdxT, kBF16>(p, w, lane);
+    u += nwarps;
+    if (u >= p.shape.num_units) break;
+    w = decode_unit(p.shape, u);
+  }
+  if (!KV_EARLY_TRIGGER) grid_dependents_launch();
+}
+
+// Element-wise gathers for non-contiguous dims or odd sizes: one warp per
+// (token, K|V, head), lanes over the head's elements.
+struct GatherElemParams {
+  const uint8_t* cache[2];
+  uint8_t* out[2];
+  int64_t cache_slot[2], cache_head[2], cache_dim[2], cache_page[2];
+  int64_t out_token[2], out_head[2], out_dim[2];
+  const float* scale[2];
+  const void* indices;
+  int64_t index_stride, size_limit, page_size;
+  uint64_t num_units;
+  int32_t num_heads, head_dim, elem_bytes;  // elem_bytes: copy only
+  kv_error_record* err;
+};
+
+template <typename IdxT, int kMode>  // kMode: 0 copy, 1 fp8 -> bf16, 2 fp8 -> fp16
+__global__ void __launch_bounds__(kThreads) kv_gather_elements(const __grid_constant__ GatherElemParams p) {
+  grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  const uint64_t per_token = 2ull * static_cast<uint64_t>(p.num_heads);
+  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+       u < p.num_units; u += nwarps) {
+    const int64_t t = static_cast<int64_t>(u / per_token);
+    const uint32_t r = static_cast<uint32_t>(u - static_cast<uint64_t>(t) * per_token);
+    const int kv = r >= static_cast<uint32_t>(p.num_heads) ? 1 : 0;
+    const int64_t h = r - kv * p.num_heads;
+    const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, t);
+    if (slot < 0 || slot >= p.size_limit) {
+      if (r == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(t));
+      continue;
+    }
+    int64_t row;
+    if (p.page_size == 1) {
+      row = slot * p.cache_page[kv];
+    } else {
+      const int64_t page = slot / p.page_size;
+      row = page * p.cache_page[kv] + (slot - page * p.page_size) * p.cache_slot[kv];
+    }
+    const uint8_t* src = p.cache[kv] + row + h * p.cache_head[kv];
+    uint8_t* dst = p.out[kv] + t * p.out_token[kv] + h * p.out_head[kv];
+    const float scale = (kMode != 0 && p.scale[kv] != nullptr) ? __ldg(p.scale[kv]) : 1.0f;
+    for (int64_t d = lane; d < p.head_dim; d += 32) {
+      const uint8_t* s = src + d * p.cache_dim[kv];
+      uint8_t* o = dst + d * p.out_dim[kv];
+      if constexpr (kMode == 0) {
+        for (int b = 0; b < p.elem_bytes; ++b) o[b] = __ldg(s + b);
+      } else {
+        const float2 x = e4m3x2_to_f32x2(__ldg(s));
+        const uint32_t v = narrow2<kMode == 1>(__fmul_rn(x.x, scale), 0.0f);
+        o[0] = static_cast<uint8_t>(v & 0xFFu);
+        o[1] = static_cast<uint8_t>((v >> 8) & 0xFFu);
+      }
+    }
+  }
+  if (!KV_EARLY_TRIGGER) grid_dependents_launch();
+}
+
+template <int VEC, typename IdxT>
+kv_status launch_gather_vec(const GatherParams& p, cudaStream_t stream) {
+  constexpr int U = VEC == 32 ? (KV_COPY_UNROLL + 1) / 2 : KV_COPY_UNROLL;
+  return launch(kv_gather_rows<VEC, U, IdxT>, p.shape.num_units, p, stream);
+}
+
+template <typename IdxT>
+kv_status launch_gather(int vec, const GatherParams& p, cudaStream_t stream) {
+  switch (vec) {
+#if KV_MAX_VEC >= 32
+    case 32: return launch_gather_vec<32, IdxT>(p, stream);
+#endif
+    case 16: return launch_gather_vec<16, IdxT>(p, stream);
+    case 8: return launch_gather_vec<8, IdxT>(p, stream);
+    case 4: return launch_gather_vec<4, IdxT>(p, stream);
+    case 2: return launch_gather_vec<2, IdxT>(p, stream);
+    default: return launch_gather_vec<1, IdxT>(p, stream);
+  }
+}
+
+template <int IN, typename IdxT>
+kv_status launch_gather_fp8_in(bool bf16, const GatherParams& p, cudaStream_t stream) {
+  constexpr int U = IN == 16 ? 2 : 4;
+  if (bf16) return launch(kv_gather_fp8_rows<IN, U, IdxT, true>, p.shape.num_units, p, stream);
+  return launch(kv_gather_fp8_rows<IN, U, IdxT, false>, p.shape.num_units, p, stream);
+}
+
+template <typename IdxT>
+kv_status launch_gather_fp8(int in, bool bf16, const GatherParams& p, cudaStream_t stream) {
+  switch (in) {
+    case 16: return launch_gather_fp8_in<16, IdxT>(bf16, p, stream);
+    case 8: return launch_gather_fp8_in<8, IdxT>(bf16, p, stream);
+    case 4: return launch_gather_fp8_in<4, IdxT>(bf16, p, stream);
+    default: return launch_gather_fp8_in<2, IdxT>(bf16, p, stream);
+  }
+}
+
+template <typename IdxT>
+kv_status launch_gather_elements(int mode, const GatherElemParams& g, cudaStream_t stream) {
+  if (mode == 0) return launch(kv_gather_elements<IdxT, 0>, g.num_units, g, stream);
+  if (mode == 1) return launch(kv_gather_elements<IdxT, 1>, g.num_units, g, stream);
+  return launch(kv_gather_elements<IdxT, 2>, g.num_units, g, stream);
+}
+
+GatherElemParams element_params(const void* k_cache, const void* v_cache, void* k_out, void* v_out,
+                                const void* indices, int64_t index_stride, int64_t num_tokens,
+                                int32_t num_heads, int32_t head_dim, const kv_strides* s,
+                                int64_t size_limit, kv_error_record* d_err) {
+  GatherElemParams g = {};
+  g.cache[0] = static_cast<const uint8_t*>(k_cache);
+  g.cache[1] = static_cast<const uint8_t*>(v_cache);
+  g.out[0] = static_cast<uint8_t*>(k_out);
+  g.out[1] = static_cast<uint8_t*>(v_out);
+  g.cache_slot[0] = s->kc_slot; g.cache_head[0] = s->kc_head; g.cache_dim[0] = s->kc_dim;
+  g.cache_slot[1] = s->vc_slot; g.cache_head[1] = s->vc_head; g.cache_dim[1] = s->vc_dim;
+  g.cache_page[0] = s->kc_slot;
+  g.cache_page[1] = s->vc_slot;
+  g.out_token[0] = s->k_token; g.out_head[0] = s->k_head; g.out_dim[0] = s->k_dim;
+  g.out_token[1] = s->v_token; g.out_head[1] = s->v_head; g.out_dim[1] = s->v_dim;
+  g.indices = indices;
+  g.index_stride = index_stride;
+  g.size_limit = size_limit;
+  g.page_size = 1;
+  g.num_units = static_cast<uint64_t>(num_tokens) * 2u * static_cast<uint64_t>(num_heads);
+  g.num_heads = num_heads;
+  g.head_dim = head_dim;
+  g.err = d_err;
+  return g;
+}
+
+}  // namespace
+}  // namespace kvimpl
+
+using namespace kvimpl;
+
+extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k_out, void* v_out,
+                               const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
+                               int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                               int32_t elem_bytes, const kv_strides* s, int64_t size_limit,
+                               kv_error_record* d_err, kv_stream_t stream_) {
+  if (num_tokens < 0) return KV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KV_OK;
+  if (!common_args_ok(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
+                      num_heads, head_dim, s, size_limit, d_err))
+    return KV_ERR_INVALID_ARG;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+    return KV_ERR_INVALID_ARG;
+  if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const bool i64 = index_dtype == KV_INDEX_I64;
+
+  if (s->k_dim != elem_bytes || s->v_dim != elem_bytes || s->kc_dim != elem_bytes ||
+      s->vc_dim != elem_bytes) {
+    GatherElemParams g = element_params(k_cache, v_cache, k_out, v_out, indices, index_stride,
+                                        num_tokens, num_heads, head_dim, s, size_limit, d_err);
+    g.elem_bytes = elem_bytes;
+    return i64 ? launch_gather_elements<int64_t>(0, g, stream)
+               : launch_gather_elements<int32_t>(0, g, stream);
+  }
+  const int64_t head_bytes = static_cast<int64_t>(head_dim) * elem_bytes;
+  const Segments sg = segments(num_heads, head_dim, head_bytes, head_bytes, s);
+  const int64_t seg_bytes = sg.elems * elem_bytes;
+  uint64_t bits = u64(k_cache) | u64(v_cache) | u64(k_out) | u64(v_out) | u64(s->k_token) |
+                  u64(s->v_token) | u64(s->kc_slot) | u64(s->vc_slot) | u64(seg_bytes);
+  if (sg.count > 1) bits |= u64(s->k_head) | u64(s->v_head) | u64(s->kc_head) | u64(s->vc_head);
+  int sms = 0;
+  kv_status st = current_sm_count(&sms);
+  if (st != KV_OK) return st;
+  const int vec0 = pow2_align(bits);
+  const uint64_t rows = static_cast<uint64_t>(num_tokens) * 2u * sg.count;
+  const uint32_t parts = auto_parts(rows, seg_bytes / vec0, sms);
+  const int64_t part_bytes = seg_bytes / parts;
+  const int vec = pow2_align(bits | u64(part_bytes));
+
+  GatherParams p = {};
+  p.side[0] = GatherSide{static_cast<const uint8_t*>(k_cache), static_cast<uint8_t*>(k_out),
+                         s->kc_slot, s->kc_head, s->kc_slot, s->k_token, s->k_head, nullptr};
+  p.side[1] = GatherSide{static_cast<const uint8_t*>(v_cache), static_cast<uint8_t*>(v_out),
+                         s->vc_slot, s->vc_head, s->vc_slot, s->v_token, s->v_head, nullptr};
+  p.indices = indices;
+  p.index_stride = index_stride;
+  p.size_limit = size_limit;
+  p.page_size = 1;
+  p.shape.parts = parts;
+  p.shape.units_per_side = sg.count * parts;
+  p.shape.units_per_token = 2u * p.shape.units_per_side;
+  p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
+  p.shape.part_chunks = static_cast<uint32_t>(part_bytes / vec);
+  p.err = d_err;
+  p.vec = vec;
+  p.prefetch = vec >= 16 ? 1 : 0;
+  return i64 ? launch_gather<int64_t>(vec, p, stream) : launch_gather<int32_t>(vec, p, stream);
+}
+
+extern "C" kv_status kv_gather_fp8(const void* k_cache, const void* v_cache, void* k_out,
+                                   void* v_out, const void* indices, kv_index_dtype index_dtype,
+                                   int64_t index_stride, int64_t num_tokens, int32_t num_heads,
+                                   int32_t head_dim, kv_src_dtype out_dtype, const kv_strides* s,
+                                   int64_t page_size, int64_t kc_page_stride,
+                                   int64_t vc_page_stride, int64_t size_limit,
+                                   const float* k_scale, const float* v_scale, int32_t use_scale,
+                                   kv_error_record* d_err, kv_stream_t stream_) {
+  if (num_tokens < 0) return KV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KV_OK;
+  if (!common_args_ok(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
+                      num_heads, head_dim, s, size_limit, d_err))
+    return KV_ERR_INVALID_ARG;
+  if (out_dtype != KV_SRC_F16 && out_dtype != KV_SRC_BF16) return KV_ERR_INVALID_ARG;
+  if (page_size < 1) return KV_ERR_INVALID_ARG;
+  if (use_scale && (!k_scale || !v_scale)) return KV_ERR_INVALID_ARG;
+  if (use_scale && ((u64(k_scale) | u64(v_scale)) & 3u) != 0) return KV_ERR_INVALID_ARG;
+  const uint64_t out_bits = u64(k_out) | u64(v_out) | u64(s->k_token) | u64(s->v_token) |
+                            u64(s->k_head) | u64(s->v_head) | u64(s->k_dim) | u64(s->v_dim);
+  if ((out_bits & 1u) != 0) return KV_ERR_INVALID_ARG;
+  if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const bool i64 = index_dtype == KV_INDEX_I64;
+  const bool bf16 = out_dtype == KV_SRC_BF16;
+  const float* sk = use_scale ? k_scale : nullptr;
+  const float* sv = use_scale ? v_scale : nullptr;
+  const bool flat = kc_page_stride == page_size * s->kc_slot && vc_page_stride == page_size * s->vc_slot;
+  const bool contiguous = s->k_dim == 2 && s->v_dim == 2 && s->kc_dim == 1 && s->vc_dim == 1;
+
+  Segments sg{0u, 0};
+  int in = 1;
+  if (contiguous) {
+    sg = segments(num_heads, head_dim, 2 * static_cast<int64_t>(head_dim), head_dim, s);
+    uint64_t cache_bits = u64(k_cache) | u64(v_cache) | u64(s->kc_slot) | u64(s->vc_slot) |
+                          u64(sg.elems);
+    uint64_t obits = u64(k_out) | u64(v_out) | u64(s->k_token) | u64(s->v_token);
+    if (sg.count > 1) {
+      cache_bits |= u64(s->kc_head) | u64(s->vc_head);
+      obits |= u64(s->k_head) | u64(s->v_head);
+    }
+    if (!flat) cache_bits |= u64(kc_page_stride) | u64(vc_page_stride);
+    in = pow2_align(cache_bits);
+    if (in > KV_MAX_VEC / 2) in = KV_MAX_VEC / 2;  // the 2*IN output bytes fit one vector
+    // an IN-byte chunk writes 2*IN output bytes with stores of at most KV_MAX_VEC bytes
+    while (in > 1 &&
+           (obits & static_cast<uint64_t>((2 * in > KV_MAX_VEC ? KV_MAX_VEC : 2 * in) - 1)) != 0)
+      in >>= 1;
+  }
+
+  if (in < 2) {
+    GatherElemParams g = element_params(k_cache, v_cache, k_out, v_out, indices, index_stride,
+                                        num_tokens, num_heads, head_dim, s, size_limit, d_err);
+    g.cache_page[0] = flat ? s->kc_slot : kc_page_stride;
+    g.cache_page[1] = flat ? s->vc_slot : vc_page_stride;
+    g.page_size = flat ? 1 : page_size;
+    g.scale[0] = sk;
+    g.scale[1] = sv;
+    return i64 ? launch_gather_elements<int64_t>(bf16 ? 1 : 2, g, stream)
+               : launch_gather_elements<int32_t>(bf16 ? 1 : 2, g, stream);
+  }
+
+  int sms = 0;
+  kv_status st = current_sm_count(&sms);
+  if (st != KV_OK) return st;
+  const uint64_t rows = static_cast<uint64_t>(num_tokens) * 2u * sg.count;
+  const uint32_t parts = auto_parts(rows, sg.elems / in, sms);
+  const int64_t part_elems = sg.elems / parts;
+
+  GatherParams p = {};
+  p.side[0] = GatherSide{static_cast<const uint8_t*>(k_cache), static_cast<uint8_t*>(k_out),
+                         s->kc_slot, s->kc_head, flat ? s->kc_slot : kc_page_stride, s->k_token,
+                         s->k_head, sk};
+  p.side[1] = GatherSide{static_cast<const uint8_t*>(v_cache), static_cast<uint8_t*>(v_out),
+                         s->vc_slot, s->vc_head, flat ? s->vc_slot : vc_page_stride, s->v_token,
+                         s->v_head, sv};
+  p.indices = indices;
+  p.index_stride = index_stride;
+  p.size_limit = size_limit;
+  p.page_size = flat ? 1 : page_size;
+  p.shape.parts = parts;
+  p.shape.units_per_side = sg.count * parts;
+  p.shape.units_per_token = 2u * p.shape.units_per_side;
+  p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
+  p.shape.part_chunks = static_cast<uint32_t>(part_elems / in);
+  p.err = d_err;
+  p.vec = in;
+  p.prefetch = in >= 16 ? 1 : 0;
+  return i64 ? launch_gather_fp8<int64_t>(in, bf16, p, stream)
+             : launch_gather_fp8<int32_t>(in, bf16, p, stream);
+}

@@ -169,6 +169,41 @@ kv_status kv_store_fp8(const void *k, const void *v, void *k_cache, void *v_cach
                        kv_error_record *d_err, kv_stream_t stream);
 
 /*
+ * kv_gather -- the inverse of kv_store: row t of k_out / v_out takes the cache
+ * row of slot indices[t], byte for byte.  The single-GPU counterpart of the
+ * materialise step of vLLM dcp_direct_kv_gather.cu
+ * (`materialize_kv_gather_kernel`), and the read-back half of a round trip.
+ *
+ * Arguments as for kv_store with the roles of the tensors swapped: k_cache /
+ * v_cache are read, k_out / v_out are written.  In `strides`, k_* / v_*
+ * describe the OUTPUT rows and kc_* / vc_* the caches.  An out-of-range slot
+ * leaves output row t untouched and is counted in d_err.  The outputs must
+ * not overlap the caches or the indices.
+ */
+kv_status kv_gather(const void *k_cache, const void *v_cache, void *k_out, void *v_out,
+                    const void *indices, kv_index_dtype index_dtype, int64_t index_stride,
+                    int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                    int32_t elem_bytes, const kv_strides *strides, int64_t size_limit,
+                    kv_error_record *d_err, kv_stream_t stream);
+
+/*
+ * kv_gather_fp8 -- dequantising gather from e4m3fn caches written by
+ * kv_store_fp8 (same page addressing: page_size, kc_page_stride,
+ * vc_page_stride).  Each code is decoded exactly to fp32, multiplied by the
+ * fp32 scale (k_scale / v_scale: DEVICE pointers, the forward scales, i.e.
+ * 1/inv) when use_scale != 0, and rounded to nearest-even bf16 or fp16
+ * (out_dtype).  NaN codes become the canonical NaN 0x7FFF; fp16 overflow
+ * becomes +-Inf.  Output strides (k_* / v_*) must be even.
+ */
+kv_status kv_gather_fp8(const void *k_cache, const void *v_cache, void *k_out, void *v_out,
+                        const void *indices, kv_index_dtype index_dtype, int64_t index_stride,
+                        int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                        kv_src_dtype out_dtype, const kv_strides *strides, int64_t page_size,
+                        int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
+                        const float *k_scale, const float *v_scale, int32_t use_scale,
+                        kv_error_record *d_err, kv_stream_t stream);
+
+/*
  * kv_store_noalloc -- kv_store for callers that cannot allocate device memory.
  * The pages have no counterpart; this entry point exists for this library's
  * users only.

@@ -69,6 +69,12 @@ def _load():
                                       P, I64, I64, I64, I64, ctypes.c_float, ctypes.c_float,
                                       I32, P, P]
         lib.kvo_store_fp8.restype = I32
+        lib.kvo_gather_copy.argtypes = lib.kvo_store_copy.argtypes
+        lib.kvo_gather_copy.restype = I32
+        lib.kvo_gather_fp8.argtypes = lib.kvo_store_fp8.argtypes
+        lib.kvo_gather_fp8.restype = I32
+        lib.kvo_f32_to_bf16_array.argtypes = [P, P, I64]
+        lib.kvo_f32_to_f16_array.argtypes = [P, P, I64]
         _lib = lib
         return lib
 
@@ -92,6 +98,22 @@ def e4m3fn_decode(codes) -> np.ndarray:
     c = np.ascontiguousarray(codes, dtype=np.uint8)
     out = np.empty(c.shape, dtype=np.float64)
     _load().kvo_decode_array(_ptr(c), _ptr(out), c.size)
+    return out
+
+
+def f32_to_bf16(x) -> np.ndarray:
+    """bf16 bits (uint16) of float32 values: nearest, ties even, NaN -> 0x7FFF."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().kvo_f32_to_bf16_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def f32_to_f16(x) -> np.ndarray:
+    """IEEE fp16 bits (uint16) of float32 values: nearest, ties even, NaN -> 0x7FFF."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().kvo_f32_to_f16_array(_ptr(x), _ptr(out), x.size)
     return out
 
 
@@ -172,6 +194,51 @@ def store_fp8(k, v, k_cache, v_cache, indices, strides: Strides, num_heads, head
                                _ptr(strides.values), page_size, kc_page_stride,
                                vc_page_stride, size_limit, float(np.float32(inv_k)),
                                float(np.float32(inv_v)), int(use_scale), _ptr(bad), _ptr(first))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return int(bad[0]), int(first[0])
+
+
+# -- the inverse path (cache rows back to token rows) -------------------------
+
+def gather_copy(k_cache, v_cache, k_out, v_out, indices, strides: Strides, num_heads, head_dim,
+                elem_bytes, size_limit, kc_off=0, vc_off=0, index_stride=1, t_end=None):
+    """Row t of the outputs takes cache row indices[t] (byte copy); out-of-range
+    slots leave the row untouched. ``strides``: k_*/v_* describe the outputs,
+    kc_*/vc_* the caches. Returns (bad_count, first_bad)."""
+    for a, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_out, "k_out"), (v_out, "v_out")):
+        _check_buf(a, n)
+    idx = np.ascontiguousarray(indices)
+    T = idx.size // index_stride if t_end is None else t_end
+    bad = np.zeros(1, np.int64)
+    first = np.zeros(1, np.int64)
+    rc = _load().kvo_gather_copy(_ptr(k_cache) + kc_off, _ptr(v_cache) + vc_off, _ptr(k_out),
+                                 _ptr(v_out), _ptr(idx), int(idx.dtype == np.int64), index_stride,
+                                 0, T, num_heads, head_dim, elem_bytes, _ptr(strides.values),
+                                 size_limit, _ptr(bad), _ptr(first))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return int(bad[0]), int(first[0])
+
+
+def gather_fp8(k_cache, v_cache, k_out, v_out, indices, strides: Strides, num_heads, head_dim,
+               out_dtype, page_size, kc_page_stride, vc_page_stride, size_limit, scale_k=1.0,
+               scale_v=1.0, use_scale=0, index_stride=1, t_end=None):
+    """Dequantising gather: e4m3fn -> fp32 (* scale) -> bf16 / fp16 rows."""
+    for a, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_out, "k_out"), (v_out, "v_out")):
+        _check_buf(a, n)
+    if out_dtype not in ("bf16", "f16"):
+        raise ValueError(out_dtype)
+    idx = np.ascontiguousarray(indices)
+    T = idx.size // index_stride if t_end is None else t_end
+    bad = np.zeros(1, np.int64)
+    first = np.zeros(1, np.int64)
+    rc = _load().kvo_gather_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(k_out), _ptr(v_out),
+                                _ptr(idx), int(idx.dtype == np.int64), index_stride, 0, T,
+                                num_heads, head_dim, int(out_dtype == "bf16"),
+                                _ptr(strides.values), page_size, kc_page_stride, vc_page_stride,
+                                size_limit, float(np.float32(scale_k)), float(np.float32(scale_v)),
+                                int(use_scale), _ptr(bad), _ptr(first))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return int(bad[0]), int(first[0])

@@ -122,6 +122,63 @@ uint8_t kvo_e4m3fn_encode(float y)
     return sign | (uint8_t)code;
 }
 
+/* Round a float to bf16 (IEEE binary32's sign and 8 exponent bits, 7 stored
+ * fraction bits): nearest, ties to even; overflow rounds to +-Inf; every NaN
+ * becomes the canonical 0x7FFF.  Same plain method as the e4m3fn encoder:
+ * scale the magnitude so the kept bits are the integer part, round once. */
+uint16_t kvo_f32_to_bf16(float x)
+{
+    double a = fabs((double)x);
+    uint16_t sign = signbit(x) ? 0x8000 : 0x0000;
+    if (isnan(x))
+        return 0x7FFF;
+    if (isinf(x))
+        return sign | 0x7F80;
+    if (a < 0x1p-126) {                /* subnormal: multiples of 2^-133 */
+        double m = nearbyint(a * 0x1p133);
+        return sign | (uint16_t)m;     /* m == 128 is the smallest normal */
+    }
+    int ex;
+    (void)frexp(a, &ex);
+    int e = ex - 1;                    /* a in [2^e, 2^(e+1)) */
+    double m = nearbyint(ldexp(a, 7 - e));   /* in [128, 256] */
+    if (m == 256.0) {
+        m = 128.0;
+        e += 1;
+    }
+    if (e > 127)
+        return sign | 0x7F80;
+    return sign | (uint16_t)(((e + 127) << 7) | ((int)m - 128));
+}
+
+/* Round a float to IEEE binary16 (5 exponent bits, bias 15, 10 fraction
+ * bits): nearest, ties to even; overflow rounds to +-Inf; every NaN becomes
+ * the canonical 0x7FFF. */
+uint16_t kvo_f32_to_f16(float x)
+{
+    double a = fabs((double)x);
+    uint16_t sign = signbit(x) ? 0x8000 : 0x0000;
+    if (isnan(x))
+        return 0x7FFF;
+    if (isinf(x))
+        return sign | 0x7C00;
+    if (a < 0x1p-14) {                 /* subnormal: multiples of 2^-24 */
+        double m = nearbyint(a * 0x1p24);
+        return sign | (uint16_t)m;     /* m == 1024 is the smallest normal */
+    }
+    int ex;
+    (void)frexp(a, &ex);
+    int e = ex - 1;
+    double m = nearbyint(ldexp(a, 10 - e));  /* in [1024, 2048] */
+    if (m == 2048.0) {
+        m = 1024.0;
+        e += 1;
+    }
+    if (e > 15)
+        return sign | 0x7C00;
+    return sign | (uint16_t)(((e + 15) << 10) | ((int)m - 1024));
+}
+
 /* fp32 product of the widened input and the fp32 inverse scale: the exact
  * float64 product of two floats rounded once to float. */
 float kvo_scale_f32(float x, float inv)
@@ -245,4 +302,100 @@ void kvo_decode_array(const uint8_t *codes, double *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)
         out[i] = kvo_e4m3fn_decode(codes[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Inverse path: gather cache rows back into token-major rows.              */
+/* The local counterpart of the gather-materialise step of                  */
+/* dcp_direct_kv_gather.cu (`materialize_kv_gather_kernel`): row t of the   */
+/* output takes the cache row named by indices[t].  strides: k_* / v_*      */
+/* describe the OUTPUT rows, kc_* / vc_* the caches.  Out-of-range slots    */
+/* leave the output row untouched and are counted.                          */
+/* ------------------------------------------------------------------------ */
+int kvo_gather_copy(const uint8_t *k_cache, const uint8_t *v_cache, uint8_t *k_out, uint8_t *v_out,
+                    const void *indices, int index_is_i64, int64_t index_stride,
+                    int64_t t_begin, int64_t t_end, int32_t num_heads, int32_t head_dim,
+                    int32_t elem_bytes, const int64_t *strides, int64_t size_limit,
+                    int64_t *bad_count, int64_t *first_bad)
+{
+    if (elem_bytes <= 0 || num_heads <= 0 || head_dim <= 0 || t_begin > t_end)
+        return KVO_ERR_ARG;
+    *bad_count = 0;
+    *first_bad = -1;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        int64_t slot = read_index(indices, index_is_i64, index_stride, t);
+        if (slot < 0 || slot >= size_limit) {
+            note_bad(t, bad_count, first_bad);
+            continue;
+        }
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint8_t *src = kv ? v_cache : k_cache;
+            uint8_t *dst = kv ? v_out : k_out;
+            const int64_t *os = strides + 3 * kv;
+            const int64_t *cs = strides + 6 + 3 * kv;
+            for (int32_t h = 0; h < num_heads; ++h)
+                for (int32_t d = 0; d < head_dim; ++d)
+                    memcpy(dst + t * os[0] + h * os[1] + d * os[2],
+                           src + slot * cs[0] + h * cs[1] + d * cs[2], (size_t)elem_bytes);
+        }
+    }
+    return KVO_OK;
+}
+
+/* FP8 gather with dequantisation: each e4m3fn code is decoded exactly,
+ * multiplied by the fp32 scale (when use_scale), and rounded to bf16
+ * (out_is_bf16) or fp16.  The cache address of slot s is
+ * (s / page_size) * page_stride + (s % page_size) * slot_stride + ...,
+ * as in the forward write. */
+int kvo_gather_fp8(const uint8_t *k_cache, const uint8_t *v_cache, uint8_t *k_out, uint8_t *v_out,
+                   const void *indices, int index_is_i64, int64_t index_stride,
+                   int64_t t_begin, int64_t t_end, int32_t num_heads, int32_t head_dim,
+                   int out_is_bf16, const int64_t *strides, int64_t page_size,
+                   int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
+                   float scale_k, float scale_v, int use_scale,
+                   int64_t *bad_count, int64_t *first_bad)
+{
+    if (num_heads <= 0 || head_dim <= 0 || page_size <= 0 || t_begin > t_end)
+        return KVO_ERR_ARG;
+    *bad_count = 0;
+    *first_bad = -1;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        int64_t slot = read_index(indices, index_is_i64, index_stride, t);
+        if (slot < 0 || slot >= size_limit) {
+            note_bad(t, bad_count, first_bad);
+            continue;
+        }
+        int64_t page_id = slot / page_size;
+        int64_t page_offset = slot % page_size;
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint8_t *src = kv ? v_cache : k_cache;
+            uint8_t *dst = kv ? v_out : k_out;
+            const int64_t *os = strides + 3 * kv;
+            const int64_t *cs = strides + 6 + 3 * kv;
+            int64_t page_stride = kv ? vc_page_stride : kc_page_stride;
+            float scale = kv ? scale_v : scale_k;
+            for (int32_t h = 0; h < num_heads; ++h) {
+                for (int32_t d = 0; d < head_dim; ++d) {
+                    uint8_t q = src[page_id * page_stride + page_offset * cs[0] + h * cs[1] + d * cs[2]];
+                    float x = (float)kvo_e4m3fn_decode(q);
+                    float y = use_scale ? kvo_scale_f32(x, scale) : x;
+                    uint16_t bits = out_is_bf16 ? kvo_f32_to_bf16(y) : kvo_f32_to_f16(y);
+                    memcpy(dst + t * os[0] + h * os[1] + d * os[2], &bits, sizeof bits);
+                }
+            }
+        }
+    }
+    return KVO_OK;
+}
+
+void kvo_f32_to_bf16_array(const float *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kvo_f32_to_bf16(x[i]);
+}
+
+void kvo_f32_to_f16_array(const float *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kvo_f32_to_f16(x[i]);
 }

@@ -37,6 +37,52 @@ def _rows_changed(torch, cache, n_slots, slot_bytes, sentinel_bytes):
     return total
 
 
+def _oracle_gather_compact(w, rows_k, rows_v):
+    """Oracle gather from the T named cache rows (compact cache, slots 0..T-1)."""
+    T = w.T
+    idx = np.arange(T, dtype=w.indices.dtype)
+    sb = w.slot_stride
+    st = oracle.Strides(k_token=w.k_view[1], k_head=w.k_view[2], k_dim=w.k_view[3],
+                        v_token=w.v_view[1], v_head=w.v_view[2], v_dim=w.v_view[3],
+                        kc_slot=sb, kc_head=w.cache_head_stride, kc_dim=w.cache_elem,
+                        vc_slot=sb, vc_head=w.cache_head_stride, vc_dim=w.cache_elem)
+    ok = np.zeros(T * w.k_view[1], np.uint8)
+    ov = np.zeros_like(ok)
+    kc, vc = rows_k.reshape(-1).copy(), rows_v.reshape(-1).copy()
+    if w.kind == "gather":
+        bad = oracle.gather_copy(kc, vc, ok, ov, idx, st, w.H, w.D, 2, T)
+    else:
+        assert w.page_stride == w.page_size * sb
+        bad = oracle.gather_fp8(kc, vc, ok, ov, idx, st, w.H, w.D, w.src_dtype, w.page_size,
+                                w.page_stride, w.page_stride, T + (-T) % w.page_size,
+                                float(np.float32(1.0) / np.float32(w.inv_k)),
+                                float(np.float32(1.0) / np.float32(w.inv_v)), 1)
+    assert bad == (0, -1)
+    return ok, ov
+
+
+@pytest.mark.parametrize("name", ["gather_decode", "gather_fp8"])
+def test_full_size_gather(name):
+    import torch
+    import bench
+    import fp8_quant_gb300 as kv
+    dev = torch.device("cuda", 0)
+    pool = bench.Pool(name, dev, pool_bytes=0)
+    w = pool.w
+    assert pool.call(0, torch.cuda.current_stream().cuda_stream) == 0
+    assert kv.kv_error_poll(pool.err)[:2] == (kv.KVStatus.OK, 0)
+    sb = w.slot_stride
+    slots = torch.from_numpy(w.indices.astype(np.int64)).to(dev)
+    rows = [c.view(torch.uint8).view(w.n_slots, sb).index_select(0, slots).cpu().numpy()
+            for c in (pool.kc, pool.vc)]
+    ok, ov = _oracle_gather_compact(w, *rows)
+    gk = pool.k[0].view(torch.uint8).reshape(-1).cpu().numpy()
+    gv = pool.v[0].view(torch.uint8).reshape(-1).cpu().numpy()
+    assert np.array_equal(gk, ok) and np.array_equal(gv, ov)
+    del pool
+    torch.cuda.empty_cache()
+
+
 def _oracle_compact(w):
     """Oracle over all tokens with slots renumbered 0..T-1 (compact caches)."""
     T = w.T

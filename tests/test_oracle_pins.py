@@ -400,3 +400,127 @@ def test_fp8_oob_skipped():
     assert bad == (2, 3)
     changed = np.any(kc.reshape(n, -1) != wl.FP8_SENTINEL, axis=1)
     assert changed.sum() == T - 2
+
+
+# ---------------------------------------------------------------------------
+# bf16 / fp16 encoders and the inverse path (gather with dequantisation)
+# ---------------------------------------------------------------------------
+
+def _random_f32(seed, n):
+    bits = (wl.splitmix64(seed, 0, n) >> np.uint64(32)).astype(np.uint32)
+    return bits.view(np.float32)
+
+
+def _ties_f32(keep_bits):
+    """float32 values exactly halfway between two representable narrow values
+    (and one ulp either side), for every narrow bit pattern."""
+    drop = 23 - keep_bits
+    base = np.arange(1 << 16, dtype=np.uint32) << 16 if keep_bits == 7 else \
+        (np.arange(1 << 16, dtype=np.uint32) << np.uint32(drop)) & np.uint32(0x7FFFFFFF)
+    half = np.uint32(1 << (drop - 1))
+    out = np.concatenate([base + half, base + half - 1, base + half + 1])
+    return out.view(np.float32)
+
+
+def test_bf16_encoder_against_library():
+    for x in (_random_f32(0xBF16, 1 << 20), _ties_f32(7)):
+        keep = ~np.isnan(x)
+        lib = torch.from_numpy(x[keep].copy()).to(torch.bfloat16).view(torch.int16).numpy()
+        assert np.array_equal(oracle.f32_to_bf16(x[keep]), lib.view(np.uint16))
+    assert np.all(oracle.f32_to_bf16(np.array([np.nan, -np.nan], np.float32)) == 0x7FFF)
+
+
+def test_f16_encoder_against_library():
+    # fp16 halfway points: widen every fp16 pattern and add half an fp16 ulp
+    h = np.arange(1 << 15, dtype=np.uint16).view(np.float16).astype(np.float64)
+    h = h[np.isfinite(h)]
+    with np.errstate(over="ignore"):
+        ulp = np.spacing(h.astype(np.float16)).astype(np.float64)
+    mids = (h + ulp / 2).astype(np.float32)
+    for x in (_random_f32(0xF16, 1 << 20), mids, -mids, np.nextafter(mids, np.float32(0))):
+        keep = ~np.isnan(x)
+        with np.errstate(over="ignore"):
+            lib = x[keep].astype(np.float16).view(np.uint16)
+        assert np.array_equal(oracle.f32_to_f16(x[keep]), lib)
+    assert np.all(oracle.f32_to_f16(np.array([np.nan], np.float32)) == 0x7FFF)
+    assert oracle.f32_to_f16(np.array([65520.0], np.float32))[0] == 0x7C00   # rounds to Inf
+    assert oracle.f32_to_f16(np.array([2.0 ** -25], np.float32))[0] == 0      # tie to even 0
+
+
+def test_gather_copy_round_trip_and_oob():
+    T, H, D, n = 150, 4, 32, 400
+    k, v, idx, kc, vc, ss = _copy_problem(T, H, D, n, 61)
+    st = _contig_strides(H, D, 2)
+    oracle.store_copy(k, v, kc, vc, idx, st, H, D, 2, n)
+    ko = np.zeros_like(k)
+    vo = np.zeros_like(v)
+    assert oracle.gather_copy(kc, vc, ko, vo, idx, st, H, D, 2, n) == (0, -1)
+    assert np.array_equal(ko, k) and np.array_equal(vo, v)
+    bad = idx.copy()
+    bad[[7, 100]] = [n, -3]
+    ko[:] = 0x1234
+    assert oracle.gather_copy(kc, vc, ko, vo, bad, st, H, D, 2, n) == (2, 7)
+    assert np.all(ko[7] == 0x1234) and np.all(ko[100] == 0x1234)
+    assert np.array_equal(ko[8], k[8])
+
+
+def _lib_dequant(codes, scale, out):
+    """Library restatement: torch's e4m3fn decode, float32 multiply, torch/numpy rounding."""
+    x = LIB[codes].astype(np.float32)
+    y = x * np.float32(scale)
+    if out == "bf16":
+        r = torch.from_numpy(y).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    else:
+        with np.errstate(over="ignore", invalid="ignore"):
+            r = y.astype(np.float16).view(np.uint16)
+    return np.where(np.isnan(y), np.uint16(0x7FFF), r)
+
+
+@pytest.mark.parametrize("out", ["bf16", "f16"])
+@pytest.mark.parametrize("scale", [None, 1.0, 0.0078125, 3.3, 1e4])
+def test_gather_fp8_every_code(out, scale):
+    # one slot per token, each cache row holding all 256 codes in some order
+    T, H, D, n = 8, 2, 128, 16
+    codes = np.concatenate([np.arange(256, dtype=np.uint8)] * (T * H * D // 256))
+    codes = codes.reshape(T, H * D)
+    rng = wl.splitmix64(71, 0, T * H * D) % np.uint64(256)
+    codes = (codes + rng.reshape(T, H * D).astype(np.uint8)).astype(np.uint8)
+    kc = np.full(n * H * D, 0x7F, np.uint8)
+    idx = wl.distinct_slots(72, n, T)
+    kc.reshape(n, H * D)[idx] = codes
+    vc = kc.copy()
+    R = H * D * 2
+    st = oracle.Strides(k_token=R, k_head=D * 2, k_dim=2, v_token=R, v_head=D * 2, v_dim=2,
+                        kc_slot=H * D, kc_head=D, kc_dim=1, vc_slot=H * D, vc_head=D, vc_dim=1)
+    ko = np.zeros(T * H * D, np.uint16)
+    vo = np.zeros_like(ko)
+    use = scale is not None
+    s = 1.0 if scale is None else scale
+    oracle.gather_fp8(kc, vc, ko, vo, idx, st, H, D, out, 4, 4 * H * D, 4 * H * D, n,
+                      s, s, int(use))
+    want = _lib_dequant(codes.ravel(), s, out)
+    assert np.array_equal(ko, want) and np.array_equal(vo, want)
+
+
+def test_fp8_store_then_gather_within_half_step():
+    T, H, D, n, ps = 64, 4, 64, 256, 16
+    w = wl.make_fp8("t", T, H, D, n, seed=73, page_size=ps)
+    st = _fp8_strides(H, D, 2, H * D)
+    kc = np.full(n * H * D, wl.FP8_SENTINEL, np.uint8)
+    vc = kc.copy()
+    oracle.store_fp8(w.k, w.v, kc, vc, w.indices, st, H, D, "bf16", ps, ps * H * D, ps * H * D,
+                     n, w.inv_k, w.inv_v, 1)
+    ko = np.zeros(T * H * D, np.uint16)
+    vo = np.zeros_like(ko)
+    sk = float(np.float32(1.0) / np.float32(w.inv_k))
+    oracle.gather_fp8(kc, vc, ko, vo, w.indices, st, H, D, "bf16", ps, ps * H * D, ps * H * D,
+                      n, sk, sk, 1)
+    x = _widen(w.k.reshape(-1), "bf16").astype(np.float64)
+    back = (ko.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    # scaled value y = x*inv is within half an e4m3 step of the code; dequantising
+    # multiplies that by 1/inv and rounds to bf16 (relative 2^-9)
+    y = x * w.inv_k
+    a = np.abs(np.clip(y, -448, 448))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+    bound = (2.0 ** (e - 4)) * sk * (1 + 2 ** -7) + np.abs(back) * 2.0 ** -8
+    assert np.all(np.abs(back - np.clip(y, -448, 448) * sk) <= bound + 1e-30)

@@ -132,7 +132,7 @@ class Workload:
     H: int
     D: int
     src_dtype: str                  # "bf16" | "f16"
-    kind: str                       # "copy" | "fp8"
+    kind: str                       # "copy" | "fp8" | "gather" | "gather_fp8"
     k: np.ndarray
     v: np.ndarray
     k_view: tuple
@@ -279,6 +279,20 @@ def odd(n_slots: int = 1 << 21) -> Workload:
                      dtype="f16", slot_stride=1280)
 
 
+def gather_decode(n_slots: int = 1 << 20) -> Workload:
+    """Inverse of ``decode``: 256 rows gathered from a 1,048,576-slot bf16 cache."""
+    w = decode(n_slots=n_slots)
+    w.name, w.kind = "gather_decode", "gather"
+    return w
+
+
+def gather_fp8(n_slots: int = 1 << 20) -> Workload:
+    """Inverse of ``fp8``: 8192 e4m3fn rows dequantised (x 1/inv) to bf16."""
+    w = fp8(n_slots=n_slots)
+    w.name, w.kind = "gather_fp8", "gather_fp8"
+    return w
+
+
 WORKLOADS = {
     "tiny": tiny,
     "decode": decode,
@@ -286,4 +300,6 @@ WORKLOADS = {
     "fp8": fp8,
     "strided": strided,
     "odd": odd,
+    "gather_decode": gather_decode,
+    "gather_fp8": gather_fp8,
 }
