@@ -65,11 +65,13 @@ DESCRIPTIONS = {
                      "1,048,576-slot cache, int64",
     "gather_fp8": "dequantising gather (inverse of fp8): T=8192 e4m3fn rows x (1/inv) -> bf16, "
                   "1,048,576-slot cache, page_size 32, int64",
+    "absmax": "per-tensor scale pass: max |x| of the fp8 batch's K and V (8192 x 8 x 128 bf16 "
+              "each) and inv = 448/amax on the device",
 }
 
 DEFAULT_STEPS = {"tiny": 200000, "decode": 200000, "prefill": 10000, "fp8": 50000,
                  "fp8_noscale": 50000, "strided": 5000, "odd": 10000, "gather_decode": 200000,
-                 "gather_fp8": 50000}
+                 "gather_fp8": 50000, "absmax": 50000}
 
 
 # ---------------------------------------------------------------------------
@@ -252,6 +254,9 @@ class Pool:
             nbytes = w.n_slots * w.slot_stride
             self.kc = torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8, device=device)
             self.vc = torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8, device=device)
+        elif w.kind == "absmax":
+            self.kc = torch.zeros(1, dtype=torch.uint8, device=device)
+            self.vc = torch.zeros(1, dtype=torch.uint8, device=device)
         elif w.kind == "copy":
             words = w.n_slots * w.slot_stride // 2
             self.kc = torch.full((words,), w.sentinel, dtype=torch.int16, device=device)
@@ -262,6 +267,7 @@ class Pool:
             self.vc = torch.full((nbytes,), w.sentinel, dtype=torch.uint8, device=device)
         self.inv = torch.tensor([w.inv_k, w.inv_v], dtype=torch.float32, device=device)
         self.scale = torch.ones(2, dtype=torch.float32, device=device) / self.inv
+        self.amax_inv = torch.zeros(4, dtype=torch.float32, device=device)
         self.err = torch.zeros(2, dtype=torch.int64, device=device)
         self.i64 = idx_dtype == torch.int64
 
@@ -302,6 +308,10 @@ class Pool:
             return kv.raw.kv_store(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(), idx_ptr,
                                    idt, 1, w.T, w.H, w.D, 2, strides, w.n_slots, w.num_split,
                                    self.err.data_ptr(), stream_handle)
+        if w.kind == "absmax":
+            return kv.raw.kv_absmax_inv(k_ptr, v_ptr, 1 if w.src_dtype == "bf16" else 0, w.T, w.H,
+                                        w.D, strides, 448.0, self.amax_inv.data_ptr(),
+                                        self.amax_inv.data_ptr() + 8, stream_handle)
         if w.kind == "gather":
             return kv.raw.kv_gather(self.kc.data_ptr(), self.vc.data_ptr(), k_ptr, v_ptr, idx_ptr,
                                     idt, 1, w.T, w.H, w.D, 2, strides, w.n_slots,
@@ -478,7 +488,7 @@ def oracle_step(name, w, tokens):
     import oracle
     key = name
     if key not in _ORACLE_CACHE:
-        cache_bytes = w.n_slots * w.slot_stride
+        cache_bytes = 1 if w.kind == "absmax" else w.n_slots * w.slot_stride
         _ORACLE_CACHE[key] = (np.empty(cache_bytes, dtype=np.uint8),
                               np.empty(cache_bytes, dtype=np.uint8),
                               np.ascontiguousarray(w.k).view(np.uint8).reshape(-1).copy(),
@@ -490,7 +500,9 @@ def oracle_step(name, w, tokens):
                                              kc_dim=w.cache_elem, vc_slot=w.slot_stride,
                                              vc_head=w.cache_head_stride, vc_dim=w.cache_elem))
     kc, vc, k, v, st = _ORACLE_CACHE[key]
-    if w.kind == "gather":
+    if w.kind == "absmax":
+        oracle.absmax_inv(k, v, st, tokens, w.H, w.D, w.src_dtype)
+    elif w.kind == "gather":
         oracle.gather_copy(kc, vc, k, v, w.indices, st, w.H, w.D, 2, w.n_slots, t_end=tokens)
     elif w.kind == "gather_fp8":
         oracle.gather_fp8(kc, vc, k, v, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
@@ -506,6 +518,8 @@ def oracle_step(name, w, tokens):
 
 
 def dtype_of(w):
+    if w.kind == "absmax":
+        return f"f32 ({w.src_dtype} in)"
     if w.kind == "fp8":
         return f"f32 ({w.src_dtype} in, e4m3fn out)"
     if w.kind == "gather_fp8":
@@ -664,7 +678,8 @@ def run_e2e(args, dist, torch, kv, pool, device):
         rc = pool.call(b, torch.cuda.current_stream().cuda_stream, kbase, vbase, base + off_i)
         if rc != 0:
             raise RuntimeError(kv.kv_status_str(rc))
-        err_host.copy_(pool.err, non_blocking=True)
+        err_host.copy_(pool.amax_inv.view(torch.int64) if w.kind == "absmax" else pool.err,
+                       non_blocking=True)
 
     steps = max(3, min(args.steps, args.e2e_steps))
     graphs = capture_graphs(torch, step, steps, min(steps, args.graph_chunk))

@@ -78,6 +78,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kv_store_fp8.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
                                      ctypes.POINTER(_Strides), I64, I64, I64, I64, P, P, I32, P, P]
         lib.kv_store_fp8.restype = I32
+        lib.kv_store_paged.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
+                                       ctypes.POINTER(_Strides), I64, I64, I64, I64, I32, P, P]
+        lib.kv_store_paged.restype = I32
         lib.kv_gather.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
                                   ctypes.POINTER(_Strides), I64, P, P]
         lib.kv_gather.restype = I32
@@ -85,6 +88,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                       ctypes.POINTER(_Strides), I64, I64, I64, I64, P, P, I32, P,
                                       P]
         lib.kv_gather_fp8.restype = I32
+        lib.kv_inv_scale.argtypes = [P, P, I64, P]
+        lib.kv_inv_scale.restype = I32
+        lib.kv_absmax_inv.argtypes = [P, P, I32, I64, I32, I32, ctypes.POINTER(_Strides),
+                                      ctypes.c_float, P, P, P]
+        lib.kv_absmax_inv.restype = I32
         lib.kv_store_noalloc.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
                                          ctypes.POINTER(_Strides), I64, I32,
                                          ctypes.POINTER(I64), ctypes.POINTER(I64), P]
@@ -138,6 +146,18 @@ class raw:
                                            inv_k_scale, inv_v_scale, use_scale, d_err, stream)
 
     @staticmethod
+    def kv_store_paged(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_tokens,
+                       num_heads, head_dim, elem_bytes, strides: Sequence[int], page_size,
+                       kc_page_stride, vc_page_stride, size_limit, num_split, d_err,
+                       stream) -> int:
+        st = _Strides(*[int(x) for x in strides])
+        return load_library().kv_store_paged(k, v, k_cache, v_cache, indices, index_dtype,
+                                             index_stride, num_tokens, num_heads, head_dim,
+                                             elem_bytes, ctypes.byref(st), page_size,
+                                             kc_page_stride, vc_page_stride, size_limit,
+                                             num_split, d_err, stream)
+
+    @staticmethod
     def kv_gather(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride, num_tokens,
                   num_heads, head_dim, elem_bytes, strides: Sequence[int], size_limit, d_err,
                   stream) -> int:
@@ -157,6 +177,17 @@ class raw:
                                             out_dtype, ctypes.byref(st), page_size,
                                             kc_page_stride, vc_page_stride, size_limit, k_scale,
                                             v_scale, use_scale, d_err, stream)
+
+    @staticmethod
+    def kv_inv_scale(scale, inv, n, stream) -> int:
+        return load_library().kv_inv_scale(scale, inv, n, stream)
+
+    @staticmethod
+    def kv_absmax_inv(k, v, src_dtype, num_tokens, num_heads, head_dim, strides: Sequence[int],
+                      fp8_max, amax, inv, stream) -> int:
+        st = _Strides(*[int(x) for x in strides])
+        return load_library().kv_absmax_inv(k, v, src_dtype, num_tokens, num_heads, head_dim,
+                                            ctypes.byref(st), float(fp8_max), amax, inv, stream)
 
     @staticmethod
     def kv_store_noalloc(k, v, k_cache, v_cache, indices, index_dtype, index_stride,

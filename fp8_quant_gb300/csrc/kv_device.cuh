@@ -209,4 +209,14 @@ __device__ __forceinline__ uint32_t quant2(uint32_t w, float inv) {
 }
 
 // One lane's chunk: OUT output bytes from OUT 2-byte inputs.
+// Byte offset of cache row `slot`: (slot / page_size) * page_stride +
+// (slot % page_size) * slot_stride.  page_size == 1 means a flat cache whose
+// page stride is the slot stride.
+__device__ __forceinline__ int64_t paged_offset(int64_t slot, int64_t page_size, int64_t page_stride,
+                                                int64_t slot_stride) {
+  if (page_size == 1) return slot * page_stride;
+  const int64_t page = slot / page_size;
+  return page * page_stride + (slot - page * page_size) * slot_stride;
+}
+
 }  // namespace kvimpl

@@ -21,7 +21,7 @@ kv_status blocks_per_sm(const void* fn, int* out);
 // capacity (a whole number of CTAs per SM); warps loop over the rest.
 template <typename Params>
 kv_status launch(void (*kernel)(Params), uint64_t num_units, const Params& params,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, uint64_t max_ctas = 0) {
   int sms = 0, per_sm = 0;
   kv_status st = current_sm_count(&sms);
   if (st != KV_OK) return st;
@@ -34,7 +34,10 @@ kv_status launch(void (*kernel)(Params), uint64_t num_units, const Params& param
   const uint64_t cap = KV_GRID_WAVES > 0
                            ? static_cast<uint64_t>(sms) * static_cast<uint64_t>(per_sm) * KV_GRID_WAVES
                            : uint64_t{0x7FFFFFFF};
-  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  uint64_t grid64 = want < cap ? want : cap;
+  if (max_ctas != 0 && grid64 > max_ctas) grid64 = max_ctas;
+  if (grid64 == 0) grid64 = 1;
+  const unsigned grid = static_cast<unsigned>(grid64);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);

@@ -1,0 +1,178 @@
+// Scale preparation on the device, so that a captured step needs no host
+// synchronisation (sglang trtllm_fp8_kv_kernel.py, `fused_fp8_set_kv_buffer`
+// forms the inverse scales 1.0 / scale on the GPU for exactly that reason):
+//
+//   kv_inv_scale   inv[i] = 1 / scale[i], fp32, round to nearest;
+//   kv_absmax_inv  per-tensor max |x| of the K rows and of the V rows (NaN
+//                  ignored) and inv = fp8_max / amax (1 when amax is 0), the
+//                  per-tensor inverse scale kv_store_fp8 consumes.
+//
+// The absmax pass is a pure HBM read stream: warps reduce their rows in
+// registers, CTAs reduce their warps in shared memory, and one atomicMax per
+// CTA and tensor lands on the float bits of the caller's amax output (for
+// non-negative floats the bit patterns order like the values).
+#include "kv_host.h"
+
+namespace kvimpl {
+namespace {
+
+struct InvParams {
+  const float* scale;
+  float* inv;
+  int64_t n;
+};
+
+__global__ void __launch_bounds__(kThreads) kv_inv_kernel(const __grid_constant__ InvParams p) {
+  grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n; i += stride)
+    p.inv[i] = __fdiv_rn(1.0f, p.scale[i]);
+}
+
+struct AbsmaxParams {
+  const uint8_t* src[2];
+  int64_t token[2], seg[2];  // byte strides of the rows and of their segments
+  UnitShape shape;           // units: (token, K|V, segment); parts = 1
+  unsigned int* amax_bits;   // two words: K, V (the caller's amax output)
+};
+
+// |x| of the two 2-byte elements in `w`, folded into m (fmaxf ignores NaN).
+template <bool kBF16>
+__device__ __forceinline__ float absmax2(float m, uint32_t w) {
+  const float2 x = widen2<kBF16>(w);
+  return fmaxf(m, fmaxf(fabsf(x.x), fabsf(x.y)));
+}
+
+template <int VEC, bool kBF16>
+__global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant__ AbsmaxParams p) {
+  __shared__ float part[2][kWarpsPerCta];
+  grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  const uint32_t nchunks = p.shape.part_chunks;
+  float m[2] = {0.0f, 0.0f};
+  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + warp; u < p.shape.num_units;
+       u += nwarps) {
+    const Unit w = decode_unit(p.shape, u);
+    const uint8_t* src = p.src[w.kv] + w.token * p.token[w.kv] + static_cast<int64_t>(w.seg) * p.seg[w.kv];
+    float acc = 0.0f;
+    for (uint32_t c = lane; c < nchunks; c += 32u) {
+      Chunk<VEC> ch;
+      ld_stream(ch, src + static_cast<size_t>(c) * VEC);
+      if constexpr (VEC >= 4) {
+#pragma unroll
+        for (int i = 0; i < VEC / 4; ++i) acc = absmax2<kBF16>(acc, ch.w[i]);
+      } else {
+        acc = absmax2<kBF16>(acc, static_cast<uint32_t>(ch.h));   // upper element is 0
+      }
+    }
+    m[w.kv] = fmaxf(m[w.kv], acc);
+  }
+#pragma unroll
+  for (int kv = 0; kv < 2; ++kv) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m[kv] = fmaxf(m[kv], __shfl_xor_sync(0xFFFFFFFFu, m[kv], o));
+    if (lane == 0) part[kv][warp] = m[kv];
+  }
+  __syncthreads();
+  if (threadIdx.x < 2) {
+    float v = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kWarpsPerCta; ++i) v = fmaxf(v, part[threadIdx.x][i]);
+    if (v > 0.0f) atomicMax(p.amax_bits + threadIdx.x, __float_as_uint(v));
+  }
+}
+
+struct FinishParams {
+  const unsigned int* amax_bits;
+  float* inv;
+  float fp8_max;
+};
+
+__global__ void __launch_bounds__(kThreads) kv_absmax_finish(const __grid_constant__ FinishParams p) {
+  grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  if (threadIdx.x < 2) {
+    const float a = __uint_as_float(p.amax_bits[threadIdx.x]);
+    p.inv[threadIdx.x] = a > 0.0f ? __fdiv_rn(p.fp8_max, a) : 1.0f;
+  }
+}
+
+template <int VEC>
+kv_status launch_absmax(bool bf16, const AbsmaxParams& p, cudaStream_t stream, uint64_t max_ctas) {
+  if (bf16) return launch(kv_absmax_rows<VEC, true>, p.shape.num_units, p, stream, max_ctas);
+  return launch(kv_absmax_rows<VEC, false>, p.shape.num_units, p, stream, max_ctas);
+}
+
+}  // namespace
+}  // namespace kvimpl
+
+using namespace kvimpl;
+
+extern "C" kv_status kv_inv_scale(const float* scale, float* inv, int64_t n, kv_stream_t stream_) {
+  if (n < 0) return KV_ERR_INVALID_ARG;
+  if (n == 0) return KV_OK;
+  if (!scale || !inv || ((u64(scale) | u64(inv)) & 3u) != 0) return KV_ERR_INVALID_ARG;
+  const uint64_t ctas = (static_cast<uint64_t>(n) + kThreads - 1) / kThreads;
+  return launch(kv_inv_kernel, ctas * kWarpsPerCta, InvParams{scale, inv, n},
+                reinterpret_cast<cudaStream_t>(stream_));
+}
+
+extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype src_dtype,
+                                   int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                                   const kv_strides* s, float fp8_max, float* amax, float* inv,
+                                   kv_stream_t stream_) {
+  if (num_tokens < 0 || num_heads < 1 || head_dim < 1) return KV_ERR_INVALID_ARG;
+  if (!s || !amax || !inv || ((u64(amax) | u64(inv)) & 3u) != 0) return KV_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!k || !v)) return KV_ERR_INVALID_ARG;
+  if (src_dtype != KV_SRC_F16 && src_dtype != KV_SRC_BF16) return KV_ERR_INVALID_ARG;
+  if (!(fp8_max > 0.0f) || fp8_max == INFINITY) return KV_ERR_INVALID_ARG;
+  if (s->k_dim != 2 || s->v_dim != 2) return KV_ERR_UNSUPPORTED;
+  if (((u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token) | u64(s->k_head) | u64(s->v_head)) & 1u) != 0)
+    return KV_ERR_INVALID_ARG;
+  if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  cudaError_t e = cudaMemsetAsync(amax, 0, 2 * sizeof(float), stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (num_tokens > 0) {
+    const int64_t head_bytes = 2 * static_cast<int64_t>(head_dim);
+    const bool merged = num_heads == 1 || (s->k_head == head_bytes && s->v_head == head_bytes);
+    const uint32_t nseg = merged ? 1u : static_cast<uint32_t>(num_heads);
+    const int64_t seg_bytes = merged ? head_bytes * num_heads : head_bytes;
+    uint64_t bits = u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token) | u64(seg_bytes);
+    if (!merged) bits |= u64(s->k_head) | u64(s->v_head);
+    int vec = pow2_align(bits);
+    if (vec > 16) vec = 16;
+    AbsmaxParams p = {};
+    p.src[0] = static_cast<const uint8_t*>(k);
+    p.src[1] = static_cast<const uint8_t*>(v);
+    p.token[0] = s->k_token;
+    p.token[1] = s->v_token;
+    p.seg[0] = s->k_head;
+    p.seg[1] = s->v_head;
+    p.shape.parts = 1;
+    p.shape.units_per_side = nseg;
+    p.shape.units_per_token = 2u * nseg;
+    p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
+    p.shape.part_chunks = static_cast<uint32_t>(seg_bytes / vec);
+    p.amax_bits = reinterpret_cast<unsigned int*>(amax);
+    int sms = 0;
+    kv_status st = current_sm_count(&sms);
+    if (st != KV_OK) return st;
+    // a few CTAs per SM keep the stream saturated with one atomic per CTA
+    const uint64_t max_ctas = static_cast<uint64_t>(sms) * 4u;
+    const bool bf16 = src_dtype == KV_SRC_BF16;
+    switch (vec) {
+      case 16: st = launch_absmax<16>(bf16, p, stream, max_ctas); break;
+      case 8: st = launch_absmax<8>(bf16, p, stream, max_ctas); break;
+      case 4: st = launch_absmax<4>(bf16, p, stream, max_ctas); break;
+      default: st = launch_absmax<2>(bf16, p, stream, max_ctas); break;
+    }
+    if (st != KV_OK) return st;
+  }
+  return launch(kv_absmax_finish, kWarpsPerCta,
+                FinishParams{reinterpret_cast<const unsigned int*>(amax), inv, fp8_max}, stream);
+}

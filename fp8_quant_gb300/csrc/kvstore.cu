@@ -45,6 +45,7 @@ struct CopySide {
   const uint8_t* src;  // element (0, 0, 0) of the input
   uint8_t* dst;        // element (slot 0, 0, 0) of the cache
   int64_t src_token, src_seg, dst_slot, dst_seg;
+  int64_t dst_page;    // page stride (the slot stride when page_size == 1)
 };
 
 struct CopyParams {
@@ -52,6 +53,7 @@ struct CopyParams {
   const void* indices;
   int64_t index_stride;
   int64_t size_limit;
+  int64_t page_size;  // 1: flat cache (slot * slot stride)
   UnitShape shape;
   kv_error_record* err;
   int prefetch;  // sources are 16-byte aligned: prefetch them into L2 before the grid wait
@@ -77,8 +79,8 @@ __device__ __forceinline__ void copy_unit(const CopyParams& p, const Unit& w, co
     if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
     return;
   }
-  uint8_t* dst = sd.dst + slot * sd.dst_slot + static_cast<int64_t>(w.seg) * sd.dst_seg +
-                 static_cast<int64_t>(w.part) * part_bytes;
+  uint8_t* dst = sd.dst + paged_offset(slot, p.page_size, sd.dst_page, sd.dst_slot) +
+                 static_cast<int64_t>(w.seg) * sd.dst_seg + static_cast<int64_t>(w.part) * part_bytes;
 #pragma unroll
   for (int j = 0; j < U; ++j) {
     const uint32_t c = lane + 32u * j;
@@ -140,9 +142,9 @@ struct GenericCopyParams {
   const uint8_t* src[2];
   uint8_t* dst[2];
   int64_t src_token[2], src_head[2], src_dim[2];
-  int64_t dst_slot[2], dst_head[2], dst_dim[2];
+  int64_t dst_slot[2], dst_head[2], dst_dim[2], dst_page[2];
   const void* indices;
-  int64_t index_stride, size_limit;
+  int64_t index_stride, size_limit, page_size;
   uint64_t num_units;  // num_tokens * 2 * num_heads
   int32_t num_heads, head_dim, elem_bytes;
   kv_error_record* err;
@@ -167,7 +169,8 @@ __global__ void __launch_bounds__(kThreads) kv_copy_elements(const __grid_consta
       continue;
     }
     const uint8_t* src = p.src[kv] + t * p.src_token[kv] + h * p.src_head[kv];
-    uint8_t* dst = p.dst[kv] + slot * p.dst_slot[kv] + h * p.dst_head[kv];
+    uint8_t* dst = p.dst[kv] + paged_offset(slot, p.page_size, p.dst_page[kv], p.dst_slot[kv]) +
+                   h * p.dst_head[kv];
     for (int64_t d = lane; d < p.head_dim; d += 32) {
       const uint8_t* s = src + d * p.src_dim[kv];
       uint8_t* o = dst + d * p.dst_dim[kv];
@@ -239,12 +242,6 @@ struct Fp8Params {
   int vec;       // bytes per chunk (the kernel's VEC / OUT)
 };
 
-__device__ __forceinline__ int64_t paged_offset(int64_t slot, int64_t page_size, int64_t page_stride,
-                                                int64_t slot_stride) {
-  if (page_size == 1) return slot * page_stride;
-  const int64_t page = slot / page_size;
-  return page * page_stride + (slot - page * page_size) * slot_stride;
-}
 
 template <int OUT, int U, typename IdxT, bool kBF16>
 __device__ __forceinline__ void fp8_unit(const Fp8Params& p, const Unit& w, const uint8_t* src,
@@ -470,11 +467,15 @@ using namespace kvimpl;
 // C ABI
 // ---------------------------------------------------------------------------
 
-extern "C" kv_status kv_store(const void* k, const void* v, void* k_cache, void* v_cache,
-                              const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
-                              int64_t num_tokens, int32_t num_heads, int32_t head_dim,
-                              int32_t elem_bytes, const kv_strides* s, int64_t size_limit,
-                              int32_t num_split, kv_error_record* d_err, kv_stream_t stream_) {
+namespace {
+
+// kv_store and kv_store_paged: a plain copy into a flat (page_size 1) or paged cache.
+kv_status store_copy(const void* k, const void* v, void* k_cache, void* v_cache,
+                     const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
+                     int64_t num_tokens, int32_t num_heads, int32_t head_dim, int32_t elem_bytes,
+                     const kv_strides* s, int64_t page_size, int64_t kc_page_stride,
+                     int64_t vc_page_stride, int64_t size_limit, int32_t num_split,
+                     kv_error_record* d_err, kv_stream_t stream_) {
   if (num_tokens < 0) return KV_ERR_INVALID_ARG;
   if (num_tokens == 0) return KV_OK;
   if (!common_args_ok(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_heads,
@@ -486,6 +487,12 @@ extern "C" kv_status kv_store(const void* k, const void* v, void* k_cache, void*
   const int64_t row_bytes = static_cast<int64_t>(num_heads) * head_dim * elem_bytes;
   if (num_split > 1 && row_bytes % (static_cast<int64_t>(num_split) * 128) != 0)
     return KV_ERR_INVALID_ARG;
+  if (page_size < 1) return KV_ERR_INVALID_ARG;
+  // A page stride of page_size slots is the flat layout: slot * slot_stride.
+  const bool flat = kc_page_stride == page_size * s->kc_slot && vc_page_stride == page_size * s->vc_slot;
+  const int64_t psize = flat ? 1 : page_size;
+  const int64_t kpage = flat ? s->kc_slot : kc_page_stride;
+  const int64_t vpage = flat ? s->vc_slot : vc_page_stride;
   if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const bool i64 = index_dtype == KV_INDEX_I64;
@@ -501,6 +508,9 @@ extern "C" kv_status kv_store(const void* k, const void* v, void* k_cache, void*
     g.src_token[1] = s->v_token; g.src_head[1] = s->v_head; g.src_dim[1] = s->v_dim;
     g.dst_slot[0] = s->kc_slot; g.dst_head[0] = s->kc_head; g.dst_dim[0] = s->kc_dim;
     g.dst_slot[1] = s->vc_slot; g.dst_head[1] = s->vc_head; g.dst_dim[1] = s->vc_dim;
+    g.dst_page[0] = kpage;
+    g.dst_page[1] = vpage;
+    g.page_size = psize;
     g.indices = indices;
     g.index_stride = index_stride;
     g.size_limit = size_limit;
@@ -519,6 +529,7 @@ extern "C" kv_status kv_store(const void* k, const void* v, void* k_cache, void*
   uint64_t bits = u64(k) | u64(v) | u64(k_cache) | u64(v_cache) | u64(s->k_token) |
                   u64(s->v_token) | u64(s->kc_slot) | u64(s->vc_slot) | u64(seg_bytes);
   if (sg.count > 1) bits |= u64(s->k_head) | u64(s->v_head) | u64(s->kc_head) | u64(s->vc_head);
+  if (!flat) bits |= u64(kc_page_stride) | u64(vc_page_stride);
 
   int sms = 0;
   kv_status st = current_sm_count(&sms);
@@ -536,12 +547,13 @@ extern "C" kv_status kv_store(const void* k, const void* v, void* k_cache, void*
 
   CopyParams p = {};
   p.side[0] = CopySide{static_cast<const uint8_t*>(k), static_cast<uint8_t*>(k_cache), s->k_token,
-                       s->k_head, s->kc_slot, s->kc_head};
+                       s->k_head, s->kc_slot, s->kc_head, kpage};
   p.side[1] = CopySide{static_cast<const uint8_t*>(v), static_cast<uint8_t*>(v_cache), s->v_token,
-                       s->v_head, s->vc_slot, s->vc_head};
+                       s->v_head, s->vc_slot, s->vc_head, vpage};
   p.indices = indices;
   p.index_stride = index_stride;
   p.size_limit = size_limit;
+  p.page_size = psize;
   p.shape.parts = parts;
   p.shape.units_per_side = sg.count * parts;
   p.shape.units_per_token = 2u * p.shape.units_per_side;
@@ -551,6 +563,32 @@ extern "C" kv_status kv_store(const void* k, const void* v, void* k_cache, void*
   p.prefetch = vec >= 16 ? 1 : 0;
   p.vec = vec;
   return i64 ? launch_copy<int64_t>(vec, p, stream) : launch_copy<int32_t>(vec, p, stream);
+}
+
+}  // namespace
+
+extern "C" kv_status kv_store(const void* k, const void* v, void* k_cache, void* v_cache,
+                              const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
+                              int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                              int32_t elem_bytes, const kv_strides* s, int64_t size_limit,
+                              int32_t num_split, kv_error_record* d_err, kv_stream_t stream) {
+  const int64_t kpage = s != nullptr ? s->kc_slot : 0;
+  const int64_t vpage = s != nullptr ? s->vc_slot : 0;
+  return store_copy(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_tokens,
+                    num_heads, head_dim, elem_bytes, s, 1, kpage, vpage, size_limit, num_split,
+                    d_err, stream);
+}
+
+extern "C" kv_status kv_store_paged(const void* k, const void* v, void* k_cache, void* v_cache,
+                                    const void* indices, kv_index_dtype index_dtype,
+                                    int64_t index_stride, int64_t num_tokens, int32_t num_heads,
+                                    int32_t head_dim, int32_t elem_bytes, const kv_strides* s,
+                                    int64_t page_size, int64_t kc_page_stride,
+                                    int64_t vc_page_stride, int64_t size_limit, int32_t num_split,
+                                    kv_error_record* d_err, kv_stream_t stream) {
+  return store_copy(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_tokens,
+                    num_heads, head_dim, elem_bytes, s, page_size, kc_page_stride, vc_page_stride,
+                    size_limit, num_split, d_err, stream);
 }
 
 extern "C" kv_status kv_store_fp8(const void* k, const void* v, void* k_cache, void* v_cache,

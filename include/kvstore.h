@@ -127,6 +127,23 @@ kv_status kv_store(const void *k, const void *v, void *k_cache, void *v_cache,
                    int32_t num_split, kv_error_record *d_err, kv_stream_t stream);
 
 /*
+ * kv_store_paged -- kv_store into a paged cache [pages, page_size, H, D]
+ * whose page stride may include padding: slot s is written at
+ * (s / page_size) * kc_page_stride + (s % page_size) * kc_slot + h * kc_head
+ * + d * kc_dim (likewise for V), the 4-D write of trtllm_fp8_kv_kernel.py
+ * `_naive_fp8_set_kv_buffer` (k_cache[page_ids, page_offsets] = k) for a
+ * cache of the input's own type.  A page stride of page_size * kc_slot is
+ * the flat layout of kv_store.  Other arguments and errors as kv_store, plus
+ * KV_ERR_INVALID_ARG for page_size < 1.
+ */
+kv_status kv_store_paged(const void *k, const void *v, void *k_cache, void *v_cache,
+                         const void *indices, kv_index_dtype index_dtype, int64_t index_stride,
+                         int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                         int32_t elem_bytes, const kv_strides *strides, int64_t page_size,
+                         int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
+                         int32_t num_split, kv_error_record *d_err, kv_stream_t stream);
+
+/*
  * kv_store_fp8 -- fused scale + FP8 e4m3fn conversion + paged write
  * (sglang trtllm_fp8_kv_kernel.py, `_fused_fp8_set_kv_buffer_kernel`,
  * `_process_kv_tensor`, wrapper `fused_fp8_set_kv_buffer`).
@@ -202,6 +219,35 @@ kv_status kv_gather_fp8(const void *k_cache, const void *v_cache, void *k_out, v
                         int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
                         const float *k_scale, const float *v_scale, int32_t use_scale,
                         kv_error_record *d_err, kv_stream_t stream);
+
+/*
+ * kv_inv_scale -- inv[i] = 1 / scale[i] in fp32, round to nearest, for
+ * i < n, on the device (trtllm_fp8_kv_kernel.py, `fused_fp8_set_kv_buffer`
+ * forms 1.0 / k_scale on the GPU so that graph capture needs no host sync).
+ * scale and inv are device pointers to n floats (4-byte aligned; they may be
+ * the same array).  n == 0: KV_OK, nothing launched.
+ */
+kv_status kv_inv_scale(const float *scale, float *inv, int64_t n, kv_stream_t stream);
+
+/*
+ * kv_absmax_inv -- per-tensor scale of the K rows and of the V rows on the
+ * device: amax[0] = max |K|, amax[1] = max |V| over all num_tokens x num_heads
+ * x head_dim elements (NaN elements ignored; 0 for an empty or all-NaN
+ * tensor), and inv[j] = fp8_max / amax[j] in fp32 round-to-nearest (1.0 when
+ * amax[j] is 0).  With fp8_max = 448 this is the per-tensor inverse scale
+ * kv_store_fp8 takes (e4m3fn's largest finite value maps to the tensor's
+ * largest magnitude).
+ *   k, v       bf16 / fp16 rows (src_dtype); strides->k_* and v_* are used
+ *              (dims must be contiguous: k_dim = v_dim = 2; else
+ *              KV_ERR_UNSUPPORTED).
+ *   amax, inv  device pointers to two floats each, written by the call
+ *              (amax is cleared first on `stream`).
+ * fp8_max must be positive and finite.
+ */
+kv_status kv_absmax_inv(const void *k, const void *v, kv_src_dtype src_dtype,
+                        int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                        const kv_strides *strides, float fp8_max, float *amax, float *inv,
+                        kv_stream_t stream);
 
 /*
  * kv_store_noalloc -- kv_store for callers that cannot allocate device memory.

@@ -69,6 +69,12 @@ def _load():
                                       P, I64, I64, I64, I64, ctypes.c_float, ctypes.c_float,
                                       I32, P, P]
         lib.kvo_store_fp8.restype = I32
+        lib.kvo_store_copy_paged.argtypes = [P, P, P, P, P, I32, I64, I64, I64, I32, I32, I32,
+                                             P, I64, I64, I64, I64, P, P]
+        lib.kvo_store_copy_paged.restype = I32
+        lib.kvo_inv_scale.argtypes = [ctypes.c_float]
+        lib.kvo_inv_scale.restype = ctypes.c_float
+        lib.kvo_absmax_inv.argtypes = [P, P, I32, I64, I32, I32, P, ctypes.c_float, P, P]
         lib.kvo_gather_copy.argtypes = lib.kvo_store_copy.argtypes
         lib.kvo_gather_copy.restype = I32
         lib.kvo_gather_fp8.argtypes = lib.kvo_store_fp8.argtypes
@@ -171,6 +177,26 @@ def store_copy(k, v, k_cache, v_cache, indices, strides: Strides, num_heads, hea
     return int(bad[0]), int(first[0])
 
 
+def store_copy_paged(k, v, k_cache, v_cache, indices, strides: Strides, num_heads, head_dim,
+                     elem_bytes, page_size, kc_page_stride, vc_page_stride, size_limit, k_off=0,
+                     v_off=0, index_stride=1, t_end=None):
+    """Paged plain copy (4-D cache). Returns (bad_count, first_bad)."""
+    for a, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_buf(a, n)
+    idx = np.ascontiguousarray(indices)
+    T = idx.size // index_stride if t_end is None else t_end
+    bad = np.zeros(1, np.int64)
+    first = np.zeros(1, np.int64)
+    rc = _load().kvo_store_copy_paged(_ptr(k) + k_off, _ptr(v) + v_off, _ptr(k_cache),
+                                      _ptr(v_cache), _ptr(idx), int(idx.dtype == np.int64),
+                                      index_stride, 0, T, num_heads, head_dim, elem_bytes,
+                                      _ptr(strides.values), page_size, kc_page_stride,
+                                      vc_page_stride, size_limit, _ptr(bad), _ptr(first))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return int(bad[0]), int(first[0])
+
+
 def store_fp8(k, v, k_cache, v_cache, indices, strides: Strides, num_heads, head_dim,
               src_dtype, page_size, kc_page_stride, vc_page_stride, size_limit,
               inv_k=1.0, inv_v=1.0, use_scale=0, k_off=0, v_off=0, index_stride=1,
@@ -242,3 +268,25 @@ def gather_fp8(k_cache, v_cache, k_out, v_out, indices, strides: Strides, num_he
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return int(bad[0]), int(first[0])
+
+
+# -- scale preparation ---------------------------------------------------------
+
+def inv_scale(scale) -> np.ndarray:
+    """fl32(1 / scale) elementwise (correctly rounded fp32 reciprocal)."""
+    sc = np.ascontiguousarray(scale, dtype=np.float32).ravel()
+    return np.array([_load().kvo_inv_scale(float(x)) for x in sc], dtype=np.float32)
+
+
+def absmax_inv(k, v, strides: Strides, num_tokens, num_heads, head_dim, src_dtype, fp8_max=448.0,
+               k_off=0, v_off=0):
+    """(amax[2], inv[2]) float32: per-tensor max |x| (NaN ignored) of K and V and
+    fp8_max / amax (1.0 when amax is 0)."""
+    for a, n in ((k, "k"), (v, "v")):
+        _check_buf(a, n)
+    amax = np.zeros(2, np.float32)
+    inv = np.zeros(2, np.float32)
+    _load().kvo_absmax_inv(_ptr(k) + k_off, _ptr(v) + v_off, int(src_dtype == "bf16"), num_tokens,
+                           num_heads, head_dim, _ptr(strides.values), float(np.float32(fp8_max)),
+                           _ptr(amax), _ptr(inv))
+    return amax, inv

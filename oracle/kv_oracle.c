@@ -242,6 +242,44 @@ int kvo_store_copy(const uint8_t *k, const uint8_t *v, uint8_t *k_cache, uint8_t
     return KVO_OK;
 }
 
+/* Paged plain copy: trtllm_fp8_kv_kernel.py `_naive_fp8_set_kv_buffer` with a
+ * 4-D cache [pages, page_size, H, D] of the input's dtype, where the write is
+ * k_cache[slot // page_size, slot % page_size] = k[t].  Slot s lands at
+ * (s / page_size) * page_stride + (s % page_size) * slot_stride. */
+int kvo_store_copy_paged(const uint8_t *k, const uint8_t *v, uint8_t *k_cache, uint8_t *v_cache,
+                         const void *indices, int index_is_i64, int64_t index_stride,
+                         int64_t t_begin, int64_t t_end, int32_t num_heads, int32_t head_dim,
+                         int32_t elem_bytes, const int64_t *strides, int64_t page_size,
+                         int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
+                         int64_t *bad_count, int64_t *first_bad)
+{
+    if (elem_bytes <= 0 || num_heads <= 0 || head_dim <= 0 || page_size <= 0 || t_begin > t_end)
+        return KVO_ERR_ARG;
+    *bad_count = 0;
+    *first_bad = -1;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        int64_t slot = read_index(indices, index_is_i64, index_stride, t);
+        if (slot < 0 || slot >= size_limit) {
+            note_bad(t, bad_count, first_bad);
+            continue;
+        }
+        int64_t page_id = slot / page_size;
+        int64_t page_offset = slot % page_size;
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint8_t *src = kv ? v : k;
+            uint8_t *dst = kv ? v_cache : k_cache;
+            const int64_t *ss = strides + 3 * kv;
+            const int64_t *ds = strides + 6 + 3 * kv;
+            int64_t page_stride = kv ? vc_page_stride : kc_page_stride;
+            for (int32_t h = 0; h < num_heads; ++h)
+                for (int32_t d = 0; d < head_dim; ++d)
+                    memcpy(dst + page_id * page_stride + page_offset * ds[0] + h * ds[1] + d * ds[2],
+                           src + t * ss[0] + h * ss[1] + d * ss[2], (size_t)elem_bytes);
+        }
+    }
+    return KVO_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Fused FP8 write: trtllm_fp8_kv_kernel.py `_fused_fp8_set_kv_buffer_kernel`
  * and `_process_kv_tensor`.  Inputs are bf16 (src_is_bf16 = 1) or fp16.
@@ -398,4 +436,44 @@ void kvo_f32_to_f16_array(const float *x, uint16_t *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)
         out[i] = kvo_f32_to_f16(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scale preparation.                                                       */
+/* ------------------------------------------------------------------------ */
+
+/* trtllm_fp8_kv_kernel.py, `fused_fp8_set_kv_buffer`: the inverse scale
+ * 1.0 / scale is formed on the device in fp32 (so that no host sync is needed
+ * during graph capture).  The float64 quotient of two floats rounded once to
+ * float is the correctly rounded fp32 quotient. */
+float kvo_inv_scale(float scale)
+{
+    return (float)(1.0 / (double)scale);
+}
+
+/* Per-tensor absolute maximum of the K rows and of the V rows (NaN elements
+ * are ignored; an all-NaN or empty tensor gives 0) and the inverse scale
+ * fp8_max / amax in fp32 (1.0 when amax is 0): the recipe of the fp8
+ * workload's per-tensor scale, inv = 448 / amax for e4m3fn.
+ * strides: the first six entries of the usual twelve (K and V rows). */
+void kvo_absmax_inv(const uint8_t *k, const uint8_t *v, int src_is_bf16, int64_t num_tokens,
+                    int32_t num_heads, int32_t head_dim, const int64_t *strides, float fp8_max,
+                    float *amax_out, float *inv_out)
+{
+    for (int kv = 0; kv < 2; ++kv) {
+        const uint8_t *src = kv ? v : k;
+        const int64_t *ss = strides + 3 * kv;
+        double amax = 0.0;
+        for (int64_t t = 0; t < num_tokens; ++t)
+            for (int32_t h = 0; h < num_heads; ++h)
+                for (int32_t d = 0; d < head_dim; ++d) {
+                    uint16_t bits;
+                    memcpy(&bits, src + t * ss[0] + h * ss[1] + d * ss[2], sizeof bits);
+                    double x = src_is_bf16 ? kvo_bf16_to_f32(bits) : kvo_f16_to_f32(bits);
+                    if (!isnan(x) && fabs(x) > amax)
+                        amax = fabs(x);
+                }
+        amax_out[kv] = (float)amax;
+        inv_out[kv] = amax > 0.0 ? (float)((double)fp8_max / amax) : 1.0f;
+    }
 }

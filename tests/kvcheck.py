@@ -54,6 +54,7 @@ class Problem:
     inv_k: float = 1.0
     inv_v: float = 1.0
     use_scale: int = 0
+    paged: bool = False        # copy through kv_store_paged (page_size, kc_page, vc_page)
 
     def strides(self):
         return (self.k_view.token, self.k_view.head, self.k_view.dim,
@@ -76,7 +77,13 @@ def run_oracle(p: Problem):
     kc = filled(p.cache_bytes, p.sentinel)
     vc = filled(p.cache_bytes, p.sentinel)
     st = oracle.Strides(**dict(zip(oracle.Strides.FIELDS, p.strides())))
-    if p.kind == "copy":
+    if p.kind == "copy" and p.paged:
+        assert p.kc_view.offset == 0 and p.vc_view.offset == 0
+        res = oracle.store_copy_paged(p.k_src, p.v_src, kc, vc, p.indices, st, p.H, p.D, p.elem,
+                                      p.page_size, p.kc_page, p.vc_page, p.size_limit,
+                                      k_off=p.k_view.offset, v_off=p.v_view.offset,
+                                      index_stride=p.index_stride, t_end=p.T)
+    elif p.kind == "copy":
         res = oracle.store_copy(p.k_src, p.v_src, kc, vc, p.indices, st, p.H, p.D, p.elem,
                                 p.size_limit, k_off=p.k_view.offset, v_off=p.v_view.offset,
                                 kc_off=p.kc_view.offset, vc_off=p.vc_view.offset,
@@ -128,6 +135,13 @@ class GpuRun:
         idt = 1 if p.indices.dtype == np.int64 else 0
         kptr = self.k_src.data_ptr() + p.k_view.offset
         vptr = self.v_src.data_ptr() + p.v_view.offset
+        if p.kind == "copy" and p.paged:
+            return kv.raw.kv_store_paged(kptr, vptr, self.kc.data_ptr(), self.vc.data_ptr(),
+                                         self.idx.data_ptr(), idt, p.index_stride, p.T, p.H, p.D,
+                                         p.elem, p.strides(), p.page_size, p.kc_page, p.vc_page,
+                                         p.size_limit,
+                                         p.num_split if num_split is None else num_split,
+                                         self.err.data_ptr(), s)
         if p.kind == "copy":
             return kv.raw.kv_store(kptr, vptr, self.kc.data_ptr() + p.kc_view.offset,
                                    self.vc.data_ptr() + p.vc_view.offset, self.idx.data_ptr(),
@@ -189,7 +203,7 @@ def rand_bytes(seed: int, n: int) -> np.ndarray:
 def copy_problem(T, H, D, n_slots, seed, elem=2, idx_dtype=np.int64, index_stride=1,
                  slot_pad=0, head_pad_src=0, head_pad_dst=0, dim_stride_mult=1,
                  src_off=0, dst_off=0, token_pad=0, num_split=0, size_limit=None,
-                 slots=None, qkv_shared=False) -> Problem:
+                 slots=None, qkv_shared=False, page_size=None, page_pad=0) -> Problem:
     """A copy problem with optional padding/offsets that exercise every path."""
     row_src_head = D * elem * dim_stride_mult + head_pad_src
     tok = H * row_src_head + token_pad
@@ -210,11 +224,18 @@ def copy_problem(T, H, D, n_slots, seed, elem=2, idx_dtype=np.int64, index_strid
     dst_head = D * elem * dim_stride_mult + head_pad_dst
     slot = H * dst_head + slot_pad
     cache_bytes = dst_off + n_slots * slot
+    paged = page_size is not None
+    ps = page_size or 1
+    page = ps * slot + page_pad
+    if paged:
+        assert dst_off == 0
+        cache_bytes = -(-n_slots // ps) * page
     if slots is None:
         slots = wl.distinct_slots(seed + 2, n_slots, T)
     idx_store = np.zeros(T * index_stride, dtype=idx_dtype)
     idx_store[::index_stride] = slots
-    return Problem(kind="copy", k_src=ksrc, v_src=vsrc, k_view=kvw, v_view=vvw,
+    return Problem(kind="copy", paged=paged, page_size=ps, kc_page=page, vc_page=page,
+                   k_src=ksrc, v_src=vsrc, k_view=kvw, v_view=vvw,
                    kc_view=View(dst_off, slot, dst_head, elem * dim_stride_mult),
                    vc_view=View(dst_off, slot, dst_head, elem * dim_stride_mult),
                    cache_bytes=cache_bytes, sentinel=SENT16 if elem % 2 == 0 else SENT8,

@@ -58,6 +58,18 @@ COPY_CASES = {
     "index_stride3_i32": dict(T=513, H=8, D=128, n_slots=2000, index_stride=3,
                               idx_dtype=np.int32),
     "single_token": dict(T=1, H=8, D=128, n_slots=8),
+    # kv_store_paged: [pages, page_size, H, D] caches, dense and padded page strides
+    "paged_dense_64": dict(T=700, H=8, D=128, n_slots=4096, page_size=64),
+    "paged_padded_16": dict(T=700, H=8, D=128, n_slots=4096, page_size=16, page_pad=512),
+    "paged_padded_odd_rows": dict(T=600, H=1, D=576, n_slots=2048, page_size=32, page_pad=128,
+                                  slot_pad=128, idx_dtype=np.int32),
+    "paged_page7_vec4": dict(T=400, H=2, D=40, n_slots=1000, page_size=7, page_pad=12),
+    "paged_segments": dict(T=500, H=8, D=64, n_slots=2000, page_size=16, page_pad=64,
+                           head_pad_dst=32),
+    "paged_generic_dims": dict(T=200, H=4, D=32, n_slots=600, page_size=8, page_pad=32,
+                               dim_stride_mult=2),
+    "paged_split4": dict(T=300, H=8, D=128, n_slots=1024, page_size=32, page_pad=256,
+                         num_split=4),
 }
 
 

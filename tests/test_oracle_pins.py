@@ -524,3 +524,66 @@ def test_fp8_store_then_gather_within_half_step():
     e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
     bound = (2.0 ** (e - 4)) * sk * (1 + 2 ** -7) + np.abs(back) * 2.0 ** -8
     assert np.all(np.abs(back - np.clip(y, -448, 448) * sk) <= bound + 1e-30)
+
+
+def test_paged_copy_layouts():
+    """Paged copy: a dense page stride equals the flat copy for any page size,
+    and a padded 4-D layout lands rows at page*page_stride + offset*slot_stride
+    (numpy fancy indexing k_cache[page_ids, page_offsets] = k as the check)."""
+    T, H, D, n = 120, 4, 16, 512
+    k, v, idx, kc0, vc0, ss = _copy_problem(T, H, D, n, 81)
+    st = _contig_strides(H, D, 2)
+    flat_k, flat_v = kc0.copy(), vc0.copy()
+    oracle.store_copy(k, v, flat_k, flat_v, idx, st, H, D, 2, n)
+    for ps in (1, 16, 64, 512):
+        pk, pv = kc0.copy(), vc0.copy()
+        assert oracle.store_copy_paged(k, v, pk, pv, idx, st, H, D, 2, ps, ps * ss, ps * ss,
+                                       n) == (0, -1)
+        assert np.array_equal(pk, flat_k) and np.array_equal(pv, flat_v)
+    ps, pad = 16, 96
+    page = ps * ss + pad
+    n_pages = n // ps
+    pk = np.full(n_pages * page // 2, wl.BF16_SENTINEL, np.uint16)
+    pv = pk.copy()
+    oracle.store_copy_paged(k, v, pk, pv, idx, st, H, D, 2, ps, page, page, n)
+    pages = pk.view(np.uint8).reshape(n_pages, page)
+    view4 = pages[:, :ps * ss].reshape(n_pages, ps, ss)
+    want = np.full((n_pages, ps, ss), 0, np.uint8)
+    want.view(np.uint16)[:] = wl.BF16_SENTINEL
+    want[idx // ps, idx % ps] = k.view(np.uint8).reshape(T, ss)
+    assert np.array_equal(view4, want)
+    assert np.all(pages[:, ps * ss:].view(np.uint16) == wl.BF16_SENTINEL)
+
+
+def test_inv_scale_is_ieee_fp32_division():
+    x = np.concatenate([wl.normal(91, 4096) * np.float32(100),
+                        np.array([1.0, 3.0, 448.0, 1e-38, 3e-39, 1e38, -7.5], np.float32),
+                        np.abs(_random_f32(92, 4096))])
+    x = x[np.isfinite(x) & (x != 0)]
+    with np.errstate(over="ignore", divide="ignore"):
+        want = np.float32(1.0) / x.astype(np.float32)
+    got = oracle.inv_scale(x)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("src", ["bf16", "f16"])
+def test_absmax_inv_against_numpy(src):
+    T, H, D = 300, 4, 32
+    w = wl.make_fp8("t", T, H, D, 1024, seed=93, dtype=src)
+    kb, vb = w.k.copy(), w.v.copy()
+    # a NaN and an outlier of each sign must not / must count
+    kb.reshape(-1)[17] = 0x7FC0 if src == "bf16" else 0x7E00
+    st = _fp8_strides(H, D, 2, H * D)
+    amax, inv = oracle.absmax_inv(kb, vb, st, T, H, D, src)
+    for bits, a, i in ((kb, amax[0], inv[0]), (vb, amax[1], inv[1])):
+        x = _widen(bits.reshape(-1), src)
+        want = np.float32(np.nanmax(np.abs(x)))
+        assert a == want
+        assert i == np.float32(448.0) / want
+    # all-zero tensors give inv = 1
+    z = np.zeros_like(kb)
+    amax, inv = oracle.absmax_inv(z, z, st, T, H, D, src)
+    assert list(amax) == [0.0, 0.0] and list(inv) == [1.0, 1.0]
+    # the fp8 workload's recipe (host numpy) is exactly this
+    amax, inv = oracle.absmax_inv(w.k, w.v, st, T, H, D, src)
+    assert inv[0] == np.float32(w.inv_k) and inv[1] == np.float32(w.inv_v)

@@ -132,7 +132,7 @@ class Workload:
     H: int
     D: int
     src_dtype: str                  # "bf16" | "f16"
-    kind: str                       # "copy" | "fp8" | "gather" | "gather_fp8"
+    kind: str                       # "copy" | "fp8" | "gather" | "gather_fp8" | "absmax"
     k: np.ndarray
     v: np.ndarray
     k_view: tuple
@@ -160,7 +160,10 @@ class Workload:
         return self.n_slots * self.slot_stride
 
     def algorithmic_bytes(self) -> int:
-        """Bytes a call must move: K and V rows read, cache rows written, indices read."""
+        """Bytes a call must move: K and V rows read, cache rows written, indices read
+        (for the absmax pass: K and V rows read, four floats written)."""
+        if self.kind == "absmax":
+            return self.T * 2 * self.row_bytes + 16
         out_row = self.H * self.D * self.cache_elem
         return self.T * (2 * self.row_bytes + 2 * out_row + self.indices.itemsize)
 
@@ -293,6 +296,13 @@ def gather_fp8(n_slots: int = 1 << 20) -> Workload:
     return w
 
 
+def absmax(n_slots: int = 1 << 20) -> Workload:
+    """Per-tensor scale pass over the ``fp8`` batch (K and V read once)."""
+    w = fp8(n_slots=n_slots)
+    w.name, w.kind = "absmax", "absmax"
+    return w
+
+
 WORKLOADS = {
     "tiny": tiny,
     "decode": decode,
@@ -302,4 +312,5 @@ WORKLOADS = {
     "odd": odd,
     "gather_decode": gather_decode,
     "gather_fp8": gather_fp8,
+    "absmax": absmax,
 }
