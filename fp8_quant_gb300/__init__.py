@@ -88,6 +88,14 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                       ctypes.POINTER(_Strides), I64, I64, I64, I64, P, P, I32, P,
                                       P]
         lib.kv_gather_fp8.restype = I32
+        lib.kv_store_fp8_ex.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
+                                        ctypes.POINTER(_Strides), I64, I64, I64, I64, I32, I32,
+                                        P, P, P, P, I64, P, P]
+        lib.kv_store_fp8_ex.restype = I32
+        lib.kv_gather_fp8_ex.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
+                                         ctypes.POINTER(_Strides), I64, I64, I64, I64, I32, I32,
+                                         P, P, P, P, I64, P, P]
+        lib.kv_gather_fp8_ex.restype = I32
         lib.kv_inv_scale.argtypes = [P, P, I64, P]
         lib.kv_inv_scale.restype = I32
         lib.kv_absmax_inv.argtypes = [P, P, I32, I64, I32, I32, ctypes.POINTER(_Strides),
@@ -177,6 +185,34 @@ class raw:
                                             out_dtype, ctypes.byref(st), page_size,
                                             kc_page_stride, vc_page_stride, size_limit, k_scale,
                                             v_scale, use_scale, d_err, stream)
+
+    @staticmethod
+    def kv_store_fp8_ex(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_tokens,
+                        num_heads, head_dim, src_dtype, strides: Sequence[int], page_size,
+                        kc_page_stride, vc_page_stride, size_limit, fmt, scale_mode, inv_k_scale,
+                        inv_v_scale, k_scales, v_scales, scales_slot_stride, d_err,
+                        stream) -> int:
+        st = _Strides(*[int(x) for x in strides])
+        return load_library().kv_store_fp8_ex(k, v, k_cache, v_cache, indices, index_dtype,
+                                              index_stride, num_tokens, num_heads, head_dim,
+                                              src_dtype, ctypes.byref(st), page_size,
+                                              kc_page_stride, vc_page_stride, size_limit, fmt,
+                                              scale_mode, inv_k_scale, inv_v_scale, k_scales,
+                                              v_scales, scales_slot_stride, d_err, stream)
+
+    @staticmethod
+    def kv_gather_fp8_ex(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
+                         num_tokens, num_heads, head_dim, out_dtype, strides: Sequence[int],
+                         page_size, kc_page_stride, vc_page_stride, size_limit, fmt, scale_mode,
+                         k_scale, v_scale, k_scales, v_scales, scales_slot_stride, d_err,
+                         stream) -> int:
+        st = _Strides(*[int(x) for x in strides])
+        return load_library().kv_gather_fp8_ex(k_cache, v_cache, k_out, v_out, indices,
+                                               index_dtype, index_stride, num_tokens, num_heads,
+                                               head_dim, out_dtype, ctypes.byref(st), page_size,
+                                               kc_page_stride, vc_page_stride, size_limit, fmt,
+                                               scale_mode, k_scale, v_scale, k_scales, v_scales,
+                                               scales_slot_stride, d_err, stream)
 
     @staticmethod
     def kv_inv_scale(scale, inv, n, stream) -> int:

@@ -16,7 +16,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = [os.path.join(CSRC, f) for f in ("kvstore.cu", "kv_gather.cu", "kv_scale.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("kvstore.cu", "kv_gather.cu", "kv_scale.cu", "kv_fp8_ex.cu")]
 SRC = SOURCES[0]
 HEADER = os.path.join(ROOT, "include", "kvstore.h")
 LIBDIR = os.path.join(HERE, "lib")

@@ -191,6 +191,23 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Same for e5m2 (largest finite 57344; infinities saturate to it too).
+__device__ __forceinline__ uint32_t e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// FP8 formats: the template parameter FMT of the conversion helpers.
+constexpr int kFmtE4M3 = 0;
+constexpr int kFmtE5M2 = 1;
+
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
+  if constexpr (FMT == kFmtE5M2) return e5m2x2(lo, hi);
+  return e4m3x2(lo, hi);
+}
+
 // Two packed 2-byte inputs -> fp32 (exact).
 template <bool kBF16>
 __device__ __forceinline__ float2 widen2(uint32_t w) {
@@ -202,10 +219,10 @@ __device__ __forceinline__ float2 widen2(uint32_t w) {
   }
 }
 
-template <bool kBF16>
+template <bool kBF16, int FMT = kFmtE4M3>
 __device__ __forceinline__ uint32_t quant2(uint32_t w, float inv) {
   const float2 x = widen2<kBF16>(w);
-  return e4m3x2(__fmul_rn(x.x, inv), __fmul_rn(x.y, inv));
+  return fp8x2<FMT>(__fmul_rn(x.x, inv), __fmul_rn(x.y, inv));
 }
 
 // One lane's chunk: OUT output bytes from OUT 2-byte inputs.

@@ -1,0 +1,290 @@
+// Extended FP8 write: e4m3fn or e5m2 caches, and dynamic scales computed in
+// the kernel per token row or per (token, head).
+//
+// The fused FP8 write's module docstring (sglang trtllm_fp8_kv_kernel.py)
+// names "per-token or per-page scale computation" but its kernel only takes
+// a per-tensor scale; this file supplies the per-token form.  For each group
+// (the K or V row of a token, or one head of it): amax = max |x| (NaN
+// ignored); inv = fmax / amax and scale = amax / fmax in fp32 (both 1 when
+// amax is 0); codes = fp8(x * inv); `scale` goes to the caller's per-slot
+// scale cache.  fmax is 448 for e4m3fn and 57344 for e5m2.
+//
+// One warp owns one group.  The group's elements are loaded once into
+// registers (up to 4 chunks per lane; longer groups are re-read from L2 in a
+// second pass), the warp reduces amax with shuffles, then converts and stores
+// the codes and lane 0 stores the group's scale.  As in the other write
+// kernels, the group's source bytes are prefetched into L2 before the
+// programmatic-launch wait.
+#include "kv_host.h"
+
+namespace kvimpl {
+namespace {
+
+struct DynSide {
+  const uint8_t* src;
+  uint8_t* dst;
+  int64_t src_token, src_seg;              // input byte strides (segment = head)
+  int64_t dst_slot, dst_seg, dst_page;     // cache byte strides
+  float* scales;                           // per-slot scale cache
+};
+
+struct DynParams {
+  DynSide side[2];
+  const void* indices;
+  int64_t index_stride, size_limit, page_size, scales_stride;
+  uint64_t num_units;  // num_tokens * 2 * groups
+  uint32_t groups;     // groups per row: 1 (token) or num_heads (token, head)
+  uint32_t gseg;       // segments per group
+  uint32_t cps;        // chunks per segment
+  float fmax;
+  kv_error_record* err;
+  int prefetch;        // segments 16-byte aligned: bulk L2 prefetch allowed
+};
+
+struct DynUnit {
+  int64_t token;
+  uint32_t kv, group, rank;
+};
+
+__device__ __forceinline__ DynUnit dyn_unit(const DynParams& p, uint64_t u) {
+  DynUnit w;
+  const uint64_t per_token = 2ull * p.groups;
+  const uint64_t t = u / per_token;
+  w.token = static_cast<int64_t>(t);
+  w.rank = static_cast<uint32_t>(u - t * per_token);
+  w.kv = w.rank >= p.groups ? 1u : 0u;
+  w.group = w.rank - w.kv * p.groups;
+  return w;
+}
+
+// amax of the CH elements of one input chunk, folded into m.
+template <int CH, bool kBF16>
+__device__ __forceinline__ float chunk_absmax(float m, const Chunk<2 * CH>& c) {
+  if constexpr (CH >= 2) {
+#pragma unroll
+    for (int i = 0; i < CH / 2; ++i) {
+      const float2 x = widen2<kBF16>(c.w[i]);
+      m = fmaxf(m, fmaxf(fabsf(x.x), fabsf(x.y)));
+    }
+  } else {
+    const float2 x = widen2<kBF16>(static_cast<uint32_t>(c.h));
+    m = fmaxf(m, fabsf(x.x));
+  }
+  return m;
+}
+
+// CH codes of one chunk.
+template <int CH, bool kBF16, int FMT>
+__device__ __forceinline__ Chunk<CH> chunk_quant(const Chunk<2 * CH>& c, float inv) {
+  Chunk<CH> o;
+  if constexpr (CH >= 4) {
+#pragma unroll
+    for (int i = 0; i < CH / 4; ++i)
+      o.w[i] = quant2<kBF16, FMT>(c.w[2 * i], inv) | (quant2<kBF16, FMT>(c.w[2 * i + 1], inv) << 16);
+  } else if constexpr (CH == 2) {
+    o.h = static_cast<uint16_t>(quant2<kBF16, FMT>(c.w[0], inv));
+  } else {
+    o.h = static_cast<uint16_t>(quant2<kBF16, FMT>(static_cast<uint32_t>(c.h), inv) & 0xFFu);
+  }
+  return o;
+}
+
+template <int CH, typename IdxT, bool kBF16, int FMT>
+__global__ void __launch_bounds__(kThreads) kv_fp8_dyn_rows(const __grid_constant__ DynParams p) {
+  constexpr int kMaxJ = 4;  // chunks per lane held in registers
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const uint32_t n = p.gseg * p.cps;  // chunks in a group
+  const int64_t seg_in = static_cast<int64_t>(p.cps) * CH * 2;
+
+  if (KV_PREFETCH && p.prefetch && u < p.num_units) {
+    const DynUnit w = dyn_unit(p, u);
+    const DynSide& sd = p.side[w.kv];
+    const uint8_t* base = sd.src + w.token * sd.src_token +
+                          static_cast<int64_t>(w.group) * p.gseg * sd.src_seg;
+    for (uint32_t sg = lane; sg < p.gseg; sg += 32u)
+      prefetch_l2_bulk(base + static_cast<int64_t>(sg) * sd.src_seg, static_cast<uint32_t>(seg_in));
+    if (lane == 0) prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
+  }
+  grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+
+  for (; u < p.num_units; u += nwarps) {
+    const DynUnit w = dyn_unit(p, u);
+    const DynSide& sd = p.side[w.kv];
+    const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
+    const uint8_t* src = sd.src + w.token * sd.src_token +
+                         static_cast<int64_t>(w.group) * p.gseg * sd.src_seg;
+    auto src_of = [&](uint32_t c) {
+      const uint32_t sg = c / p.cps;
+      return src + static_cast<int64_t>(sg) * sd.src_seg + static_cast<int64_t>(c - sg * p.cps) * (2 * CH);
+    };
+    const bool in_regs = n <= 32u * kMaxJ;
+    Chunk<2 * CH> buf[kMaxJ];
+    float amax = 0.0f;
+    if (in_regs) {
+#pragma unroll
+      for (int j = 0; j < kMaxJ; ++j) {
+        const uint32_t c = lane + 32u * j;
+        if (c < n) ld_stream(buf[j], src_of(c));
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxJ; ++j)
+        if (lane + 32u * j < n) amax = chunk_absmax<CH, kBF16>(amax, buf[j]);
+    } else {
+      for (uint32_t c = lane; c < n; c += 32u) {
+        Chunk<2 * CH> t;
+        ld_stream(t, src_of(c));
+        amax = chunk_absmax<CH, kBF16>(amax, t);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (slot < 0 || slot >= p.size_limit) {
+      if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
+      continue;
+    }
+    const bool pos = amax > 0.0f;
+    const float inv = pos ? __fdiv_rn(p.fmax, amax) : 1.0f;
+    uint8_t* dst = sd.dst + paged_offset(slot, p.page_size, sd.dst_page, sd.dst_slot) +
+                   static_cast<int64_t>(w.group) * p.gseg * sd.dst_seg;
+    auto dst_of = [&](uint32_t c) {
+      const uint32_t sg = c / p.cps;
+      return dst + static_cast<int64_t>(sg) * sd.dst_seg + static_cast<int64_t>(c - sg * p.cps) * CH;
+    };
+    if (in_regs) {
+#pragma unroll
+      for (int j = 0; j < kMaxJ; ++j) {
+        const uint32_t c = lane + 32u * j;
+        if (c < n) st_stream(dst_of(c), chunk_quant<CH, kBF16, FMT>(buf[j], inv));
+      }
+    } else {
+      for (uint32_t c = lane; c < n; c += 32u) {
+        Chunk<2 * CH> t;
+        ld_stream(t, src_of(c));
+        st_stream(dst_of(c), chunk_quant<CH, kBF16, FMT>(t, inv));
+      }
+    }
+    if (lane == 0)
+      sd.scales[slot * p.scales_stride + w.group] = pos ? __fdiv_rn(amax, p.fmax) : 1.0f;
+  }
+  if (!KV_EARLY_TRIGGER) grid_dependents_launch();
+}
+
+template <int CH, typename IdxT, int FMT>
+kv_status launch_dyn_fmt(bool bf16, const DynParams& p, cudaStream_t stream) {
+  if (bf16) return launch(kv_fp8_dyn_rows<CH, IdxT, true, FMT>, p.num_units, p, stream);
+  return launch(kv_fp8_dyn_rows<CH, IdxT, false, FMT>, p.num_units, p, stream);
+}
+
+template <int CH, typename IdxT>
+kv_status launch_dyn_ch(int fmt, bool bf16, const DynParams& p, cudaStream_t stream) {
+  if (fmt == kFmtE5M2) return launch_dyn_fmt<CH, IdxT, kFmtE5M2>(bf16, p, stream);
+  return launch_dyn_fmt<CH, IdxT, kFmtE4M3>(bf16, p, stream);
+}
+
+template <typename IdxT>
+kv_status launch_dyn(int ch, int fmt, bool bf16, const DynParams& p, cudaStream_t stream) {
+  switch (ch) {
+    case 8: return launch_dyn_ch<8, IdxT>(fmt, bf16, p, stream);
+    case 4: return launch_dyn_ch<4, IdxT>(fmt, bf16, p, stream);
+    case 2: return launch_dyn_ch<2, IdxT>(fmt, bf16, p, stream);
+    default: return launch_dyn_ch<1, IdxT>(fmt, bf16, p, stream);
+  }
+}
+
+}  // namespace
+}  // namespace kvimpl
+
+using namespace kvimpl;
+
+extern "C" kv_status kv_store_fp8_ex(const void* k, const void* v, void* k_cache, void* v_cache,
+                                     const void* indices, kv_index_dtype index_dtype,
+                                     int64_t index_stride, int64_t num_tokens, int32_t num_heads,
+                                     int32_t head_dim, kv_src_dtype src_dtype, const kv_strides* s,
+                                     int64_t page_size, int64_t kc_page_stride,
+                                     int64_t vc_page_stride, int64_t size_limit,
+                                     kv_fp8_format format, kv_scale_mode scale_mode,
+                                     const float* inv_k_scale, const float* inv_v_scale,
+                                     float* k_scales, float* v_scales, int64_t scales_slot_stride,
+                                     kv_error_record* d_err, kv_stream_t stream_) {
+  if (format != KV_FP8_E4M3FN && format != KV_FP8_E5M2) return KV_ERR_INVALID_ARG;
+  if (scale_mode != KV_SCALE_NONE && scale_mode != KV_SCALE_TENSOR && scale_mode != KV_SCALE_TOKEN &&
+      scale_mode != KV_SCALE_TOKEN_HEAD)
+    return KV_ERR_INVALID_ARG;
+  const int fmt = format == KV_FP8_E5M2 ? kFmtE5M2 : kFmtE4M3;
+  if (scale_mode == KV_SCALE_NONE || scale_mode == KV_SCALE_TENSOR)
+    return store_fp8_static(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_tokens,
+                            num_heads, head_dim, src_dtype, s, page_size, kc_page_stride,
+                            vc_page_stride, size_limit, inv_k_scale, inv_v_scale,
+                            scale_mode == KV_SCALE_TENSOR ? 1 : 0, fmt, d_err, stream_);
+
+  // dynamic scales
+  if (num_tokens < 0) return KV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KV_OK;
+  if (!common_args_ok(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_heads,
+                      head_dim, s, size_limit, d_err))
+    return KV_ERR_INVALID_ARG;
+  if (src_dtype != KV_SRC_F16 && src_dtype != KV_SRC_BF16) return KV_ERR_INVALID_ARG;
+  if (page_size < 1) return KV_ERR_INVALID_ARG;
+  const bool per_head = scale_mode == KV_SCALE_TOKEN_HEAD;
+  if (!k_scales || !v_scales || ((u64(k_scales) | u64(v_scales)) & 3u) != 0) return KV_ERR_INVALID_ARG;
+  if (scales_slot_stride < (per_head ? num_heads : 1)) return KV_ERR_INVALID_ARG;
+  if ((u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token) | u64(s->k_head) | u64(s->v_head)) & 1u)
+    return KV_ERR_INVALID_ARG;
+  if (s->k_dim != 2 || s->v_dim != 2 || s->kc_dim != 1 || s->vc_dim != 1) return KV_ERR_UNSUPPORTED;
+  if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const bool flat = kc_page_stride == page_size * s->kc_slot && vc_page_stride == page_size * s->vc_slot;
+
+  // group layout: per head, or the whole row (one segment when heads are
+  // contiguous on both sides, else one segment per head)
+  const int64_t D = head_dim;
+  const bool merged = !per_head && (num_heads == 1 || (s->k_head == 2 * D && s->v_head == 2 * D &&
+                                                       s->kc_head == D && s->vc_head == D));
+  const uint32_t groups = per_head ? static_cast<uint32_t>(num_heads) : 1u;
+  const uint32_t gseg = (per_head || merged) ? 1u : static_cast<uint32_t>(num_heads);
+  const int64_t seg_elems = merged ? D * num_heads : D;
+  const bool segs_used = !merged;  // head strides address segments
+  uint64_t sbits = u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token);
+  uint64_t dbits = u64(k_cache) | u64(v_cache) | u64(s->kc_slot) | u64(s->vc_slot);
+  if (segs_used) {
+    sbits |= u64(s->k_head) | u64(s->v_head);
+    dbits |= u64(s->kc_head) | u64(s->vc_head);
+  }
+  if (!flat) dbits |= u64(kc_page_stride) | u64(vc_page_stride);
+  // chunk of CH elements: 2*CH input bytes, CH output bytes; prefer enough
+  // chunks per group to keep every lane busy
+  int ch = 1;
+  for (int c = 8; c >= 1; c >>= 1) {
+    const bool ok = seg_elems % c == 0 && (sbits & static_cast<uint64_t>(2 * c - 1)) == 0 &&
+                    (dbits & static_cast<uint64_t>(c - 1)) == 0;
+    if (!ok) continue;
+    ch = c;
+    if (static_cast<int64_t>(gseg) * (seg_elems / c) >= 32) break;
+  }
+
+  DynParams p = {};
+  p.side[0] = DynSide{static_cast<const uint8_t*>(k), static_cast<uint8_t*>(k_cache), s->k_token,
+                      s->k_head, s->kc_slot, s->kc_head, flat ? s->kc_slot : kc_page_stride,
+                      k_scales};
+  p.side[1] = DynSide{static_cast<const uint8_t*>(v), static_cast<uint8_t*>(v_cache), s->v_token,
+                      s->v_head, s->vc_slot, s->vc_head, flat ? s->vc_slot : vc_page_stride,
+                      v_scales};
+  p.indices = indices;
+  p.index_stride = index_stride;
+  p.size_limit = size_limit;
+  p.page_size = flat ? 1 : page_size;
+  p.scales_stride = scales_slot_stride;
+  p.groups = groups;
+  p.gseg = gseg;
+  p.cps = static_cast<uint32_t>(seg_elems / ch);
+  p.num_units = static_cast<uint64_t>(num_tokens) * 2u * groups;
+  p.fmax = fmt == kFmtE5M2 ? 57344.0f : 448.0f;
+  p.err = d_err;
+  p.prefetch = ((sbits & 15u) == 0 && (seg_elems * 2) % 16 == 0) ? 1 : 0;
+  const bool bf16 = src_dtype == KV_SRC_BF16;
+  return index_dtype == KV_INDEX_I64 ? launch_dyn<int64_t>(ch, fmt, bf16, p, stream)
+                                     : launch_dyn<int32_t>(ch, fmt, bf16, p, stream);
+}

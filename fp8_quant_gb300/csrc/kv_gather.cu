@@ -21,7 +21,8 @@ struct GatherSide {
   uint8_t* out;          // element (0, 0, 0) of the token-major output
   int64_t cache_slot, cache_seg, cache_page;
   int64_t out_token, out_seg;
-  const float* scale;    // fp8 only: device scalar, or nullptr (scale 1)
+  const float* scale;    // fp8, per-tensor mode: device scalar
+  const float* scales;   // fp8, per-token / per-head modes: per-slot scale cache
 };
 
 struct GatherParams {
@@ -30,9 +31,22 @@ struct GatherParams {
   int64_t index_stride, size_limit, page_size;
   UnitShape shape;
   kv_error_record* err;
-  int vec;       // cache bytes per chunk
-  int prefetch;  // cache rows are 16-byte aligned: speculative L2 prefetch allowed
+  int vec;          // cache bytes per chunk
+  int prefetch;     // cache rows are 16-byte aligned: speculative L2 prefetch allowed
+  int scale_mode;   // fp8: kv_scale_mode (per-head mode: one head per unit segment)
+  int64_t scales_stride;
 };
+
+// Dequantisation multiplier of a unit (fp8 gathers).
+__device__ __forceinline__ float unit_scale(const GatherParams& p, const GatherSide& sd,
+                                            int64_t slot, uint32_t seg) {
+  switch (p.scale_mode) {
+    case KV_SCALE_TENSOR: return __ldg(sd.scale);
+    case KV_SCALE_TOKEN: return __ldg(sd.scales + slot * p.scales_stride);
+    case KV_SCALE_TOKEN_HEAD: return __ldg(sd.scales + slot * p.scales_stride + seg);
+    default: return 1.0f;
+  }
+}
 
 
 // Slot id read before the programmatic-launch wait, at L2 only (no L1 line
@@ -132,12 +146,18 @@ __global__ void __launch_bounds__(kThreads) kv_gather_rows(const __grid_constant
 // FP8 dequantising gather
 // ---------------------------------------------------------------------------
 
-// Two e4m3fn codes (lo in bits 0-7) to two fp32 values, exactly: every e4m3fn
-// value is an fp16 value, and fp16 widens exactly to fp32.
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t codes16) {
+// Two FP8 codes (lo in bits 0-7) to two fp32 values, exactly.  Every e4m3fn
+// value is an fp16 value (hardware conversion); an e5m2 code is the top byte
+// of the fp16 with the same value; fp16 widens exactly to fp32.
+template <int FMT>
+__device__ __forceinline__ float2 fp8x2_to_f32x2(uint32_t codes16) {
   uint32_t h2;
-  const uint16_t c = static_cast<uint16_t>(codes16);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  if constexpr (FMT == kFmtE5M2) {
+    h2 = ((codes16 & 0xFFu) << 8) | ((codes16 & 0xFF00u) << 16);
+  } else {
+    const uint16_t c = static_cast<uint16_t>(codes16);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  }
   return make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu))),
                      __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16))));
 }
@@ -155,27 +175,27 @@ __device__ __forceinline__ uint32_t narrow2(float lo, float hi) {
 }
 
 // Four codes (one 32-bit word) to four 2-byte outputs (two words).
-template <bool kBF16>
+template <bool kBF16, int FMT>
 __device__ __forceinline__ void dequant4(uint32_t codes, float scale, uint32_t& o0, uint32_t& o1) {
-  const float2 a = e4m3x2_to_f32x2(codes & 0xFFFFu);
-  const float2 b = e4m3x2_to_f32x2(codes >> 16);
+  const float2 a = fp8x2_to_f32x2<FMT>(codes & 0xFFFFu);
+  const float2 b = fp8x2_to_f32x2<FMT>(codes >> 16);
   o0 = narrow2<kBF16>(__fmul_rn(a.x, scale), __fmul_rn(a.y, scale));
   o1 = narrow2<kBF16>(__fmul_rn(b.x, scale), __fmul_rn(b.y, scale));
 }
 
 // IN cache bytes (codes) per lane chunk -> 2*IN output bytes.
-template <int IN, int U, typename IdxT, bool kBF16>
+template <int IN, int U, typename IdxT, bool kBF16, int FMT>
 __device__ __forceinline__ void gather_fp8_unit(const GatherParams& p, const Unit& w,
                                                 uint32_t lane) {
   const uint32_t nchunks = p.shape.part_chunks;
   const int64_t part_in = static_cast<int64_t>(nchunks) * IN;
   const GatherSide& sd = p.side[w.kv];
   const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
-  const float scale = sd.scale != nullptr ? __ldg(sd.scale) : 1.0f;
   if (slot < 0 || slot >= p.size_limit) {
     if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
     return;
   }
+  const float scale = unit_scale(p, sd, slot, w.seg);
   const uint8_t* src = sd.cache + gather_slot_offset(p, sd, slot) +
                        static_cast<int64_t>(w.seg) * sd.cache_seg +
                        static_cast<int64_t>(w.part) * part_in;
@@ -197,11 +217,12 @@ __device__ __forceinline__ void gather_fp8_unit(const GatherParams& p, const Uni
       if constexpr (IN >= 4) {
         Chunk<2 * IN> out;
 #pragma unroll
-        for (int i = 0; i < kWords; ++i) dequant4<kBF16>(buf[j].w[i], scale, out.w[2 * i], out.w[2 * i + 1]);
+        for (int i = 0; i < kWords; ++i)
+          dequant4<kBF16, FMT>(buf[j].w[i], scale, out.w[2 * i], out.w[2 * i + 1]);
         st_stream(o, out);
       } else {
         static_assert(IN == 2, "IN");
-        const float2 a = e4m3x2_to_f32x2(buf[j].h);
+        const float2 a = fp8x2_to_f32x2<FMT>(buf[j].h);
         Chunk<4> out;
         out.w[0] = narrow2<kBF16>(__fmul_rn(a.x, scale), __fmul_rn(a.y, scale));
         st_stream(o, out);
@@ -210,7 +231,7 @@ __device__ __forceinline__ void gather_fp8_unit(const GatherParams& p, const Uni
   }
 }
 
-template <int IN, int U, typename IdxT, bool kBF16>
+template <int IN, int U, typename IdxT, bool kBF16, int FMT>
 __global__ void __launch_bounds__(kThreads) kv_gather_fp8_rows(const __grid_constant__ GatherParams p) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
@@ -224,7 +245,7 @@ __global__ void __launch_bounds__(kThreads) kv_gather_fp8_rows(const __grid_cons
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
   while (u < p.shape.num_units) {
-    gather_fp8_unit<IN, U, IdxT, kBF16>(p, w, lane);
+    gather_fp8_unit<IN, U, IdxT, kBF16, FMT>(p, w, lane);
     u += nwarps;
     if (u >= p.shape.num_units) break;
     w = decode_unit(p.shape, u);
@@ -240,14 +261,16 @@ struct GatherElemParams {
   int64_t cache_slot[2], cache_head[2], cache_dim[2], cache_page[2];
   int64_t out_token[2], out_head[2], out_dim[2];
   const float* scale[2];
+  const float* scales[2];
   const void* indices;
-  int64_t index_stride, size_limit, page_size;
+  int64_t index_stride, size_limit, page_size, scales_stride;
   uint64_t num_units;
   int32_t num_heads, head_dim, elem_bytes;  // elem_bytes: copy only
+  int scale_mode;                           // fp8 only
   kv_error_record* err;
 };
 
-template <typename IdxT, int kMode>  // kMode: 0 copy, 1 fp8 -> bf16, 2 fp8 -> fp16
+template <typename IdxT, int kMode, int FMT>  // kMode: 0 copy, 1 fp8 -> bf16, 2 fp8 -> fp16
 __global__ void __launch_bounds__(kThreads) kv_gather_elements(const __grid_constant__ GatherElemParams p) {
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
@@ -274,14 +297,20 @@ __global__ void __launch_bounds__(kThreads) kv_gather_elements(const __grid_cons
     }
     const uint8_t* src = p.cache[kv] + row + h * p.cache_head[kv];
     uint8_t* dst = p.out[kv] + t * p.out_token[kv] + h * p.out_head[kv];
-    const float scale = (kMode != 0 && p.scale[kv] != nullptr) ? __ldg(p.scale[kv]) : 1.0f;
+    float scale = 1.0f;
+    if (kMode != 0) {
+      if (p.scale_mode == KV_SCALE_TENSOR) scale = __ldg(p.scale[kv]);
+      else if (p.scale_mode == KV_SCALE_TOKEN) scale = __ldg(p.scales[kv] + slot * p.scales_stride);
+      else if (p.scale_mode == KV_SCALE_TOKEN_HEAD)
+        scale = __ldg(p.scales[kv] + slot * p.scales_stride + h);
+    }
     for (int64_t d = lane; d < p.head_dim; d += 32) {
       const uint8_t* s = src + d * p.cache_dim[kv];
       uint8_t* o = dst + d * p.out_dim[kv];
       if constexpr (kMode == 0) {
         for (int b = 0; b < p.elem_bytes; ++b) o[b] = __ldg(s + b);
       } else {
-        const float2 x = e4m3x2_to_f32x2(__ldg(s));
+        const float2 x = fp8x2_to_f32x2<FMT>(__ldg(s));
         const uint32_t v = narrow2<kMode == 1>(__fmul_rn(x.x, scale), 0.0f);
         o[0] = static_cast<uint8_t>(v & 0xFFu);
         o[1] = static_cast<uint8_t>((v >> 8) & 0xFFu);
@@ -311,28 +340,40 @@ kv_status launch_gather(int vec, const GatherParams& p, cudaStream_t stream) {
   }
 }
 
-template <int IN, typename IdxT>
-kv_status launch_gather_fp8_in(bool bf16, const GatherParams& p, cudaStream_t stream) {
+template <int IN, typename IdxT, int FMT>
+kv_status launch_gather_fp8_fmt(bool bf16, const GatherParams& p, cudaStream_t stream) {
   constexpr int U = IN == 16 ? 2 : 4;
-  if (bf16) return launch(kv_gather_fp8_rows<IN, U, IdxT, true>, p.shape.num_units, p, stream);
-  return launch(kv_gather_fp8_rows<IN, U, IdxT, false>, p.shape.num_units, p, stream);
+  if (bf16) return launch(kv_gather_fp8_rows<IN, U, IdxT, true, FMT>, p.shape.num_units, p, stream);
+  return launch(kv_gather_fp8_rows<IN, U, IdxT, false, FMT>, p.shape.num_units, p, stream);
+}
+
+template <int IN, typename IdxT>
+kv_status launch_gather_fp8_in(int fmt, bool bf16, const GatherParams& p, cudaStream_t stream) {
+  if (fmt == kFmtE5M2) return launch_gather_fp8_fmt<IN, IdxT, kFmtE5M2>(bf16, p, stream);
+  return launch_gather_fp8_fmt<IN, IdxT, kFmtE4M3>(bf16, p, stream);
 }
 
 template <typename IdxT>
-kv_status launch_gather_fp8(int in, bool bf16, const GatherParams& p, cudaStream_t stream) {
+kv_status launch_gather_fp8(int in, int fmt, bool bf16, const GatherParams& p, cudaStream_t stream) {
   switch (in) {
-    case 16: return launch_gather_fp8_in<16, IdxT>(bf16, p, stream);
-    case 8: return launch_gather_fp8_in<8, IdxT>(bf16, p, stream);
-    case 4: return launch_gather_fp8_in<4, IdxT>(bf16, p, stream);
-    default: return launch_gather_fp8_in<2, IdxT>(bf16, p, stream);
+    case 16: return launch_gather_fp8_in<16, IdxT>(fmt, bf16, p, stream);
+    case 8: return launch_gather_fp8_in<8, IdxT>(fmt, bf16, p, stream);
+    case 4: return launch_gather_fp8_in<4, IdxT>(fmt, bf16, p, stream);
+    default: return launch_gather_fp8_in<2, IdxT>(fmt, bf16, p, stream);
   }
 }
 
+template <typename IdxT, int FMT>
+kv_status launch_gather_elements_fmt(int mode, const GatherElemParams& g, cudaStream_t stream) {
+  if (mode == 0) return launch(kv_gather_elements<IdxT, 0, FMT>, g.num_units, g, stream);
+  if (mode == 1) return launch(kv_gather_elements<IdxT, 1, FMT>, g.num_units, g, stream);
+  return launch(kv_gather_elements<IdxT, 2, FMT>, g.num_units, g, stream);
+}
+
 template <typename IdxT>
-kv_status launch_gather_elements(int mode, const GatherElemParams& g, cudaStream_t stream) {
-  if (mode == 0) return launch(kv_gather_elements<IdxT, 0>, g.num_units, g, stream);
-  if (mode == 1) return launch(kv_gather_elements<IdxT, 1>, g.num_units, g, stream);
-  return launch(kv_gather_elements<IdxT, 2>, g.num_units, g, stream);
+kv_status launch_gather_elements(int mode, int fmt, const GatherElemParams& g, cudaStream_t stream) {
+  if (fmt == kFmtE5M2) return launch_gather_elements_fmt<IdxT, kFmtE5M2>(mode, g, stream);
+  return launch_gather_elements_fmt<IdxT, kFmtE4M3>(mode, g, stream);
 }
 
 GatherElemParams element_params(const void* k_cache, const void* v_cache, void* k_out, void* v_out,
@@ -387,8 +428,8 @@ extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k
     GatherElemParams g = element_params(k_cache, v_cache, k_out, v_out, indices, index_stride,
                                         num_tokens, num_heads, head_dim, s, size_limit, d_err);
     g.elem_bytes = elem_bytes;
-    return i64 ? launch_gather_elements<int64_t>(0, g, stream)
-               : launch_gather_elements<int32_t>(0, g, stream);
+    return i64 ? launch_gather_elements<int64_t>(0, kFmtE4M3, g, stream)
+               : launch_gather_elements<int32_t>(0, kFmtE4M3, g, stream);
   }
   const int64_t head_bytes = static_cast<int64_t>(head_dim) * elem_bytes;
   const Segments sg = segments(num_heads, head_dim, head_bytes, head_bytes, s);
@@ -407,9 +448,9 @@ extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k
 
   GatherParams p = {};
   p.side[0] = GatherSide{static_cast<const uint8_t*>(k_cache), static_cast<uint8_t*>(k_out),
-                         s->kc_slot, s->kc_head, s->kc_slot, s->k_token, s->k_head, nullptr};
+                         s->kc_slot, s->kc_head, s->kc_slot, s->k_token, s->k_head, nullptr, nullptr};
   p.side[1] = GatherSide{static_cast<const uint8_t*>(v_cache), static_cast<uint8_t*>(v_out),
-                         s->vc_slot, s->vc_head, s->vc_slot, s->v_token, s->v_head, nullptr};
+                         s->vc_slot, s->vc_head, s->vc_slot, s->v_token, s->v_head, nullptr, nullptr};
   p.indices = indices;
   p.index_stride = index_stride;
   p.size_limit = size_limit;
@@ -425,14 +466,17 @@ extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k
   return i64 ? launch_gather<int64_t>(vec, p, stream) : launch_gather<int32_t>(vec, p, stream);
 }
 
-extern "C" kv_status kv_gather_fp8(const void* k_cache, const void* v_cache, void* k_out,
-                                   void* v_out, const void* indices, kv_index_dtype index_dtype,
-                                   int64_t index_stride, int64_t num_tokens, int32_t num_heads,
-                                   int32_t head_dim, kv_src_dtype out_dtype, const kv_strides* s,
-                                   int64_t page_size, int64_t kc_page_stride,
-                                   int64_t vc_page_stride, int64_t size_limit,
-                                   const float* k_scale, const float* v_scale, int32_t use_scale,
-                                   kv_error_record* d_err, kv_stream_t stream_) {
+namespace {
+
+// kv_gather_fp8 and kv_gather_fp8_ex.
+kv_status gather_fp8(const void* k_cache, const void* v_cache, void* k_out, void* v_out,
+                     const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
+                     int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                     kv_src_dtype out_dtype, const kv_strides* s, int64_t page_size,
+                     int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit, int fmt,
+                     int scale_mode, const float* k_scale, const float* v_scale,
+                     const float* k_scales, const float* v_scales, int64_t scales_stride,
+                     kv_error_record* d_err, kv_stream_t stream_) {
   if (num_tokens < 0) return KV_ERR_INVALID_ARG;
   if (num_tokens == 0) return KV_OK;
   if (!common_args_ok(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
@@ -440,8 +484,13 @@ extern "C" kv_status kv_gather_fp8(const void* k_cache, const void* v_cache, voi
     return KV_ERR_INVALID_ARG;
   if (out_dtype != KV_SRC_F16 && out_dtype != KV_SRC_BF16) return KV_ERR_INVALID_ARG;
   if (page_size < 1) return KV_ERR_INVALID_ARG;
-  if (use_scale && (!k_scale || !v_scale)) return KV_ERR_INVALID_ARG;
-  if (use_scale && ((u64(k_scale) | u64(v_scale)) & 3u) != 0) return KV_ERR_INVALID_ARG;
+  if (scale_mode == KV_SCALE_TENSOR &&
+      (!k_scale || !v_scale || ((u64(k_scale) | u64(v_scale)) & 3u) != 0))
+    return KV_ERR_INVALID_ARG;
+  const bool per_slot = scale_mode == KV_SCALE_TOKEN || scale_mode == KV_SCALE_TOKEN_HEAD;
+  if (per_slot && (!k_scales || !v_scales || ((u64(k_scales) | u64(v_scales)) & 3u) != 0 ||
+                   scales_stride < (scale_mode == KV_SCALE_TOKEN_HEAD ? num_heads : 1)))
+    return KV_ERR_INVALID_ARG;
   const uint64_t out_bits = u64(k_out) | u64(v_out) | u64(s->k_token) | u64(s->v_token) |
                             u64(s->k_head) | u64(s->v_head) | u64(s->k_dim) | u64(s->v_dim);
   if ((out_bits & 1u) != 0) return KV_ERR_INVALID_ARG;
@@ -449,8 +498,8 @@ extern "C" kv_status kv_gather_fp8(const void* k_cache, const void* v_cache, voi
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const bool i64 = index_dtype == KV_INDEX_I64;
   const bool bf16 = out_dtype == KV_SRC_BF16;
-  const float* sk = use_scale ? k_scale : nullptr;
-  const float* sv = use_scale ? v_scale : nullptr;
+  const float* sk = scale_mode == KV_SCALE_TENSOR ? k_scale : nullptr;
+  const float* sv = scale_mode == KV_SCALE_TENSOR ? v_scale : nullptr;
   const bool flat = kc_page_stride == page_size * s->kc_slot && vc_page_stride == page_size * s->vc_slot;
   const bool contiguous = s->k_dim == 2 && s->v_dim == 2 && s->kc_dim == 1 && s->vc_dim == 1;
 
@@ -458,6 +507,8 @@ extern "C" kv_status kv_gather_fp8(const void* k_cache, const void* v_cache, voi
   int in = 1;
   if (contiguous) {
     sg = segments(num_heads, head_dim, 2 * static_cast<int64_t>(head_dim), head_dim, s);
+    if (scale_mode == KV_SCALE_TOKEN_HEAD)  // one head per unit: its segment index is the head
+      sg = Segments{static_cast<uint32_t>(num_heads), static_cast<int64_t>(head_dim)};
     uint64_t cache_bits = u64(k_cache) | u64(v_cache) | u64(s->kc_slot) | u64(s->vc_slot) |
                           u64(sg.elems);
     uint64_t obits = u64(k_out) | u64(v_out) | u64(s->k_token) | u64(s->v_token);
@@ -482,8 +533,12 @@ extern "C" kv_status kv_gather_fp8(const void* k_cache, const void* v_cache, voi
     g.page_size = flat ? 1 : page_size;
     g.scale[0] = sk;
     g.scale[1] = sv;
-    return i64 ? launch_gather_elements<int64_t>(bf16 ? 1 : 2, g, stream)
-               : launch_gather_elements<int32_t>(bf16 ? 1 : 2, g, stream);
+    g.scales[0] = k_scales;
+    g.scales[1] = v_scales;
+    g.scales_stride = scales_stride;
+    g.scale_mode = scale_mode;
+    return i64 ? launch_gather_elements<int64_t>(bf16 ? 1 : 2, fmt, g, stream)
+               : launch_gather_elements<int32_t>(bf16 ? 1 : 2, fmt, g, stream);
   }
 
   int sms = 0;
@@ -496,10 +551,10 @@ extern "C" kv_status kv_gather_fp8(const void* k_cache, const void* v_cache, voi
   GatherParams p = {};
   p.side[0] = GatherSide{static_cast<const uint8_t*>(k_cache), static_cast<uint8_t*>(k_out),
                          s->kc_slot, s->kc_head, flat ? s->kc_slot : kc_page_stride, s->k_token,
-                         s->k_head, sk};
+                         s->k_head, sk, k_scales};
   p.side[1] = GatherSide{static_cast<const uint8_t*>(v_cache), static_cast<uint8_t*>(v_out),
                          s->vc_slot, s->vc_head, flat ? s->vc_slot : vc_page_stride, s->v_token,
-                         s->v_head, sv};
+                         s->v_head, sv, v_scales};
   p.indices = indices;
   p.index_stride = index_stride;
   p.size_limit = size_limit;
@@ -512,6 +567,47 @@ extern "C" kv_status kv_gather_fp8(const void* k_cache, const void* v_cache, voi
   p.err = d_err;
   p.vec = in;
   p.prefetch = in >= 16 ? 1 : 0;
-  return i64 ? launch_gather_fp8<int64_t>(in, bf16, p, stream)
-             : launch_gather_fp8<int32_t>(in, bf16, p, stream);
+  p.scale_mode = scale_mode;
+  p.scales_stride = scales_stride;
+  return i64 ? launch_gather_fp8<int64_t>(in, fmt, bf16, p, stream)
+             : launch_gather_fp8<int32_t>(in, fmt, bf16, p, stream);
+}
+
+}  // namespace
+
+extern "C" kv_status kv_gather_fp8(const void* k_cache, const void* v_cache, void* k_out,
+                                   void* v_out, const void* indices, kv_index_dtype index_dtype,
+                                   int64_t index_stride, int64_t num_tokens, int32_t num_heads,
+                                   int32_t head_dim, kv_src_dtype out_dtype, const kv_strides* s,
+                                   int64_t page_size, int64_t kc_page_stride,
+                                   int64_t vc_page_stride, int64_t size_limit,
+                                   const float* k_scale, const float* v_scale, int32_t use_scale,
+                                   kv_error_record* d_err, kv_stream_t stream) {
+  return gather_fp8(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
+                    num_tokens, num_heads, head_dim, out_dtype, s, page_size, kc_page_stride,
+                    vc_page_stride, size_limit, kFmtE4M3,
+                    use_scale ? KV_SCALE_TENSOR : KV_SCALE_NONE, k_scale, v_scale, nullptr,
+                    nullptr, 0, d_err, stream);
+}
+
+extern "C" kv_status kv_gather_fp8_ex(const void* k_cache, const void* v_cache, void* k_out,
+                                      void* v_out, const void* indices, kv_index_dtype index_dtype,
+                                      int64_t index_stride, int64_t num_tokens, int32_t num_heads,
+                                      int32_t head_dim, kv_src_dtype out_dtype,
+                                      const kv_strides* s, int64_t page_size,
+                                      int64_t kc_page_stride, int64_t vc_page_stride,
+                                      int64_t size_limit, kv_fp8_format format,
+                                      kv_scale_mode scale_mode, const float* k_scale,
+                                      const float* v_scale, const float* k_scales,
+                                      const float* v_scales, int64_t scales_slot_stride,
+                                      kv_error_record* d_err, kv_stream_t stream) {
+  if (format != KV_FP8_E4M3FN && format != KV_FP8_E5M2) return KV_ERR_INVALID_ARG;
+  if (scale_mode != KV_SCALE_NONE && scale_mode != KV_SCALE_TENSOR && scale_mode != KV_SCALE_TOKEN &&
+      scale_mode != KV_SCALE_TOKEN_HEAD)
+    return KV_ERR_INVALID_ARG;
+  return gather_fp8(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
+                    num_tokens, num_heads, head_dim, out_dtype, s, page_size, kc_page_stride,
+                    vc_page_stride, size_limit, format == KV_FP8_E5M2 ? kFmtE5M2 : kFmtE4M3,
+                    scale_mode, k_scale, v_scale, k_scales, v_scales, scales_slot_stride, d_err,
+                    stream);
 }

@@ -14,6 +14,16 @@ namespace kvimpl {
 extern thread_local int g_last_cuda_error;
 
 kv_status cuda_fail(cudaError_t e);
+
+// The FP8 write with a per-tensor inverse scale (or none) in format fmt
+// (kFmtE4M3 / kFmtE5M2): kv_store_fp8 and the static modes of kv_store_fp8_ex.
+kv_status store_fp8_static(const void* k, const void* v, void* k_cache, void* v_cache,
+                           const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
+                           int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                           kv_src_dtype src_dtype, const kv_strides* s, int64_t page_size,
+                           int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
+                           const float* inv_k_scale, const float* inv_v_scale, int32_t use_scale,
+                           int fmt, kv_error_record* d_err, kv_stream_t stream);
 kv_status current_sm_count(int* out);
 kv_status blocks_per_sm(const void* fn, int* out);
 

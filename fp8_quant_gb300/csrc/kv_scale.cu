@@ -7,10 +7,10 @@
 //                  ignored) and inv = fp8_max / amax (1 when amax is 0), the
 //                  per-tensor inverse scale kv_store_fp8 consumes.
 //
-// The absmax pass is a pure HBM read stream: warps reduce their rows in
-// registers, CTAs reduce their warps in shared memory, and one atomicMax per
-// CTA and tensor lands on the float bits of the caller's amax output (for
-// non-negative floats the bit patterns order like the values).
+// The absmax pass is a pure HBM read stream: one warp per row with all of the
+// row's loads in flight, CTAs reduce their warps in shared memory, and one
+// atomicMax per CTA and tensor lands on the float bits of the caller's amax
+// output (for non-negative floats the bit patterns order like the values).
 #include "kv_host.h"
 
 namespace kvimpl {
@@ -44,7 +44,9 @@ __device__ __forceinline__ float absmax2(float m, uint32_t w) {
   return fmaxf(m, fmaxf(fabsf(x.x), fabsf(x.y)));
 }
 
-template <int VEC, bool kBF16>
+// One warp per (token, K|V, segment) unit; a lane issues up to U vector loads
+// of the unit before it reduces them, so a warp keeps 32*U*VEC bytes in flight.
+template <int VEC, int U, bool kBF16>
 __global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant__ AbsmaxParams p) {
   __shared__ float part[2][kWarpsPerCta];
   grid_dependency_wait();
@@ -59,14 +61,23 @@ __global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant
     const Unit w = decode_unit(p.shape, u);
     const uint8_t* src = p.src[w.kv] + w.token * p.token[w.kv] + static_cast<int64_t>(w.seg) * p.seg[w.kv];
     float acc = 0.0f;
-    for (uint32_t c = lane; c < nchunks; c += 32u) {
-      Chunk<VEC> ch;
-      ld_stream(ch, src + static_cast<size_t>(c) * VEC);
-      if constexpr (VEC >= 4) {
+    for (uint32_t c0 = 0; c0 < nchunks; c0 += 32u * U) {
+      Chunk<VEC> ch[U];
 #pragma unroll
-        for (int i = 0; i < VEC / 4; ++i) acc = absmax2<kBF16>(acc, ch.w[i]);
-      } else {
-        acc = absmax2<kBF16>(acc, static_cast<uint32_t>(ch.h));   // upper element is 0
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + lane + 32u * j;
+        if (c < nchunks) ld_stream(ch[j], src + static_cast<size_t>(c) * VEC);
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + lane + 32u * j;
+        if (c >= nchunks) continue;
+        if constexpr (VEC >= 4) {
+#pragma unroll
+          for (int i = 0; i < VEC / 4; ++i) acc = absmax2<kBF16>(acc, ch[j].w[i]);
+        } else {
+          acc = absmax2<kBF16>(acc, static_cast<uint32_t>(ch[j].h));   // upper element is 0
+        }
       }
     }
     m[w.kv] = fmaxf(m[w.kv], acc);
@@ -102,9 +113,10 @@ __global__ void __launch_bounds__(kThreads) kv_absmax_finish(const __grid_consta
 }
 
 template <int VEC>
-kv_status launch_absmax(bool bf16, const AbsmaxParams& p, cudaStream_t stream, uint64_t max_ctas) {
-  if (bf16) return launch(kv_absmax_rows<VEC, true>, p.shape.num_units, p, stream, max_ctas);
-  return launch(kv_absmax_rows<VEC, false>, p.shape.num_units, p, stream, max_ctas);
+kv_status launch_absmax(bool bf16, const AbsmaxParams& p, cudaStream_t stream) {
+  constexpr int U = VEC == 32 ? 2 : 4;
+  if (bf16) return launch(kv_absmax_rows<VEC, U, true>, p.shape.num_units, p, stream);
+  return launch(kv_absmax_rows<VEC, U, false>, p.shape.num_units, p, stream);
 }
 
 }  // namespace
@@ -144,8 +156,7 @@ extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype sr
     const int64_t seg_bytes = merged ? head_bytes * num_heads : head_bytes;
     uint64_t bits = u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token) | u64(seg_bytes);
     if (!merged) bits |= u64(s->k_head) | u64(s->v_head);
-    int vec = pow2_align(bits);
-    if (vec > 16) vec = 16;
+    const int vec = pow2_align(bits);
     AbsmaxParams p = {};
     p.src[0] = static_cast<const uint8_t*>(k);
     p.src[1] = static_cast<const uint8_t*>(v);
@@ -159,17 +170,17 @@ extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype sr
     p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
     p.shape.part_chunks = static_cast<uint32_t>(seg_bytes / vec);
     p.amax_bits = reinterpret_cast<unsigned int*>(amax);
-    int sms = 0;
-    kv_status st = current_sm_count(&sms);
-    if (st != KV_OK) return st;
-    // a few CTAs per SM keep the stream saturated with one atomic per CTA
-    const uint64_t max_ctas = static_cast<uint64_t>(sms) * 4u;
+    // one warp per row (one atomic per CTA and tensor)
     const bool bf16 = src_dtype == KV_SRC_BF16;
+    kv_status st;
     switch (vec) {
-      case 16: st = launch_absmax<16>(bf16, p, stream, max_ctas); break;
-      case 8: st = launch_absmax<8>(bf16, p, stream, max_ctas); break;
-      case 4: st = launch_absmax<4>(bf16, p, stream, max_ctas); break;
-      default: st = launch_absmax<2>(bf16, p, stream, max_ctas); break;
+#if KV_MAX_VEC >= 32
+      case 32: st = launch_absmax<32>(bf16, p, stream); break;
+#endif
+      case 16: st = launch_absmax<16>(bf16, p, stream); break;
+      case 8: st = launch_absmax<8>(bf16, p, stream); break;
+      case 4: st = launch_absmax<4>(bf16, p, stream); break;
+      default: st = launch_absmax<2>(bf16, p, stream); break;
     }
     if (st != KV_OK) return st;
   }

@@ -209,17 +209,17 @@ __device__ __forceinline__ void ld_in(Fp8Chunk<OUT>& c, const uint8_t* p) {
   }
 }
 
-template <int OUT, bool kBF16>
+template <int OUT, bool kBF16, int FMT>
 __device__ __forceinline__ void quant_store(uint8_t* p, const Fp8Chunk<OUT>& c, float inv) {
   if constexpr (OUT >= 4) {
     Chunk<OUT> o;
 #pragma unroll
     for (int i = 0; i < OUT / 4; ++i)
-      o.w[i] = quant2<kBF16>(c.in[2 * i], inv) | (quant2<kBF16>(c.in[2 * i + 1], inv) << 16);
+      o.w[i] = quant2<kBF16, FMT>(c.in[2 * i], inv) | (quant2<kBF16, FMT>(c.in[2 * i + 1], inv) << 16);
     st_stream(p, o);
   } else {
     Chunk<2> o;
-    o.h = static_cast<uint16_t>(quant2<kBF16>(c.in[0], inv));
+    o.h = static_cast<uint16_t>(quant2<kBF16, FMT>(c.in[0], inv));
     st_stream(p, o);
   }
 }
@@ -243,7 +243,7 @@ struct Fp8Params {
 };
 
 
-template <int OUT, int U, typename IdxT, bool kBF16>
+template <int OUT, int U, typename IdxT, bool kBF16, int FMT>
 __device__ __forceinline__ void fp8_unit(const Fp8Params& p, const Unit& w, const uint8_t* src,
                                          uint32_t lane) {
   const uint32_t nchunks = p.shape.part_chunks;
@@ -266,7 +266,7 @@ __device__ __forceinline__ void fp8_unit(const Fp8Params& p, const Unit& w, cons
 #pragma unroll
   for (int j = 0; j < U; ++j) {
     const uint32_t c = lane + 32u * j;
-    if (c < nchunks) quant_store<OUT, kBF16>(dst + static_cast<size_t>(c) * OUT, buf[j], inv);
+    if (c < nchunks) quant_store<OUT, kBF16, FMT>(dst + static_cast<size_t>(c) * OUT, buf[j], inv);
   }
   for (uint32_t c0 = 32u * U; c0 < nchunks; c0 += 32u * U) {
 #pragma unroll
@@ -277,7 +277,7 @@ __device__ __forceinline__ void fp8_unit(const Fp8Params& p, const Unit& w, cons
 #pragma unroll
     for (int j = 0; j < U; ++j) {
       const uint32_t c = c0 + lane + 32u * j;
-      if (c < nchunks) quant_store<OUT, kBF16>(dst + static_cast<size_t>(c) * OUT, buf[j], inv);
+      if (c < nchunks) quant_store<OUT, kBF16, FMT>(dst + static_cast<size_t>(c) * OUT, buf[j], inv);
     }
   }
 }
@@ -288,7 +288,7 @@ __device__ __forceinline__ const uint8_t* fp8_src(const Fp8Params& p, const Unit
          static_cast<int64_t>(w.part) * p.shape.part_chunks * 2 * static_cast<int64_t>(p.vec);
 }
 
-template <int OUT, int U, typename IdxT, bool kBF16>
+template <int OUT, int U, typename IdxT, bool kBF16, int FMT>
 __global__ void __launch_bounds__(kThreads) kv_fp8_rows(const __grid_constant__ Fp8Params p) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_rows(const __grid_constant__ 
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
 
   while (u < p.shape.num_units) {
-    fp8_unit<OUT, U, IdxT, kBF16>(p, w, src, lane);
+    fp8_unit<OUT, U, IdxT, kBF16, FMT>(p, w, src, lane);
     u += nwarps;
     if (u >= p.shape.num_units) break;
     w = decode_unit(p.shape, u);
@@ -329,7 +329,7 @@ struct GenericFp8Params {
   kv_error_record* err;
 };
 
-template <typename IdxT, bool kBF16>
+template <typename IdxT, bool kBF16, int FMT>
 __global__ void __launch_bounds__(kThreads) kv_fp8_elements(const __grid_constant__ GenericFp8Params p) {
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_elements(const __grid_constan
                    h * p.dst_head[kv];
     for (int64_t d = lane; d < p.head_dim; d += 32) {
       const uint32_t bits = __ldg(reinterpret_cast<const unsigned short*>(src + d * p.src_dim[kv]));
-      dst[d * p.dst_dim[kv]] = static_cast<uint8_t>(quant2<kBF16>(bits, inv) & 0xFFu);
+      dst[d * p.dst_dim[kv]] = static_cast<uint8_t>(quant2<kBF16, FMT>(bits, inv) & 0xFFu);
     }
   }
   if (!KV_EARLY_TRIGGER) grid_dependents_launch();
@@ -439,24 +439,42 @@ kv_status launch_copy(int vec, const CopyParams& p, cudaStream_t stream) {
   }
 }
 
-template <int OUT, typename IdxT>
-kv_status launch_fp8_out(bool bf16, const Fp8Params& p, cudaStream_t stream) {
+template <int OUT, typename IdxT, int FMT>
+kv_status launch_fp8_fmt(bool bf16, const Fp8Params& p, cudaStream_t stream) {
   constexpr int U = OUT == 32 ? 1 : OUT == 16 ? KV_FP8_UNROLL : 4;
-  if (bf16) return launch(kv_fp8_rows<OUT, U, IdxT, true>, p.shape.num_units, p, stream);
-  return launch(kv_fp8_rows<OUT, U, IdxT, false>, p.shape.num_units, p, stream);
+  if (bf16) return launch(kv_fp8_rows<OUT, U, IdxT, true, FMT>, p.shape.num_units, p, stream);
+  return launch(kv_fp8_rows<OUT, U, IdxT, false, FMT>, p.shape.num_units, p, stream);
+}
+
+template <int OUT, typename IdxT>
+kv_status launch_fp8_out(int fmt, bool bf16, const Fp8Params& p, cudaStream_t stream) {
+  if (fmt == kFmtE5M2) return launch_fp8_fmt<OUT, IdxT, kFmtE5M2>(bf16, p, stream);
+  return launch_fp8_fmt<OUT, IdxT, kFmtE4M3>(bf16, p, stream);
 }
 
 template <typename IdxT>
-kv_status launch_fp8(int out, bool bf16, const Fp8Params& p, cudaStream_t stream) {
+kv_status launch_fp8(int out, int fmt, bool bf16, const Fp8Params& p, cudaStream_t stream) {
   switch (out) {
 #if KV_MAX_VEC >= 32
-    case 32: return launch_fp8_out<32, IdxT>(bf16, p, stream);
+    case 32: return launch_fp8_out<32, IdxT>(fmt, bf16, p, stream);
 #endif
-    case 16: return launch_fp8_out<16, IdxT>(bf16, p, stream);
-    case 8: return launch_fp8_out<8, IdxT>(bf16, p, stream);
-    case 4: return launch_fp8_out<4, IdxT>(bf16, p, stream);
-    default: return launch_fp8_out<2, IdxT>(bf16, p, stream);
+    case 16: return launch_fp8_out<16, IdxT>(fmt, bf16, p, stream);
+    case 8: return launch_fp8_out<8, IdxT>(fmt, bf16, p, stream);
+    case 4: return launch_fp8_out<4, IdxT>(fmt, bf16, p, stream);
+    default: return launch_fp8_out<2, IdxT>(fmt, bf16, p, stream);
   }
+}
+
+template <typename IdxT, int FMT>
+kv_status launch_fp8_elements_fmt(bool bf16, const GenericFp8Params& g, cudaStream_t stream) {
+  if (bf16) return launch(kv_fp8_elements<IdxT, true, FMT>, g.num_units, g, stream);
+  return launch(kv_fp8_elements<IdxT, false, FMT>, g.num_units, g, stream);
+}
+
+template <typename IdxT>
+kv_status launch_fp8_elements(int fmt, bool bf16, const GenericFp8Params& g, cudaStream_t stream) {
+  if (fmt == kFmtE5M2) return launch_fp8_elements_fmt<IdxT, kFmtE5M2>(bf16, g, stream);
+  return launch_fp8_elements_fmt<IdxT, kFmtE4M3>(bf16, g, stream);
 }
 
 }  // namespace kvimpl
@@ -591,14 +609,17 @@ extern "C" kv_status kv_store_paged(const void* k, const void* v, void* k_cache,
                     size_limit, num_split, d_err, stream);
 }
 
-extern "C" kv_status kv_store_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
-                                  const void* indices, kv_index_dtype index_dtype,
-                                  int64_t index_stride, int64_t num_tokens, int32_t num_heads,
-                                  int32_t head_dim, kv_src_dtype src_dtype, const kv_strides* s,
-                                  int64_t page_size, int64_t kc_page_stride, int64_t vc_page_stride,
-                                  int64_t size_limit, const float* inv_k_scale,
-                                  const float* inv_v_scale, int32_t use_scale,
-                                  kv_error_record* d_err, kv_stream_t stream_) {
+// kv_store_fp8, and the static scale modes of kv_store_fp8_ex: one inverse
+// scale per tensor (or none), output format fmt (kFmtE4M3 / kFmtE5M2).
+kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, void* v_cache,
+                                   const void* indices, kv_index_dtype index_dtype,
+                                   int64_t index_stride, int64_t num_tokens, int32_t num_heads,
+                                   int32_t head_dim, kv_src_dtype src_dtype, const kv_strides* s,
+                                   int64_t page_size, int64_t kc_page_stride,
+                                   int64_t vc_page_stride, int64_t size_limit,
+                                   const float* inv_k_scale, const float* inv_v_scale,
+                                   int32_t use_scale, int fmt, kv_error_record* d_err,
+                                   kv_stream_t stream_) {
   if (num_tokens < 0) return KV_ERR_INVALID_ARG;
   if (num_tokens == 0) return KV_OK;
   if (!common_args_ok(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_heads,
@@ -662,11 +683,8 @@ extern "C" kv_status kv_store_fp8(const void* k, const void* v, void* k_cache, v
     g.num_heads = num_heads;
     g.head_dim = head_dim;
     g.err = d_err;
-    if (i64)
-      return bf16 ? launch(kv_fp8_elements<int64_t, true>, g.num_units, g, stream)
-                  : launch(kv_fp8_elements<int64_t, false>, g.num_units, g, stream);
-    return bf16 ? launch(kv_fp8_elements<int32_t, true>, g.num_units, g, stream)
-                : launch(kv_fp8_elements<int32_t, false>, g.num_units, g, stream);
+    return i64 ? launch_fp8_elements<int64_t>(fmt, bf16, g, stream)
+               : launch_fp8_elements<int32_t>(fmt, bf16, g, stream);
   }
 
   int sms = 0;
@@ -693,7 +711,22 @@ extern "C" kv_status kv_store_fp8(const void* k, const void* v, void* k_cache, v
   p.err = d_err;
   p.prefetch = out >= 8 ? 1 : 0;  // 2*OUT input bytes per chunk, 16-byte aligned
   p.vec = out;
-  return i64 ? launch_fp8<int64_t>(out, bf16, p, stream) : launch_fp8<int32_t>(out, bf16, p, stream);
+  return i64 ? launch_fp8<int64_t>(out, fmt, bf16, p, stream)
+             : launch_fp8<int32_t>(out, fmt, bf16, p, stream);
+}
+
+extern "C" kv_status kv_store_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                                  const void* indices, kv_index_dtype index_dtype,
+                                  int64_t index_stride, int64_t num_tokens, int32_t num_heads,
+                                  int32_t head_dim, kv_src_dtype src_dtype, const kv_strides* s,
+                                  int64_t page_size, int64_t kc_page_stride, int64_t vc_page_stride,
+                                  int64_t size_limit, const float* inv_k_scale,
+                                  const float* inv_v_scale, int32_t use_scale,
+                                  kv_error_record* d_err, kv_stream_t stream) {
+  return store_fp8_static(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_tokens,
+                          num_heads, head_dim, src_dtype, s, page_size, kc_page_stride,
+                          vc_page_stride, size_limit, inv_k_scale, inv_v_scale, use_scale,
+                          kFmtE4M3, d_err, stream);
 }
 
 extern "C" kv_status kv_error_poll(kv_error_record* d_err, kv_stream_t stream_, int64_t* oob_count,

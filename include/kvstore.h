@@ -220,6 +220,80 @@ kv_status kv_gather_fp8(const void *k_cache, const void *v_cache, void *k_out, v
                         const float *k_scale, const float *v_scale, int32_t use_scale,
                         kv_error_record *d_err, kv_stream_t stream);
 
+/* FP8 cache formats of the extended calls. */
+typedef enum kv_fp8_format {
+    KV_FP8_E4M3FN = 0,   /* largest finite 448, no infinities */
+    KV_FP8_E5M2 = 1      /* largest finite 57344 */
+} kv_fp8_format;
+
+/* Scale modes of the extended calls. */
+typedef enum kv_scale_mode {
+    KV_SCALE_NONE = 0,        /* values converted unscaled */
+    KV_SCALE_TENSOR = 1,      /* one fp32 scale per tensor, a device scalar */
+    KV_SCALE_TOKEN = 2,       /* one scale per token row (all heads), computed per call */
+    KV_SCALE_TOKEN_HEAD = 3   /* one scale per (token, head), computed per call */
+} kv_scale_mode;
+
+/*
+ * kv_store_fp8_ex -- kv_store_fp8 with a choice of FP8 format and of scale
+ * granularity, including scales computed in the kernel.  The fused FP8
+ * write's module docstring (trtllm_fp8_kv_kernel.py) names per-token scale
+ * computation and e5m2 caches; its kernel implements the per-tensor e4m3fn
+ * case only, which is kv_store_fp8 (= this call with KV_FP8_E4M3FN and
+ * KV_SCALE_TENSOR or KV_SCALE_NONE).
+ *
+ * Arguments as kv_store_fp8, plus:
+ *   format       KV_FP8_E4M3FN or KV_FP8_E5M2 (rounding: nearest even; finite
+ *                overflow and infinities saturate to the largest finite
+ *                value; every NaN becomes 0x7F).
+ *   scale_mode   KV_SCALE_NONE / KV_SCALE_TENSOR: as kv_store_fp8 with
+ *                use_scale 0 / 1 (inv_k_scale, inv_v_scale are device
+ *                pointers to the inverse scales).
+ *                KV_SCALE_TOKEN / KV_SCALE_TOKEN_HEAD: for each group (the
+ *                token's K row or V row, or one head of it) the kernel takes
+ *                amax = max |x| (NaN ignored), inv = fmax / amax and
+ *                scale = amax / fmax in fp32 round-to-nearest (both 1 when
+ *                amax is 0; fmax = 448 or 57344), writes the codes of
+ *                fl32(x * inv), and stores `scale` (the dequantisation
+ *                multiplier) at k_scales[slot * scales_slot_stride + g],
+ *                g = head (TOKEN_HEAD) or 0 (TOKEN); likewise V.  The scale
+ *                caches are device float arrays indexed by slot, not by page.
+ *   k_scales,
+ *   v_scales,
+ *   scales_slot_stride   used by the dynamic modes only: non-NULL, 4-byte
+ *                aligned, stride >= num_heads (TOKEN_HEAD) or >= 1 (TOKEN).
+ * The dynamic modes need contiguous dims (k_dim = v_dim = 2, kc_dim = vc_dim
+ * = 1), else KV_ERR_UNSUPPORTED.  Out-of-range slots write neither codes nor
+ * scales.
+ */
+kv_status kv_store_fp8_ex(const void *k, const void *v, void *k_cache, void *v_cache,
+                          const void *indices, kv_index_dtype index_dtype, int64_t index_stride,
+                          int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                          kv_src_dtype src_dtype, const kv_strides *strides, int64_t page_size,
+                          int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
+                          kv_fp8_format format, kv_scale_mode scale_mode,
+                          const float *inv_k_scale, const float *inv_v_scale, float *k_scales,
+                          float *v_scales, int64_t scales_slot_stride, kv_error_record *d_err,
+                          kv_stream_t stream);
+
+/*
+ * kv_gather_fp8_ex -- kv_gather_fp8 for every layout kv_store_fp8_ex writes:
+ * codes of `format` decoded exactly, multiplied by the scale of `scale_mode`
+ * (NONE: none; TENSOR: *k_scale / *v_scale, the forward scales; TOKEN /
+ * TOKEN_HEAD: k_scales[slot * scales_slot_stride + g] as written by
+ * kv_store_fp8_ex), rounded to bf16 / fp16.  kv_gather_fp8 is this call
+ * with KV_FP8_E4M3FN and NONE / TENSOR.
+ */
+kv_status kv_gather_fp8_ex(const void *k_cache, const void *v_cache, void *k_out, void *v_out,
+                           const void *indices, kv_index_dtype index_dtype, int64_t index_stride,
+                           int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                           kv_src_dtype out_dtype, const kv_strides *strides, int64_t page_size,
+                           int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
+                           kv_fp8_format format, kv_scale_mode scale_mode, const float *k_scale,
+                           const float *v_scale, const float *k_scales, const float *v_scales,
+                           int64_t scales_slot_stride, kv_error_record *d_err,
+                           kv_stream_t stream);
+
 /*
  * kv_inv_scale -- inv[i] = 1 / scale[i] in fp32, round to nearest, for
  * i < n, on the device (trtllm_fp8_kv_kernel.py, `fused_fp8_set_kv_buffer`

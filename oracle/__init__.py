@@ -75,6 +75,16 @@ def _load():
         lib.kvo_inv_scale.argtypes = [ctypes.c_float]
         lib.kvo_inv_scale.restype = ctypes.c_float
         lib.kvo_absmax_inv.argtypes = [P, P, I32, I64, I32, I32, P, ctypes.c_float, P, P]
+        lib.kvo_e5m2_encode_array.argtypes = [P, P, I64]
+        lib.kvo_e5m2_decode_array.argtypes = [P, P, I64]
+        lib.kvo_store_fp8_ex.argtypes = [P, P, P, P, P, I32, I64, I64, I64, I32, I32, I32, P, I64,
+                                         I64, I64, I64, I32, I32, ctypes.c_float, ctypes.c_float,
+                                         P, P, I64, P, P]
+        lib.kvo_store_fp8_ex.restype = I32
+        lib.kvo_gather_fp8_ex.argtypes = [P, P, P, P, P, I32, I64, I64, I64, I32, I32, I32, P,
+                                          I64, I64, I64, I64, I32, I32, ctypes.c_float,
+                                          ctypes.c_float, P, P, I64, P, P]
+        lib.kvo_gather_fp8_ex.restype = I32
         lib.kvo_gather_copy.argtypes = lib.kvo_store_copy.argtypes
         lib.kvo_gather_copy.restype = I32
         lib.kvo_gather_fp8.argtypes = lib.kvo_store_fp8.argtypes
@@ -290,3 +300,78 @@ def absmax_inv(k, v, strides: Strides, num_tokens, num_heads, head_dim, src_dtyp
                            num_heads, head_dim, _ptr(strides.values), float(np.float32(fp8_max)),
                            _ptr(amax), _ptr(inv))
     return amax, inv
+
+
+# -- e5m2 and the extended FP8 write / gather -------------------------------------
+
+FMT = {"e4m3fn": 0, "e5m2": 1}
+SCALE_MODE = {"none": 0, "tensor": 1, "token": 2, "token_head": 3}
+
+
+def e5m2_encode(x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().kvo_e5m2_encode_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def e5m2_decode(codes) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().kvo_e5m2_decode_array(_ptr(c), _ptr(out), c.size)
+    return out
+
+
+def _null_or(a):
+    return None if a is None else _ptr(a)
+
+
+def store_fp8_ex(k, v, k_cache, v_cache, indices, strides: Strides, num_heads, head_dim,
+                 src_dtype, page_size, kc_page_stride, vc_page_stride, size_limit, fmt="e4m3fn",
+                 scale_mode="none", inv_k=1.0, inv_v=1.0, k_scales=None, v_scales=None,
+                 scales_slot_stride=1, k_off=0, v_off=0, index_stride=1, t_end=None):
+    """Extended FP8 write (format, scale mode, per-slot scale caches); in place.
+    Returns (bad_count, first_bad)."""
+    for a, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_buf(a, n)
+    for a in (k_scales, v_scales):
+        if a is not None:
+            assert a.dtype == np.float32 and a.flags.c_contiguous
+    idx = np.ascontiguousarray(indices)
+    T = idx.size // index_stride if t_end is None else t_end
+    bad = np.zeros(1, np.int64)
+    first = np.zeros(1, np.int64)
+    rc = _load().kvo_store_fp8_ex(_ptr(k) + k_off, _ptr(v) + v_off, _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(idx), int(idx.dtype == np.int64), index_stride, 0, T,
+                                  num_heads, head_dim, int(src_dtype == "bf16"),
+                                  _ptr(strides.values), page_size, kc_page_stride, vc_page_stride,
+                                  size_limit, FMT[fmt], SCALE_MODE[scale_mode],
+                                  float(np.float32(inv_k)), float(np.float32(inv_v)),
+                                  _null_or(k_scales), _null_or(v_scales), scales_slot_stride,
+                                  _ptr(bad), _ptr(first))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return int(bad[0]), int(first[0])
+
+
+def gather_fp8_ex(k_cache, v_cache, k_out, v_out, indices, strides: Strides, num_heads, head_dim,
+                  out_dtype, page_size, kc_page_stride, vc_page_stride, size_limit,
+                  fmt="e4m3fn", scale_mode="none", scale_k=1.0, scale_v=1.0, k_scales=None,
+                  v_scales=None, scales_slot_stride=1, index_stride=1, t_end=None):
+    for a, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_out, "k_out"), (v_out, "v_out")):
+        _check_buf(a, n)
+    idx = np.ascontiguousarray(indices)
+    T = idx.size // index_stride if t_end is None else t_end
+    bad = np.zeros(1, np.int64)
+    first = np.zeros(1, np.int64)
+    rc = _load().kvo_gather_fp8_ex(_ptr(k_cache), _ptr(v_cache), _ptr(k_out), _ptr(v_out),
+                                   _ptr(idx), int(idx.dtype == np.int64), index_stride, 0, T,
+                                   num_heads, head_dim, int(out_dtype == "bf16"),
+                                   _ptr(strides.values), page_size, kc_page_stride,
+                                   vc_page_stride, size_limit, FMT[fmt], SCALE_MODE[scale_mode],
+                                   float(np.float32(scale_k)), float(np.float32(scale_v)),
+                                   _null_or(k_scales), _null_or(v_scales), scales_slot_stride,
+                                   _ptr(bad), _ptr(first))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return int(bad[0]), int(first[0])

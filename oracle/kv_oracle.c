@@ -477,3 +477,205 @@ void kvo_absmax_inv(const uint8_t *k, const uint8_t *v, int src_is_bf16, int64_t
         inv_out[kv] = amax > 0.0 ? (float)((double)fp8_max / amax) : 1.0f;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* FP8 e5m2, and the extended FP8 write with dynamic per-group scales.      */
+/* ------------------------------------------------------------------------ */
+
+/* FP8 E5M2 (OCP 8-bit floating point): 1 sign, 5 exponent bits (bias 15), 2
+ * mantissa bits; E = 31 holds +-Inf (m = 0) and NaN (m != 0); largest finite
+ * magnitude 1.75 * 2^15 = 57344.  Value = 2^(E-15) * (1 + m/4) for
+ * 1 <= E <= 30, 2^-14 * (m/4) for E = 0. */
+double kvo_e5m2_decode(uint8_t code)
+{
+    int s = code >> 7;
+    int E = (code >> 2) & 0x1F;
+    int m = code & 0x3;
+    double mag;
+    if (E == 0x1F)
+        return m ? NAN : (s ? -INFINITY : INFINITY);
+    if (E == 0)
+        mag = ldexp((double)m, -16);
+    else
+        mag = ldexp(4.0 + (double)m, E - 17);
+    return s ? -mag : mag;
+}
+
+#define KVO_E5M2_NAN 0x7F
+#define KVO_E5M2_MAXFIN 0x7B   /* 57344 */
+
+/* Nearest e5m2 value, ties to even mantissa, finite overflow and +-Inf
+ * saturated to +-57344 (the same satfinite rule as the e4m3fn encoder), every
+ * NaN to 0x7F. */
+uint8_t kvo_e5m2_encode(float y)
+{
+    double a = fabs((double)y);
+    uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    if (isnan(y))
+        return KVO_E5M2_NAN;
+    if (a >= 57344.0)
+        return sign | KVO_E5M2_MAXFIN;
+    if (a < 0x1p-14) {                 /* subnormal: multiples of 2^-16 */
+        double m = nearbyint(a * 0x1p16);
+        return sign | (uint8_t)m;      /* m == 4 is the smallest normal */
+    }
+    int ex;
+    (void)frexp(a, &ex);
+    int e = ex - 1;
+    double m = nearbyint(ldexp(a, 2 - e));   /* in [4, 8] */
+    if (m == 8.0) {
+        m = 4.0;
+        e += 1;
+    }
+    int code = ((e + 15) << 2) | ((int)m - 4);
+    if (code > KVO_E5M2_MAXFIN)
+        code = KVO_E5M2_MAXFIN;
+    return sign | (uint8_t)code;
+}
+
+void kvo_e5m2_encode_array(const float *x, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kvo_e5m2_encode(x[i]);
+}
+
+void kvo_e5m2_decode_array(const uint8_t *codes, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kvo_e5m2_decode(codes[i]);
+}
+
+/* Extended FP8 write.  fmt: 0 e4m3fn, 1 e5m2.  scale_mode: 0 none, 1 one fp32
+ * inverse scale per tensor (inv_k / inv_v), 2 dynamic per token row, 3
+ * dynamic per (token, head).  Dynamic: over the group's elements x (the whole
+ * K row of the token, or one head of it), amax = max |x| (NaN ignored); when
+ * amax > 0, inv = fl32(fmax / amax) and scale = fl32(amax / fmax), else both
+ * are 1; the codes are enc(fl32(x * inv)) and `scale` is stored at
+ * k_scales[slot * scales_slot_stride + g] (g = head for mode 3, 0 for mode 2),
+ * likewise for V.  fmax is 448 (e4m3fn) or 57344 (e5m2).  This is the
+ * "per-token scale computation" the fused FP8 write's module docstring
+ * (trtllm_fp8_kv_kernel.py) names and does not implement; the reading above is
+ * this library's. */
+int kvo_store_fp8_ex(const uint8_t *k, const uint8_t *v, uint8_t *k_cache, uint8_t *v_cache,
+                     const void *indices, int index_is_i64, int64_t index_stride,
+                     int64_t t_begin, int64_t t_end, int32_t num_heads, int32_t head_dim,
+                     int src_is_bf16, const int64_t *strides, int64_t page_size,
+                     int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
+                     int fmt, int scale_mode, float inv_k, float inv_v, float *k_scales,
+                     float *v_scales, int64_t scales_slot_stride,
+                     int64_t *bad_count, int64_t *first_bad)
+{
+    if (num_heads <= 0 || head_dim <= 0 || page_size <= 0 || t_begin > t_end)
+        return KVO_ERR_ARG;
+    if (fmt < 0 || fmt > 1 || scale_mode < 0 || scale_mode > 3)
+        return KVO_ERR_ARG;
+    const double fmax = fmt ? 57344.0 : 448.0;
+    *bad_count = 0;
+    *first_bad = -1;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        int64_t slot = read_index(indices, index_is_i64, index_stride, t);
+        if (slot < 0 || slot >= size_limit) {
+            note_bad(t, bad_count, first_bad);
+            continue;
+        }
+        int64_t page_id = slot / page_size;
+        int64_t page_offset = slot % page_size;
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint8_t *src = kv ? v : k;
+            uint8_t *dst = kv ? v_cache : k_cache;
+            const int64_t *ss = strides + 3 * kv;
+            const int64_t *ds = strides + 6 + 3 * kv;
+            int64_t page_stride = kv ? vc_page_stride : kc_page_stride;
+            float *scales = kv ? v_scales : k_scales;
+            int groups = scale_mode == 3 ? num_heads : 1;
+            int heads_per_group = scale_mode == 3 ? 1 : num_heads;
+            for (int g = 0; g < groups; ++g) {
+                float inv = 1.0f;
+                if (scale_mode == 1) {
+                    inv = kv ? inv_v : inv_k;
+                } else if (scale_mode >= 2) {
+                    double amax = 0.0;
+                    for (int32_t hh = 0; hh < heads_per_group; ++hh)
+                        for (int32_t d = 0; d < head_dim; ++d) {
+                            int32_t h = g * heads_per_group + hh;
+                            uint16_t bits;
+                            memcpy(&bits, src + t * ss[0] + h * ss[1] + d * ss[2], sizeof bits);
+                            double x = src_is_bf16 ? kvo_bf16_to_f32(bits) : kvo_f16_to_f32(bits);
+                            if (!isnan(x) && fabs(x) > amax)
+                                amax = fabs(x);
+                        }
+                    float scale = 1.0f;
+                    if (amax > 0.0) {
+                        inv = (float)(fmax / amax);     /* correctly rounded fp32 quotients */
+                        scale = (float)(amax / fmax);
+                    }
+                    scales[slot * scales_slot_stride + g] = scale;
+                }
+                for (int32_t hh = 0; hh < heads_per_group; ++hh)
+                    for (int32_t d = 0; d < head_dim; ++d) {
+                        int32_t h = g * heads_per_group + hh;
+                        uint16_t bits;
+                        memcpy(&bits, src + t * ss[0] + h * ss[1] + d * ss[2], sizeof bits);
+                        float x = src_is_bf16 ? kvo_bf16_to_f32(bits) : kvo_f16_to_f32(bits);
+                        float y = scale_mode ? kvo_scale_f32(x, inv) : x;
+                        dst[page_id * page_stride + page_offset * ds[0] + h * ds[1] + d * ds[2]] =
+                            fmt ? kvo_e5m2_encode(y) : kvo_e4m3fn_encode(y);
+                    }
+            }
+        }
+    }
+    return KVO_OK;
+}
+
+/* Extended dequantising gather: codes of format fmt decoded exactly, times
+ * the scale (mode 0: none; 1: scale_k / scale_v per tensor; 2/3: the per-slot
+ * scale k_scales[slot * scales_slot_stride + g] written by the extended
+ * write), rounded to bf16 / fp16. */
+int kvo_gather_fp8_ex(const uint8_t *k_cache, const uint8_t *v_cache, uint8_t *k_out,
+                      uint8_t *v_out, const void *indices, int index_is_i64,
+                      int64_t index_stride, int64_t t_begin, int64_t t_end, int32_t num_heads,
+                      int32_t head_dim, int out_is_bf16, const int64_t *strides,
+                      int64_t page_size, int64_t kc_page_stride, int64_t vc_page_stride,
+                      int64_t size_limit, int fmt, int scale_mode, float scale_k,
+                      float scale_v, const float *k_scales, const float *v_scales,
+                      int64_t scales_slot_stride, int64_t *bad_count, int64_t *first_bad)
+{
+    if (num_heads <= 0 || head_dim <= 0 || page_size <= 0 || t_begin > t_end)
+        return KVO_ERR_ARG;
+    if (fmt < 0 || fmt > 1 || scale_mode < 0 || scale_mode > 3)
+        return KVO_ERR_ARG;
+    *bad_count = 0;
+    *first_bad = -1;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        int64_t slot = read_index(indices, index_is_i64, index_stride, t);
+        if (slot < 0 || slot >= size_limit) {
+            note_bad(t, bad_count, first_bad);
+            continue;
+        }
+        int64_t page_id = slot / page_size;
+        int64_t page_offset = slot % page_size;
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint8_t *src = kv ? v_cache : k_cache;
+            uint8_t *dst = kv ? v_out : k_out;
+            const int64_t *os = strides + 3 * kv;
+            const int64_t *cs = strides + 6 + 3 * kv;
+            int64_t page_stride = kv ? vc_page_stride : kc_page_stride;
+            const float *scales = kv ? v_scales : k_scales;
+            for (int32_t h = 0; h < num_heads; ++h) {
+                float scale = 1.0f;
+                if (scale_mode == 1)
+                    scale = kv ? scale_v : scale_k;
+                else if (scale_mode >= 2)
+                    scale = scales[slot * scales_slot_stride + (scale_mode == 3 ? h : 0)];
+                for (int32_t d = 0; d < head_dim; ++d) {
+                    uint8_t q = src[page_id * page_stride + page_offset * cs[0] + h * cs[1] + d * cs[2]];
+                    float x = (float)(fmt ? kvo_e5m2_decode(q) : kvo_e4m3fn_decode(q));
+                    float y = scale_mode ? kvo_scale_f32(x, scale) : x;
+                    uint16_t bits = out_is_bf16 ? kvo_f32_to_bf16(y) : kvo_f32_to_f16(y);
+                    memcpy(dst + t * os[0] + h * os[1] + d * os[2], &bits, sizeof bits);
+                }
+            }
+        }
+    }
+    return KVO_OK;
+}

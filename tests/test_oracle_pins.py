@@ -587,3 +587,127 @@ def test_absmax_inv_against_numpy(src):
     # the fp8 workload's recipe (host numpy) is exactly this
     amax, inv = oracle.absmax_inv(w.k, w.v, st, T, H, D, src)
     assert inv[0] == np.float32(w.inv_k) and inv[1] == np.float32(w.inv_v)
+
+
+# ---------------------------------------------------------------------------
+# e5m2 and the extended FP8 write (formats, dynamic per-token / per-head scales)
+# ---------------------------------------------------------------------------
+
+LIB52 = (torch.arange(256, dtype=torch.uint8).view(torch.float8_e5m2).to(torch.float64).numpy())
+POS52 = np.arange(0x7C)          # 0x00 .. 0x7B finite non-negative
+
+
+def brute_encode_e5m2(x32):
+    x = np.asarray(x32, dtype=np.float32).ravel()
+    out = np.empty(x.size, dtype=np.uint8)
+    vals = LIB52[POS52]
+    for c0 in range(0, x.size, 1 << 14):
+        with np.errstate(invalid="ignore"):
+            xs = x[c0:c0 + (1 << 14)].astype(np.float64)
+        a = np.minimum(np.abs(xs), 1e6)
+        d = np.abs(a[:, None] - vals[None, :])
+        tied = d == d.min(axis=1, keepdims=True)
+        even = tied & ((POS52[None, :] & 1) == 0)
+        code = np.where(even.any(axis=1), np.argmax(even, axis=1), np.argmax(tied, axis=1))
+        code = code.astype(np.uint8) | np.where(np.signbit(xs), 0x80, 0).astype(np.uint8)
+        out[c0:c0 + xs.size] = np.where(np.isnan(xs), 0x7F, code)
+    return out
+
+
+def test_e5m2_decode_and_encode():
+    d = oracle.e5m2_decode(np.arange(256))
+    nan = np.isnan(LIB52)
+    assert np.array_equal(np.isnan(d), nan) and np.array_equal(d[~nan], LIB52[~nan])
+    assert d[0x7B] == 57344.0 and d[0x7C] == np.inf and d[0x04] == 2.0 ** -14
+    for x in (all_bf16_as_f32(), all_f16_as_f32(), _random_f32(0xE5, 1 << 18)):
+        assert np.array_equal(oracle.e5m2_encode(x), brute_encode_e5m2(x))
+    pts = np.array([57344, 61439, 61440, 1e20, np.inf, -np.inf, 2 ** -17, 1.125, 1.375],
+                   np.float32)
+    assert list(oracle.e5m2_encode(pts)) == [0x7B, 0x7B, 0x7B, 0x7B, 0x7B, 0xFB, 0x00, 0x3C,
+                                             0x3E]
+
+
+def _ex_problem(T, H, D, n, seed, src="bf16", ps=8):
+    w = wl.make_fp8("x", T, H, D, n, seed=seed, dtype=src, page_size=ps, scale=3.0)
+    st = _fp8_strides(H, D, 2, H * D)
+    return w, st
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("mode", ["token", "token_head"])
+def test_store_fp8_ex_dynamic_groups(fmt, mode):
+    T, H, D, n, ps = 40, 4, 32, 128, 8
+    w, st = _ex_problem(T, H, D, n, seed=101)
+    kb = w.k.copy()
+    kb.reshape(T, -1)[3] = 0                    # an all-zero row: scale 1
+    kb.reshape(-1)[200] = 0x7FC0                # a NaN element: ignored by amax
+    kc = np.full(n * H * D, 0x7F, np.uint8)
+    vc = kc.copy()
+    G = H if mode == "token_head" else 1
+    ks = np.full(n * G, -1.0, np.float32)
+    vs = ks.copy()
+    oracle.store_fp8_ex(kb, w.v, kc, vc, w.indices, st, H, D, "bf16", ps, ps * H * D, ps * H * D,
+                        n, fmt=fmt, scale_mode=mode, k_scales=ks, v_scales=vs,
+                        scales_slot_stride=G)
+    fmax = np.float32(448.0 if fmt == "e4m3fn" else 57344.0)
+    enc = brute_encode if fmt == "e4m3fn" else brute_encode_e5m2
+    for bits, cache, sc in ((kb, kc, ks), (w.v, vc, vs)):
+        x = _widen(bits.reshape(T, H, D), "bf16")
+        groups = x.reshape(T, G, -1)
+        amax = np.nanmax(np.abs(groups), axis=2).astype(np.float32)
+        with np.errstate(divide="ignore"):
+            inv = np.where(amax > 0, fmax / amax, np.float32(1)).astype(np.float32)
+            scale = np.where(amax > 0, amax / fmax, np.float32(1)).astype(np.float32)
+        y = (groups * inv[:, :, None]).astype(np.float32)
+        want = enc(y).reshape(T, -1)
+        assert np.array_equal(cache.reshape(n, -1)[w.indices], want)
+        assert np.array_equal(sc.reshape(n, G)[w.indices], scale)
+        untouched = np.setdiff1d(np.arange(n), w.indices)
+        assert np.all(sc.reshape(n, G)[untouched] == -1.0)
+    assert ks.reshape(n, G)[w.indices[3]][0] == 1.0
+
+
+def test_store_fp8_ex_static_modes_match_store_fp8():
+    T, H, D, n, ps = 64, 2, 64, 256, 16
+    w, st = _ex_problem(T, H, D, n, seed=102, ps=ps)
+    for mode, use in (("none", 0), ("tensor", 1)):
+        a = [np.full(n * H * D, 0x7F, np.uint8) for _ in range(4)]
+        oracle.store_fp8(w.k, w.v, a[0], a[1], w.indices, st, H, D, "bf16", ps, ps * H * D,
+                         ps * H * D, n, w.inv_k, w.inv_v, use)
+        oracle.store_fp8_ex(w.k, w.v, a[2], a[3], w.indices, st, H, D, "bf16", ps, ps * H * D,
+                            ps * H * D, n, fmt="e4m3fn", scale_mode=mode, inv_k=w.inv_k,
+                            inv_v=w.inv_v)
+        assert np.array_equal(a[0], a[2]) and np.array_equal(a[1], a[3])
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_gather_fp8_ex_per_slot_scales(fmt):
+    T, H, D, n, ps = 48, 4, 32, 128, 8
+    w, st = _ex_problem(T, H, D, n, seed=103, ps=ps)
+    kc = np.full(n * H * D, 0x7F, np.uint8)
+    vc = kc.copy()
+    ks = np.zeros(n * H, np.float32)
+    vs = ks.copy()
+    oracle.store_fp8_ex(w.k, w.v, kc, vc, w.indices, st, H, D, "bf16", ps, ps * H * D,
+                        ps * H * D, n, fmt=fmt, scale_mode="token_head", k_scales=ks, v_scales=vs,
+                        scales_slot_stride=H)
+    ko = np.zeros(T * H * D, np.uint16)
+    vo = ko.copy()
+    R = H * D * 2
+    ost = oracle.Strides(k_token=R, k_head=D * 2, k_dim=2, v_token=R, v_head=D * 2, v_dim=2,
+                         kc_slot=H * D, kc_head=D, kc_dim=1, vc_slot=H * D, vc_head=D, vc_dim=1)
+    oracle.gather_fp8_ex(kc, vc, ko, vo, w.indices, ost, H, D, "bf16", ps, ps * H * D, ps * H * D,
+                         n, fmt=fmt, scale_mode="token_head", k_scales=ks, v_scales=vs,
+                         scales_slot_stride=H)
+    table = LIB if fmt == "e4m3fn" else LIB52
+    codes = kc.reshape(n, H, D)[w.indices]
+    sc = ks.reshape(n, H)[w.indices]
+    y = (table[codes].astype(np.float32) * sc[:, :, None]).astype(np.float32)
+    want = torch.from_numpy(y.reshape(-1)).to(torch.bfloat16).view(torch.int16).numpy()
+    want = np.where(np.isnan(y.reshape(-1)), 0x7FFF, want.view(np.uint16))
+    assert np.array_equal(ko, want)
+    # and the round trip is close: within one fp8 step of the group scale
+    x = _widen(w.k.reshape(-1), "bf16").reshape(T, H, D)
+    back = (ko.astype(np.uint32) << 16).view(np.float32).reshape(T, H, D)
+    step = 2.0 ** -3 if fmt == "e4m3fn" else 2.0 ** -2
+    assert np.all(np.abs(back - x) <= np.abs(x) * step + sc[:, :, None] * 2.0 ** -9 * 16)
