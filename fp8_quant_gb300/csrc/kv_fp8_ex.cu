@@ -236,6 +236,12 @@ extern "C" kv_status kv_store_fp8_ex(const void* k, const void* v, void* k_cache
   if (s->k_dim != 2 || s->v_dim != 2 || s->kc_dim != 1 || s->vc_dim != 1) return KV_ERR_UNSUPPORTED;
   if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  bool on_device = true;
+  {
+    const void* in[3] = {k, v, indices};
+    const kv_status cs = classify_inputs(in, 3, &on_device);
+    if (cs != KV_OK) return cs;
+  }
   const bool flat = kc_page_stride == page_size * s->kc_slot && vc_page_stride == page_size * s->vc_slot;
 
   // group layout: per head, or the whole row (one segment when heads are
@@ -283,7 +289,7 @@ extern "C" kv_status kv_store_fp8_ex(const void* k, const void* v, void* k_cache
   p.num_units = static_cast<uint64_t>(num_tokens) * 2u * groups;
   p.fmax = fmt == kFmtE5M2 ? 57344.0f : 448.0f;
   p.err = d_err;
-  p.prefetch = ((sbits & 15u) == 0 && (seg_elems * 2) % 16 == 0) ? 1 : 0;
+  p.prefetch = (on_device && (sbits & 15u) == 0 && (seg_elems * 2) % 16 == 0) ? 1 : 0;
   const bool bf16 = src_dtype == KV_SRC_BF16;
   return index_dtype == KV_INDEX_I64 ? launch_dyn<int64_t>(ch, fmt, bf16, p, stream)
                                      : launch_dyn<int32_t>(ch, fmt, bf16, p, stream);

@@ -422,6 +422,12 @@ extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k
   if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const bool i64 = index_dtype == KV_INDEX_I64;
+  bool on_device = true;
+  {
+    const void* in[4] = {k_cache, v_cache, indices, k_out};
+    const kv_status cs = classify_inputs(in, 4, &on_device);
+    if (cs != KV_OK) return cs;
+  }
 
   if (s->k_dim != elem_bytes || s->v_dim != elem_bytes || s->kc_dim != elem_bytes ||
       s->vc_dim != elem_bytes) {
@@ -462,7 +468,7 @@ extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k
   p.shape.part_chunks = static_cast<uint32_t>(part_bytes / vec);
   p.err = d_err;
   p.vec = vec;
-  p.prefetch = vec >= 16 ? 1 : 0;
+  p.prefetch = vec >= 16 && on_device ? 1 : 0;
   return i64 ? launch_gather<int64_t>(vec, p, stream) : launch_gather<int32_t>(vec, p, stream);
 }
 
@@ -498,6 +504,12 @@ kv_status gather_fp8(const void* k_cache, const void* v_cache, void* k_out, void
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const bool i64 = index_dtype == KV_INDEX_I64;
   const bool bf16 = out_dtype == KV_SRC_BF16;
+  bool on_device = true;
+  {
+    const void* in[4] = {k_cache, v_cache, indices, k_out};
+    const kv_status cs = classify_inputs(in, 4, &on_device);
+    if (cs != KV_OK) return cs;
+  }
   const float* sk = scale_mode == KV_SCALE_TENSOR ? k_scale : nullptr;
   const float* sv = scale_mode == KV_SCALE_TENSOR ? v_scale : nullptr;
   const bool flat = kc_page_stride == page_size * s->kc_slot && vc_page_stride == page_size * s->vc_slot;
@@ -566,7 +578,7 @@ kv_status gather_fp8(const void* k_cache, const void* v_cache, void* k_out, void
   p.shape.part_chunks = static_cast<uint32_t>(part_elems / in);
   p.err = d_err;
   p.vec = in;
-  p.prefetch = in >= 16 ? 1 : 0;
+  p.prefetch = in >= 16 && on_device ? 1 : 0;
   p.scale_mode = scale_mode;
   p.scales_stride = scales_stride;
   return i64 ? launch_gather_fp8<int64_t>(in, fmt, bf16, p, stream)

@@ -15,6 +15,13 @@ extern thread_local int g_last_cuda_error;
 
 kv_status cuda_fail(cudaError_t e);
 
+// Where the input buffers live.  Inputs may be device memory or page-locked
+// host memory the device reads directly (NVLink-C2C / PCIe); memory unknown to
+// CUDA is rejected with KV_ERR_INVALID_ARG.  *all_device is true when every
+// input is device (or managed-free device-resident) memory, which is when the
+// kernels may prefetch inputs into L2 with bulk copies.
+kv_status classify_inputs(const void* const* ptrs, int n, bool* all_device);
+
 // The FP8 write with a per-tensor inverse scale (or none) in format fmt
 // (kFmtE4M3 / kFmtE5M2): kv_store_fp8 and the static modes of kv_store_fp8_ex.
 kv_status store_fp8_static(const void* k, const void* v, void* k_cache, void* v_cache,

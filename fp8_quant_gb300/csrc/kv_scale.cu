@@ -13,6 +13,10 @@
 // output (for non-negative floats the bit patterns order like the values).
 #include "kv_host.h"
 
+#ifndef KV_ABSMAX_CTAS_PER_SM
+#define KV_ABSMAX_CTAS_PER_SM 4
+#endif
+
 namespace kvimpl {
 namespace {
 
@@ -97,6 +101,14 @@ __global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant
   }
 }
 
+// Clears the two accumulator words.  A kernel rather than a memset so that
+// zeroing, reduction and finish chain by programmatic launch.
+__global__ void __launch_bounds__(kThreads) kv_absmax_zero(const __grid_constant__ AbsmaxParams p) {
+  grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  if (blockIdx.x == 0 && threadIdx.x < 2) p.amax_bits[threadIdx.x] = 0u;
+}
+
 struct FinishParams {
   const unsigned int* amax_bits;
   float* inv;
@@ -113,10 +125,10 @@ __global__ void __launch_bounds__(kThreads) kv_absmax_finish(const __grid_consta
 }
 
 template <int VEC>
-kv_status launch_absmax(bool bf16, const AbsmaxParams& p, cudaStream_t stream) {
+kv_status launch_absmax(bool bf16, const AbsmaxParams& p, cudaStream_t stream, uint64_t max_ctas) {
   constexpr int U = VEC == 32 ? 2 : 4;
-  if (bf16) return launch(kv_absmax_rows<VEC, U, true>, p.shape.num_units, p, stream);
-  return launch(kv_absmax_rows<VEC, U, false>, p.shape.num_units, p, stream);
+  if (bf16) return launch(kv_absmax_rows<VEC, U, true>, p.shape.num_units, p, stream, max_ctas);
+  return launch(kv_absmax_rows<VEC, U, false>, p.shape.num_units, p, stream, max_ctas);
 }
 
 }  // namespace
@@ -147,8 +159,10 @@ extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype sr
     return KV_ERR_INVALID_ARG;
   if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  cudaError_t e = cudaMemsetAsync(amax, 0, 2 * sizeof(float), stream);
-  if (e != cudaSuccess) return cuda_fail(e);
+  AbsmaxParams zp = {};
+  zp.amax_bits = reinterpret_cast<unsigned int*>(amax);
+  kv_status st = launch(kv_absmax_zero, kWarpsPerCta, zp, stream);
+  if (st != KV_OK) return st;
   if (num_tokens > 0) {
     const int64_t head_bytes = 2 * static_cast<int64_t>(head_dim);
     const bool merged = num_heads == 1 || (s->k_head == head_bytes && s->v_head == head_bytes);
@@ -170,17 +184,21 @@ extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype sr
     p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
     p.shape.part_chunks = static_cast<uint32_t>(seg_bytes / vec);
     p.amax_bits = reinterpret_cast<unsigned int*>(amax);
-    // one warp per row (one atomic per CTA and tensor)
+    // a few resident waves of CTAs loop over the rows, so only a few hundred
+    // same-address atomics land at the end
+    int sms = 0;
+    st = current_sm_count(&sms);
+    if (st != KV_OK) return st;
+    const uint64_t max_ctas = static_cast<uint64_t>(sms) * KV_ABSMAX_CTAS_PER_SM;
     const bool bf16 = src_dtype == KV_SRC_BF16;
-    kv_status st;
     switch (vec) {
 #if KV_MAX_VEC >= 32
-      case 32: st = launch_absmax<32>(bf16, p, stream); break;
+      case 32: st = launch_absmax<32>(bf16, p, stream, max_ctas); break;
 #endif
-      case 16: st = launch_absmax<16>(bf16, p, stream); break;
-      case 8: st = launch_absmax<8>(bf16, p, stream); break;
-      case 4: st = launch_absmax<4>(bf16, p, stream); break;
-      default: st = launch_absmax<2>(bf16, p, stream); break;
+      case 16: st = launch_absmax<16>(bf16, p, stream, max_ctas); break;
+      case 8: st = launch_absmax<8>(bf16, p, stream, max_ctas); break;
+      case 4: st = launch_absmax<4>(bf16, p, stream, max_ctas); break;
+      default: st = launch_absmax<2>(bf16, p, stream, max_ctas); break;
     }
     if (st != KV_OK) return st;
   }

@@ -368,6 +368,21 @@ kv_status cuda_fail(cudaError_t e) {
   return KV_ERR_CUDA;
 }
 
+kv_status classify_inputs(const void* const* ptrs, int n, bool* all_device) {
+  *all_device = true;
+  for (int i = 0; i < n; ++i) {
+    cudaPointerAttributes a;
+    const cudaError_t e = cudaPointerGetAttributes(&a, ptrs[i]);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();  // the query's own error is not sticky: clear it
+      return cuda_fail(e);
+    }
+    if (a.type == cudaMemoryTypeUnregistered) return KV_ERR_INVALID_ARG;
+    if (a.type != cudaMemoryTypeDevice) *all_device = false;
+  }
+  return KV_OK;
+}
+
 // SM count of the current device, cached per device.
 std::atomic<int> g_sm_count[kMaxDevices];
 
@@ -514,6 +529,12 @@ kv_status store_copy(const void* k, const void* v, void* k_cache, void* v_cache,
   if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const bool i64 = index_dtype == KV_INDEX_I64;
+  bool on_device = true;
+  {
+    const void* in[3] = {k, v, indices};
+    const kv_status cs = classify_inputs(in, 3, &on_device);
+    if (cs != KV_OK) return cs;
+  }
 
   if (s->k_dim != elem_bytes || s->v_dim != elem_bytes || s->kc_dim != elem_bytes ||
       s->vc_dim != elem_bytes) {
@@ -578,7 +599,7 @@ kv_status store_copy(const void* k, const void* v, void* k_cache, void* v_cache,
   p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
   p.shape.part_chunks = static_cast<uint32_t>(part_bytes / vec);
   p.err = d_err;
-  p.prefetch = vec >= 16 ? 1 : 0;
+  p.prefetch = vec >= 16 && on_device ? 1 : 0;
   p.vec = vec;
   return i64 ? launch_copy<int64_t>(vec, p, stream) : launch_copy<int32_t>(vec, p, stream);
 }
@@ -636,6 +657,12 @@ kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const bool i64 = index_dtype == KV_INDEX_I64;
   const bool bf16 = src_dtype == KV_SRC_BF16;
+  bool on_device = true;
+  {
+    const void* in[3] = {k, v, indices};
+    const kv_status cs = classify_inputs(in, 3, &on_device);
+    if (cs != KV_OK) return cs;
+  }
   const float* inv_k = use_scale ? inv_k_scale : nullptr;
   const float* inv_v = use_scale ? inv_v_scale : nullptr;
   // A page stride equal to page_size slots is the flat 3-D layout: s * slot_stride.
@@ -709,7 +736,7 @@ kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, 
   p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
   p.shape.part_chunks = static_cast<uint32_t>(part_elems / out);
   p.err = d_err;
-  p.prefetch = out >= 8 ? 1 : 0;  // 2*OUT input bytes per chunk, 16-byte aligned
+  p.prefetch = out >= 8 && on_device ? 1 : 0;  // 2*OUT input bytes per chunk, 16-byte aligned
   p.vec = out;
   return i64 ? launch_fp8<int64_t>(out, fmt, bf16, p, stream)
              : launch_fp8<int32_t>(out, fmt, bf16, p, stream);

@@ -315,7 +315,7 @@ kv_status kv_inv_scale(const float *scale, float *inv, int64_t n, kv_stream_t st
  *              (dims must be contiguous: k_dim = v_dim = 2; else
  *              KV_ERR_UNSUPPORTED).
  *   amax, inv  device pointers to two floats each, written by the call
- *              (amax is cleared first on `stream`).
+ *              (cleared first by a kernel on `stream`).
  * fp8_max must be positive and finite.
  */
 kv_status kv_absmax_inv(const void *k, const void *v, kv_src_dtype src_dtype,

@@ -294,3 +294,59 @@ def test_fp8_exhaustive_input_patterns(src, inv):
                     use_scale=0 if inv is None else 1,
                     inv=None if inv is None else (inv, inv))
     assert_same(p)
+
+
+# ---------------------------------------------------------------------------
+# Inputs in page-locked host memory (read by the kernels over NVLink-C2C)
+# ---------------------------------------------------------------------------
+
+def _pinned(a: np.ndarray):
+    import torch
+    return torch.from_numpy(a).pin_memory()
+
+
+@pytest.mark.parametrize("kind", ["copy", "fp8"])
+def test_pinned_host_inputs(kind):
+    """K, V and the slot ids in pinned host memory, caches on the device: the
+    same bytes as the oracle (the library reads the host buffers in place)."""
+    import torch
+    import fp8_quant_gb300 as kv
+    if kind == "copy":
+        p = copy_problem(T=700, H=8, D=128, n_slots=4096, seed=601)
+    else:
+        p = fp8_problem(T=700, H=8, D=128, n_slots=4096, seed=602, page_size=16)
+    g = GpuRun(p)
+    hk, hv, hi = _pinned(p.k_src), _pinned(p.v_src), _pinned(p.indices)
+    s = torch.cuda.current_stream().cuda_stream
+    idt = 1 if p.indices.dtype == np.int64 else 0
+    if kind == "copy":
+        rc = kv.raw.kv_store(hk.data_ptr(), hv.data_ptr(), g.kc.data_ptr(), g.vc.data_ptr(),
+                             hi.data_ptr(), idt, 1, p.T, p.H, p.D, 2, p.strides(), p.size_limit,
+                             0, g.err.data_ptr(), s)
+    else:
+        rc = kv.raw.kv_store_fp8(hk.data_ptr(), hv.data_ptr(), g.kc.data_ptr(), g.vc.data_ptr(),
+                                 hi.data_ptr(), idt, 1, p.T, p.H, p.D, 1, p.strides(), p.page_size,
+                                 p.kc_page, p.vc_page, p.size_limit, g.inv.data_ptr(),
+                                 g.inv.data_ptr() + 4, 1, g.err.data_ptr(), s)
+    assert rc == 0, kv.kv_status_str(rc)
+    assert g.poll()[:2] == (0, 0)
+    kc, vc = g.caches()
+    okc, ovc, _ = run_oracle(p)
+    assert np.array_equal(kc, okc) and np.array_equal(vc, ovc)
+
+
+def test_unregistered_host_memory_is_rejected():
+    """Pageable host memory unknown to CUDA is an argument error, found before
+    any launch."""
+    import torch
+    import fp8_quant_gb300 as kv
+    p = copy_problem(T=64, H=2, D=64, n_slots=256, seed=603)
+    g = GpuRun(p)
+    s = torch.cuda.current_stream().cuda_stream
+    k_host = p.k_src.ctypes.data                      # plain numpy buffer
+    rc = kv.raw.kv_store(k_host, g.v_src.data_ptr(), g.kc.data_ptr(), g.vc.data_ptr(),
+                         g.idx.data_ptr(), 1, 1, p.T, p.H, p.D, 2, p.strides(), p.size_limit, 0,
+                         g.err.data_ptr(), s)
+    assert rc == kv.KVStatus.ERR_INVALID_ARG
+    kc, _ = g.caches()
+    assert np.all(kc.view(np.uint16) == wl.BF16_SENTINEL)
