@@ -691,8 +691,13 @@ def run_e2e(args, dist, torch, kv, pool, device):
         rc = pool.call(b, torch.cuda.current_stream().cuda_stream, kbase, vbase, hbase + off_i)
         if rc != 0:
             raise RuntimeError(kv.kv_status_str(rc))
-        err_host.copy_(pool.amax_inv.view(torch.int64) if w.kind == "absmax" else pool.err,
-                       non_blocking=True)
+        if w.kind == "absmax":
+            err_host.copy_(pool.amax_inv.view(torch.int64), non_blocking=True)
+        else:   # the record lands in pinned host memory by a chained kernel
+            rc = kv.raw.kv_error_snapshot(pool.err.data_ptr(), err_host.data_ptr(),
+                                          torch.cuda.current_stream().cuda_stream)
+            if rc != 0:
+                raise RuntimeError(kv.kv_status_str(rc))
 
     steps = max(3, min(args.steps, args.e2e_steps))
     out = {}
@@ -708,8 +713,8 @@ def run_e2e(args, dist, torch, kv, pool, device):
                      "packed) into a device buffer, the call on the staged inputs, and a "
                      "device -> host read of the error record; back-to-back from CUDA graphs",
            "zero_copy": "every step: the call reads the batch (K, V, slot ids) directly from "
-                        "pinned host memory over NVLink-C2C, then a device -> host read of the "
-                        "error record; back-to-back from CUDA graphs"}
+                        "pinned host memory over NVLink-C2C, then kv_error_snapshot writes the "
+                        "error record into pinned host memory; back-to-back from CUDA graphs"}
     return {"value": out[best], "unit": "tokens/s", "h2d_bytes_per_step": total,
             "d2h_bytes_per_step": d2h, "steps": steps, "mode": best, "how": how[best],
             "by_mode": out}

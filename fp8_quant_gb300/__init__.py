@@ -107,6 +107,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kv_store_noalloc.restype = I32
         lib.kv_error_poll.argtypes = [P, P, ctypes.POINTER(I64), ctypes.POINTER(I64)]
         lib.kv_error_poll.restype = I32
+        lib.kv_error_snapshot.argtypes = [P, P, P]
+        lib.kv_error_snapshot.restype = I32
         lib.kv_error_reset.argtypes = [P, P]
         lib.kv_error_reset.restype = I32
         lib.kv_status_str.argtypes = [I32]
@@ -247,6 +249,10 @@ class raw:
         first = ctypes.c_int64(0)
         rc = load_library().kv_error_poll(d_err, stream, ctypes.byref(n), ctypes.byref(first))
         return rc, n.value, first.value
+
+    @staticmethod
+    def kv_error_snapshot(d_err, dst, stream) -> int:
+        return load_library().kv_error_snapshot(d_err, dst, stream)
 
     @staticmethod
     def kv_error_reset(d_err, stream) -> int:

@@ -775,6 +775,42 @@ extern "C" kv_status kv_error_poll(kv_error_record* d_err, kv_stream_t stream_, 
   return h.oob_count ? KV_ERR_INDEX_OOB : KV_OK;
 }
 
+namespace kvimpl {
+namespace {
+
+struct SnapshotParams {
+  const kv_error_record* src;
+  kv_error_record* dst;
+};
+
+// Copies the record after the preceding grid has finished (programmatic
+// launch wait), so a captured step can hand its status to the host without a
+// copy-engine round trip.
+__global__ void __launch_bounds__(kThreads) kv_error_snapshot_kernel(const __grid_constant__ SnapshotParams p) {
+  grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    const unsigned long long n = *reinterpret_cast<const volatile unsigned long long*>(&p.src->oob_count);
+    const unsigned long long f = *reinterpret_cast<const volatile unsigned long long*>(&p.src->first_bad_key);
+    p.dst->oob_count = n;
+    p.dst->first_bad_key = f;
+  }
+}
+
+}  // namespace
+}  // namespace kvimpl
+
+extern "C" kv_status kv_error_snapshot(const kv_error_record* d_err, kv_error_record* dst,
+                                       kv_stream_t stream_) {
+  if (!d_err || !dst || ((u64(d_err) | u64(dst)) & 7u) != 0) return KV_ERR_INVALID_ARG;
+  bool on_device = true;
+  const void* ptrs[2] = {d_err, dst};
+  const kv_status cs = classify_inputs(ptrs, 2, &on_device);
+  if (cs != KV_OK) return cs;
+  return launch(kv_error_snapshot_kernel, kWarpsPerCta, SnapshotParams{d_err, dst},
+                reinterpret_cast<cudaStream_t>(stream_));
+}
+
 extern "C" kv_status kv_error_reset(kv_error_record* d_err, kv_stream_t stream_) {
   if (!d_err || (u64(d_err) & 7u) != 0) return KV_ERR_INVALID_ARG;
   const cudaError_t e =

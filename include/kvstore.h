@@ -18,9 +18,15 @@
  * read on the device, e4m3fn conversion).
  *
  * Conventions shared by every call:
- *  - All tensor pointers are device memory owned by the caller; the library
- *    never allocates, frees or retains them, and never allocates memory of
- *    its own during a call.
+ *  - All tensor pointers are memory owned by the caller; the library never
+ *    allocates, frees or retains them, and never allocates memory of its own
+ *    during a call.  Caches, outputs and error records are device memory
+ *    (kv_error_snapshot may also write to page-locked host memory).  The
+ *    inputs of the write calls (k, v, indices) may also be page-locked host
+ *    memory (cudaHostAlloc / cudaHostRegister), which the kernels read in
+ *    place over NVLink-C2C or PCIe; pointers CUDA does not know (pageable
+ *    host memory, stray addresses) are rejected with KV_ERR_INVALID_ARG
+ *    before anything is launched.
  *  - Calls are asynchronous on `stream` and do not synchronise the host,
  *    except kv_error_poll.  They may be captured in a CUDA graph.
  *  - Every kernel launched here waits for the work that precedes it on the
@@ -377,6 +383,16 @@ kv_status kv_store_noalloc(const void *k, const void *v, void *k_cache, void *v_
  */
 kv_status kv_error_poll(kv_error_record *d_err, kv_stream_t stream, int64_t *oob_count,
                         int64_t *first_bad_token);
+
+/* kv_error_snapshot -- copy the record to `dst` asynchronously on `stream`,
+ * as it stands once the work before it on the stream has finished.  A small
+ * kernel (capturable, chained by programmatic launch), so a captured step can
+ * hand its status to the host without a copy-engine transfer: `dst` may be
+ * device memory or page-locked host memory (read it after synchronising).
+ * The record is not cleared.  Both pointers 8-byte aligned; memory unknown to
+ * CUDA is rejected with KV_ERR_INVALID_ARG. */
+kv_status kv_error_snapshot(const kv_error_record *d_err, kv_error_record *dst,
+                            kv_stream_t stream);
 
 /* kv_error_reset -- zero the record asynchronously on `stream` (capturable). */
 kv_status kv_error_reset(kv_error_record *d_err, kv_stream_t stream);

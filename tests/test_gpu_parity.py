@@ -350,3 +350,26 @@ def test_unregistered_host_memory_is_rejected():
     assert rc == kv.KVStatus.ERR_INVALID_ARG
     kc, _ = g.caches()
     assert np.all(kc.view(np.uint16) == wl.BF16_SENTINEL)
+
+
+def test_error_snapshot_to_pinned_host_and_device():
+    import torch
+    import fp8_quant_gb300 as kv
+    slots = wl.distinct_slots(611, 1000, 300)
+    slots[[7, 9]] = [-1, 5000]
+    p = copy_problem(T=300, H=2, D=64, n_slots=1000, seed=612, slots=slots)
+    g = GpuRun(p)
+    assert g.call() == 0
+    s = torch.cuda.current_stream().cuda_stream
+    host = torch.zeros(2, dtype=torch.int64).pin_memory()
+    dev = torch.zeros(2, dtype=torch.int64, device="cuda")
+    assert kv.raw.kv_error_snapshot(g.err.data_ptr(), host.data_ptr(), s) == 0
+    assert kv.raw.kv_error_snapshot(g.err.data_ptr(), dev.data_ptr(), s) == 0
+    torch.cuda.synchronize()
+    n, key = (int(x) for x in host.numpy().view(np.uint64))
+    assert n == 2 and (~key & 0xFFFFFFFFFFFFFFFF) == 7
+    assert torch.equal(dev.cpu(), host)
+    assert g.poll()[:3] == (4, 2, 7)           # the snapshot left the record intact
+    unregistered = np.zeros(2, np.int64)
+    assert kv.raw.kv_error_snapshot(g.err.data_ptr(), unregistered.ctypes.data,
+                                    s) == kv.KVStatus.ERR_INVALID_ARG
