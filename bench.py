@@ -620,18 +620,28 @@ def run_ours(args, dist):
         print(json.dumps(line), flush=True)
 
 
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources (csrc/, sorted by name): what the traffic
+    counters in profiles/ were taken with."""
+    import hashlib
+    csrc = os.path.join(ROOT, "fp8_quant_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()
+
+
 def load_traffic(name):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source has changed since those counters were taken."""
-    import hashlib
+    kernel sources have changed since those counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "fp8_quant_gb300", "csrc", "kvstore.cu")
     try:
         with open(path) as f:
             d = json.load(f)
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
-        if not sha.startswith(d["source_sha256_prefix"]):
+        if not kernel_source_hash().startswith(d["source_sha256_prefix"]):
             return None
         return d.get(name)
     except Exception:
