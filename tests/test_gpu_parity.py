@@ -373,3 +373,78 @@ def test_error_snapshot_to_pinned_host_and_device():
     unregistered = np.zeros(2, np.int64)
     assert kv.raw.kv_error_snapshot(g.err.data_ptr(), unregistered.ctypes.data,
                                     s) == kv.KVStatus.ERR_INVALID_ARG
+
+
+def test_concurrent_streams_disjoint_slots():
+    """A copy and an FP8 write on two streams at once, into different caches
+    with disjoint slots, each with its own error record: both equal the oracle."""
+    import torch
+    import fp8_quant_gb300 as kv
+    pc = copy_problem(T=3000, H=8, D=128, n_slots=8192, seed=621)
+    pf = fp8_problem(T=3000, H=8, D=128, n_slots=8192, seed=622, page_size=16)
+    gc, gf = GpuRun(pc), GpuRun(pf)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        assert gc.call(stream=s1.cuda_stream) == 0
+        assert gf.call(stream=s2.cuda_stream) == 0
+    torch.cuda.synchronize()
+    for g, p in ((gc, pc), (gf, pf)):
+        kc, vc = g.caches()
+        okc, ovc, _ = run_oracle(p)
+        assert np.array_equal(kc, okc) and np.array_equal(vc, ovc)
+        assert g.poll()[:2] == (0, 0)
+
+
+def test_graph_of_dynamic_fp8_write_and_gather():
+    """kv_store_fp8_ex (per-head dynamic scales) then kv_gather_fp8_ex captured
+    in one CUDA graph and replayed on new data: equals the eager calls."""
+    import torch
+    import fp8_quant_gb300 as kv
+    T, H, D, n, ps = 512, 8, 128, 4096, 16
+    dev = torch.device("cuda")
+    k = torch.randn(T, H, D, device=dev, dtype=torch.bfloat16)
+    v = torch.randn(T, H, D, device=dev, dtype=torch.bfloat16)
+    idx = torch.randperm(n, device=dev)[:T]
+    kc = torch.zeros(n, H, D, dtype=torch.uint8, device=dev)
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros(n, H, dtype=torch.float32, device=dev)
+    vs = torch.zeros_like(ks)
+    ko = torch.zeros(T, H, D, dtype=torch.bfloat16, device=dev)
+    vo = torch.zeros_like(ko)
+    err = kv.error_record(dev)
+    R = H * D * 2
+    st_in = (R, D * 2, 2, R, D * 2, 2, H * D, D, 1, H * D, D, 1)
+
+    def step(stream):
+        s = stream.cuda_stream
+        assert kv.raw.kv_store_fp8_ex(k.data_ptr(), v.data_ptr(), kc.data_ptr(), vc.data_ptr(),
+                                      idx.data_ptr(), 1, 1, T, H, D, 1, st_in, ps, ps * H * D,
+                                      ps * H * D, n, 0, 3, None, None, ks.data_ptr(),
+                                      vs.data_ptr(), H, err.data_ptr(), s) == 0
+        assert kv.raw.kv_gather_fp8_ex(kc.data_ptr(), vc.data_ptr(), ko.data_ptr(), vo.data_ptr(),
+                                       idx.data_ptr(), 1, 1, T, H, D, 1, st_in, ps, ps * H * D,
+                                       ps * H * D, n, 0, 3, None, None, ks.data_ptr(),
+                                       vs.data_ptr(), H, err.data_ptr(), s) == 0
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(side)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(torch.cuda.current_stream())
+    k.normal_()
+    v.normal_()
+    g.replay()
+    torch.cuda.synchronize()
+    got = (ko.clone(), vo.clone(), kc.clone(), ks.clone())
+    step(torch.cuda.current_stream())            # eager on the same new data
+    torch.cuda.synchronize()
+    assert torch.equal(got[0], ko) and torch.equal(got[1], vo)
+    assert torch.equal(got[2], kc) and torch.equal(got[3], ks)
+    # and the dequantised rows are close to the inputs (per-head e4m3fn scale)
+    rel = ((ko.float() - k.float()).abs() / (k.float().abs() + ks[idx][:, :, None] * 2 ** -9))
+    assert float(rel.max()) < 0.07
+    assert kv.kv_error_poll(err)[1] == 0
