@@ -10,8 +10,7 @@
 // The absmax pass is a pure HBM read stream: one warp per row with all of the
 // row's loads in flight, CTAs reduce their warps in shared memory, and one
 // atomicMax per CTA and tensor lands on the float bits of the caller's amax
-// output (for non-negative floats the bit patterns order like the values);
-// the last CTA to finish computes the inverse scales (no extra launch).
+// output (for non-negative floats the bit patterns order like the values).
 #include "kv_host.h"
 
 #ifndef KV_ABSMAX_CTAS_PER_SM
@@ -40,9 +39,6 @@ struct AbsmaxParams {
   int64_t token[2], seg[2];  // byte strides of the rows and of their segments
   UnitShape shape;           // units: (token, K|V, segment); parts = 1
   unsigned int* amax_bits;   // two words: K, V (the caller's amax output)
-  float* inv;                // two words: the caller's inv output; inv[0] counts
-                             // finished CTAs until the last one overwrites it
-  float fmax;
 };
 
 // |x| of the two 2-byte elements in `w`, folded into m (fmaxf ignores NaN).
@@ -102,31 +98,15 @@ __global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant
 #pragma unroll
     for (int i = 0; i < kWarpsPerCta; ++i) v = fmaxf(v, part[threadIdx.x][i]);
     if (v > 0.0f) atomicMax(p.amax_bits + threadIdx.x, __float_as_uint(v));
-    __threadfence();  // this CTA's maxima are visible before it counts itself done
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    // The last CTA to finish turns the maxima into inverse scales; it waits
-    // for nothing (every other CTA has already counted itself).
-    unsigned int* counter = reinterpret_cast<unsigned int*>(p.inv);
-    if (atomicAdd(counter, 1u) == gridDim.x - 1) {
-      __threadfence();
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-        const float a = __uint_as_float(atomicAdd(p.amax_bits + kv, 0u));
-        p.inv[kv] = a > 0.0f ? __fdiv_rn(p.fmax, a) : 1.0f;
-      }
-    }
   }
 }
 
-// Clears the two accumulator words and the CTA counter.  A kernel rather than
-// a memset so that zeroing and reduction chain by programmatic launch.
+// Clears the two accumulator words.  A kernel rather than a memset so that
+// zeroing, reduction and finish chain by programmatic launch.
 __global__ void __launch_bounds__(kThreads) kv_absmax_zero(const __grid_constant__ AbsmaxParams p) {
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
   if (blockIdx.x == 0 && threadIdx.x < 2) p.amax_bits[threadIdx.x] = 0u;
-  if (blockIdx.x == 0 && threadIdx.x == 2) *reinterpret_cast<unsigned int*>(p.inv) = 0u;
 }
 
 struct FinishParams {
@@ -181,7 +161,6 @@ extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype sr
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   AbsmaxParams zp = {};
   zp.amax_bits = reinterpret_cast<unsigned int*>(amax);
-  zp.inv = inv;
   kv_status st = launch(kv_absmax_zero, kWarpsPerCta, zp, stream);
   if (st != KV_OK) return st;
   if (num_tokens > 0) {
@@ -205,8 +184,6 @@ extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype sr
     p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
     p.shape.part_chunks = static_cast<uint32_t>(seg_bytes / vec);
     p.amax_bits = reinterpret_cast<unsigned int*>(amax);
-    p.inv = inv;
-    p.fmax = fp8_max;
     // a few resident waves of CTAs loop over the rows, so only a few hundred
     // same-address atomics land at the end
     int sms = 0;
@@ -223,9 +200,8 @@ extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype sr
       case 4: st = launch_absmax<4>(bf16, p, stream, max_ctas); break;
       default: st = launch_absmax<2>(bf16, p, stream, max_ctas); break;
     }
-    return st;
+    if (st != KV_OK) return st;
   }
-  // an empty tensor: no reduction ran, so write amax = 0 and inv = 1 here
   return launch(kv_absmax_finish, kWarpsPerCta,
                 FinishParams{reinterpret_cast<const unsigned int*>(amax), inv, fp8_max}, stream);
 }

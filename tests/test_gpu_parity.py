@@ -444,7 +444,11 @@ def test_graph_of_dynamic_fp8_write_and_gather():
     torch.cuda.synchronize()
     assert torch.equal(got[0], ko) and torch.equal(got[1], vo)
     assert torch.equal(got[2], kc) and torch.equal(got[3], ks)
-    # and the dequantised rows are close to the inputs (per-head e4m3fn scale)
-    rel = ((ko.float() - k.float()).abs() / (k.float().abs() + ks[idx][:, :, None] * 2 ** -9))
-    assert float(rel.max()) < 0.07
+    # and the dequantised rows are close to the inputs: half an e4m3fn step
+    # (relative 2^-4 for normals, absolute 2^-10 of the head's scale for
+    # subnormals) plus the bf16 rounding of the output
+    x = k.float()
+    sc = ks[idx][:, :, None]
+    bound = x.abs() * (2 ** -4 + 2 ** -8) + sc * 2 ** -10 * 1.01
+    assert bool(((ko.float() - x).abs() <= bound).all())
     assert kv.kv_error_poll(err)[1] == 0
