@@ -84,6 +84,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kv_gather.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
                                   ctypes.POINTER(_Strides), I64, P, P]
         lib.kv_gather.restype = I32
+        lib.kv_gather_paged.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
+                                        ctypes.POINTER(_Strides), I64, I64, I64, I64, P, P]
+        lib.kv_gather_paged.restype = I32
         lib.kv_gather_fp8.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
                                       ctypes.POINTER(_Strides), I64, I64, I64, I64, P, P, I32, P,
                                       P]
@@ -175,6 +178,18 @@ class raw:
         return load_library().kv_gather(k_cache, v_cache, k_out, v_out, indices, index_dtype,
                                         index_stride, num_tokens, num_heads, head_dim, elem_bytes,
                                         ctypes.byref(st), size_limit, d_err, stream)
+
+    @staticmethod
+    def kv_gather_paged(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
+                        num_tokens, num_heads, head_dim, elem_bytes, strides: Sequence[int],
+                        page_size, kc_page_stride, vc_page_stride, size_limit, d_err,
+                        stream) -> int:
+        st = _Strides(*[int(x) for x in strides])
+        return load_library().kv_gather_paged(k_cache, v_cache, k_out, v_out, indices,
+                                              index_dtype, index_stride, num_tokens, num_heads,
+                                              head_dim, elem_bytes, ctypes.byref(st), page_size,
+                                              kc_page_stride, vc_page_stride, size_limit, d_err,
+                                              stream)
 
     @staticmethod
     def kv_gather_fp8(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,

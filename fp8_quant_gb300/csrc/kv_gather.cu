@@ -407,11 +407,15 @@ GatherElemParams element_params(const void* k_cache, const void* v_cache, void* 
 
 using namespace kvimpl;
 
-extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k_out, void* v_out,
-                               const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
-                               int64_t num_tokens, int32_t num_heads, int32_t head_dim,
-                               int32_t elem_bytes, const kv_strides* s, int64_t size_limit,
-                               kv_error_record* d_err, kv_stream_t stream_) {
+namespace {
+
+// kv_gather and kv_gather_paged.
+kv_status gather_copy(const void* k_cache, const void* v_cache, void* k_out, void* v_out,
+                      const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
+                      int64_t num_tokens, int32_t num_heads, int32_t head_dim, int32_t elem_bytes,
+                      const kv_strides* s, int64_t page_size, int64_t kc_page_stride,
+                      int64_t vc_page_stride, int64_t size_limit, kv_error_record* d_err,
+                      kv_stream_t stream_) {
   if (num_tokens < 0) return KV_ERR_INVALID_ARG;
   if (num_tokens == 0) return KV_OK;
   if (!common_args_ok(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
@@ -419,13 +423,15 @@ extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k
     return KV_ERR_INVALID_ARG;
   if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
     return KV_ERR_INVALID_ARG;
+  if (page_size < 1) return KV_ERR_INVALID_ARG;
+  const bool flat = kc_page_stride == page_size * s->kc_slot && vc_page_stride == page_size * s->vc_slot;
   if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const bool i64 = index_dtype == KV_INDEX_I64;
   bool on_device = true;
   {
-    const void* in[4] = {k_cache, v_cache, indices, k_out};
-    const kv_status cs = classify_inputs(in, 4, &on_device);
+    const void* in[5] = {k_cache, v_cache, indices, k_out, v_out};
+    const kv_status cs = classify_inputs(in, 5, &on_device);
     if (cs != KV_OK) return cs;
   }
 
@@ -434,6 +440,9 @@ extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k
     GatherElemParams g = element_params(k_cache, v_cache, k_out, v_out, indices, index_stride,
                                         num_tokens, num_heads, head_dim, s, size_limit, d_err);
     g.elem_bytes = elem_bytes;
+    g.cache_page[0] = flat ? s->kc_slot : kc_page_stride;
+    g.cache_page[1] = flat ? s->vc_slot : vc_page_stride;
+    g.page_size = flat ? 1 : page_size;
     return i64 ? launch_gather_elements<int64_t>(0, kFmtE4M3, g, stream)
                : launch_gather_elements<int32_t>(0, kFmtE4M3, g, stream);
   }
@@ -443,6 +452,7 @@ extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k
   uint64_t bits = u64(k_cache) | u64(v_cache) | u64(k_out) | u64(v_out) | u64(s->k_token) |
                   u64(s->v_token) | u64(s->kc_slot) | u64(s->vc_slot) | u64(seg_bytes);
   if (sg.count > 1) bits |= u64(s->k_head) | u64(s->v_head) | u64(s->kc_head) | u64(s->vc_head);
+  if (!flat) bits |= u64(kc_page_stride) | u64(vc_page_stride);
   int sms = 0;
   kv_status st = current_sm_count(&sms);
   if (st != KV_OK) return st;
@@ -454,13 +464,15 @@ extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k
 
   GatherParams p = {};
   p.side[0] = GatherSide{static_cast<const uint8_t*>(k_cache), static_cast<uint8_t*>(k_out),
-                         s->kc_slot, s->kc_head, s->kc_slot, s->k_token, s->k_head, nullptr, nullptr};
+                         s->kc_slot, s->kc_head, flat ? s->kc_slot : kc_page_stride, s->k_token,
+                         s->k_head, nullptr, nullptr};
   p.side[1] = GatherSide{static_cast<const uint8_t*>(v_cache), static_cast<uint8_t*>(v_out),
-                         s->vc_slot, s->vc_head, s->vc_slot, s->v_token, s->v_head, nullptr, nullptr};
+                         s->vc_slot, s->vc_head, flat ? s->vc_slot : vc_page_stride, s->v_token,
+                         s->v_head, nullptr, nullptr};
   p.indices = indices;
   p.index_stride = index_stride;
   p.size_limit = size_limit;
-  p.page_size = 1;
+  p.page_size = flat ? 1 : page_size;
   p.shape.parts = parts;
   p.shape.units_per_side = sg.count * parts;
   p.shape.units_per_token = 2u * p.shape.units_per_side;
@@ -470,6 +482,32 @@ extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k
   p.vec = vec;
   p.prefetch = vec >= 16 && on_device ? 1 : 0;
   return i64 ? launch_gather<int64_t>(vec, p, stream) : launch_gather<int32_t>(vec, p, stream);
+}
+
+}  // namespace
+
+extern "C" kv_status kv_gather(const void* k_cache, const void* v_cache, void* k_out, void* v_out,
+                               const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
+                               int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                               int32_t elem_bytes, const kv_strides* s, int64_t size_limit,
+                               kv_error_record* d_err, kv_stream_t stream) {
+  const int64_t kpage = s != nullptr ? s->kc_slot : 0;
+  const int64_t vpage = s != nullptr ? s->vc_slot : 0;
+  return gather_copy(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
+                     num_tokens, num_heads, head_dim, elem_bytes, s, 1, kpage, vpage, size_limit,
+                     d_err, stream);
+}
+
+extern "C" kv_status kv_gather_paged(const void* k_cache, const void* v_cache, void* k_out,
+                                     void* v_out, const void* indices, kv_index_dtype index_dtype,
+                                     int64_t index_stride, int64_t num_tokens, int32_t num_heads,
+                                     int32_t head_dim, int32_t elem_bytes, const kv_strides* s,
+                                     int64_t page_size, int64_t kc_page_stride,
+                                     int64_t vc_page_stride, int64_t size_limit,
+                                     kv_error_record* d_err, kv_stream_t stream) {
+  return gather_copy(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
+                     num_tokens, num_heads, head_dim, elem_bytes, s, page_size, kc_page_stride,
+                     vc_page_stride, size_limit, d_err, stream);
 }
 
 namespace {
@@ -506,8 +544,8 @@ kv_status gather_fp8(const void* k_cache, const void* v_cache, void* k_out, void
   const bool bf16 = out_dtype == KV_SRC_BF16;
   bool on_device = true;
   {
-    const void* in[4] = {k_cache, v_cache, indices, k_out};
-    const kv_status cs = classify_inputs(in, 4, &on_device);
+    const void* in[5] = {k_cache, v_cache, indices, k_out, v_out};
+    const kv_status cs = classify_inputs(in, 5, &on_device);
     if (cs != KV_OK) return cs;
   }
   const float* sk = scale_mode == KV_SCALE_TENSOR ? k_scale : nullptr;

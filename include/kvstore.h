@@ -20,13 +20,14 @@
  * Conventions shared by every call:
  *  - All tensor pointers are memory owned by the caller; the library never
  *    allocates, frees or retains them, and never allocates memory of its own
- *    during a call.  Caches, outputs and error records are device memory
+ *    during a call.  Caches and error records are device memory
  *    (kv_error_snapshot may also write to page-locked host memory).  The
- *    inputs of the write calls (k, v, indices) may also be page-locked host
- *    memory (cudaHostAlloc / cudaHostRegister), which the kernels read in
- *    place over NVLink-C2C or PCIe; pointers CUDA does not know (pageable
- *    host memory, stray addresses) are rejected with KV_ERR_INVALID_ARG
- *    before anything is launched.
+ *    token-major side of every call -- the inputs of the writes (k, v) and
+ *    the outputs of the gathers (k_out, v_out) -- and the slot ids may also
+ *    be page-locked host memory (cudaHostAlloc / cudaHostRegister), which the
+ *    kernels read or write in place over NVLink-C2C or PCIe.  Pointers CUDA
+ *    does not know (pageable host memory, stray addresses) are rejected with
+ *    KV_ERR_INVALID_ARG before anything is launched.
  *  - Calls are asynchronous on `stream` and do not synchronise the host,
  *    except kv_error_poll.  They may be captured in a CUDA graph.
  *  - Every kernel launched here waits for the work that precedes it on the
@@ -208,6 +209,20 @@ kv_status kv_gather(const void *k_cache, const void *v_cache, void *k_out, void 
                     int64_t num_tokens, int32_t num_heads, int32_t head_dim,
                     int32_t elem_bytes, const kv_strides *strides, int64_t size_limit,
                     kv_error_record *d_err, kv_stream_t stream);
+
+/*
+ * kv_gather_paged -- kv_gather from a paged cache [pages, page_size, H, D]
+ * (the inverse of kv_store_paged): slot s is read at
+ * (s / page_size) * kc_page_stride + (s % page_size) * kc_slot + ... .
+ * Other arguments and errors as kv_gather, plus KV_ERR_INVALID_ARG for
+ * page_size < 1.
+ */
+kv_status kv_gather_paged(const void *k_cache, const void *v_cache, void *k_out, void *v_out,
+                          const void *indices, kv_index_dtype index_dtype, int64_t index_stride,
+                          int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                          int32_t elem_bytes, const kv_strides *strides, int64_t page_size,
+                          int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
+                          kv_error_record *d_err, kv_stream_t stream);
 
 /*
  * kv_gather_fp8 -- dequantising gather from e4m3fn caches written by

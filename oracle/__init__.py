@@ -87,6 +87,8 @@ def _load():
         lib.kvo_gather_fp8_ex.restype = I32
         lib.kvo_gather_copy.argtypes = lib.kvo_store_copy.argtypes
         lib.kvo_gather_copy.restype = I32
+        lib.kvo_gather_copy_paged.argtypes = lib.kvo_store_copy_paged.argtypes
+        lib.kvo_gather_copy_paged.restype = I32
         lib.kvo_gather_fp8.argtypes = lib.kvo_store_fp8.argtypes
         lib.kvo_gather_fp8.restype = I32
         lib.kvo_f32_to_bf16_array.argtypes = [P, P, I64]
@@ -252,6 +254,26 @@ def gather_copy(k_cache, v_cache, k_out, v_out, indices, strides: Strides, num_h
                                  _ptr(v_out), _ptr(idx), int(idx.dtype == np.int64), index_stride,
                                  0, T, num_heads, head_dim, elem_bytes, _ptr(strides.values),
                                  size_limit, _ptr(bad), _ptr(first))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return int(bad[0]), int(first[0])
+
+
+def gather_copy_paged(k_cache, v_cache, k_out, v_out, indices, strides: Strides, num_heads,
+                      head_dim, elem_bytes, page_size, kc_page_stride, vc_page_stride,
+                      size_limit, index_stride=1, t_end=None):
+    """Gather from a paged cache (the inverse of store_copy_paged)."""
+    for a, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_out, "k_out"), (v_out, "v_out")):
+        _check_buf(a, n)
+    idx = np.ascontiguousarray(indices)
+    T = idx.size // index_stride if t_end is None else t_end
+    bad = np.zeros(1, np.int64)
+    first = np.zeros(1, np.int64)
+    rc = _load().kvo_gather_copy_paged(_ptr(k_cache), _ptr(v_cache), _ptr(k_out), _ptr(v_out),
+                                       _ptr(idx), int(idx.dtype == np.int64), index_stride, 0, T,
+                                       num_heads, head_dim, elem_bytes, _ptr(strides.values),
+                                       page_size, kc_page_stride, vc_page_stride, size_limit,
+                                       _ptr(bad), _ptr(first))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return int(bad[0]), int(first[0])

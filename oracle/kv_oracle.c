@@ -380,6 +380,43 @@ int kvo_gather_copy(const uint8_t *k_cache, const uint8_t *v_cache, uint8_t *k_o
     return KVO_OK;
 }
 
+/* Paged gather (the inverse of the paged copy): slot s is read at
+ * (s / page_size) * page_stride + (s % page_size) * slot_stride + ... . */
+int kvo_gather_copy_paged(const uint8_t *k_cache, const uint8_t *v_cache, uint8_t *k_out,
+                          uint8_t *v_out, const void *indices, int index_is_i64,
+                          int64_t index_stride, int64_t t_begin, int64_t t_end, int32_t num_heads,
+                          int32_t head_dim, int32_t elem_bytes, const int64_t *strides,
+                          int64_t page_size, int64_t kc_page_stride, int64_t vc_page_stride,
+                          int64_t size_limit, int64_t *bad_count, int64_t *first_bad)
+{
+    if (elem_bytes <= 0 || num_heads <= 0 || head_dim <= 0 || page_size <= 0 || t_begin > t_end)
+        return KVO_ERR_ARG;
+    *bad_count = 0;
+    *first_bad = -1;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        int64_t slot = read_index(indices, index_is_i64, index_stride, t);
+        if (slot < 0 || slot >= size_limit) {
+            note_bad(t, bad_count, first_bad);
+            continue;
+        }
+        int64_t page_id = slot / page_size;
+        int64_t page_offset = slot % page_size;
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint8_t *src = kv ? v_cache : k_cache;
+            uint8_t *dst = kv ? v_out : k_out;
+            const int64_t *os = strides + 3 * kv;
+            const int64_t *cs = strides + 6 + 3 * kv;
+            int64_t page_stride = kv ? vc_page_stride : kc_page_stride;
+            for (int32_t h = 0; h < num_heads; ++h)
+                for (int32_t d = 0; d < head_dim; ++d)
+                    memcpy(dst + t * os[0] + h * os[1] + d * os[2],
+                           src + page_id * page_stride + page_offset * cs[0] + h * cs[1] + d * cs[2],
+                           (size_t)elem_bytes);
+        }
+    }
+    return KVO_OK;
+}
+
 /* FP8 gather with dequantisation: each e4m3fn code is decoded exactly,
  * multiplied by the fp32 scale (when use_scale), and rounded to bf16
  * (out_is_bf16) or fp16.  The cache address of slot s is

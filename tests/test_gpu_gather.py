@@ -88,21 +88,32 @@ def make(kind, T, H, D, n, seed, elem=2, idx_dtype=np.int64, index_stride=1, slo
 SENT = bytes([0xC0, 0x7F])
 
 
-def run_both(g: G):
+def run_both(g: G, host_out=False):
+    """host_out: the gathered rows are written straight into pinned host memory."""
     import torch
     import fp8_quant_gb300 as kv
     dev = torch.device("cuda")
     filled = np.frombuffer(SENT * (g.out_bytes // 2 + 1), np.uint8)[:g.out_bytes].copy()
     kc = torch.from_numpy(g.cache).to(dev)
     vc = torch.from_numpy(g.vcache).to(dev)
-    ko = torch.from_numpy(filled).to(dev)
-    vo = ko.clone()
+    if host_out:
+        ko = torch.from_numpy(filled.copy()).pin_memory()
+        vo = torch.from_numpy(filled.copy()).pin_memory()
+    else:
+        ko = torch.from_numpy(filled).to(dev)
+        vo = ko.clone()
     idx = torch.from_numpy(g.idx).to(dev)
     err = torch.zeros(2, dtype=torch.int64, device=dev)
     sc = torch.tensor([g.scale, g.scale], dtype=torch.float32, device=dev)
     s = torch.cuda.current_stream().cuda_stream
     idt = 1 if g.idx.dtype == np.int64 else 0
-    if g.kind == "copy":
+    paged_copy = g.kind == "copy" and g.cpage != g.page_size * g.cslot
+    if paged_copy:
+        rc = kv.raw.kv_gather_paged(kc.data_ptr(), vc.data_ptr(), ko.data_ptr() + g.ooff,
+                                    vo.data_ptr() + g.ooff, idx.data_ptr(), idt, g.index_stride,
+                                    g.T, g.H, g.D, g.elem, g.strides(), g.page_size, g.cpage,
+                                    g.cpage, g.size_limit, err.data_ptr(), s)
+    elif g.kind == "copy":
         rc = kv.raw.kv_gather(kc.data_ptr(), vc.data_ptr(), ko.data_ptr() + g.ooff,
                               vo.data_ptr() + g.ooff, idx.data_ptr(), idt, g.index_stride, g.T,
                               g.H, g.D, g.elem, g.strides(), g.size_limit, err.data_ptr(), s)
@@ -116,12 +127,17 @@ def run_both(g: G):
                                   err.data_ptr(), s)
     assert rc == 0, kv.kv_status_str(rc)
     prc, pn, pfirst = kv.raw.kv_error_poll(err.data_ptr(), s)
-    gk, gv = ko.cpu().numpy(), vo.cpu().numpy()
+    torch.cuda.synchronize()
+    gk, gv = ko.cpu().numpy().copy(), vo.cpu().numpy().copy()
 
     ok, ov = filled.copy(), filled.copy()
     st = oracle.Strides(**dict(zip(oracle.Strides.FIELDS, g.strides())))
     okv, ovv = ok[g.ooff:], ov[g.ooff:]
-    if g.kind == "copy":
+    if paged_copy:
+        res = oracle.gather_copy_paged(g.cache, g.vcache, okv, ovv, g.idx, st, g.H, g.D, g.elem,
+                                       g.page_size, g.cpage, g.cpage, g.size_limit,
+                                       index_stride=g.index_stride, t_end=g.T)
+    elif g.kind == "copy":
         res = oracle.gather_copy(g.cache, g.vcache, okv, ovv, g.idx, st, g.H, g.D, g.elem,
                                  g.size_limit, index_stride=g.index_stride, t_end=g.T)
     else:
@@ -148,6 +164,11 @@ COPY = {
     "index_stride2": dict(T=513, H=8, D=128, n=2000, index_stride=2, idx_dtype=np.int32),
     "small_batch": dict(T=3, H=8, D=128, n=64),
     "oob": dict(T=600, H=8, D=128, n=2000, bad=((0, -1), (17, 2000), (599, 2 ** 40))),
+    # kv_gather_paged: padded pages
+    "paged_padded_16": dict(T=700, H=8, D=128, n=4096, page_size=16, page_pad=512),
+    "paged_odd_rows": dict(T=500, H=1, D=576, n=2048, page_size=32, page_pad=128, slot_pad=128,
+                           idx_dtype=np.int32),
+    "paged_page7_generic": dict(T=300, H=2, D=20, n=700, page_size=7, page_pad=12, dim_mult=2),
 }
 
 FP8 = {
@@ -220,3 +241,15 @@ def test_store_fp8_then_gather_round_trip():
                       n, float(sk), float(sv), 1)
     assert np.array_equal(ko.view(torch.int16).cpu().numpy().view(np.uint16).ravel(), ok)
     assert np.array_equal(vo.view(torch.int16).cpu().numpy().view(np.uint16).ravel(), ov)
+
+
+@pytest.mark.parametrize("kind", ["copy", "fp8"])
+def test_gather_into_pinned_host_memory(kind):
+    """Swap-out: the gathered (and dequantised) rows are written straight into
+    pinned host memory by the kernel."""
+    if kind == "copy":
+        g = make("copy", T=900, H=8, D=128, n=4096, seed=801)
+    else:
+        g = make("fp8", T=900, H=8, D=128, n=4096, seed=802, page_size=16, page_pad=64,
+                 scale=0.05)
+    run_both(g, host_out=True)

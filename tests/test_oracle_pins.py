@@ -711,3 +711,20 @@ def test_gather_fp8_ex_per_slot_scales(fmt):
     back = (ko.astype(np.uint32) << 16).view(np.float32).reshape(T, H, D)
     step = 2.0 ** -3 if fmt == "e4m3fn" else 2.0 ** -2
     assert np.all(np.abs(back - x) <= np.abs(x) * step + sc[:, :, None] * 2.0 ** -9 * 16)
+
+
+def test_paged_gather_round_trip():
+    T, H, D, n, ps, pad = 100, 4, 16, 512, 16, 96
+    k, v, idx, _, _, ss = _copy_problem(T, H, D, n, 85)
+    st = _contig_strides(H, D, 2)
+    page = ps * ss + pad
+    pk = np.full(n // ps * page // 2, wl.BF16_SENTINEL, np.uint16)
+    pv = pk.copy()
+    oracle.store_copy_paged(k, v, pk, pv, idx, st, H, D, 2, ps, page, page, n)
+    ko, vo = np.zeros_like(k), np.zeros_like(v)
+    bad = idx.copy()
+    bad[5] = -1
+    assert oracle.gather_copy_paged(pk, pv, ko, vo, bad, st, H, D, 2, ps, page, page, n) == (1, 5)
+    keep = np.arange(T) != 5
+    assert np.array_equal(ko[keep], k[keep]) and np.array_equal(vo[keep], v[keep])
+    assert np.all(ko[5] == 0)
