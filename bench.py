@@ -856,6 +856,9 @@ def main(argv=None):
         if dist.rank == 0:
             run_reference(args, dist)
         return
+    import torch
+    if torch.cuda.is_available():
+        torch.cuda.set_device(dist.local_rank)   # before the process group binds a device
     dist.init("nccl")
     try:
         run_ours(args, dist)
