@@ -8,6 +8,9 @@ the same names:
   (sglang ``kvcache.cuh``, ``store_kvcache``).
 * :func:`kv_store_fp8`  -- fused fp32 scale + FP8 e4m3fn conversion + paged
   scatter (sglang ``trtllm_fp8_kv_kernel.py``, ``fused_fp8_set_kv_buffer``).
+* :func:`kv_store_paged`, :func:`kv_store_fp8_ex` (e5m2, per-token scales),
+  :func:`kv_gather`, :func:`kv_gather_fp8` (the inverse), :func:`kv_inv_scale`,
+  :func:`kv_absmax_inv` (scale preparation).
 * :func:`kv_error_poll`, :func:`kv_error_reset`, :func:`kv_status_str`.
 
 The tensor-level functions take torch tensors (device memory and streams come
@@ -28,8 +31,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libkvstore.so")
 
 __all__ = [
-    "KVStatus", "KVError", "kv_store", "kv_store_fp8", "kv_error_poll", "kv_error_reset",
-    "kv_status_str", "error_record", "load_library", "raw", "STRIDE_FIELDS",
+    "KVStatus", "KVError", "kv_store", "kv_store_fp8", "kv_store_paged", "kv_store_fp8_ex",
+    "kv_gather", "kv_gather_fp8", "kv_inv_scale", "kv_absmax_inv", "kv_error_poll",
+    "kv_error_reset", "kv_status_str", "error_record", "load_library", "raw", "STRIDE_FIELDS",
 ]
 
 
@@ -445,3 +449,149 @@ def kv_error_reset(err=None, stream=None, device=None) -> None:
         err = _default_record(device or torch.device("cuda", torch.cuda.current_device()))
     _check(raw.kv_error_reset(err.data_ptr(), _stream_handle(stream, err.device)),
            "kv_error_reset")
+
+
+# ---------------------------------------------------------------------------
+# Tensor-level wrappers of the other entry points
+# ---------------------------------------------------------------------------
+
+FP8_FORMATS = {"e4m3fn": 0, "e5m2": 1}
+SCALE_MODES = {"none": 0, "tensor": 1, "token": 2, "token_head": 3}
+
+
+def _paged_cache(cache, page_size, H, D):
+    """(slot, head, dim, page) byte strides of a [slots, H, D] or [pages, ps, H, D] cache."""
+    if cache.dim() == 4:
+        if cache.shape[1] != page_size:
+            raise ValueError("page_size does not match the cache")
+        e = cache.element_size()
+        sp, ss, sh, sd = (x * e for x in cache.stride())
+        return ss, sh, sd, sp
+    ss, sh, sd = _rows3(cache, H, D)
+    return ss, sh, sd, ss * page_size
+
+
+def _device_ptr_or_none(t):
+    return None if t is None else t.data_ptr()
+
+
+def kv_store_paged(k, v, k_cache, v_cache, indices, *, page_size: int, size_limit=None,
+                   num_split: int = 0, err=None, stream=None) -> None:
+    """Plain copy into [pages, page_size, H, D] caches (any page stride)."""
+    slots, H, D = _cache_shape(k_cache)
+    e = k.element_size()
+    kt, kh, kd = _rows3(k, H, D)
+    vt, vh, vd = _rows3(v, H, D)
+    ks, khc, kdc, kp = _paged_cache(k_cache, page_size, H, D)
+    vs, vhc, vdc, vp = _paged_cache(v_cache, page_size, H, D)
+    idt, istride = _index_args(indices)
+    rec = err if err is not None else _default_record(k.device)
+    _check(raw.kv_store_paged(k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                              indices.data_ptr(), idt, istride, indices.shape[0], H, D, e,
+                              (kt, kh, kd, vt, vh, vd, ks, khc, kdc, vs, vhc, vdc), page_size, kp,
+                              vp, slots if size_limit is None else size_limit, num_split,
+                              rec.data_ptr(), _stream_handle(stream, k.device)), "kv_store_paged")
+
+
+def kv_store_fp8_ex(k, v, k_cache, v_cache, indices, *, page_size: int = 1,
+                    fmt: str = "e4m3fn", scale_mode: str = "none", inv_k_scale=None,
+                    inv_v_scale=None, k_scales=None, v_scales=None, size_limit=None, err=None,
+                    stream=None) -> None:
+    """FP8 write in e4m3fn / e5m2 with no, per-tensor, per-token or per-(token, head)
+    scales. Dynamic modes write the dequantisation scale of slot s (head h) to
+    k_scales[s, h] / v_scales[s, h] (fp32 device tensors [slots, >= groups])."""
+    slots, H, D = _cache_shape(k_cache)
+    kt, kh, kd = _rows3(k, H, D)
+    vt, vh, vd = _rows3(v, H, D)
+    ks, khc, kdc, kp = _paged_cache(k_cache, page_size, H, D)
+    vs, vhc, vdc, vp = _paged_cache(v_cache, page_size, H, D)
+    idt, istride = _index_args(indices)
+    sstride = 0
+    if k_scales is not None:
+        if k_scales.dim() != 2 or k_scales.stride(1) != 1 or v_scales.stride() != k_scales.stride():
+            raise ValueError("scale caches must be [slots, groups] with unit inner stride")
+        sstride = k_scales.stride(0)
+    rec = err if err is not None else _default_record(k.device)
+    import torch
+    _check(raw.kv_store_fp8_ex(
+        k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), indices.data_ptr(),
+        idt, istride, indices.shape[0], H, D, 1 if k.dtype == torch.bfloat16 else 0,
+        (kt, kh, kd, vt, vh, vd, ks, khc, kdc, vs, vhc, vdc), page_size, kp, vp,
+        slots if size_limit is None else size_limit, FP8_FORMATS[fmt], SCALE_MODES[scale_mode],
+        _device_ptr_or_none(inv_k_scale), _device_ptr_or_none(inv_v_scale),
+        _device_ptr_or_none(k_scales), _device_ptr_or_none(v_scales), sstride, rec.data_ptr(),
+        _stream_handle(stream, k.device)), "kv_store_fp8_ex")
+
+
+def kv_gather(k_cache, v_cache, k_out, v_out, indices, *, page_size: int = 1, size_limit=None,
+              err=None, stream=None) -> None:
+    """Row t of k_out / v_out takes the cache row of indices[t] (byte copy)."""
+    slots, H, D = _cache_shape(k_cache)
+    e = k_out.element_size()
+    kt, kh, kd = _rows3(k_out, H, D)
+    vt, vh, vd = _rows3(v_out, H, D)
+    ks, khc, kdc, kp = _paged_cache(k_cache, page_size, H, D)
+    vs, vhc, vdc, vp = _paged_cache(v_cache, page_size, H, D)
+    idt, istride = _index_args(indices)
+    rec = err if err is not None else _default_record(k_cache.device)
+    _check(raw.kv_gather_paged(k_cache.data_ptr(), v_cache.data_ptr(), k_out.data_ptr(),
+                               v_out.data_ptr(), indices.data_ptr(), idt, istride,
+                               indices.shape[0], H, D, e,
+                               (kt, kh, kd, vt, vh, vd, ks, khc, kdc, vs, vhc, vdc), page_size,
+                               kp, vp, slots if size_limit is None else size_limit,
+                               rec.data_ptr(), _stream_handle(stream, k_cache.device)),
+           "kv_gather")
+
+
+def kv_gather_fp8(k_cache, v_cache, k_out, v_out, indices, *, page_size: int = 1,
+                  fmt: str = "e4m3fn", scale_mode: str = "none", k_scale=None, v_scale=None,
+                  k_scales=None, v_scales=None, size_limit=None, err=None, stream=None) -> None:
+    """Dequantising gather into bf16 / fp16 rows (the dtype of k_out)."""
+    import torch
+    slots, H, D = _cache_shape(k_cache)
+    kt, kh, kd = _rows3(k_out, H, D)
+    vt, vh, vd = _rows3(v_out, H, D)
+    ks, khc, kdc, kp = _paged_cache(k_cache, page_size, H, D)
+    vs, vhc, vdc, vp = _paged_cache(v_cache, page_size, H, D)
+    idt, istride = _index_args(indices)
+    sstride = k_scales.stride(0) if k_scales is not None else 0
+    rec = err if err is not None else _default_record(k_cache.device)
+    _check(raw.kv_gather_fp8_ex(
+        k_cache.data_ptr(), v_cache.data_ptr(), k_out.data_ptr(), v_out.data_ptr(),
+        indices.data_ptr(), idt, istride, indices.shape[0], H, D,
+        1 if k_out.dtype == torch.bfloat16 else 0,
+        (kt, kh, kd, vt, vh, vd, ks, khc, kdc, vs, vhc, vdc), page_size, kp, vp,
+        slots if size_limit is None else size_limit, FP8_FORMATS[fmt], SCALE_MODES[scale_mode],
+        _device_ptr_or_none(k_scale), _device_ptr_or_none(v_scale),
+        _device_ptr_or_none(k_scales), _device_ptr_or_none(v_scales), sstride, rec.data_ptr(),
+        _stream_handle(stream, k_cache.device)), "kv_gather_fp8")
+
+
+def kv_inv_scale(scale, out=None, stream=None):
+    """1 / scale in fp32 on the device; returns `out` (a new tensor if None)."""
+    import torch
+    if scale.dtype != torch.float32 or not scale.is_contiguous():
+        raise TypeError("scale must be a contiguous fp32 tensor")
+    out = torch.empty_like(scale) if out is None else out
+    _check(raw.kv_inv_scale(scale.data_ptr(), out.data_ptr(), scale.numel(),
+                            _stream_handle(stream, scale.device)), "kv_inv_scale")
+    return out
+
+
+def kv_absmax_inv(k, v, *, fp8_max: float = 448.0, num_heads=None, head_dim=None, out=None,
+                  stream=None):
+    """Per-tensor max |K|, max |V| and fp8_max / amax on the device: returns a
+    4-float tensor [amax_k, amax_v, inv_k, inv_v]."""
+    import torch
+    if k.dim() == 3:
+        H, D = k.shape[1], k.shape[2]
+    else:
+        H, D = num_heads, head_dim
+    kt, kh, kd = _rows3(k, H, D)
+    vt, vh, vd = _rows3(v, H, D)
+    out = torch.empty(4, dtype=torch.float32, device=k.device) if out is None else out
+    _check(raw.kv_absmax_inv(k.data_ptr(), v.data_ptr(), 1 if k.dtype == torch.bfloat16 else 0,
+                             k.shape[0], H, D, (kt, kh, kd, vt, vh, vd, 0, 0, 0, 0, 0, 0), fp8_max,
+                             out.data_ptr(), out.data_ptr() + 8, _stream_handle(stream, k.device)),
+           "kv_absmax_inv")
+    return out

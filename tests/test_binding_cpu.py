@@ -95,3 +95,69 @@ def test_binding_rejects_mismatches(monkeypatch):
         kv.kv_store(k, k, kc, kc, torch.arange(5))
     with pytest.raises(ValueError):
         kv.kv_store(torch.zeros(4, 3, 8, dtype=torch.bfloat16), k, kc, kc, torch.arange(4))
+
+
+class CaptureAll(Capture):
+    def __init__(self, monkeypatch):
+        super().__init__(monkeypatch)
+        for name in ("kv_store_paged", "kv_store_fp8_ex", "kv_gather_paged", "kv_gather_fp8_ex",
+                     "kv_inv_scale", "kv_absmax_inv"):
+            monkeypatch.setattr(kv.raw, name, self._make(name))
+
+    def _make(self, name):
+        def f(*a):
+            self.calls.append((name, a))
+            return 0
+        return f
+
+
+def test_paged_and_gather_wrappers(monkeypatch):
+    cap = CaptureAll(monkeypatch)
+    T, H, D, ps, pages = 6, 4, 32, 8, 16
+    k = torch.zeros(T, H, D, dtype=torch.bfloat16)
+    big = torch.zeros(pages, ps * H * D + 64, dtype=torch.bfloat16)
+    cache = big[:, :ps * H * D].view(pages, ps, H, D)
+    idx = torch.arange(T, dtype=torch.int32)
+    kv.kv_store_paged(k, k, cache, cache, idx, page_size=ps)
+    name, a = cap.calls[-1]
+    assert name == "kv_store_paged"
+    assert a[11] == (256, 64, 2, 256, 64, 2, 256, 64, 2, 256, 64, 2)
+    assert (a[12], a[13], a[14], a[15]) == (ps, (ps * H * D + 64) * 2, (ps * H * D + 64) * 2,
+                                            ps * pages)
+    out = torch.zeros(T, H * D, dtype=torch.bfloat16)
+    kv.kv_gather(cache, cache, out, out, idx, page_size=ps)
+    name, a = cap.calls[-1]
+    assert name == "kv_gather_paged" and a[10] == 2
+    assert a[11][:6] == (256, 64, 2, 256, 64, 2)
+
+
+def test_fp8_ex_wrappers(monkeypatch):
+    cap = CaptureAll(monkeypatch)
+    T, H, D, n = 5, 2, 64, 32
+    k = torch.zeros(T, H, D, dtype=torch.float16)
+    c = torch.zeros(n, H, D, dtype=torch.uint8)
+    sc = torch.zeros(n, H + 2, dtype=torch.float32)
+    idx = torch.arange(T, dtype=torch.int64)
+    kv.kv_store_fp8_ex(k, k, c, c, idx, page_size=4, fmt="e5m2", scale_mode="token_head",
+                       k_scales=sc, v_scales=sc)
+    name, a = cap.calls[-1]
+    assert name == "kv_store_fp8_ex"
+    assert a[10] == 0 and (a[16], a[17]) == (1, 3)               # fp16, e5m2, token_head
+    assert a[22] == H + 2 and a[20] == sc.data_ptr()
+    assert (a[12], a[13]) == (4, 4 * H * D)
+    out = torch.zeros(T, H, D, dtype=torch.bfloat16)
+    kv.kv_gather_fp8(c, c, out, out, idx, page_size=4, scale_mode="token_head", k_scales=sc,
+                     v_scales=sc)
+    name, a = cap.calls[-1]
+    assert name == "kv_gather_fp8_ex" and a[10] == 1 and a[22] == H + 2
+
+
+def test_scale_wrappers(monkeypatch):
+    cap = CaptureAll(monkeypatch)
+    s = torch.ones(3, dtype=torch.float32)
+    out = kv.kv_inv_scale(s)
+    assert cap.calls[-1][0] == "kv_inv_scale" and cap.calls[-1][1][2] == 3 and out.shape == (3,)
+    k = torch.zeros(7, 2, 16, dtype=torch.bfloat16)
+    kv.kv_absmax_inv(k, k)
+    name, a = cap.calls[-1]
+    assert name == "kv_absmax_inv" and a[2:6] == (1, 7, 2, 16) and a[7] == 448.0

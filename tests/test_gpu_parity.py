@@ -452,3 +452,41 @@ def test_graph_of_dynamic_fp8_write_and_gather():
     bound = x.abs() * (2 ** -4 + 2 ** -8) + sc * 2 ** -10 * 1.01
     assert bool(((ko.float() - x).abs() <= bound).all())
     assert kv.kv_error_poll(err)[1] == 0
+
+
+def test_tensor_wrappers_round_trips():
+    import torch
+    import fp8_quant_gb300 as kv
+    dev = torch.device("cuda")
+    T, H, D, ps, pages = 300, 8, 128, 16, 64
+    k = torch.randn(T, H, D, device=dev, dtype=torch.bfloat16)
+    v = torch.randn(T, H, D, device=dev, dtype=torch.bfloat16)
+    idx = torch.randperm(ps * pages, device=dev)[:T]
+    # paged copy and paged gather give the rows back exactly
+    big = torch.zeros(pages, ps * H * D + 256, dtype=torch.bfloat16, device=dev)
+    kc = big[:, :ps * H * D].view(pages, ps, H, D)
+    vc = torch.zeros_like(big)[:, :ps * H * D].view(pages, ps, H, D)
+    kv.kv_store_paged(k, v, kc, vc, idx, page_size=ps)
+    ko, vo = torch.empty_like(k), torch.empty_like(v)
+    kv.kv_gather(kc, vc, ko, vo, idx, page_size=ps)
+    assert torch.equal(ko, k) and torch.equal(vo, v)
+    assert int((big[:, ps * H * D:] != 0).sum()) == 0          # page padding untouched
+    # dynamic per-(token, head) e5m2 and back: within half an e5m2 step
+    c8 = torch.zeros(pages * ps, H, D, dtype=torch.uint8, device=dev)
+    c8v = torch.zeros_like(c8)
+    ks = torch.zeros(pages * ps, H, dtype=torch.float32, device=dev)
+    vs = torch.zeros_like(ks)
+    kv.kv_store_fp8_ex(k, v, c8, c8v, idx, page_size=ps, fmt="e5m2", scale_mode="token_head",
+                       k_scales=ks, v_scales=vs)
+    kv.kv_gather_fp8(c8, c8v, ko, vo, idx, page_size=ps, fmt="e5m2", scale_mode="token_head",
+                     k_scales=ks, v_scales=vs)
+    x, sc = k.float(), ks[idx][:, :, None]
+    assert bool(((ko.float() - x).abs() <= x.abs() * (2 ** -3 + 2 ** -8) + sc * 2 ** -17).all())
+    # device absmax -> per-tensor write equals the host recipe's write
+    s = kv.kv_absmax_inv(k, v)
+    amax = torch.stack([k.float().abs().max(), v.float().abs().max()])
+    assert torch.equal(s[:2], amax)
+    assert torch.equal(s[2:], (torch.tensor(448.0, device=dev) / amax))
+    inv = kv.kv_inv_scale(torch.tensor([2.0, 8.0], device=dev))
+    assert inv.tolist() == [0.5, 0.125]
+    assert kv.kv_error_poll()[1] == 0
