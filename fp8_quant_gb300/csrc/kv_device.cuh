@@ -12,13 +12,22 @@
 
 // Tuning constants (defaults chosen by measurement on GB300).
 #ifndef KV_THREADS
-#define KV_THREADS 256          // threads per CTA
+#define KV_THREADS 256          // threads per CTA of small (latency-bound) launches
+#endif
+#ifndef KV_THREADS_LARGE
+#define KV_THREADS_LARGE 128    // threads per CTA of large launches
+#endif
+#ifndef KV_LARGE_LAUNCH_WARPS
+#define KV_LARGE_LAUNCH_WARPS 4096  // a launch with at least this many warps of work is large
 #endif
 #ifndef KV_COPY_UNROLL
 #define KV_COPY_UNROLL 4        // chunks per lane loaded before the first store
 #endif
 #ifndef KV_FP8_UNROLL
 #define KV_FP8_UNROLL 2
+#endif
+#ifndef KV_FP8_MAX_OUT
+#define KV_FP8_MAX_OUT 16       // widest FP8 output chunk per lane, bytes (16 or 32)
 #endif
 #ifndef KV_MAX_VEC
 #define KV_MAX_VEC 32           // widest per-lane vector, bytes (32 = 256-bit ld/st)
@@ -38,14 +47,18 @@
 
 namespace kvimpl {
 
-constexpr int kThreads = KV_THREADS;
-constexpr int kWarpsPerCta = kThreads / 32;
+constexpr int kThreads = KV_THREADS > KV_THREADS_LARGE ? KV_THREADS : KV_THREADS_LARGE;  // the most
+constexpr int kMaxWarpsPerCta = kThreads / 32;
+static_assert(KV_THREADS % 32 == 0 && KV_THREADS_LARGE % 32 == 0, "whole warps");
 constexpr int kMaxDevices = 64;
 static_assert(KV_MAX_VEC == 16 || KV_MAX_VEC == 32, "KV_MAX_VEC");
 
 // ---------------------------------------------------------------------------
 // Device helpers
 // ---------------------------------------------------------------------------
+
+// Warps per CTA of the running launch (the host picks the CTA size per launch).
+__device__ __forceinline__ uint32_t warps_per_cta() { return blockDim.x >> 5; }
 
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -93,8 +93,8 @@ template <int CH, typename IdxT, bool kBF16, int FMT>
 __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_rows(const __grid_constant__ DynParams p) {
   constexpr int kMaxJ = 4;  // chunks per lane held in registers
   const uint32_t lane = threadIdx.x & 31u;
-  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
-  uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
+  uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + (threadIdx.x >> 5);
   const uint32_t n = p.gseg * p.cps;  // chunks in a group
   const int64_t seg_in = static_cast<int64_t>(p.cps) * CH * 2;
 

@@ -123,8 +123,8 @@ __device__ __forceinline__ void gather_unit(const GatherParams& p, const Unit& w
 template <int VEC, int U, typename IdxT>
 __global__ void __launch_bounds__(kThreads) kv_gather_rows(const __grid_constant__ GatherParams p) {
   const uint32_t lane = threadIdx.x & 31u;
-  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
-  uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
+  uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + (threadIdx.x >> 5);
   const bool active = u < p.shape.num_units;
   Unit w = decode_unit(p.shape, active ? u : 0);
   if (KV_PREFETCH && lane == 0 && active) {
@@ -234,8 +234,8 @@ __device__ __forceinline__ void gather_fp8_unit(const GatherParams& p, const Uni
 template <int IN, int U, typename IdxT, bool kBF16, int FMT>
 __global__ void __launch_bounds__(kThreads) kv_gather_fp8_rows(const __grid_constant__ GatherParams p) {
   const uint32_t lane = threadIdx.x & 31u;
-  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
-  uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
+  uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + (threadIdx.x >> 5);
   const bool active = u < p.shape.num_units;
   Unit w = decode_unit(p.shape, active ? u : 0);
   if (KV_PREFETCH && lane == 0 && active) {
@@ -275,9 +275,9 @@ __global__ void __launch_bounds__(kThreads) kv_gather_elements(const __grid_cons
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
   const uint32_t lane = threadIdx.x & 31u;
-  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
   const uint64_t per_token = 2ull * static_cast<uint64_t>(p.num_heads);
-  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + (threadIdx.x >> 5);
        u < p.num_units; u += nwarps) {
     const int64_t t = static_cast<int64_t>(u / per_token);
     const uint32_t r = static_cast<uint32_t>(u - static_cast<uint64_t>(t) * per_token);

@@ -14,7 +14,7 @@
 #include "kv_host.h"
 
 #ifndef KV_ABSMAX_CTAS_PER_SM
-#define KV_ABSMAX_CTAS_PER_SM 4
+#define KV_ABSMAX_CTAS_PER_SM 8
 #endif
 
 namespace kvimpl {
@@ -52,15 +52,15 @@ __device__ __forceinline__ float absmax2(float m, uint32_t w) {
 // of the unit before it reduces them, so a warp keeps 32*U*VEC bytes in flight.
 template <int VEC, int U, bool kBF16>
 __global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant__ AbsmaxParams p) {
-  __shared__ float part[2][kWarpsPerCta];
+  __shared__ float part[2][kMaxWarpsPerCta];
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;
-  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
   const uint32_t nchunks = p.shape.part_chunks;
   float m[2] = {0.0f, 0.0f};
-  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + warp; u < p.shape.num_units;
+  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + warp; u < p.shape.num_units;
        u += nwarps) {
     const Unit w = decode_unit(p.shape, u);
     const uint8_t* src = p.src[w.kv] + w.token * p.token[w.kv] + static_cast<int64_t>(w.seg) * p.seg[w.kv];
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant
   if (threadIdx.x < 2) {
     float v = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kWarpsPerCta; ++i) v = fmaxf(v, part[threadIdx.x][i]);
+    for (uint32_t i = 0; i < warps_per_cta(); ++i) v = fmaxf(v, part[threadIdx.x][i]);
     if (v > 0.0f) atomicMax(p.amax_bits + threadIdx.x, __float_as_uint(v));
   }
 }
@@ -140,8 +140,8 @@ extern "C" kv_status kv_inv_scale(const float* scale, float* inv, int64_t n, kv_
   if (n < 0) return KV_ERR_INVALID_ARG;
   if (n == 0) return KV_OK;
   if (!scale || !inv || ((u64(scale) | u64(inv)) & 3u) != 0) return KV_ERR_INVALID_ARG;
-  const uint64_t ctas = (static_cast<uint64_t>(n) + kThreads - 1) / kThreads;
-  return launch(kv_inv_kernel, ctas * kWarpsPerCta, InvParams{scale, inv, n},
+  // one thread per value: as many warps as 32-value groups
+  return launch(kv_inv_kernel, (static_cast<uint64_t>(n) + 31) / 32, InvParams{scale, inv, n},
                 reinterpret_cast<cudaStream_t>(stream_));
 }
 
@@ -161,7 +161,7 @@ extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype sr
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   AbsmaxParams zp = {};
   zp.amax_bits = reinterpret_cast<unsigned int*>(amax);
-  kv_status st = launch(kv_absmax_zero, kWarpsPerCta, zp, stream);
+  kv_status st = launch(kv_absmax_zero, 1, zp, stream);
   if (st != KV_OK) return st;
   if (num_tokens > 0) {
     const int64_t head_bytes = 2 * static_cast<int64_t>(head_dim);
@@ -202,6 +202,6 @@ extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype sr
     }
     if (st != KV_OK) return st;
   }
-  return launch(kv_absmax_finish, kWarpsPerCta,
+  return launch(kv_absmax_finish, 1,
                 FinishParams{reinterpret_cast<const unsigned int*>(amax), inv, fp8_max}, stream);
 }

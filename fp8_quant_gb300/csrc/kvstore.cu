@@ -110,8 +110,8 @@ __device__ __forceinline__ const uint8_t* copy_src(const CopyParams& p, const Un
 template <int VEC, int U, typename IdxT>
 __global__ void __launch_bounds__(kThreads) kv_copy_rows(const __grid_constant__ CopyParams p) {
   const uint32_t lane = threadIdx.x & 31u;
-  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
-  uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
+  uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + (threadIdx.x >> 5);
   const bool active = u < p.shape.num_units;
 
   // Everything that needs no memory written by the previous grid happens
@@ -155,9 +155,9 @@ __global__ void __launch_bounds__(kThreads) kv_copy_elements(const __grid_consta
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
   const uint32_t lane = threadIdx.x & 31u;
-  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
   const uint64_t per_token = 2ull * static_cast<uint64_t>(p.num_heads);
-  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + (threadIdx.x >> 5);
        u < p.num_units; u += nwarps) {
     const int64_t t = static_cast<int64_t>(u / per_token);
     const uint32_t r = static_cast<uint32_t>(u - static_cast<uint64_t>(t) * per_token);
@@ -291,8 +291,8 @@ __device__ __forceinline__ const uint8_t* fp8_src(const Fp8Params& p, const Unit
 template <int OUT, int U, typename IdxT, bool kBF16, int FMT>
 __global__ void __launch_bounds__(kThreads) kv_fp8_rows(const __grid_constant__ Fp8Params p) {
   const uint32_t lane = threadIdx.x & 31u;
-  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
-  uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
+  uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + (threadIdx.x >> 5);
   const bool active = u < p.shape.num_units;
 
   Unit w = decode_unit(p.shape, active ? u : 0);
@@ -334,9 +334,9 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_elements(const __grid_constan
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
   const uint32_t lane = threadIdx.x & 31u;
-  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
   const uint64_t per_token = 2ull * static_cast<uint64_t>(p.num_heads);
-  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + (threadIdx.x >> 5);
        u < p.num_units; u += nwarps) {
     const int64_t t = static_cast<int64_t>(u / per_token);
     const uint32_t r = static_cast<uint32_t>(u - static_cast<uint64_t>(t) * per_token);
@@ -410,26 +410,27 @@ kv_status current_sm_count(int* out) {
 std::mutex g_occ_mutex;
 struct OccEntry {
   const void* fn;
+  int threads;
   int blocks;
 };
-OccEntry g_occ[128];
+OccEntry g_occ[256];
 int g_occ_n = 0;
 
-kv_status blocks_per_sm(const void* fn, int* out) {
+kv_status blocks_per_sm(const void* fn, int threads, int* out) {
   {
     std::lock_guard<std::mutex> lock(g_occ_mutex);
     for (int i = 0; i < g_occ_n; ++i)
-      if (g_occ[i].fn == fn) {
+      if (g_occ[i].fn == fn && g_occ[i].threads == threads) {
         *out = g_occ[i].blocks;
         return KV_OK;
       }
   }
   int b = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, kThreads, 0);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, 0);
   if (e != cudaSuccess) return cuda_fail(e);
   if (b < 1) b = 1;
   std::lock_guard<std::mutex> lock(g_occ_mutex);
-  if (g_occ_n < 128) g_occ[g_occ_n++] = OccEntry{fn, b};
+  if (g_occ_n < 256) g_occ[g_occ_n++] = OccEntry{fn, threads, b};
   *out = b;
   return KV_OK;
 }
@@ -682,6 +683,7 @@ kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, 
     }
     if (!flat) dst_bits |= u64(kc_page_stride) | u64(vc_page_stride);
     out = pow2_align(dst_bits);
+    if (out > KV_FP8_MAX_OUT) out = KV_FP8_MAX_OUT;
     // an OUT-byte chunk reads 2*OUT input bytes with loads of at most KV_MAX_VEC bytes
     while (out > 1 &&
            (sbits & static_cast<uint64_t>((2 * out > KV_MAX_VEC ? KV_MAX_VEC : 2 * out) - 1)) != 0)
@@ -807,7 +809,7 @@ extern "C" kv_status kv_error_snapshot(const kv_error_record* d_err, kv_error_re
   const void* ptrs[2] = {d_err, dst};
   const kv_status cs = classify_inputs(ptrs, 2, &on_device);
   if (cs != KV_OK) return cs;
-  return launch(kv_error_snapshot_kernel, kWarpsPerCta, SnapshotParams{d_err, dst},
+  return launch(kv_error_snapshot_kernel, 1, SnapshotParams{d_err, dst},
                 reinterpret_cast<cudaStream_t>(stream_));
 }
 
