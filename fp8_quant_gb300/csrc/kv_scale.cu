@@ -14,7 +14,7 @@
 #include "kv_host.h"
 
 #ifndef KV_ABSMAX_CTAS_PER_SM
-#define KV_ABSMAX_CTAS_PER_SM 8
+#define KV_ABSMAX_CTAS_PER_SM 16
 #endif
 
 namespace kvimpl {
