@@ -41,6 +41,9 @@
 #ifndef KV_GRID_WAVES
 #define KV_GRID_WAVES 0         // grid cap in resident-capacity waves (0 = one warp per unit)
 #endif
+#ifndef KV_GATHER_PAIR
+#define KV_GATHER_PAIR 1        // row gathers pair K and V per warp: 0 never, 1 large launches, 2 always
+#endif
 #ifndef KV_PREFETCH
 #define KV_PREFETCH 1           // L2 prefetch of the unit's source bytes before the grid wait
 #endif

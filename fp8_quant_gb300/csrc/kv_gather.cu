@@ -74,53 +74,64 @@ __device__ __forceinline__ int64_t gather_slot_offset(const GatherParams& p, con
   return page * sd.cache_page + (slot - page * p.page_size) * sd.cache_slot;
 }
 
-// Before the wait: guess the unit's slot and prefetch that cache row part into
-// L2 when the guess is in range.
-template <typename IdxT>
+// Before the wait: guess the unit's slot and prefetch that cache row part
+// (of both sides when NS == 2) into L2 when the guess is in range.
+template <int NS, typename IdxT>
 __device__ __forceinline__ void gather_prefetch(const GatherParams& p, const Unit& w) {
   const int64_t s = speculative_slot<IdxT>(p.indices, p.index_stride, w.token);
   if (s < 0 || s >= p.size_limit) return;
-  const GatherSide& sd = p.side[w.kv];
   const int64_t part_bytes = static_cast<int64_t>(p.shape.part_chunks) * p.vec;
-  const int64_t off = (p.page_size == 1)
-                          ? s * sd.cache_page
-                          : (s / p.page_size) * sd.cache_page + (s % p.page_size) * sd.cache_slot;
-  prefetch_l2_bulk(sd.cache + off + static_cast<int64_t>(w.seg) * sd.cache_seg +
-                       static_cast<int64_t>(w.part) * part_bytes,
-                   static_cast<uint32_t>(part_bytes));
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    const GatherSide& sd = p.side[NS == 2 ? i : w.kv];
+    prefetch_l2_bulk(sd.cache + gather_slot_offset(p, sd, s) +
+                         static_cast<int64_t>(w.seg) * sd.cache_seg +
+                         static_cast<int64_t>(w.part) * part_bytes,
+                     static_cast<uint32_t>(part_bytes));
+  }
 }
 
-template <int VEC, int U, typename IdxT>
+// One unit of a gather: the slot is read once; NS == 2 moves the K and the V
+// part of the unit (one slot load for both), NS == 1 the side w.kv.
+template <int VEC, int U, int NS, typename IdxT>
 __device__ __forceinline__ void gather_unit(const GatherParams& p, const Unit& w, uint32_t lane) {
   const uint32_t nchunks = p.shape.part_chunks;
   const int64_t part_bytes = static_cast<int64_t>(nchunks) * VEC;
-  const GatherSide& sd = p.side[w.kv];
   const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
   if (slot < 0 || slot >= p.size_limit) {
     if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
     return;
   }
-  const uint8_t* src = sd.cache + gather_slot_offset(p, sd, slot) +
-                       static_cast<int64_t>(w.seg) * sd.cache_seg +
-                       static_cast<int64_t>(w.part) * part_bytes;
-  uint8_t* dst = sd.out + w.token * sd.out_token + static_cast<int64_t>(w.seg) * sd.out_seg +
-                 static_cast<int64_t>(w.part) * part_bytes;
-  Chunk<VEC> buf[U];
+  const uint8_t* src[NS];
+  uint8_t* dst[NS];
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    const GatherSide& sd = p.side[NS == 2 ? i : w.kv];
+    src[i] = sd.cache + gather_slot_offset(p, sd, slot) + static_cast<int64_t>(w.seg) * sd.cache_seg +
+             static_cast<int64_t>(w.part) * part_bytes;
+    dst[i] = sd.out + w.token * sd.out_token + static_cast<int64_t>(w.seg) * sd.out_seg +
+             static_cast<int64_t>(w.part) * part_bytes;
+  }
+  Chunk<VEC> buf[NS][U];
   for (uint32_t c0 = 0; c0 < nchunks; c0 += 32u * U) {
 #pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const uint32_t c = c0 + lane + 32u * j;
-      if (c < nchunks) ld_stream(buf[j], src + static_cast<size_t>(c) * VEC);
-    }
+    for (int i = 0; i < NS; ++i)
 #pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const uint32_t c = c0 + lane + 32u * j;
-      if (c < nchunks) st_stream(dst + static_cast<size_t>(c) * VEC, buf[j]);
-    }
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + lane + 32u * j;
+        if (c < nchunks) ld_stream(buf[i][j], src[i] + static_cast<size_t>(c) * VEC);
+      }
+#pragma unroll
+    for (int i = 0; i < NS; ++i)
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + lane + 32u * j;
+        if (c < nchunks) st_stream(dst[i] + static_cast<size_t>(c) * VEC, buf[i][j]);
+      }
   }
 }
 
-template <int VEC, int U, typename IdxT>
+template <int VEC, int U, int NS, typename IdxT>
 __global__ void __launch_bounds__(kThreads) kv_gather_rows(const __grid_constant__ GatherParams p) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
@@ -128,13 +139,13 @@ __global__ void __launch_bounds__(kThreads) kv_gather_rows(const __grid_constant
   const bool active = u < p.shape.num_units;
   Unit w = decode_unit(p.shape, active ? u : 0);
   if (KV_PREFETCH && lane == 0 && active) {
-    if (p.prefetch) gather_prefetch<IdxT>(p, w);
+    if (p.prefetch) gather_prefetch<NS, IdxT>(p, w);
     else prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
   }
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
   while (u < p.shape.num_units) {
-    gather_unit<VEC, U, IdxT>(p, w, lane);
+    gather_unit<VEC, U, NS, IdxT>(p, w, lane);
     u += nwarps;
     if (u >= p.shape.num_units) break;
     w = decode_unit(p.shape, u);
@@ -183,55 +194,65 @@ __device__ __forceinline__ void dequant4(uint32_t codes, float scale, uint32_t& 
   o1 = narrow2<kBF16>(__fmul_rn(b.x, scale), __fmul_rn(b.y, scale));
 }
 
-// IN cache bytes (codes) per lane chunk -> 2*IN output bytes.
-template <int IN, int U, typename IdxT, bool kBF16, int FMT>
+// IN cache bytes (codes) per lane chunk -> 2*IN output bytes; NS as in
+// gather_unit.
+template <int IN, int U, int NS, typename IdxT, bool kBF16, int FMT>
 __device__ __forceinline__ void gather_fp8_unit(const GatherParams& p, const Unit& w,
                                                 uint32_t lane) {
   const uint32_t nchunks = p.shape.part_chunks;
   const int64_t part_in = static_cast<int64_t>(nchunks) * IN;
-  const GatherSide& sd = p.side[w.kv];
   const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
   if (slot < 0 || slot >= p.size_limit) {
     if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
     return;
   }
-  const float scale = unit_scale(p, sd, slot, w.seg);
-  const uint8_t* src = sd.cache + gather_slot_offset(p, sd, slot) +
-                       static_cast<int64_t>(w.seg) * sd.cache_seg +
-                       static_cast<int64_t>(w.part) * part_in;
-  uint8_t* dst = sd.out + w.token * sd.out_token + static_cast<int64_t>(w.seg) * sd.out_seg +
-                 static_cast<int64_t>(w.part) * part_in * 2;
+  const uint8_t* src[NS];
+  uint8_t* dst[NS];
+  float scale[NS];
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    const GatherSide& sd = p.side[NS == 2 ? i : w.kv];
+    scale[i] = unit_scale(p, sd, slot, w.seg);
+    src[i] = sd.cache + gather_slot_offset(p, sd, slot) + static_cast<int64_t>(w.seg) * sd.cache_seg +
+             static_cast<int64_t>(w.part) * part_in;
+    dst[i] = sd.out + w.token * sd.out_token + static_cast<int64_t>(w.seg) * sd.out_seg +
+             static_cast<int64_t>(w.part) * part_in * 2;
+  }
   constexpr int kWords = IN >= 4 ? IN / 4 : 1;
-  Chunk<IN> buf[U];
+  Chunk<IN> buf[NS][U];
   for (uint32_t c0 = 0; c0 < nchunks; c0 += 32u * U) {
 #pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const uint32_t c = c0 + lane + 32u * j;
-      if (c < nchunks) ld_stream(buf[j], src + static_cast<size_t>(c) * IN);
-    }
+    for (int i = 0; i < NS; ++i)
 #pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const uint32_t c = c0 + lane + 32u * j;
-      if (c >= nchunks) continue;
-      uint8_t* o = dst + static_cast<size_t>(c) * (2 * IN);
-      if constexpr (IN >= 4) {
-        Chunk<2 * IN> out;
-#pragma unroll
-        for (int i = 0; i < kWords; ++i)
-          dequant4<kBF16, FMT>(buf[j].w[i], scale, out.w[2 * i], out.w[2 * i + 1]);
-        st_stream(o, out);
-      } else {
-        static_assert(IN == 2, "IN");
-        const float2 a = fp8x2_to_f32x2<FMT>(buf[j].h);
-        Chunk<4> out;
-        out.w[0] = narrow2<kBF16>(__fmul_rn(a.x, scale), __fmul_rn(a.y, scale));
-        st_stream(o, out);
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + lane + 32u * j;
+        if (c < nchunks) ld_stream(buf[i][j], src[i] + static_cast<size_t>(c) * IN);
       }
-    }
+#pragma unroll
+    for (int i = 0; i < NS; ++i)
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + lane + 32u * j;
+        if (c >= nchunks) continue;
+        uint8_t* o = dst[i] + static_cast<size_t>(c) * (2 * IN);
+        if constexpr (IN >= 4) {
+          Chunk<2 * IN> out;
+#pragma unroll
+          for (int q = 0; q < kWords; ++q)
+            dequant4<kBF16, FMT>(buf[i][j].w[q], scale[i], out.w[2 * q], out.w[2 * q + 1]);
+          st_stream(o, out);
+        } else {
+          static_assert(IN == 2, "IN");
+          const float2 a = fp8x2_to_f32x2<FMT>(buf[i][j].h);
+          Chunk<4> out;
+          out.w[0] = narrow2<kBF16>(__fmul_rn(a.x, scale[i]), __fmul_rn(a.y, scale[i]));
+          st_stream(o, out);
+        }
+      }
   }
 }
 
-template <int IN, int U, typename IdxT, bool kBF16, int FMT>
+template <int IN, int U, int NS, typename IdxT, bool kBF16, int FMT>
 __global__ void __launch_bounds__(kThreads) kv_gather_fp8_rows(const __grid_constant__ GatherParams p) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
@@ -239,13 +260,13 @@ __global__ void __launch_bounds__(kThreads) kv_gather_fp8_rows(const __grid_cons
   const bool active = u < p.shape.num_units;
   Unit w = decode_unit(p.shape, active ? u : 0);
   if (KV_PREFETCH && lane == 0 && active) {
-    if (p.prefetch) gather_prefetch<IdxT>(p, w);
+    if (p.prefetch) gather_prefetch<NS, IdxT>(p, w);
     else prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
   }
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
   while (u < p.shape.num_units) {
-    gather_fp8_unit<IN, U, IdxT, kBF16, FMT>(p, w, lane);
+    gather_fp8_unit<IN, U, NS, IdxT, kBF16, FMT>(p, w, lane);
     u += nwarps;
     if (u >= p.shape.num_units) break;
     w = decode_unit(p.shape, u);
@@ -320,10 +341,24 @@ __global__ void __launch_bounds__(kThreads) kv_gather_elements(const __grid_cons
   if (!KV_EARLY_TRIGGER) grid_dependents_launch();
 }
 
+// Sides moved per warp by the row gathers: large launches pair the K and the V
+// part of a slot in one warp (one slot load, twice the bytes in flight per
+// dependent load); small, latency-bound launches keep one side per warp so
+// that more warps share the round trips.  Rewrites the shape for pairing.
+inline int gather_sides(GatherParams& p) {
+  const bool pair = KV_GATHER_PAIR == 2 ||
+                    (KV_GATHER_PAIR == 1 && p.shape.num_units >= KV_LARGE_LAUNCH_WARPS);
+  if (!pair) return 1;
+  p.shape.units_per_token = p.shape.units_per_side;
+  p.shape.num_units /= 2;
+  return 2;
+}
+
 template <int VEC, typename IdxT>
-kv_status launch_gather_vec(const GatherParams& p, cudaStream_t stream) {
+kv_status launch_gather_vec(GatherParams p, cudaStream_t stream) {
   constexpr int U = VEC == 32 ? (KV_COPY_UNROLL + 1) / 2 : KV_COPY_UNROLL;
-  return launch(kv_gather_rows<VEC, U, IdxT>, p.shape.num_units, p, stream);
+  if (gather_sides(p) == 2) return launch(kv_gather_rows<VEC, U, 2, IdxT>, p.shape.num_units, p, stream);
+  return launch(kv_gather_rows<VEC, U, 1, IdxT>, p.shape.num_units, p, stream);
 }
 
 template <typename IdxT>
@@ -343,8 +378,13 @@ kv_status launch_gather(int vec, const GatherParams& p, cudaStream_t stream) {
 template <int IN, typename IdxT, int FMT>
 kv_status launch_gather_fp8_fmt(bool bf16, const GatherParams& p, cudaStream_t stream) {
   constexpr int U = IN == 16 ? 2 : 4;
-  if (bf16) return launch(kv_gather_fp8_rows<IN, U, IdxT, true, FMT>, p.shape.num_units, p, stream);
-  return launch(kv_gather_fp8_rows<IN, U, IdxT, false, FMT>, p.shape.num_units, p, stream);
+  GatherParams q = p;
+  if (gather_sides(q) == 2) {
+    if (bf16) return launch(kv_gather_fp8_rows<IN, U, 2, IdxT, true, FMT>, q.shape.num_units, q, stream);
+    return launch(kv_gather_fp8_rows<IN, U, 2, IdxT, false, FMT>, q.shape.num_units, q, stream);
+  }
+  if (bf16) return launch(kv_gather_fp8_rows<IN, U, 1, IdxT, true, FMT>, p.shape.num_units, p, stream);
+  return launch(kv_gather_fp8_rows<IN, U, 1, IdxT, false, FMT>, p.shape.num_units, p, stream);
 }
 
 template <int IN, typename IdxT>

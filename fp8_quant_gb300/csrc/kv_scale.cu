@@ -16,6 +16,12 @@
 #ifndef KV_ABSMAX_CTAS_PER_SM
 #define KV_ABSMAX_CTAS_PER_SM 16
 #endif
+#ifndef KV_ABSMAX_ILP
+#define KV_ABSMAX_ILP 1          // units whose loads a warp keeps in flight together
+#endif
+#ifndef KV_ABSMAX_PREFETCH
+#define KV_ABSMAX_PREFETCH 1     // L2 prefetch of each warp's first units before the grid wait
+#endif
 
 namespace kvimpl {
 namespace {
@@ -39,6 +45,8 @@ struct AbsmaxParams {
   int64_t token[2], seg[2];  // byte strides of the rows and of their segments
   UnitShape shape;           // units: (token, K|V, segment); parts = 1
   unsigned int* amax_bits;   // two words: K, V (the caller's amax output)
+  int vec;                   // bytes per chunk
+  int prefetch;              // rows are device memory with 16-byte aligned segments
 };
 
 // |x| of the two 2-byte elements in `w`, folded into m (fmaxf ignores NaN).
@@ -48,44 +56,79 @@ __device__ __forceinline__ float absmax2(float m, uint32_t w) {
   return fmaxf(m, fmaxf(fabsf(x.x), fabsf(x.y)));
 }
 
-// One warp per (token, K|V, segment) unit; a lane issues up to U vector loads
-// of the unit before it reduces them, so a warp keeps 32*U*VEC bytes in flight.
-template <int VEC, int U, bool kBF16>
+__device__ __forceinline__ const uint8_t* absmax_row(const AbsmaxParams& p, const Unit& w) {
+  return p.src[w.kv] + w.token * p.token[w.kv] + static_cast<int64_t>(w.seg) * p.seg[w.kv];
+}
+
+// One warp per (token, K|V, segment) unit, ILP units at a time (units u,
+// u + nwarps, ...); a lane issues up to U vector loads of each of them before
+// it reduces, so a warp keeps 32*U*VEC*ILP bytes in flight.
+template <int VEC, int U, int ILP, bool kBF16>
 __global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant__ AbsmaxParams p) {
   __shared__ float part[2][kMaxWarpsPerCta];
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
+  const uint64_t first = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + warp;
   const uint32_t nchunks = p.shape.part_chunks;
-  float m[2] = {0.0f, 0.0f};
-  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + warp; u < p.shape.num_units;
-       u += nwarps) {
-    const Unit w = decode_unit(p.shape, u);
-    const uint8_t* src = p.src[w.kv] + w.token * p.token[w.kv] + static_cast<int64_t>(w.seg) * p.seg[w.kv];
-    float acc = 0.0f;
-    for (uint32_t c0 = 0; c0 < nchunks; c0 += 32u * U) {
-      Chunk<VEC> ch[U];
+  if (KV_ABSMAX_PREFETCH && p.prefetch && lane == 0) {
 #pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const uint32_t c = c0 + lane + 32u * j;
-        if (c < nchunks) ld_stream(ch[j], src + static_cast<size_t>(c) * VEC);
-      }
+    for (int i = 0; i < ILP; ++i) {
+      const uint64_t u = first + i * nwarps;
+      if (u < p.shape.num_units)
+        prefetch_l2_bulk(absmax_row(p, decode_unit(p.shape, u)),
+                         nchunks * static_cast<uint32_t>(p.vec));
+    }
+  }
+  grid_dependency_wait();
+  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  float m0 = 0.0f, m1 = 0.0f;
+  for (uint64_t u = first; u < p.shape.num_units; u += nwarps * ILP) {
+    const uint8_t* src[ILP];
+    uint32_t side[ILP];
+    float acc[ILP];
 #pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const uint32_t c = c0 + lane + 32u * j;
-        if (c >= nchunks) continue;
-        if constexpr (VEC >= 4) {
-#pragma unroll
-          for (int i = 0; i < VEC / 4; ++i) acc = absmax2<kBF16>(acc, ch[j].w[i]);
-        } else {
-          acc = absmax2<kBF16>(acc, static_cast<uint32_t>(ch[j].h));   // upper element is 0
-        }
+    for (int i = 0; i < ILP; ++i) {
+      const uint64_t ui = u + i * nwarps;
+      acc[i] = 0.0f;
+      side[i] = 0;
+      src[i] = nullptr;
+      if (ui < p.shape.num_units) {
+        const Unit w = decode_unit(p.shape, ui);
+        src[i] = absmax_row(p, w);
+        side[i] = w.kv;
       }
     }
-    m[w.kv] = fmaxf(m[w.kv], acc);
+    for (uint32_t c0 = 0; c0 < nchunks; c0 += 32u * U) {
+      Chunk<VEC> ch[ILP][U];
+#pragma unroll
+      for (int i = 0; i < ILP; ++i)
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const uint32_t c = c0 + lane + 32u * j;
+          if (src[i] != nullptr && c < nchunks) ld_stream(ch[i][j], src[i] + static_cast<size_t>(c) * VEC);
+        }
+#pragma unroll
+      for (int i = 0; i < ILP; ++i)
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const uint32_t c = c0 + lane + 32u * j;
+          if (src[i] == nullptr || c >= nchunks) continue;
+          if constexpr (VEC >= 4) {
+#pragma unroll
+            for (int q = 0; q < VEC / 4; ++q) acc[i] = absmax2<kBF16>(acc[i], ch[i][j].w[q]);
+          } else {
+            acc[i] = absmax2<kBF16>(acc[i], static_cast<uint32_t>(ch[i][j].h));  // upper element is 0
+          }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < ILP; ++i) {
+      if (side[i]) m1 = fmaxf(m1, acc[i]);
+      else m0 = fmaxf(m0, acc[i]);
+    }
   }
+  float m[2] = {m0, m1};
 #pragma unroll
   for (int kv = 0; kv < 2; ++kv) {
 #pragma unroll
@@ -127,8 +170,10 @@ __global__ void __launch_bounds__(kThreads) kv_absmax_finish(const __grid_consta
 template <int VEC>
 kv_status launch_absmax(bool bf16, const AbsmaxParams& p, cudaStream_t stream, uint64_t max_ctas) {
   constexpr int U = VEC == 32 ? 2 : 4;
-  if (bf16) return launch(kv_absmax_rows<VEC, U, true>, p.shape.num_units, p, stream, max_ctas);
-  return launch(kv_absmax_rows<VEC, U, false>, p.shape.num_units, p, stream, max_ctas);
+  constexpr int ILP = KV_ABSMAX_ILP;
+  const uint64_t warps = (p.shape.num_units + ILP - 1) / ILP;
+  if (bf16) return launch(kv_absmax_rows<VEC, U, ILP, true>, warps, p, stream, max_ctas);
+  return launch(kv_absmax_rows<VEC, U, ILP, false>, warps, p, stream, max_ctas);
 }
 
 }  // namespace
@@ -159,6 +204,12 @@ extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype sr
     return KV_ERR_INVALID_ARG;
   if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  bool on_device = true;
+  if (num_tokens > 0) {
+    const void* in[4] = {k, v, amax, inv};
+    const kv_status cs = classify_inputs(in, 4, &on_device);
+    if (cs != KV_OK) return cs;
+  }
   AbsmaxParams zp = {};
   zp.amax_bits = reinterpret_cast<unsigned int*>(amax);
   kv_status st = launch(kv_absmax_zero, 1, zp, stream);
@@ -184,6 +235,8 @@ extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype sr
     p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
     p.shape.part_chunks = static_cast<uint32_t>(seg_bytes / vec);
     p.amax_bits = reinterpret_cast<unsigned int*>(amax);
+    p.vec = vec;
+    p.prefetch = vec >= 16 && on_device ? 1 : 0;
     // a few resident waves of CTAs loop over the rows, so only a few hundred
     // same-address atomics land at the end
     int sms = 0;

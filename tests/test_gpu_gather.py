@@ -6,7 +6,9 @@ code, NaNs included, appears for the FP8 gather), pre-fills the outputs with
 a sentinel, gathers, and compares every output byte and the out-of-range
 report with the oracle. Layouts cover contiguous and padded rows, head
 segments, strided dims (element kernels), misaligned views, 3-D and padded
-4-D paged caches, both index types, index strides and out-of-range slots.
+4-D paged caches, both index types, index strides and out-of-range slots,
+in launches small enough for one side per warp and large enough for the
+paired K/V form.
 """
 
 import zlib
@@ -169,6 +171,11 @@ COPY = {
     "paged_odd_rows": dict(T=500, H=1, D=576, n=2048, page_size=32, page_pad=128, slot_pad=128,
                            idx_dtype=np.int32),
     "paged_page7_generic": dict(T=300, H=2, D=20, n=700, page_size=7, page_pad=12, dim_mult=2),
+    # launches of at least 4096 warps pair the K and V rows of a slot in one warp
+    "paired_rows_parts2": dict(T=1111, H=8, D=128, n=8192),
+    "paired_oob": dict(T=3001, H=8, D=128, n=8192, bad=((0, -1), (1500, 8192), (3000, -5))),
+    "paired_paged_i32": dict(T=2500, H=8, D=128, n=8192, page_size=16, page_pad=512,
+                             idx_dtype=np.int32),
 }
 
 FP8 = {
@@ -187,6 +194,12 @@ FP8 = {
     "misaligned_out": dict(T=300, H=4, D=64, n=900, ooff=2, scale=0.75),
     "oob_int32": dict(T=600, H=8, D=128, n=2000, idx_dtype=np.int32,
                       bad=((5, -9), (6, 2000)), scale=1.0),
+    "paired_scaled_oob": dict(T=3001, H=8, D=128, n=8192, scale=0.37,
+                              bad=((7, -1), (3000, 8192))),
+    "paired_f16_pages": dict(T=2222, H=8, D=128, n=8192, out="f16", page_size=32, page_pad=256,
+                             scale=2.5),
+    "paired_parts2": dict(T=1111, H=8, D=128, n=4096, scale=1.0),
+    "paired_in8_heads": dict(T=900, H=3, D=24, n=2048, scale=0.5),
 }
 
 

@@ -40,7 +40,8 @@ def test_inv_scale_bits():
     assert kv.raw.kv_inv_scale(None, None, 0, _stream()) == 0
 
 
-def _absmax_case(T, H, D, src, seed, head_pad=0, nan_at=(), inf_at=(), zero=False, fp8_max=448.0):
+def _absmax_case(T, H, D, src, seed, head_pad=0, nan_at=(), inf_at=(), zero=False, fp8_max=448.0,
+                 host=False):
     import torch
     import fp8_quant_gb300 as kv
     w = wl.make_fp8("t", T, H, D, max(T, 64), seed=seed, dtype=src)
@@ -65,7 +66,7 @@ def _absmax_case(T, H, D, src, seed, head_pad=0, nan_at=(), inf_at=(), zero=Fals
                         kc_slot=0, kc_head=0, kc_dim=0, vc_slot=0, vc_head=0, vc_dim=0)
     want_amax, want_inv = oracle.absmax_inv(buf[0].copy(), buf[1].copy(), st, T, H, D, src,
                                             fp8_max)
-    dbuf = torch.from_numpy(buf).cuda()
+    dbuf = torch.from_numpy(buf).pin_memory() if host else torch.from_numpy(buf).cuda()
     out = torch.full((4,), 123.0, dtype=torch.float32, device="cuda")
     rc = kv.raw.kv_absmax_inv(dbuf[0].data_ptr(), dbuf[1].data_ptr(), 1 if src == "bf16" else 0,
                               T, H, D, tuple(int(x) for x in st.values), fp8_max,
@@ -91,6 +92,22 @@ def test_absmax_inv_special_values():
     _, got = _absmax_case(64, 4, 64, "bf16", seed=5, zero=True)
     assert list(got) == [0.0, 0.0, 1.0, 1.0]
     _absmax_case(1000, 8, 128, "bf16", seed=6, fp8_max=57344.0)
+
+
+def test_absmax_inv_host_rows():
+    """Rows in pinned host memory are read in place (no L2 prefetch of host
+    memory); pageable host memory is rejected before any launch."""
+    import torch
+    import fp8_quant_gb300 as kv
+    _absmax_case(3000, 8, 128, "bf16", seed=7, host=True)
+    _absmax_case(300, 3, 40, "f16", seed=8, host=True)
+    rows = np.zeros(2 * 64 * 256, np.uint8)
+    out = torch.full((4,), 123.0, dtype=torch.float32, device="cuda")
+    st = (256, 128, 2, 256, 128, 2) + (0,) * 6
+    rc = kv.raw.kv_absmax_inv(rows.ctypes.data, rows.ctypes.data + 64 * 256, 1, 64, 2, 64, st,
+                              448.0, out.data_ptr(), out.data_ptr() + 8, _stream())
+    assert rc == kv.KVStatus.ERR_INVALID_ARG
+    assert out.cpu().tolist() == [123.0] * 4
 
 
 def test_fp8_workload_recipe_on_device():
