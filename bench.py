@@ -270,6 +270,8 @@ class Pool:
         self.amax_inv = torch.zeros(4, dtype=torch.float32, device=device)
         self.err = torch.zeros(2, dtype=torch.int64, device=device)
         self.i64 = idx_dtype == torch.int64
+        # kernels one call launches: kv_absmax_inv zeroes, reduces and finishes
+        self.launches_per_call = 3 if w.kind == "absmax" else 1
 
     def _slots(self, g, idx_dtype):
         import torch
@@ -613,37 +615,44 @@ def run_ours(args, dist):
                      "peak_source": peak_src},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * pool.launches_per_call,
         "clocks": clock_summary,
     }
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
 
 
-def kernel_source_hash() -> str:
-    """sha256 over the CUDA sources (csrc/, sorted by name): what the traffic
+# The sources each workload's kernels are compiled from: the shared headers
+# plus the translation unit that holds the workload's kernel.
+_COMMON_SOURCES = ("include/kvstore.h", "fp8_quant_gb300/csrc/kv_abi.h",
+                   "fp8_quant_gb300/csrc/kv_device.cuh", "fp8_quant_gb300/csrc/kv_host.h")
+
+
+def kernel_source_hash(name: str) -> str:
+    """sha256 over the sources of workload `name`'s kernels: what the traffic
     counters in profiles/ were taken with."""
     import hashlib
-    csrc = os.path.join(ROOT, "fp8_quant_gb300", "csrc")
+    unit = ("kv_gather.cu" if name.startswith("gather") else
+            "kv_scale.cu" if name == "absmax" else "kvstore.cu")
+    files = _COMMON_SOURCES + ("fp8_quant_gb300/csrc/" + unit,)
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in files:
+        h.update(f.encode())
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()
 
 
 def load_traffic(name):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel sources have changed since those counters were taken."""
+    workload's kernel sources have changed since those counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            d = json.load(f)
-        if not kernel_source_hash().startswith(d["source_sha256_prefix"]):
+            entry = json.load(f)["workloads"][name]
+        if not kernel_source_hash(name).startswith(entry["sources_sha256_prefix"]):
             return None
-        return d.get(name)
+        return entry["bytes"]
     except Exception:
         return None
 
