@@ -44,6 +44,9 @@
 #ifndef KV_GATHER_PAIR
 #define KV_GATHER_PAIR 1        // row gathers pair K and V per warp: 0 never, 1 large launches, 2 always
 #endif
+#ifndef KV_LOOKAHEAD
+#define KV_LOOKAHEAD 1          // multi-wave gathers: each warp prefetches the unit one resident wave ahead
+#endif
 #ifndef KV_PREFETCH
 #define KV_PREFETCH 1           // L2 prefetch of the unit's source bytes before the grid wait
 #endif

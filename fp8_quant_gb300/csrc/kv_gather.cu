@@ -9,8 +9,12 @@
 //
 // Same decomposition as the write kernels: one warp per (token, K|V, segment,
 // part) unit, lane l moving chunks l, l+32, ...  Here the source address
-// depends on the slot, so only the slot id can be prefetched into L2 before
-// the programmatic-launch wait; the row loads follow the slot load.
+// depends on the slot, so the row loads follow the slot load.  Three things
+// shorten that chain: before the programmatic-launch wait a warp reads its
+// slot speculatively and prefetches the guessed rows into L2; large launches
+// pair the K and the V part of a slot in one warp (one slot load for both);
+// and in launches of more than one resident wave each warp also prefetches
+// the rows of the unit one wave ahead.
 #include "kv_host.h"
 
 namespace kvimpl {
@@ -35,6 +39,7 @@ struct GatherParams {
   int prefetch;     // cache rows are 16-byte aligned: speculative L2 prefetch allowed
   int scale_mode;   // fp8: kv_scale_mode (per-head mode: one head per unit segment)
   int64_t scales_stride;
+  uint64_t ahead;   // > 0: also prefetch the cache rows of unit u + ahead (set by launch_rows)
 };
 
 // Dequantisation multiplier of a unit (fp8 gathers).
@@ -74,11 +79,10 @@ __device__ __forceinline__ int64_t gather_slot_offset(const GatherParams& p, con
   return page * sd.cache_page + (slot - page * p.page_size) * sd.cache_slot;
 }
 
-// Before the wait: guess the unit's slot and prefetch that cache row part
-// (of both sides when NS == 2) into L2 when the guess is in range.
-template <int NS, typename IdxT>
-__device__ __forceinline__ void gather_prefetch(const GatherParams& p, const Unit& w) {
-  const int64_t s = speculative_slot<IdxT>(p.indices, p.index_stride, w.token);
+// L2 prefetch of unit w's cache row part (of both sides when NS == 2) at
+// slot s, when s is in range.
+template <int NS>
+__device__ __forceinline__ void gather_prefetch_rows(const GatherParams& p, const Unit& w, int64_t s) {
   if (s < 0 || s >= p.size_limit) return;
   const int64_t part_bytes = static_cast<int64_t>(p.shape.part_chunks) * p.vec;
 #pragma unroll
@@ -89,6 +93,32 @@ __device__ __forceinline__ void gather_prefetch(const GatherParams& p, const Uni
                          static_cast<int64_t>(w.part) * part_bytes,
                      static_cast<uint32_t>(part_bytes));
   }
+}
+
+// Before the wait: guess the unit's slot and prefetch its rows.
+template <int NS, typename IdxT>
+__device__ __forceinline__ void gather_prefetch(const GatherParams& p, const Unit& w) {
+  gather_prefetch_rows<NS>(p, w, speculative_slot<IdxT>(p.indices, p.index_stride, w.token));
+}
+
+// After the wait, before moving unit u: lane 0 reads the slot of unit
+// u + ahead (the unit a warp will take one resident wave later) and, once
+// the unit's own loads are issued, prefetches that unit's rows into L2.
+// Only the paired form (NS == 2) does this: multi-wave launches are large,
+// and large launches pair; the small one-side launches keep their code.
+struct Lookahead {
+  Unit w{};
+  int64_t slot = -1;
+};
+
+template <int NS, typename IdxT>
+__device__ __forceinline__ Lookahead lookahead_slot(const GatherParams& p, uint64_t u, uint32_t lane) {
+  Lookahead a;
+  if (KV_LOOKAHEAD && NS == 2 && p.ahead != 0 && lane == 0 && u + p.ahead < p.shape.num_units) {
+    a.w = decode_unit(p.shape, u + p.ahead);
+    a.slot = load_slot<IdxT>(p.indices, p.index_stride, a.w.token);
+  }
+  return a;
 }
 
 // One unit of a gather: the slot is read once; NS == 2 moves the K and the V
@@ -145,7 +175,9 @@ __global__ void __launch_bounds__(kThreads) kv_gather_rows(const __grid_constant
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
   while (u < p.shape.num_units) {
+    const Lookahead next = lookahead_slot<NS, IdxT>(p, u, lane);
     gather_unit<VEC, U, NS, IdxT>(p, w, lane);
+    if (KV_LOOKAHEAD && NS == 2 && lane == 0) gather_prefetch_rows<NS>(p, next.w, next.slot);
     u += nwarps;
     if (u >= p.shape.num_units) break;
     w = decode_unit(p.shape, u);
@@ -266,7 +298,9 @@ __global__ void __launch_bounds__(kThreads) kv_gather_fp8_rows(const __grid_cons
   grid_dependency_wait();
   if (KV_EARLY_TRIGGER) grid_dependents_launch();
   while (u < p.shape.num_units) {
+    const Lookahead next = lookahead_slot<NS, IdxT>(p, u, lane);
     gather_fp8_unit<IN, U, NS, IdxT, kBF16, FMT>(p, w, lane);
+    if (KV_LOOKAHEAD && NS == 2 && lane == 0) gather_prefetch_rows<NS>(p, next.w, next.slot);
     u += nwarps;
     if (u >= p.shape.num_units) break;
     w = decode_unit(p.shape, u);
@@ -357,8 +391,8 @@ inline int gather_sides(GatherParams& p) {
 template <int VEC, typename IdxT>
 kv_status launch_gather_vec(GatherParams p, cudaStream_t stream) {
   constexpr int U = VEC == 32 ? (KV_COPY_UNROLL + 1) / 2 : KV_COPY_UNROLL;
-  if (gather_sides(p) == 2) return launch(kv_gather_rows<VEC, U, 2, IdxT>, p.shape.num_units, p, stream);
-  return launch(kv_gather_rows<VEC, U, 1, IdxT>, p.shape.num_units, p, stream);
+  if (gather_sides(p) == 2) return launch_rows(kv_gather_rows<VEC, U, 2, IdxT>, p.shape.num_units, p, stream);
+  return launch_rows(kv_gather_rows<VEC, U, 1, IdxT>, p.shape.num_units, p, stream);
 }
 
 template <typename IdxT>
@@ -380,11 +414,11 @@ kv_status launch_gather_fp8_fmt(bool bf16, const GatherParams& p, cudaStream_t s
   constexpr int U = IN == 16 ? 2 : 4;
   GatherParams q = p;
   if (gather_sides(q) == 2) {
-    if (bf16) return launch(kv_gather_fp8_rows<IN, U, 2, IdxT, true, FMT>, q.shape.num_units, q, stream);
-    return launch(kv_gather_fp8_rows<IN, U, 2, IdxT, false, FMT>, q.shape.num_units, q, stream);
+    if (bf16) return launch_rows(kv_gather_fp8_rows<IN, U, 2, IdxT, true, FMT>, q.shape.num_units, q, stream);
+    return launch_rows(kv_gather_fp8_rows<IN, U, 2, IdxT, false, FMT>, q.shape.num_units, q, stream);
   }
-  if (bf16) return launch(kv_gather_fp8_rows<IN, U, 1, IdxT, true, FMT>, p.shape.num_units, p, stream);
-  return launch(kv_gather_fp8_rows<IN, U, 1, IdxT, false, FMT>, p.shape.num_units, p, stream);
+  if (bf16) return launch_rows(kv_gather_fp8_rows<IN, U, 1, IdxT, true, FMT>, p.shape.num_units, p, stream);
+  return launch_rows(kv_gather_fp8_rows<IN, U, 1, IdxT, false, FMT>, p.shape.num_units, p, stream);
 }
 
 template <int IN, typename IdxT>

@@ -7,8 +7,9 @@ a sentinel, gathers, and compares every output byte and the out-of-range
 report with the oracle. Layouts cover contiguous and padded rows, head
 segments, strided dims (element kernels), misaligned views, 3-D and padded
 4-D paged caches, both index types, index strides and out-of-range slots,
-in launches small enough for one side per warp and large enough for the
-paired K/V form.
+in launches small enough for one side per warp, large enough for the
+paired K/V form, and larger than one wave of resident warps (look-ahead
+prefetch).
 """
 
 import zlib
@@ -176,6 +177,12 @@ COPY = {
     "paired_oob": dict(T=3001, H=8, D=128, n=8192, bad=((0, -1), (1500, 8192), (3000, -5))),
     "paired_paged_i32": dict(T=2500, H=8, D=128, n=8192, page_size=16, page_pad=512,
                              idx_dtype=np.int32),
+    # more units than resident warps: each warp also prefetches the rows of the
+    # unit one resident wave ahead
+    "multiwave_rows_oob": dict(T=20000, H=8, D=128, n=32768,
+                               bad=((5, -1), (10000, 40000), (19999, 32768))),
+    "multiwave_heads_paged": dict(T=3000, H=8, D=64, n=8192, head_pad_c=64, head_pad_o=32,
+                                  page_size=16, page_pad=256),
 }
 
 FP8 = {
@@ -200,6 +207,10 @@ FP8 = {
                              scale=2.5),
     "paired_parts2": dict(T=1111, H=8, D=128, n=4096, scale=1.0),
     "paired_in8_heads": dict(T=900, H=3, D=24, n=2048, scale=0.5),
+    "multiwave_scaled_oob": dict(T=12000, H=8, D=128, n=16384, scale=0.3,
+                                 bad=((1, -1), (6000, 16384), (11999, -7))),
+    "multiwave_f16_heads": dict(T=3000, H=8, D=64, n=8192, head_pad_c=32, head_pad_o=64,
+                                out="f16", scale=2.0),
 }
 
 
