@@ -107,8 +107,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_rows(const __grid_constan
       prefetch_l2_bulk(base + static_cast<int64_t>(sg) * sd.src_seg, static_cast<uint32_t>(seg_in));
     if (lane == 0) prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
   }
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover();
 
   for (; u < p.num_units; u += nwarps) {
     const DynUnit w = dyn_unit(p, u);

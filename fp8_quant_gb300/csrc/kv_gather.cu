@@ -172,8 +172,7 @@ __global__ void __launch_bounds__(kThreads) kv_gather_rows(const __grid_constant
     if (p.prefetch) gather_prefetch<NS, IdxT>(p, w);
     else prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
   }
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover();
   while (u < p.shape.num_units) {
     const Lookahead next = lookahead_slot<NS, IdxT>(p, u, lane);
     gather_unit<VEC, U, NS, IdxT>(p, w, lane);
@@ -295,8 +294,7 @@ __global__ void __launch_bounds__(kThreads) kv_gather_fp8_rows(const __grid_cons
     if (p.prefetch) gather_prefetch<NS, IdxT>(p, w);
     else prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
   }
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover();
   while (u < p.shape.num_units) {
     const Lookahead next = lookahead_slot<NS, IdxT>(p, u, lane);
     gather_fp8_unit<IN, U, NS, IdxT, kBF16, FMT>(p, w, lane);
@@ -327,8 +325,7 @@ struct GatherElemParams {
 
 template <typename IdxT, int kMode, int FMT>  // kMode: 0 copy, 1 fp8 -> bf16, 2 fp8 -> fp16
 __global__ void __launch_bounds__(kThreads) kv_gather_elements(const __grid_constant__ GatherElemParams p) {
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover();
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
   const uint64_t per_token = 2ull * static_cast<uint64_t>(p.num_heads);

@@ -33,8 +33,7 @@ struct InvParams {
 };
 
 __global__ void __launch_bounds__(kThreads) kv_inv_kernel(const __grid_constant__ InvParams p) {
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover<true>();  // small bookkeeping kernel: let the next kernel in early
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n; i += stride)
     p.inv[i] = __fdiv_rn(1.0f, p.scale[i]);
@@ -80,8 +79,7 @@ __global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant
                          nchunks * static_cast<uint32_t>(p.vec));
     }
   }
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover();
   float m0 = 0.0f, m1 = 0.0f;
   for (uint64_t u = first; u < p.shape.num_units; u += nwarps * ILP) {
     const uint8_t* src[ILP];
@@ -147,8 +145,7 @@ __global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant
 // Clears the two accumulator words.  A kernel rather than a memset so that
 // zeroing, reduction and finish chain by programmatic launch.
 __global__ void __launch_bounds__(kThreads) kv_absmax_zero(const __grid_constant__ AbsmaxParams p) {
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover<true>();  // small bookkeeping kernel: let the next kernel in early
   if (blockIdx.x == 0 && threadIdx.x < 2) p.amax_bits[threadIdx.x] = 0u;
 }
 
@@ -159,8 +156,7 @@ struct FinishParams {
 };
 
 __global__ void __launch_bounds__(kThreads) kv_absmax_finish(const __grid_constant__ FinishParams p) {
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover<true>();  // small bookkeeping kernel: let the next kernel in early
   if (threadIdx.x < 2) {
     const float a = __uint_as_float(p.amax_bits[threadIdx.x]);
     p.inv[threadIdx.x] = a > 0.0f ? __fdiv_rn(p.fp8_max, a) : 1.0f;

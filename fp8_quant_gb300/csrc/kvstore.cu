@@ -123,8 +123,7 @@ __global__ void __launch_bounds__(kThreads) kv_copy_rows(const __grid_constant__
     prefetch_l2_bulk(src, p.shape.part_chunks * static_cast<uint32_t>(VEC));
     prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
   }
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover();
 
   while (u < p.shape.num_units) {
     copy_unit<VEC, U, IdxT>(p, w, src, lane);
@@ -152,8 +151,7 @@ struct GenericCopyParams {
 
 template <typename IdxT>
 __global__ void __launch_bounds__(kThreads) kv_copy_elements(const __grid_constant__ GenericCopyParams p) {
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover();
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
   const uint64_t per_token = 2ull * static_cast<uint64_t>(p.num_heads);
@@ -301,8 +299,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_rows(const __grid_constant__ 
     prefetch_l2_bulk(src, p.shape.part_chunks * 2u * static_cast<uint32_t>(OUT));
     prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
   }
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover();
 
   while (u < p.shape.num_units) {
     fp8_unit<OUT, U, IdxT, kBF16, FMT>(p, w, src, lane);
@@ -331,8 +328,7 @@ struct GenericFp8Params {
 
 template <typename IdxT, bool kBF16, int FMT>
 __global__ void __launch_bounds__(kThreads) kv_fp8_elements(const __grid_constant__ GenericFp8Params p) {
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover();
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
   const uint64_t per_token = 2ull * static_cast<uint64_t>(p.num_heads);
@@ -789,8 +785,7 @@ struct SnapshotParams {
 // launch wait), so a captured step can hand its status to the host without a
 // copy-engine round trip.
 __global__ void __launch_bounds__(kThreads) kv_error_snapshot_kernel(const __grid_constant__ SnapshotParams p) {
-  grid_dependency_wait();
-  if (KV_EARLY_TRIGGER) grid_dependents_launch();
+  grid_handover<true>();  // small bookkeeping kernel: let the next kernel in early
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     const unsigned long long n = *reinterpret_cast<const volatile unsigned long long*>(&p.src->oob_count);
     const unsigned long long f = *reinterpret_cast<const volatile unsigned long long*>(&p.src->first_bad_key);
