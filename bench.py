@@ -381,12 +381,17 @@ def time_region(torch, dist, fn, device):
 
 
 def single_call_cold_us(torch, pool, stream_handle, reps=30):
-    """Median latency of one call with L2 flushed before it (informational)."""
+    """Median device time of one call with L2 flushed before it (informational).
+
+    A short device-side delay after the flush keeps the GPU busy while the
+    host submits the call, so the events bracket device time only, not the
+    host's submission latency."""
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=pool.dev)
     times = []
     st = torch.cuda.current_stream()
     for r in range(reps):
         flush.fill_(float(r))
+        torch.cuda._sleep(200_000)          # ~0.1 ms of GPU clock cycles
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(st)
@@ -579,11 +584,14 @@ def run_ours(args, dist):
     achieved_gbs = bytes_per_step / sec_per_step / 1e9
     peak, peak_src = hbm_peak()
 
+    # row splits under the headline's conditions, right after it
+    splits = (split_timings(torch, kv, pool, steps=args.steps, chunk=args.graph_chunk)
+              if not args.no_split_timings else {})
+
     # --- end to end: pinned host -> device inputs, error record back --------
     e2e = run_e2e(args, dist, torch, kv, pool, device)
 
     cold_us = single_call_cold_us(torch, pool, stream_handle())
-    splits = split_timings(torch, kv, pool) if not args.no_split_timings else {}
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -799,8 +807,10 @@ def run_e2e_gather(args, dist, torch, kv, pool, device):
             "by_mode": out}
 
 
-def split_timings(torch, kv, pool, steps=2000):
-    """Per-call time of the copy workload with each legal row split (1, 2, 4)."""
+def split_timings(torch, kv, pool, steps, chunk):
+    """Per-call time of the copy workload with each legal row split (1, 2, 4),
+    timed like the headline: the same number of steps from CUDA graphs of
+    `chunk` calls, after one untimed replay."""
     w = pool.w
     out = {}
     if w.kind != "copy":
@@ -815,8 +825,7 @@ def split_timings(torch, kv, pool, steps=2000):
             def step(i):
                 assert pool.call(i % pool.num_batches, torch.cuda.current_stream().cuda_stream) == 0
 
-            n = min(steps, 1000)
-            graphs = capture_graphs(torch, step, steps, n)
+            graphs = capture_graphs(torch, step, steps, min(steps, chunk))
             run_graphs(graphs)
             torch.cuda.synchronize()
             e0 = torch.cuda.Event(enable_timing=True)
