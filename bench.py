@@ -408,23 +408,86 @@ def single_call_cold_us(torch, pool, stream_handle, reps=30):
 # CPU oracle timing
 # ---------------------------------------------------------------------------
 
-def oracle_tokens_per_s(name: str, seconds: float):
-    """Time the CPU oracle (as it stands, one thread) on a bounded sample of
-    the workload: its whole batch, repeated until `seconds` elapse (at least
-    three times). Returns (tokens/s, description of the sample)."""
+# Workload kinds whose oracle call takes a token range, so that host threads
+# can split a batch (ctypes releases the GIL during the call).
+_ORACLE_SPLITS = ("copy", "fp8")
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_batch_runner(name, w, threads, tokens=None):
+    """fn() that pushes the first `tokens` tokens of the workload's batch
+    (default: all) through the CPU oracle, split over `threads` host threads
+    by token range when the kind allows, and the thread count it uses."""
+    tokens = w.T if tokens is None else tokens
+    oracle_step(name, w, 1)       # loads the oracle and its host caches in this thread
+    if threads <= 1 or w.kind not in _ORACLE_SPLITS:
+        return (lambda: oracle_step(name, w, tokens)), 1
+    from concurrent.futures import ThreadPoolExecutor
+    threads = min(threads, tokens)
+    cuts = [tokens * i // threads for i in range(threads + 1)]
+    ranges = list(zip(cuts[:-1], cuts[1:]))
+    ex = ThreadPoolExecutor(threads)
+    return (lambda: list(ex.map(lambda r: oracle_step(name, w, r[1], t_begin=r[0]), ranges))), threads
+
+
+def oracle_tokens_per_s(name: str, seconds: float, threads: int = 1):
+    """Time the CPU oracle (as it stands) on a bounded sample of the workload:
+    its whole batch, repeated until `seconds` elapse (at least three times),
+    on `threads` host threads (token ranges) where the kind allows.
+    Returns (tokens/s, description of the sample, threads used)."""
     w = load_workload(name)
-    oracle_step(name, w, w.T)                   # first touch of the written pages
-    n = 0
-    t0 = time.perf_counter()
-    while True:
-        oracle_step(name, w, w.T)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds and n >= 3:
-            break
-    sample = (f"{n} repetitions of the workload's batch of {w.T} tokens "
-              f"({el:.1f} s, one thread, full-size host caches)")
-    return n * w.T / el, sample
+    run, used = oracle_batch_runner(name, w, threads)
+    run()                                       # first touch of the written pages
+    if used == 1:
+        n = 0
+        t0 = time.perf_counter()
+        while True:
+            run()
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= seconds and n >= 3:
+                break
+        sample = (f"{n} repetitions of the workload's batch of {w.T} tokens "
+                  f"({el:.1f} s, one thread, full-size host caches)")
+        return n * w.T / el, sample, 1
+    # each thread repeats its own token range until the deadline (no per-batch
+    # hand-off between threads); throughput = all tokens / the longest thread
+    import threading
+    cuts = [w.T * i // used for i in range(used + 1)]
+    counts = [0] * used
+    ends = [0.0] * used
+    start = threading.Barrier(used + 1)
+    t0 = [0.0]
+
+    def worker(i):
+        start.wait()
+        deadline = t0[0] + seconds
+        while True:
+            oracle_step(name, w, cuts[i + 1], t_begin=cuts[i])
+            counts[i] += 1
+            now = time.perf_counter()
+            if now >= deadline and counts[i] >= 3:
+                ends[i] = now
+                return
+
+    ts = [threading.Thread(target=worker, args=(i,)) for i in range(used)]
+    for t in ts:
+        t.start()
+    t0[0] = time.perf_counter()
+    start.wait()
+    for t in ts:
+        t.join()
+    el = max(ends) - t0[0]
+    tokens = sum(c * (cuts[i + 1] - cuts[i]) for i, c in enumerate(counts))
+    sample = (f"{tokens} tokens of the workload's batch of {w.T} ({el:.1f} s, {used} threads, "
+              f"each repeating its own token range, full-size host caches)")
+    return tokens / el, sample, used
 
 
 def cpu_model():
@@ -450,16 +513,19 @@ def run_reference(args, dist):
     w = load_workload(name)
     # calibrate on one whole batch (after a first pass that touches the pages),
     # then size each step's sample so that the whole run takes about two minutes
-    oracle_step(name, w, w.T)
+    run, used = oracle_batch_runner(name, w, host_threads())
+    run()
     t0 = time.perf_counter()
-    oracle_step(name, w, w.T)
+    run()
     rate = w.T / (time.perf_counter() - t0)
     per_step_s = 120.0 / max(1, args.steps + args.warmup)
     tokens = max(1, min(w.T, int(rate * per_step_s)))
+    if tokens < w.T:
+        run, used = oracle_batch_runner(name, w, host_threads(), tokens)
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle_step(name, w, tokens)
+        run()
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     total = sum(times)
@@ -471,9 +537,12 @@ def run_reference(args, dist):
         "vs_baseline": None, "dtype": dtype_of(w), "data": "synthetic",
         "config": {"workload": DESCRIPTIONS[name], "tokens_per_step": tokens,
                    "achieved_gbs": value * w.algorithmic_bytes() / w.T / 1e9},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
                          "sample": f"each step: the first {tokens} of the workload's {w.T} "
-                                   f"tokens through the CPU oracle, one thread ({cpu_model()})"},
+                                   f"tokens through the CPU oracle, "
+                                   + ("one thread" if used == 1 else
+                                      f"{used} threads, one token range each")
+                                   + f" ({cpu_model()})"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -491,7 +560,9 @@ def load_workload(name, n_slots=None):
 _ORACLE_CACHE = {}
 
 
-def oracle_step(name, w, tokens):
+def oracle_step(name, w, tokens, t_begin=0):
+    """Tokens [t_begin, tokens) of the workload through the CPU oracle
+    (t_begin > 0 only for the kinds in _ORACLE_SPLITS)."""
     import oracle
     key = name
     if key not in _ORACLE_CACHE:
@@ -517,11 +588,11 @@ def oracle_step(name, w, tokens):
                           1, t_end=tokens)
     elif w.kind == "copy":
         oracle.store_copy(k, v, kc, vc, w.indices, st, w.H, w.D, 2, w.n_slots,
-                          k_off=w.k_view[0], v_off=w.v_view[0], t_end=tokens)
+                          k_off=w.k_view[0], v_off=w.v_view[0], t_begin=t_begin, t_end=tokens)
     else:
         oracle.store_fp8(k, v, kc, vc, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
                          w.page_stride, w.page_stride, w.n_slots, w.inv_k, w.inv_v,
-                         w.use_scale, t_end=tokens)
+                         w.use_scale, t_begin=t_begin, t_end=tokens)
 
 
 def dtype_of(w):
@@ -595,9 +666,11 @@ def run_ours(args, dist):
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        rate, sample = oracle_tokens_per_s(name, args.cpu_seconds)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": sample + f"; host CPU: {cpu_model()}"}
+        rate1, sample1, _ = oracle_tokens_per_s(name, args.cpu_seconds / 2)
+        rate, sample, used = oracle_tokens_per_s(name, args.cpu_seconds / 2, host_threads())
+        cpu = {"value": rate, "unit": "tokens/s", "cores": used, "kind": "oracle",
+               "sample": sample + f"; host CPU: {cpu_model()}",
+               "one_thread": {"value": rate1, "sample": sample1}}
 
     traffic = load_traffic(name)
     line = {
@@ -850,7 +923,8 @@ def parse_args(argv=None):
     ap.add_argument("--pool-mb", type=int, default=512)
     ap.add_argument("--graph-chunk", type=int, default=1000)
     ap.add_argument("--e2e-steps", type=int, default=20000)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0,
+                    help="CPU oracle timing: half on one thread, half on all host threads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-split-timings", action="store_true")
     ap.add_argument("--slots", type=int, default=None,

@@ -1,0 +1,54 @@
+"""Host-side pieces of bench.py that need no GPU: the CPU-oracle timing
+(one thread, and split over host threads by token range) and the reference
+arm's JSON line."""
+
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_split_oracle_run_writes_the_same_caches():
+    """Token ranges on several threads write exactly what one whole-batch
+    call writes."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for name in ("tiny",):
+        w = bench.load_workload(name)
+        run1, used1 = bench.oracle_batch_runner(name, w, 1)
+        kc, vc = bench._ORACLE_CACHE[name][:2]
+        kc[:] = 0
+        vc[:] = 0
+        run1()
+        want = kc.copy(), vc.copy()
+        run4, used4 = bench.oracle_batch_runner(name, w, 4)
+        assert (used1, used4) == (1, 4)
+        kc[:] = 0
+        vc[:] = 0
+        run4()
+        assert np.array_equal(kc, want[0]) and np.array_equal(vc, want[1])
+        assert np.count_nonzero(want[0]) > 0
+
+
+def test_oracle_rates_are_positive():
+    sys.path.insert(0, ROOT)
+    import bench
+    r1, s1, c1 = bench.oracle_tokens_per_s("tiny", 0.2)
+    r4, s4, c4 = bench.oracle_tokens_per_s("tiny", 0.2, threads=4)
+    assert r1 > 0 and r4 > 0 and c1 == 1 and c4 == 4
+    assert "one thread" in s1 and "4 threads" in s4
+
+
+def test_reference_arm_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "tiny", "--steps", "3", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
