@@ -254,6 +254,13 @@ FP8_CASES = {
     "long_rows_d576": dict(T=200, H=1, D=576, n_slots=600),
     "many_heads_long": dict(T=64, H=64, D=128, n_slots=128),
     "single_token": dict(T=1, H=8, D=128, n_slots=16),
+    # launches of at least 4096 warps: one warp writes the K and the V row of a token
+    "paired_rows_parts2": dict(T=1111, H=8, D=128, n_slots=4096, page_size=32),
+    "paired_pages_i32": dict(T=3000, H=8, D=128, n_slots=8192, page_size=16, page_pad=256,
+                             idx_dtype=np.int32),
+    "paired_heads_f16": dict(T=700, H=8, D=64, n_slots=2048, head_pad_src=64, head_pad_dst=32,
+                             src_dtype="f16"),
+    "paired_unscaled_odd_rows": dict(T=5000, H=1, D=576, n_slots=8192, use_scale=0),
 }
 
 
@@ -266,6 +273,12 @@ def test_fp8_parity(name):
 def test_fp8_out_of_range():
     p = fp8_problem(T=300, H=8, D=128, n_slots=1000, seed=91, page_size=16)
     p.indices[[0, 5, 299]] = [-7, 1000, 2 ** 50]
+    assert_same(p)
+
+
+def test_fp8_out_of_range_paired():
+    p = fp8_problem(T=3000, H=8, D=128, n_slots=8192, seed=94, page_size=16)
+    p.indices[[0, 1500, 2999]] = [-1, 8192, 2 ** 40]
     assert_same(p)
 
 
