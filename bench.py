@@ -57,6 +57,11 @@ DESCRIPTIONS = {
     "fp8": "fused FP8 write: T=8192, H_kv=8, D=128 bf16 4*N(0,1) with 0.1% outliers, "
            "inv_scale=448/amax (use_scale=1), e4m3fn cache 1,048,576 slots, page_size 32, int64",
     "fp8_noscale": "fused FP8 write as fp8 with use_scale=0",
+    "fp8_dynamic": "dynamic FP8 write: the fp8 batch with per-(token, head) scales computed in "
+                   "the kernel (amax/448 per head, stored per slot as fp32), e4m3fn cache "
+                   "1,048,576 slots, page_size 32, int64",
+    "paged": "paged copy: the prefill batch into 4-D pages [65536, 64, 8, 128] padded by one "
+             "slot per page (page stride 133,120 B), int32",
     "strided": "strided copy: fp16 K/V views into QKV [65536, 6144] (token stride 12,288 B), "
                "cache 2,097,152 slots, int32",
     "odd": "odd-size copy: fp16 H_kv=1, D=576 (1152 B rows), 1280 B slot stride, "
@@ -71,7 +76,7 @@ DESCRIPTIONS = {
 
 DEFAULT_STEPS = {"tiny": 200000, "decode": 200000, "prefill": 10000, "fp8": 50000,
                  "fp8_noscale": 50000, "strided": 5000, "odd": 10000, "gather_decode": 200000,
-                 "gather_fp8": 50000, "absmax": 50000}
+                 "gather_fp8": 50000, "absmax": 50000, "fp8_dynamic": 50000, "paged": 10000}
 
 
 # ---------------------------------------------------------------------------
@@ -245,26 +250,29 @@ class Pool:
             self.idx.append(ib)
         # caches (for the gather workloads: seeded random content to read back)
         if w.kind == "gather":
-            words = w.n_slots * w.slot_stride // 2
+            words = w.cache_bytes // 2
             self.kc = torch.randint(-32768, 32767, (words,), generator=g, dtype=torch.int16,
                                     device=device)
             self.vc = torch.randint(-32768, 32767, (words,), generator=g, dtype=torch.int16,
                                     device=device)
         elif w.kind == "gather_fp8":
-            nbytes = w.n_slots * w.slot_stride
+            nbytes = w.cache_bytes
             self.kc = torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8, device=device)
             self.vc = torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8, device=device)
         elif w.kind == "absmax":
             self.kc = torch.zeros(1, dtype=torch.uint8, device=device)
             self.vc = torch.zeros(1, dtype=torch.uint8, device=device)
         elif w.kind == "copy":
-            words = w.n_slots * w.slot_stride // 2
+            words = w.cache_bytes // 2
             self.kc = torch.full((words,), w.sentinel, dtype=torch.int16, device=device)
             self.vc = torch.full((words,), w.sentinel, dtype=torch.int16, device=device)
         else:
-            nbytes = w.n_slots * w.slot_stride
+            nbytes = w.cache_bytes
             self.kc = torch.full((nbytes,), w.sentinel, dtype=torch.uint8, device=device)
             self.vc = torch.full((nbytes,), w.sentinel, dtype=torch.uint8, device=device)
+        if w.kind == "fp8_dyn":       # per-slot, per-head fp32 scale caches
+            self.ks = torch.full((w.n_slots * w.H,), -1.0, dtype=torch.float32, device=device)
+            self.vs = torch.full_like(self.ks, -1.0)
         self.inv = torch.tensor([w.inv_k, w.inv_v], dtype=torch.float32, device=device)
         self.scale = torch.ones(2, dtype=torch.float32, device=device) / self.inv
         self.amax_inv = torch.zeros(4, dtype=torch.float32, device=device)
@@ -276,7 +284,7 @@ class Pool:
     def _slots(self, g, idx_dtype):
         import torch
         w = self.w
-        if w.name == "prefill":
+        if w.notes.get("whole_pages"):
             ps = w.page_size
             pages = torch.randperm(w.n_slots // ps, generator=g, device=self.dev)[: w.T // ps]
             s = (pages[:, None] * ps + torch.arange(ps, device=self.dev)[None, :]).reshape(-1)
@@ -306,10 +314,22 @@ class Pool:
         v_ptr = vbase if v_ptr is None else v_ptr
         idx_ptr = self.idx[b].data_ptr() if idx_ptr is None else idx_ptr
         idt = 1 if self.i64 else 0
+        if w.kind == "copy" and w.paged:
+            return kv.raw.kv_store_paged(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(),
+                                         idx_ptr, idt, 1, w.T, w.H, w.D, 2, strides, w.page_size,
+                                         w.page_stride, w.page_stride, w.n_slots, w.num_split,
+                                         self.err.data_ptr(), stream_handle)
         if w.kind == "copy":
             return kv.raw.kv_store(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(), idx_ptr,
                                    idt, 1, w.T, w.H, w.D, 2, strides, w.n_slots, w.num_split,
                                    self.err.data_ptr(), stream_handle)
+        if w.kind == "fp8_dyn":
+            return kv.raw.kv_store_fp8_ex(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(),
+                                          idx_ptr, idt, 1, w.T, w.H, w.D,
+                                          1 if w.src_dtype == "bf16" else 0, strides, w.page_size,
+                                          w.page_stride, w.page_stride, w.n_slots, 0, 3, None,
+                                          None, self.ks.data_ptr(), self.vs.data_ptr(), w.H,
+                                          self.err.data_ptr(), stream_handle)
         if w.kind == "absmax":
             return kv.raw.kv_absmax_inv(k_ptr, v_ptr, 1 if w.src_dtype == "bf16" else 0, w.T, w.H,
                                         w.D, strides, 448.0, self.amax_inv.data_ptr(),
@@ -409,7 +429,8 @@ def single_call_cold_us(torch, pool, stream_handle, reps=30):
 # ---------------------------------------------------------------------------
 
 # Workload kinds whose oracle call takes a token range, so that host threads
-# can split a batch (ctypes releases the GIL during the call).
+# can split a batch (ctypes releases the GIL during the call); the padded-page
+# copy has no token-range form and runs on one thread.
 _ORACLE_SPLITS = ("copy", "fp8")
 
 
@@ -426,7 +447,7 @@ def oracle_batch_runner(name, w, threads, tokens=None):
     by token range when the kind allows, and the thread count it uses."""
     tokens = w.T if tokens is None else tokens
     oracle_step(name, w, 1)       # loads the oracle and its host caches in this thread
-    if threads <= 1 or w.kind not in _ORACLE_SPLITS:
+    if threads <= 1 or w.kind not in _ORACLE_SPLITS or w.paged:
         return (lambda: oracle_step(name, w, tokens)), 1
     from concurrent.futures import ThreadPoolExecutor
     threads = min(threads, tokens)
@@ -552,8 +573,8 @@ def run_reference(args, dist):
 def load_workload(name, n_slots=None):
     import workloads as wl
     kw = {} if n_slots is None else {"n_slots": n_slots}
-    if name.startswith("fp8"):
-        return wl.fp8(use_scale=0 if name == "fp8_noscale" else 1, **kw)
+    if name == "fp8_noscale":
+        return wl.fp8(use_scale=0, **kw)
     return wl.WORKLOADS[name](**kw)
 
 
@@ -566,7 +587,10 @@ def oracle_step(name, w, tokens, t_begin=0):
     import oracle
     key = name
     if key not in _ORACLE_CACHE:
-        cache_bytes = 1 if w.kind == "absmax" else w.n_slots * w.slot_stride
+        cache_bytes = 1 if w.kind == "absmax" else w.cache_bytes
+        if w.kind == "fp8_dyn":
+            _ORACLE_CACHE[key + "/scales"] = (np.empty(w.n_slots * w.H, dtype=np.float32),
+                                              np.empty(w.n_slots * w.H, dtype=np.float32))
         _ORACLE_CACHE[key] = (np.empty(cache_bytes, dtype=np.uint8),
                               np.empty(cache_bytes, dtype=np.uint8),
                               np.ascontiguousarray(w.k).view(np.uint8).reshape(-1).copy(),
@@ -586,9 +610,19 @@ def oracle_step(name, w, tokens, t_begin=0):
         oracle.gather_fp8(kc, vc, k, v, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
                           w.page_stride, w.page_stride, w.n_slots, 1.0 / w.inv_k, 1.0 / w.inv_v,
                           1, t_end=tokens)
+    elif w.kind == "copy" and w.paged:
+        oracle.store_copy_paged(k, v, kc, vc, w.indices, st, w.H, w.D, 2, w.page_size,
+                                w.page_stride, w.page_stride, w.n_slots, k_off=w.k_view[0],
+                                v_off=w.v_view[0], t_end=tokens)
     elif w.kind == "copy":
         oracle.store_copy(k, v, kc, vc, w.indices, st, w.H, w.D, 2, w.n_slots,
                           k_off=w.k_view[0], v_off=w.v_view[0], t_begin=t_begin, t_end=tokens)
+    elif w.kind == "fp8_dyn":
+        ks, vs = _ORACLE_CACHE[key + "/scales"]
+        oracle.store_fp8_ex(k, v, kc, vc, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
+                            w.page_stride, w.page_stride, w.n_slots, fmt="e4m3fn",
+                            scale_mode="token_head", k_scales=ks, v_scales=vs,
+                            scales_slot_stride=w.H, t_end=tokens)
     else:
         oracle.store_fp8(k, v, kc, vc, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
                          w.page_stride, w.page_stride, w.n_slots, w.inv_k, w.inv_v,
@@ -598,7 +632,7 @@ def oracle_step(name, w, tokens, t_begin=0):
 def dtype_of(w):
     if w.kind == "absmax":
         return f"f32 ({w.src_dtype} in)"
-    if w.kind == "fp8":
+    if w.kind in ("fp8", "fp8_dyn"):
         return f"f32 ({w.src_dtype} in, e4m3fn out)"
     if w.kind == "gather_fp8":
         return f"f32 (e4m3fn in, {w.src_dtype} out)"
@@ -714,7 +748,8 @@ def kernel_source_hash(name: str) -> str:
     counters in profiles/ were taken with."""
     import hashlib
     unit = ("kv_gather.cu" if name.startswith("gather") else
-            "kv_scale.cu" if name == "absmax" else "kvstore.cu")
+            "kv_scale.cu" if name == "absmax" else
+            "kv_fp8_ex.cu" if name == "fp8_dynamic" else "kvstore.cu")
     files = _COMMON_SOURCES + ("fp8_quant_gb300/csrc/" + unit,)
     h = hashlib.sha256()
     for f in files:

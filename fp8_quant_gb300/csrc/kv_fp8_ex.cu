@@ -171,6 +171,130 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_rows(const __grid_constan
   if (!KV_EARLY_TRIGGER) grid_dependents_launch();
 }
 
+// Fast path for rows whose heads are contiguous on both sides: the layout of
+// the static FP8 write (lane l converts the 16-element chunks l, l+32, ... of
+// a row: 32 input bytes, 16 output bytes each), with each group's amax
+// reduced over the lanes that hold it.  A head of D elements is D/16
+// consecutive chunks, so in every 32-chunk slab of the row it sits on an
+// aligned run of D/16 lanes; a shuffle over those lanes gives its amax.  In
+// the per-token mode the group is the whole row.  Large launches pair the K
+// and the V row of a token in one warp (NS == 2).
+struct DynRowParams {
+  DynSide side[2];
+  const void* indices;
+  int64_t index_stride, size_limit, page_size, scales_stride;
+  UnitShape shape;          // units: (token, K|V) rows, or tokens when paired
+  uint32_t chunks;          // 16-element chunks per row
+  uint32_t group_chunks;    // chunks per scale group (D / 16), or 0: the whole row
+  float fmax;
+  kv_error_record* err;
+  int prefetch;             // rows in device memory: bulk L2 prefetch allowed
+};
+
+template <int J, int NS, typename IdxT, bool kBF16, int FMT>
+__global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant__ DynRowParams p) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
+  uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + (threadIdx.x >> 5);
+  const uint32_t n = p.chunks;
+  const uint32_t g = p.group_chunks;
+  if (KV_PREFETCH && p.prefetch && lane == 0 && u < p.shape.num_units) {
+    const Unit w = decode_unit(p.shape, u);
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const DynSide& sd = p.side[NS == 2 ? i : w.kv];
+      prefetch_l2_bulk(sd.src + w.token * sd.src_token, n * 32u);
+    }
+    prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
+  }
+  grid_handover();
+
+  for (; u < p.shape.num_units; u += nwarps) {
+    const Unit w = decode_unit(p.shape, u);
+    const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
+    Chunk<32> buf[NS][J];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const DynSide& sd = p.side[NS == 2 ? i : w.kv];
+      const uint8_t* src = sd.src + w.token * sd.src_token;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const uint32_t c = lane + 32u * j;
+        if (c < n) ld_stream(buf[i][j], src + static_cast<size_t>(c) * 32u);
+      }
+    }
+    float a[NS][J];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        a[i][j] = lane + 32u * j < n ? chunk_absmax<16, kBF16>(0.0f, buf[i][j]) : 0.0f;
+      if (g != 0) {             // per head: the aligned run of g lanes
+        for (uint32_t o = 1; o < g; o <<= 1)
+#pragma unroll
+          for (int j = 0; j < J; ++j) a[i][j] = fmaxf(a[i][j], __shfl_xor_sync(0xFFFFFFFFu, a[i][j], o));
+      } else {                  // per token: the whole row
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < J; ++j) m = fmaxf(m, a[i][j]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+#pragma unroll
+        for (int j = 0; j < J; ++j) a[i][j] = m;
+      }
+    }
+    if (slot < 0 || slot >= p.size_limit) {
+      if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
+      continue;
+    }
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const DynSide& sd = p.side[NS == 2 ? i : w.kv];
+      uint8_t* dst = sd.dst + paged_offset(slot, p.page_size, sd.dst_page, sd.dst_slot);
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const uint32_t c = lane + 32u * j;
+        if (c >= n) continue;
+        const bool pos = a[i][j] > 0.0f;
+        const float inv = pos ? __fdiv_rn(p.fmax, a[i][j]) : 1.0f;
+        st_stream(dst + static_cast<size_t>(c) * 16u, chunk_quant<16, kBF16, FMT>(buf[i][j], inv));
+        const bool first = g != 0 ? (c % g) == 0 : c == 0;   // one lane stores the group's scale
+        if (first)
+          sd.scales[slot * p.scales_stride + (g != 0 ? c / g : 0u)] =
+              pos ? __fdiv_rn(a[i][j], p.fmax) : 1.0f;
+      }
+    }
+  }
+  if (!KV_EARLY_TRIGGER) grid_dependents_launch();
+}
+
+template <int J, typename IdxT, int FMT>
+kv_status launch_dyn_row_j(bool bf16, const DynRowParams& p, cudaStream_t stream) {
+  if (p.shape.num_units >= KV_LARGE_LAUNCH_WARPS) {
+    DynRowParams q = p;   // one warp per token: K and V rows together
+    q.shape.units_per_token = 1;
+    q.shape.units_per_side = 1;
+    q.shape.num_units /= 2;
+    if (bf16) return launch(kv_fp8_dyn_row<J, 2, IdxT, true, FMT>, q.shape.num_units, q, stream);
+    return launch(kv_fp8_dyn_row<J, 2, IdxT, false, FMT>, q.shape.num_units, q, stream);
+  }
+  if (bf16) return launch(kv_fp8_dyn_row<J, 1, IdxT, true, FMT>, p.shape.num_units, p, stream);
+  return launch(kv_fp8_dyn_row<J, 1, IdxT, false, FMT>, p.shape.num_units, p, stream);
+}
+
+template <typename IdxT, int FMT>
+kv_status launch_dyn_row_fmt(int j, bool bf16, const DynRowParams& p, cudaStream_t stream) {
+  if (j == 1) return launch_dyn_row_j<1, IdxT, FMT>(bf16, p, stream);
+  if (j == 2) return launch_dyn_row_j<2, IdxT, FMT>(bf16, p, stream);
+  return launch_dyn_row_j<4, IdxT, FMT>(bf16, p, stream);
+}
+
+template <typename IdxT>
+kv_status launch_dyn_row(int j, int fmt, bool bf16, const DynRowParams& p, cudaStream_t stream) {
+  if (fmt == kFmtE5M2) return launch_dyn_row_fmt<IdxT, kFmtE5M2>(j, bf16, p, stream);
+  return launch_dyn_row_fmt<IdxT, kFmtE4M3>(j, bf16, p, stream);
+}
+
 template <int CH, typename IdxT, int FMT>
 kv_status launch_dyn_fmt(bool bf16, const DynParams& p, cudaStream_t stream) {
   if (bf16) return launch(kv_fp8_dyn_rows<CH, IdxT, true, FMT>, p.num_units, p, stream);
@@ -242,6 +366,51 @@ extern "C" kv_status kv_store_fp8_ex(const void* k, const void* v, void* k_cache
     if (cs != KV_OK) return cs;
   }
   const bool flat = kc_page_stride == page_size * s->kc_slot && vc_page_stride == page_size * s->vc_slot;
+  const bool bf16 = src_dtype == KV_SRC_BF16;
+
+  // fast path: heads contiguous on both sides, 32-byte aligned input rows,
+  // 16-byte aligned cache rows, rows of at most 128 chunks, and (per head) a
+  // head of D/16 chunks with D/16 a power of two up to 32
+  {
+    const int64_t row = static_cast<int64_t>(num_heads) * head_dim;
+    const bool contiguous = num_heads == 1 || (s->k_head == 2 * static_cast<int64_t>(head_dim) &&
+                                               s->v_head == 2 * static_cast<int64_t>(head_dim) &&
+                                               s->kc_head == head_dim && s->vc_head == head_dim);
+    const uint64_t in_bits = u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token);
+    uint64_t out_bits = u64(k_cache) | u64(v_cache) | u64(s->kc_slot) | u64(s->vc_slot);
+    if (!flat) out_bits |= u64(kc_page_stride) | u64(vc_page_stride);
+    const int64_t gch = head_dim / 16;
+    const bool groups_ok = !per_head || (head_dim % 16 == 0 && gch <= 32 && (gch & (gch - 1)) == 0);
+    const int64_t chunks = row / 16;
+    if (contiguous && row % 16 == 0 && chunks <= 128 && (in_bits & 31u) == 0 &&
+        (out_bits & 15u) == 0 && groups_ok) {
+      DynRowParams p = {};
+      p.side[0] = DynSide{static_cast<const uint8_t*>(k), static_cast<uint8_t*>(k_cache),
+                          s->k_token, s->k_head, s->kc_slot, s->kc_head,
+                          flat ? s->kc_slot : kc_page_stride, k_scales};
+      p.side[1] = DynSide{static_cast<const uint8_t*>(v), static_cast<uint8_t*>(v_cache),
+                          s->v_token, s->v_head, s->vc_slot, s->vc_head,
+                          flat ? s->vc_slot : vc_page_stride, v_scales};
+      p.indices = indices;
+      p.index_stride = index_stride;
+      p.size_limit = size_limit;
+      p.page_size = flat ? 1 : page_size;
+      p.scales_stride = scales_slot_stride;
+      p.shape.parts = 1;
+      p.shape.units_per_side = 1;
+      p.shape.units_per_token = 2;
+      p.shape.num_units = static_cast<uint64_t>(num_tokens) * 2u;
+      p.shape.part_chunks = static_cast<uint32_t>(chunks);
+      p.chunks = static_cast<uint32_t>(chunks);
+      p.group_chunks = per_head ? static_cast<uint32_t>(gch) : 0u;
+      p.fmax = fmt == kFmtE5M2 ? 57344.0f : 448.0f;
+      p.err = d_err;
+      p.prefetch = on_device ? 1 : 0;
+      const int j = chunks <= 32 ? 1 : chunks <= 64 ? 2 : 4;
+      return index_dtype == KV_INDEX_I64 ? launch_dyn_row<int64_t>(j, fmt, bf16, p, stream)
+                                         : launch_dyn_row<int32_t>(j, fmt, bf16, p, stream);
+    }
+  }
 
   // group layout: per head, or the whole row (one segment when heads are
   // contiguous on both sides, else one segment per head)
@@ -289,7 +458,6 @@ extern "C" kv_status kv_store_fp8_ex(const void* k, const void* v, void* k_cache
   p.fmax = fmt == kFmtE5M2 ? 57344.0f : 448.0f;
   p.err = d_err;
   p.prefetch = (on_device && (sbits & 15u) == 0 && (seg_elems * 2) % 16 == 0) ? 1 : 0;
-  const bool bf16 = src_dtype == KV_SRC_BF16;
   return index_dtype == KV_INDEX_I64 ? launch_dyn<int64_t>(ch, fmt, bf16, p, stream)
                                      : launch_dyn<int32_t>(ch, fmt, bf16, p, stream);
 }

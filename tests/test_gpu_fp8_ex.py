@@ -1,10 +1,11 @@
 """GPU parity of the extended FP8 write and gather (kv_store_fp8_ex,
 kv_gather_fp8_ex) against the CPU oracle: e4m3fn and e5m2 caches; no scale,
 per-tensor scales, and scales computed per token row or per (token, head),
-whose per-slot scale caches are compared too. Layouts: contiguous rows,
-head-segmented rows, padded 4-D pages, odd head dims (narrow chunks), groups
-longer than a warp holds in registers (two-pass), both index types and
-out-of-range slots. All 65,536 bf16 and fp16 patterns go through the e5m2
+whose per-slot scale caches are compared too. Layouts: contiguous rows (the
+row-layout kernel, one side or K and V paired per warp), head-segmented
+rows, padded 4-D pages, odd head dims (narrow chunks), groups longer than a
+warp holds in registers (two-pass), both index types and out-of-range
+slots. All 65,536 bf16 and fp16 patterns go through the e5m2
 conversion."""
 
 import zlib
@@ -86,6 +87,9 @@ CASES = {
     "odd_d_narrow": dict(T=300, H=3, D=45, n_slots=1024, src_dtype="f16"),
     "d24_i32": dict(T=300, H=2, D=24, n_slots=1024, idx_dtype=np.int32, index_stride=2),
     "single_head_576": dict(T=256, H=1, D=576, n_slots=1024),
+    # at least 4096 rows: one warp converts the K and the V row of a token
+    "paired_rows_pages": dict(T=2500, H=8, D=128, n_slots=8192, page_size=16, page_pad=256),
+    "paired_long_rows_i32": dict(T=2100, H=16, D=128, n_slots=4096, idx_dtype=np.int32),
 }
 
 
@@ -103,6 +107,14 @@ def test_store_fp8_ex_dynamic_oob_and_scale_stride(mode):
     p = fp8_problem(T=300, H=4, D=64, n_slots=1000, seed=71, page_size=8)
     p.indices[[2, 150]] = [-1, 1000]
     run_store(p, "e4m3fn", mode, sstride=p.H + 3)
+
+
+@pytest.mark.parametrize("fmt", sorted(FMTS))
+@pytest.mark.parametrize("mode", ["token", "token_head"])
+def test_store_fp8_ex_dynamic_paired_oob(mode, fmt):
+    p = fp8_problem(T=4000, H=8, D=64, n_slots=8192, seed=77, page_size=32)
+    p.indices[[0, 1999, 3999]] = [-3, 8192, 2 ** 40]
+    run_store(p, fmt, mode, sstride=p.H + 1)
 
 
 @pytest.mark.parametrize("src", ["bf16", "f16"])

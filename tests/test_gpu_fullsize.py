@@ -141,3 +141,90 @@ def test_full_size_workload(name, split):
         assert _rows_changed(torch, cache, w.n_slots, sb, sent) == w.T, f"{what}: stray rows"
     del pool
     torch.cuda.empty_cache()
+
+
+def test_full_size_paged_copy():
+    """The prefill batch into padded 4-D pages through kv_store_paged: the
+    touched pages (pad bytes included) equal the oracle's, and no other page
+    changed."""
+    import torch
+    import bench
+    import fp8_quant_gb300 as kv
+    dev = torch.device("cuda", 0)
+    pool = bench.Pool("paged", dev, pool_bytes=0)
+    w = pool.w
+    assert w.paged and pool.num_batches == 1
+    assert pool.call(0, torch.cuda.current_stream().cuda_stream) == 0
+    assert kv.kv_error_poll(pool.err) == (kv.KVStatus.OK, 0, -1)
+    ps, pstride = w.page_size, w.page_stride
+    n_pages = w.cache_bytes // pstride
+    slots = w.indices.astype(np.int64)
+    pages = np.unique(slots // ps)
+    compact = {int(p): j for j, p in enumerate(pages)}
+    cidx = np.array([compact[int(s // ps)] * ps + int(s % ps) for s in slots], dtype=w.indices.dtype)
+    sent = w.sentinel.to_bytes(2, "little")
+    okc = np.frombuffer(sent * (len(pages) * pstride // 2), dtype=np.uint8).copy()
+    ovc = okc.copy()
+    st = oracle.Strides(k_token=w.k_view[1], k_head=w.k_view[2], k_dim=w.k_view[3],
+                        v_token=w.v_view[1], v_head=w.v_view[2], v_dim=w.v_view[3],
+                        kc_slot=w.slot_stride, kc_head=w.cache_head_stride, kc_dim=2,
+                        vc_slot=w.slot_stride, vc_head=w.cache_head_stride, vc_dim=2)
+    k = np.ascontiguousarray(w.k).view(np.uint8).reshape(-1)
+    v = np.ascontiguousarray(w.v).view(np.uint8).reshape(-1)
+    assert oracle.store_copy_paged(k, v, okc, ovc, cidx, st, w.H, w.D, 2, ps, pstride, pstride,
+                                   len(pages) * ps) == (0, -1)
+    sel = torch.from_numpy(pages).to(dev)
+    pat = torch.tensor(list(sent) * (pstride // 2), dtype=torch.uint8, device=dev)
+    for cache, want, what in ((pool.kc, okc, "K"), (pool.vc, ovc, "V")):
+        view = cache.view(torch.uint8)[: n_pages * pstride].view(n_pages, pstride)
+        got = view.index_select(0, sel).cpu().numpy().reshape(-1)
+        assert np.array_equal(got, want), f"{what}: touched pages differ"
+        changed = 0
+        for p0 in range(0, n_pages, 2048):
+            changed += int((view[p0:p0 + 2048] != pat).any(dim=1).sum().item())
+        assert changed == len(pages), f"{what}: stray pages"
+    del pool
+    torch.cuda.empty_cache()
+
+
+def test_full_size_dynamic_fp8():
+    """The fp8 batch with per-(token, head) scales computed in the kernel:
+    every written row and scale equals the oracle's, nothing else changed."""
+    import torch
+    import bench
+    import fp8_quant_gb300 as kv
+    dev = torch.device("cuda", 0)
+    pool = bench.Pool("fp8_dynamic", dev, pool_bytes=0)
+    w = pool.w
+    assert not w.paged and pool.num_batches == 1
+    assert pool.call(0, torch.cuda.current_stream().cuda_stream) == 0
+    assert kv.kv_error_poll(pool.err) == (kv.KVStatus.OK, 0, -1)
+    T, H, sb = w.T, w.H, w.slot_stride
+    idx = np.arange(T, dtype=w.indices.dtype)
+    okc = np.full(T * sb, w.sentinel, np.uint8)
+    ovc = okc.copy()
+    oks = np.full(T * H, -1.0, np.float32)
+    ovs = oks.copy()
+    st = oracle.Strides(k_token=w.k_view[1], k_head=w.k_view[2], k_dim=w.k_view[3],
+                        v_token=w.v_view[1], v_head=w.v_view[2], v_dim=w.v_view[3],
+                        kc_slot=sb, kc_head=w.cache_head_stride, kc_dim=1,
+                        vc_slot=sb, vc_head=w.cache_head_stride, vc_dim=1)
+    k = np.ascontiguousarray(w.k).view(np.uint8).reshape(-1)
+    v = np.ascontiguousarray(w.v).view(np.uint8).reshape(-1)
+    assert w.page_stride == w.page_size * sb
+    bad = oracle.store_fp8_ex(k, v, okc, ovc, idx, st, H, w.D, w.src_dtype, w.page_size,
+                              w.page_stride, w.page_stride, T + (-T) % w.page_size,
+                              fmt="e4m3fn", scale_mode="token_head", k_scales=oks,
+                              v_scales=ovs, scales_slot_stride=H)
+    assert bad == (0, -1)
+    slots = torch.from_numpy(w.indices.astype(np.int64)).to(dev)
+    for cache, scales, want, wscale, what in ((pool.kc, pool.ks, okc, oks, "K"),
+                                              (pool.vc, pool.vs, ovc, ovs, "V")):
+        rows = cache.view(w.n_slots, sb).index_select(0, slots).cpu().numpy().reshape(-1)
+        assert np.array_equal(rows, want), f"{what} cache rows differ"
+        got_s = scales.view(w.n_slots, H).index_select(0, slots).cpu().numpy().reshape(-1)
+        assert np.array_equal(got_s.view(np.uint32), wscale.view(np.uint32)), f"{what} scales"
+        assert _rows_changed(torch, cache, w.n_slots, sb, bytes([w.sentinel])) == T
+        assert int((scales != -1.0).sum().item()) == T * H
+    del pool
+    torch.cuda.empty_cache()

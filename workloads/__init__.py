@@ -26,6 +26,13 @@ measured on; ``T`` tokens, ``H`` KV heads, ``D`` head dim):
                cache 2,097,152 slots, int32.
 * ``odd``      fp16 H=1, D=576 (1152-byte rows), 1280-byte slot stride,
                cache 2,097,152 slots, int32.
+* ``paged``    the prefill batch into 4-D pages [65536, 64, 8, 128] padded by
+               one slot per page (page stride 133,120 B).
+* ``fp8_dynamic`` the fp8 batch with per-(token, head) scales computed in the
+               kernel and stored per slot.
+
+The gather workloads read these caches back (``gather_decode``,
+``gather_fp8``), and ``absmax`` reads the fp8 batch once.
 """
 
 from __future__ import annotations
@@ -132,7 +139,7 @@ class Workload:
     H: int
     D: int
     src_dtype: str                  # "bf16" | "f16"
-    kind: str                       # "copy" | "fp8" | "gather" | "gather_fp8" | "absmax"
+    kind: str                       # "copy" | "fp8" | "fp8_dyn" | "gather" | "gather_fp8" | "absmax"
     k: np.ndarray
     v: np.ndarray
     k_view: tuple
@@ -156,16 +163,24 @@ class Workload:
         return self.H * self.D * 2
 
     @property
+    def paged(self) -> bool:
+        """Pages padded beyond page_size slots (the 4-D [pages, page_size, H, D] layout)."""
+        return self.page_stride != self.page_size * self.slot_stride
+
+    @property
     def cache_bytes(self) -> int:
-        return self.n_slots * self.slot_stride
+        pages = -(-self.n_slots // self.page_size)
+        return pages * self.page_stride if self.paged else self.n_slots * self.slot_stride
 
     def algorithmic_bytes(self) -> int:
         """Bytes a call must move: K and V rows read, cache rows written, indices read
-        (for the absmax pass: K and V rows read, four floats written)."""
+        (for the absmax pass: K and V rows read, four floats written; for the
+        dynamic FP8 write also one fp32 scale per token and head, K and V)."""
         if self.kind == "absmax":
             return self.T * 2 * self.row_bytes + 16
         out_row = self.H * self.D * self.cache_elem
-        return self.T * (2 * self.row_bytes + 2 * out_row + self.indices.itemsize)
+        scales = 2 * self.H * 4 if self.kind == "fp8_dyn" else 0
+        return self.T * (2 * self.row_bytes + 2 * out_row + self.indices.itemsize + scales)
 
 
 def _contig_view(H: int, D: int, elem: int = 2):
@@ -245,8 +260,10 @@ def decode(num_split: int = 0, n_slots: int = 1 << 20) -> Workload:
 
 def prefill(n_slots: int = 1 << 22) -> Workload:
     slots = page_run_slots(0x5EED0002 * 4 + 3, n_pages=n_slots // 64, page_size=64, k_pages=512)
-    return make_copy("prefill", T=32768, H=8, D=128, n_slots=n_slots, seed=0x5EED0002,
-                     slots=slots, page_size=64)
+    w = make_copy("prefill", T=32768, H=8, D=128, n_slots=n_slots, seed=0x5EED0002,
+                  slots=slots, page_size=64)
+    w.notes["whole_pages"] = True
+    return w
 
 
 def fp8(use_scale: int = 1, n_slots: int = 1 << 20) -> Workload:
@@ -273,6 +290,25 @@ def strided(n_slots: int = 1 << 21) -> Workload:
                  cache_head_stride=D * 2, cache_elem=2, sentinel=BF16_SENTINEL,
                  page_size=16, page_stride=16 * H * D * 2)
     w.notes["shared_source"] = True
+    return w
+
+
+def paged(n_slots: int = 1 << 22) -> Workload:
+    """The prefill batch into a 4-D cache [pages, 64, 8, 128] whose pages are
+    padded by one slot (page stride 133,120 B): kv_store_paged."""
+    w = prefill(n_slots=n_slots)
+    w.name = "paged"
+    w.page_stride = w.page_size * w.slot_stride + w.slot_stride
+    w.notes["whole_pages"] = True
+    return w
+
+
+def fp8_dynamic(n_slots: int = 1 << 20) -> Workload:
+    """The ``fp8`` batch written with scales computed in the kernel per
+    (token, head): amax of each head's 128 elements, codes of x * (448/amax),
+    and amax/448 stored per slot and head in an fp32 scale cache."""
+    w = fp8(n_slots=n_slots)
+    w.name, w.kind = "fp8_dynamic", "fp8_dyn"
     return w
 
 
@@ -310,6 +346,8 @@ WORKLOADS = {
     "fp8": fp8,
     "strided": strided,
     "odd": odd,
+    "paged": paged,
+    "fp8_dynamic": fp8_dynamic,
     "gather_decode": gather_decode,
     "gather_fp8": gather_fp8,
     "absmax": absmax,
