@@ -247,6 +247,28 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant
       if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
       continue;
     }
+    // The warp holds NS * gps groups (gps per row).  Lane k computes the
+    // two divisions of group k, once: its amax comes from the lane holding
+    // the group's first chunk, and every lane then takes the inverse scale
+    // of its chunks' groups from lane k.
+    const uint32_t gps = g != 0 ? n / g : 1u;
+    const uint32_t gk = lane % gps;                       // lane's group within its side
+    const uint32_t c0 = g != 0 ? gk * g : 0u;             // first chunk of that group
+    float amax_k = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NS; ++i)
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const float v = __shfl_sync(0xFFFFFFFFu, a[i][j], c0 % 32u);
+        if (lane / gps == static_cast<uint32_t>(i) && c0 / 32u == static_cast<uint32_t>(j)) amax_k = v;
+      }
+    const bool pos_k = amax_k > 0.0f;
+    const bool owner = lane < NS * gps;
+    const float inv_k = owner && pos_k ? __fdiv_rn(p.fmax, amax_k) : 1.0f;
+    if (owner) {
+      const DynSide& sd = p.side[NS == 2 ? lane / gps : w.kv];
+      sd.scales[slot * p.scales_stride + gk] = pos_k ? __fdiv_rn(amax_k, p.fmax) : 1.0f;
+    }
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
       const DynSide& sd = p.side[NS == 2 ? i : w.kv];
@@ -254,14 +276,9 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const uint32_t c = lane + 32u * j;
-        if (c >= n) continue;
-        const bool pos = a[i][j] > 0.0f;
-        const float inv = pos ? __fdiv_rn(p.fmax, a[i][j]) : 1.0f;
-        st_stream(dst + static_cast<size_t>(c) * 16u, chunk_quant<16, kBF16, FMT>(buf[i][j], inv));
-        const bool first = g != 0 ? (c % g) == 0 : c == 0;   // one lane stores the group's scale
-        if (first)
-          sd.scales[slot * p.scales_stride + (g != 0 ? c / g : 0u)] =
-              pos ? __fdiv_rn(a[i][j], p.fmax) : 1.0f;
+        const uint32_t k = static_cast<uint32_t>(i) * gps + (g != 0 ? c / g : 0u);
+        const float inv = __shfl_sync(0xFFFFFFFFu, inv_k, k < 32u ? k : 0u);
+        if (c < n) st_stream(dst + static_cast<size_t>(c) * 16u, chunk_quant<16, kBF16, FMT>(buf[i][j], inv));
       }
     }
   }
@@ -370,7 +387,8 @@ extern "C" kv_status kv_store_fp8_ex(const void* k, const void* v, void* k_cache
 
   // fast path: heads contiguous on both sides, 32-byte aligned input rows,
   // 16-byte aligned cache rows, rows of at most 128 chunks, and (per head) a
-  // head of D/16 chunks with D/16 a power of two up to 32
+  // head of D/16 chunks with D/16 a power of two up to 32 and at most 16
+  // heads (a paired warp holds 2 * H groups, one per lane)
   {
     const int64_t row = static_cast<int64_t>(num_heads) * head_dim;
     const bool contiguous = num_heads == 1 || (s->k_head == 2 * static_cast<int64_t>(head_dim) &&
@@ -380,7 +398,8 @@ extern "C" kv_status kv_store_fp8_ex(const void* k, const void* v, void* k_cache
     uint64_t out_bits = u64(k_cache) | u64(v_cache) | u64(s->kc_slot) | u64(s->vc_slot);
     if (!flat) out_bits |= u64(kc_page_stride) | u64(vc_page_stride);
     const int64_t gch = head_dim / 16;
-    const bool groups_ok = !per_head || (head_dim % 16 == 0 && gch <= 32 && (gch & (gch - 1)) == 0);
+    const bool groups_ok = !per_head || (head_dim % 16 == 0 && gch <= 32 && (gch & (gch - 1)) == 0 &&
+                                         2 * num_heads <= 32);
     const int64_t chunks = row / 16;
     if (contiguous && row % 16 == 0 && chunks <= 128 && (in_bits & 31u) == 0 &&
         (out_bits & 15u) == 0 && groups_ok) {
