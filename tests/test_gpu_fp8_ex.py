@@ -127,6 +127,23 @@ def test_e5m2_exhaustive_input_patterns(src, inv):
     run_store(p, "e5m2", "none" if inv is None else "tensor")
 
 
+@pytest.mark.parametrize("src", ["bf16", "f16"])
+@pytest.mark.parametrize("fmt", sorted(FMTS))
+@pytest.mark.parametrize("mode", ["token", "token_head"])
+@pytest.mark.parametrize("tokens", [64, 2560])
+def test_dynamic_exhaustive_input_patterns(src, fmt, mode, tokens):
+    """Every 16-bit pattern (NaNs, infinities, subnormals, zeros) inside the
+    dynamically scaled groups: groups whose amax is infinite, groups of only
+    zeros or NaNs. 64 tokens run one side per warp, 2560 the paired form."""
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    rep = tokens * 8 * 128 // bits.size
+    kb = np.tile(bits, rep).reshape(tokens, 8, 128)
+    vb = np.tile(bits[::-1], rep).reshape(tokens, 8, 128)
+    p = fp8_problem(T=tokens, H=8, D=128, n_slots=4 * tokens, seed=78, src_dtype=src,
+                    src_bits=(kb, vb))
+    run_store(p, fmt, mode)
+
+
 def _gather(kc, vc, p, fmt, mode, ks=None, vs=None, sstride=1, out="bf16", scale=(1.0, 1.0)):
     import torch
     import fp8_quant_gb300 as kv
