@@ -97,7 +97,7 @@ def run_oracle(p: Problem):
     return kc, vc, res
 
 
-class GpuRun:
+class DeviceRun:
     """Device copies of a problem's inputs and caches, and the C-ABI call."""
 
     def __init__(self, p: Problem, device="cuda"):
@@ -177,7 +177,7 @@ def diff_report(got: np.ndarray, want: np.ndarray, row: int) -> str:
 
 def assert_same(p: Problem, row_bytes: Optional[int] = None, num_split=None):
     """Run both sides; compare every cache byte and the error report."""
-    g = GpuRun(p)
+    g = DeviceRun(p)
     rc = g.call(num_split=num_split)
     assert rc == 0, f"launch status {rc}"
     prc, pn, pfirst = g.poll()

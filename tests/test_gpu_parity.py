@@ -15,7 +15,7 @@ import numpy as np
 import pytest
 
 import workloads as wl
-from kvcheck import Problem, View, GpuRun, assert_same, copy_problem, fp8_problem, run_oracle
+from kvcheck import Problem, View, DeviceRun, assert_same, copy_problem, fp8_problem, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -141,7 +141,7 @@ def test_copy_duplicate_slots_take_a_candidate():
     T, n, H, D = 512, 64, 4, 64
     slots = (wl.splitmix64(83, 0, T) % np.uint64(n)).astype(np.int64)
     p = copy_problem(T=T, H=H, D=D, n_slots=n, seed=84, slots=slots)
-    g = GpuRun(p)
+    g = DeviceRun(p)
     assert g.call() == 0
     kc, vc = g.caches()
     E = H * D
@@ -283,8 +283,8 @@ def test_fp8_out_of_range_paired():
 
 
 def test_fp8_use_scale_off_equals_inv_one():
-    a = GpuRun(fp8_problem(T=512, H=8, D=128, n_slots=2048, seed=92, use_scale=0))
-    b = GpuRun(fp8_problem(T=512, H=8, D=128, n_slots=2048, seed=92, use_scale=1,
+    a = DeviceRun(fp8_problem(T=512, H=8, D=128, n_slots=2048, seed=92, use_scale=0))
+    b = DeviceRun(fp8_problem(T=512, H=8, D=128, n_slots=2048, seed=92, use_scale=1,
                            inv=(1.0, 1.0)))
     assert a.call() == 0 and b.call() == 0
     ka, va = a.caches()
@@ -328,7 +328,7 @@ def test_pinned_host_inputs(kind):
         p = copy_problem(T=700, H=8, D=128, n_slots=4096, seed=601)
     else:
         p = fp8_problem(T=700, H=8, D=128, n_slots=4096, seed=602, page_size=16)
-    g = GpuRun(p)
+    g = DeviceRun(p)
     hk, hv, hi = _pinned(p.k_src), _pinned(p.v_src), _pinned(p.indices)
     s = torch.cuda.current_stream().cuda_stream
     idt = 1 if p.indices.dtype == np.int64 else 0
@@ -354,7 +354,7 @@ def test_unregistered_host_memory_is_rejected():
     import torch
     import fp8_quant_gb300 as kv
     p = copy_problem(T=64, H=2, D=64, n_slots=256, seed=603)
-    g = GpuRun(p)
+    g = DeviceRun(p)
     s = torch.cuda.current_stream().cuda_stream
     k_host = p.k_src.ctypes.data                      # plain numpy buffer
     rc = kv.raw.kv_store(k_host, g.v_src.data_ptr(), g.kc.data_ptr(), g.vc.data_ptr(),
@@ -371,7 +371,7 @@ def test_error_snapshot_to_pinned_host_and_device():
     slots = wl.distinct_slots(611, 1000, 300)
     slots[[7, 9]] = [-1, 5000]
     p = copy_problem(T=300, H=2, D=64, n_slots=1000, seed=612, slots=slots)
-    g = GpuRun(p)
+    g = DeviceRun(p)
     assert g.call() == 0
     s = torch.cuda.current_stream().cuda_stream
     host = torch.zeros(2, dtype=torch.int64).pin_memory()
@@ -395,7 +395,7 @@ def test_concurrent_streams_disjoint_slots():
     import fp8_quant_gb300 as kv
     pc = copy_problem(T=3000, H=8, D=128, n_slots=8192, seed=621)
     pf = fp8_problem(T=3000, H=8, D=128, n_slots=8192, seed=622, page_size=16)
-    gc, gf = GpuRun(pc), GpuRun(pf)
+    gc, gf = DeviceRun(pc), DeviceRun(pf)
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
     torch.cuda.synchronize()
     for _ in range(3):

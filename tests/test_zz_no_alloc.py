@@ -18,7 +18,7 @@ import numpy as np
 import pytest
 
 import workloads as wl
-from kvcheck import GpuRun, copy_problem, run_oracle
+from kvcheck import DeviceRun, copy_problem, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -51,10 +51,10 @@ def test_noalloc_matches_kv_store_on_two_calls_in_a_row():
     ]
     expect = [(4, 3, 4), (0, 0, -1)]          # (status, oob_count, first_bad_token)
     for p, (want_rc, want_n, want_first) in zip(problems, expect):
-        ref = GpuRun(p)                       # existing entry point, caller's record
+        ref = DeviceRun(p)                       # existing entry point, caller's record
         assert ref.call() == 0
         ref_rc, ref_n, ref_first = ref.poll()
-        new = GpuRun(p)                       # same inputs, fresh sentinel caches
+        new = DeviceRun(p)                       # same inputs, fresh sentinel caches
         rc, nbad, first = _noalloc_call(new)
         assert (ref_rc, ref_n, ref_first) == (want_rc, want_n, want_first)
         assert (rc, nbad, first) == (want_rc, want_n, want_first)
@@ -72,6 +72,6 @@ def test_noalloc_argument_errors_and_empty_batch():
     assert kv.raw.kv_store_noalloc(None, None, None, None, None, 0, 1, 0, 8, 128, 2, zeros, 0, 0,
                                    None) == (0, 0, -1)
     p = copy_problem(T=16, H=2, D=64, n_slots=64, seed=504, num_split=4)   # 256 B rows
-    g = GpuRun(p)
+    g = DeviceRun(p)
     rc, _, _ = _noalloc_call(g)
     assert rc == kv.KVStatus.ERR_INVALID_ARG                               # split rule
