@@ -66,6 +66,8 @@ DESCRIPTIONS = {
                "cache 2,097,152 slots, int32",
     "odd": "odd-size copy: fp16 H_kv=1, D=576 (1152 B rows), 1280 B slot stride, "
            "cache 2,097,152 slots, int32",
+    "gather_prefill": "gather (inverse of prefill): T=32768 rows (512 whole pages) of H_kv=8, "
+                      "D=128 bf16 from a 4,194,304-slot cache, int32",
     "gather_decode": "gather (inverse of decode): T=256 rows of H_kv=8, D=128 bf16 from a "
                      "1,048,576-slot cache, int64",
     "gather_fp8": "dequantising gather (inverse of fp8): T=8192 e4m3fn rows x (1/inv) -> bf16, "
@@ -76,7 +78,8 @@ DESCRIPTIONS = {
 
 DEFAULT_STEPS = {"tiny": 200000, "decode": 200000, "prefill": 10000, "fp8": 50000,
                  "fp8_noscale": 50000, "strided": 5000, "odd": 10000, "gather_decode": 200000,
-                 "gather_fp8": 50000, "absmax": 50000, "fp8_dynamic": 50000, "paged": 10000}
+                 "gather_fp8": 50000, "absmax": 50000, "fp8_dynamic": 50000, "paged": 10000,
+                 "gather_prefill": 10000}
 
 
 # ---------------------------------------------------------------------------

@@ -61,7 +61,7 @@ def _oracle_gather_compact(w, rows_k, rows_v):
     return ok, ov
 
 
-@pytest.mark.parametrize("name", ["gather_decode", "gather_fp8"])
+@pytest.mark.parametrize("name", ["gather_decode", "gather_prefill", "gather_fp8"])
 def test_full_size_gather(name):
     import torch
     import bench

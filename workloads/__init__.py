@@ -32,7 +32,7 @@ measured on; ``T`` tokens, ``H`` KV heads, ``D`` head dim):
                kernel and stored per slot.
 
 The gather workloads read these caches back (``gather_decode``,
-``gather_fp8``), and ``absmax`` reads the fp8 batch once.
+``gather_prefill``, ``gather_fp8``), and ``absmax`` reads the fp8 batch once.
 """
 
 from __future__ import annotations
@@ -325,6 +325,14 @@ def gather_decode(n_slots: int = 1 << 20) -> Workload:
     return w
 
 
+def gather_prefill(n_slots: int = 1 << 22) -> Workload:
+    """Inverse of ``prefill``: 32768 rows (512 whole pages) gathered from a
+    4,194,304-slot bf16 cache."""
+    w = prefill(n_slots=n_slots)
+    w.name, w.kind = "gather_prefill", "gather"
+    return w
+
+
 def gather_fp8(n_slots: int = 1 << 20) -> Workload:
     """Inverse of ``fp8``: 8192 e4m3fn rows dequantised (x 1/inv) to bf16."""
     w = fp8(n_slots=n_slots)
@@ -349,6 +357,7 @@ WORKLOADS = {
     "paged": paged,
     "fp8_dynamic": fp8_dynamic,
     "gather_decode": gather_decode,
+    "gather_prefill": gather_prefill,
     "gather_fp8": gather_fp8,
     "absmax": absmax,
 }
