@@ -52,3 +52,27 @@ def test_reference_arm_line():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_workload_sizes():
+    """Cache sizes and algorithmic bytes of the bench workloads, from their
+    definitions: rows read, rows (and scales) written, slot ids read."""
+    sys.path.insert(0, ROOT)
+    import workloads as wl
+    d = wl.decode()
+    assert d.algorithmic_bytes() == 256 * (2 * 2048 + 2 * 2048 + 8)
+    assert d.cache_bytes == (1 << 20) * 2048 and not d.paged
+    f = wl.fp8()
+    assert f.algorithmic_bytes() == 8192 * (2 * 2048 + 2 * 1024 + 8)
+    fd = wl.fp8_dynamic()
+    assert fd.kind == "fp8_dyn" and fd.algorithmic_bytes() == f.algorithmic_bytes() + 8192 * 2 * 8 * 4
+    pg = wl.paged()
+    assert pg.paged and pg.page_stride == 64 * 2048 + 2048
+    assert pg.cache_bytes == (1 << 22) // 64 * pg.page_stride
+    # whole pages: every page named holds 64 consecutive slots
+    pages, counts = np.unique(pg.indices // 64, return_counts=True)
+    assert len(pages) == 512 and (counts == 64).all()
+    gp = wl.gather_prefill()
+    assert gp.kind == "gather" and gp.algorithmic_bytes() == 32768 * (4 * 2048 + 4)
+    o = wl.odd()
+    assert o.slot_stride == 1280 and o.algorithmic_bytes() == 65536 * (4 * 1152 + 4)
