@@ -60,6 +60,10 @@ DESCRIPTIONS = {
     "fp8_dynamic": "dynamic FP8 write: the fp8 batch with per-(token, head) scales computed in "
                    "the kernel (amax/448 per head, stored per slot as fp32), e4m3fn cache "
                    "1,048,576 slots, page_size 32, int64",
+    "fp8_dynamic_token": "dynamic FP8 write as fp8_dynamic with one scale per token row "
+                         "(amax over the 1024 elements of the K or V row)",
+    "fp8_e5m2": "FP8 write into an e5m2 cache: the fp8 batch, per-tensor inv_scale=57344/amax, "
+                "kv_store_fp8_ex",
     "paged": "paged copy: the prefill batch into 4-D pages [65536, 64, 8, 128] padded by one "
              "slot per page (page stride 133,120 B), int32",
     "strided": "strided copy: fp16 K/V views into QKV [65536, 6144] (token stride 12,288 B), "
@@ -79,6 +83,7 @@ DESCRIPTIONS = {
 DEFAULT_STEPS = {"tiny": 200000, "decode": 200000, "prefill": 10000, "fp8": 50000,
                  "fp8_noscale": 50000, "strided": 5000, "odd": 10000, "gather_decode": 200000,
                  "gather_fp8": 50000, "absmax": 50000, "fp8_dynamic": 50000, "paged": 10000,
+                 "fp8_dynamic_token": 50000, "fp8_e5m2": 50000,
                  "gather_prefill": 10000}
 
 
@@ -273,8 +278,10 @@ class Pool:
             nbytes = w.cache_bytes
             self.kc = torch.full((nbytes,), w.sentinel, dtype=torch.uint8, device=device)
             self.vc = torch.full((nbytes,), w.sentinel, dtype=torch.uint8, device=device)
-        if w.kind == "fp8_dyn":       # per-slot, per-head fp32 scale caches
-            self.ks = torch.full((w.n_slots * w.H,), -1.0, dtype=torch.float32, device=device)
+        if w.kind == "fp8_dyn":       # per-slot fp32 scale caches (per head or per row)
+            self.groups = w.H if w.notes.get("scale_mode", "token_head") == "token_head" else 1
+            self.ks = torch.full((w.n_slots * self.groups,), -1.0, dtype=torch.float32,
+                                 device=device)
             self.vs = torch.full_like(self.ks, -1.0)
         self.inv = torch.tensor([w.inv_k, w.inv_v], dtype=torch.float32, device=device)
         self.scale = torch.ones(2, dtype=torch.float32, device=device) / self.inv
@@ -330,9 +337,17 @@ class Pool:
             return kv.raw.kv_store_fp8_ex(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(),
                                           idx_ptr, idt, 1, w.T, w.H, w.D,
                                           1 if w.src_dtype == "bf16" else 0, strides, w.page_size,
-                                          w.page_stride, w.page_stride, w.n_slots, 0, 3, None,
-                                          None, self.ks.data_ptr(), self.vs.data_ptr(), w.H,
+                                          w.page_stride, w.page_stride, w.n_slots, 0,
+                                          3 if self.groups > 1 else 2, None, None,
+                                          self.ks.data_ptr(), self.vs.data_ptr(), self.groups,
                                           self.err.data_ptr(), stream_handle)
+        if w.notes.get("fmt") == "e5m2":
+            return kv.raw.kv_store_fp8_ex(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(),
+                                          idx_ptr, idt, 1, w.T, w.H, w.D,
+                                          1 if w.src_dtype == "bf16" else 0, strides, w.page_size,
+                                          w.page_stride, w.page_stride, w.n_slots, 1, 1,
+                                          self.inv.data_ptr(), self.inv.data_ptr() + 4, None,
+                                          None, 1, self.err.data_ptr(), stream_handle)
         if w.kind == "absmax":
             return kv.raw.kv_absmax_inv(k_ptr, v_ptr, 1 if w.src_dtype == "bf16" else 0, w.T, w.H,
                                         w.D, strides, 448.0, self.amax_inv.data_ptr(),
@@ -450,7 +465,7 @@ def oracle_batch_runner(name, w, threads, tokens=None):
     by token range when the kind allows, and the thread count it uses."""
     tokens = w.T if tokens is None else tokens
     oracle_step(name, w, 1)       # loads the oracle and its host caches in this thread
-    if threads <= 1 or w.kind not in _ORACLE_SPLITS or w.paged:
+    if threads <= 1 or w.kind not in _ORACLE_SPLITS or w.paged or "fmt" in w.notes:
         return (lambda: oracle_step(name, w, tokens)), 1
     from concurrent.futures import ThreadPoolExecutor
     threads = min(threads, tokens)
@@ -622,10 +637,15 @@ def oracle_step(name, w, tokens, t_begin=0):
                           k_off=w.k_view[0], v_off=w.v_view[0], t_begin=t_begin, t_end=tokens)
     elif w.kind == "fp8_dyn":
         ks, vs = _ORACLE_CACHE[key + "/scales"]
+        mode = w.notes.get("scale_mode", "token_head")
         oracle.store_fp8_ex(k, v, kc, vc, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
                             w.page_stride, w.page_stride, w.n_slots, fmt="e4m3fn",
-                            scale_mode="token_head", k_scales=ks, v_scales=vs,
-                            scales_slot_stride=w.H, t_end=tokens)
+                            scale_mode=mode, k_scales=ks, v_scales=vs,
+                            scales_slot_stride=w.H if mode == "token_head" else 1, t_end=tokens)
+    elif w.notes.get("fmt") == "e5m2":
+        oracle.store_fp8_ex(k, v, kc, vc, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
+                            w.page_stride, w.page_stride, w.n_slots, fmt="e5m2",
+                            scale_mode="tensor", inv_k=w.inv_k, inv_v=w.inv_v, t_end=tokens)
     else:
         oracle.store_fp8(k, v, kc, vc, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
                          w.page_stride, w.page_stride, w.n_slots, w.inv_k, w.inv_v,
@@ -636,7 +656,7 @@ def dtype_of(w):
     if w.kind == "absmax":
         return f"f32 ({w.src_dtype} in)"
     if w.kind in ("fp8", "fp8_dyn"):
-        return f"f32 ({w.src_dtype} in, e4m3fn out)"
+        return f"f32 ({w.src_dtype} in, {w.notes.get('fmt', 'e4m3fn')} out)"
     if w.kind == "gather_fp8":
         return f"f32 (e4m3fn in, {w.src_dtype} out)"
     return w.src_dtype
@@ -752,7 +772,7 @@ def kernel_source_hash(name: str) -> str:
     import hashlib
     unit = ("kv_gather.cu" if name.startswith("gather") else
             "kv_scale.cu" if name == "absmax" else
-            "kv_fp8_ex.cu" if name == "fp8_dynamic" else "kvstore.cu")
+            "kv_fp8_ex.cu" if name.startswith("fp8_dynamic") else "kvstore.cu")
     files = _COMMON_SOURCES + ("fp8_quant_gb300/csrc/" + unit,)
     h = hashlib.sha256()
     for f in files:

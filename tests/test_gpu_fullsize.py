@@ -100,6 +100,12 @@ def _oracle_compact(w):
     if w.kind == "copy":
         bad = oracle.store_copy(k, v, kc, vc, idx, st, w.H, w.D, 2, T,
                                 k_off=w.k_view[0], v_off=w.v_view[0])
+    elif w.notes.get("fmt") == "e5m2":
+        assert w.page_stride == w.page_size * sb
+        bad = oracle.store_fp8_ex(k, v, kc, vc, idx, st, w.H, w.D, w.src_dtype, w.page_size,
+                                  w.page_stride, w.page_stride, T + (-T) % w.page_size,
+                                  fmt="e5m2", scale_mode="tensor", inv_k=w.inv_k, inv_v=w.inv_v,
+                                  k_off=w.k_view[0], v_off=w.v_view[0])
     else:
         # compact slot j sits at j * slot_stride for any page size when pages are dense
         assert w.page_stride == w.page_size * sb
@@ -113,7 +119,7 @@ def _oracle_compact(w):
 
 @pytest.mark.parametrize("name,split", [
     ("tiny", 0), ("decode", 0), ("decode", 1), ("decode", 2), ("decode", 4),
-    ("prefill", 0), ("fp8", 0), ("fp8_noscale", 0), ("strided", 0), ("odd", 0),
+    ("prefill", 0), ("fp8", 0), ("fp8_noscale", 0), ("fp8_e5m2", 0), ("strided", 0), ("odd", 0),
 ])
 def test_full_size_workload(name, split):
     import torch
@@ -187,19 +193,22 @@ def test_full_size_paged_copy():
     torch.cuda.empty_cache()
 
 
-def test_full_size_dynamic_fp8():
-    """The fp8 batch with per-(token, head) scales computed in the kernel:
-    every written row and scale equals the oracle's, nothing else changed."""
+@pytest.mark.parametrize("name", ["fp8_dynamic", "fp8_dynamic_token"])
+def test_full_size_dynamic_fp8(name):
+    """The fp8 batch with scales computed in the kernel per (token, head) or
+    per token row: every written row and scale equals the oracle's, nothing
+    else changed."""
     import torch
     import bench
     import fp8_quant_gb300 as kv
     dev = torch.device("cuda", 0)
-    pool = bench.Pool("fp8_dynamic", dev, pool_bytes=0)
+    pool = bench.Pool(name, dev, pool_bytes=0)
     w = pool.w
     assert not w.paged and pool.num_batches == 1
     assert pool.call(0, torch.cuda.current_stream().cuda_stream) == 0
     assert kv.kv_error_poll(pool.err) == (kv.KVStatus.OK, 0, -1)
-    T, H, sb = w.T, w.H, w.slot_stride
+    mode = w.notes.get("scale_mode", "token_head")
+    T, H, sb = w.T, pool.groups, w.slot_stride
     idx = np.arange(T, dtype=w.indices.dtype)
     okc = np.full(T * sb, w.sentinel, np.uint8)
     ovc = okc.copy()
@@ -212,9 +221,9 @@ def test_full_size_dynamic_fp8():
     k = np.ascontiguousarray(w.k).view(np.uint8).reshape(-1)
     v = np.ascontiguousarray(w.v).view(np.uint8).reshape(-1)
     assert w.page_stride == w.page_size * sb
-    bad = oracle.store_fp8_ex(k, v, okc, ovc, idx, st, H, w.D, w.src_dtype, w.page_size,
+    bad = oracle.store_fp8_ex(k, v, okc, ovc, idx, st, w.H, w.D, w.src_dtype, w.page_size,
                               w.page_stride, w.page_stride, T + (-T) % w.page_size,
-                              fmt="e4m3fn", scale_mode="token_head", k_scales=oks,
+                              fmt="e4m3fn", scale_mode=mode, k_scales=oks,
                               v_scales=ovs, scales_slot_stride=H)
     assert bad == (0, -1)
     slots = torch.from_numpy(w.indices.astype(np.int64)).to(dev)

@@ -29,7 +29,9 @@ measured on; ``T`` tokens, ``H`` KV heads, ``D`` head dim):
 * ``paged``    the prefill batch into 4-D pages [65536, 64, 8, 128] padded by
                one slot per page (page stride 133,120 B).
 * ``fp8_dynamic`` the fp8 batch with per-(token, head) scales computed in the
-               kernel and stored per slot.
+               kernel and stored per slot (``fp8_dynamic_token``: one scale
+               per token row).
+* ``fp8_e5m2`` the fp8 batch into an e5m2 cache, per-tensor scales 57344/amax.
 
 The gather workloads read these caches back (``gather_decode``,
 ``gather_prefill``, ``gather_fp8``), and ``absmax`` reads the fp8 batch once.
@@ -179,7 +181,8 @@ class Workload:
         if self.kind == "absmax":
             return self.T * 2 * self.row_bytes + 16
         out_row = self.H * self.D * self.cache_elem
-        scales = 2 * self.H * 4 if self.kind == "fp8_dyn" else 0
+        groups = self.H if self.notes.get("scale_mode", "token_head") == "token_head" else 1
+        scales = 2 * groups * 4 if self.kind == "fp8_dyn" else 0
         return self.T * (2 * self.row_bytes + 2 * out_row + self.indices.itemsize + scales)
 
 
@@ -194,14 +197,15 @@ def _normal_rows(seed: int, T: int, H: int, D: int, dtype: str, scale: float = 1
     return to_bits(x, dtype).reshape(T, H, D)
 
 
-def _amax_inv(bits: np.ndarray, dtype: str) -> float:
-    """Per-tensor inverse scale 448/amax in fp32 (the fp8 workload's input recipe)."""
+def _amax_inv(bits: np.ndarray, dtype: str, fmax: float = 448.0) -> float:
+    """Per-tensor inverse scale fmax/amax in fp32 (the fp8 workload's input
+    recipe; fmax is 448 for e4m3fn caches, 57344 for e5m2)."""
     if dtype == "bf16":
         vals = (bits.astype(np.uint32) << 16).view(np.float32)
     else:
         vals = bits.view(np.float16).astype(np.float32)
     amax = np.float32(np.max(np.abs(vals)))
-    return float(np.float32(448.0) / amax)
+    return float(np.float32(fmax) / amax)
 
 
 def make_copy(name, T, H, D, n_slots, seed, dtype="bf16", index_dtype=np.int32,
@@ -312,6 +316,26 @@ def fp8_dynamic(n_slots: int = 1 << 20) -> Workload:
     return w
 
 
+def fp8_dynamic_token(n_slots: int = 1 << 20) -> Workload:
+    """As ``fp8_dynamic`` with one scale per token row (amax over all 1024
+    elements of the K or V row)."""
+    w = fp8_dynamic(n_slots=n_slots)
+    w.name = "fp8_dynamic_token"
+    w.notes["scale_mode"] = "token"
+    return w
+
+
+def fp8_e5m2(n_slots: int = 1 << 20) -> Workload:
+    """The ``fp8`` batch into an e5m2 cache with per-tensor inverse scales
+    57344/amax (kv_store_fp8_ex)."""
+    w = fp8(n_slots=n_slots)
+    w.name = "fp8_e5m2"
+    w.notes["fmt"] = "e5m2"
+    w.inv_k = _amax_inv(w.k, w.src_dtype, 57344.0)
+    w.inv_v = _amax_inv(w.v, w.src_dtype, 57344.0)
+    return w
+
+
 def odd(n_slots: int = 1 << 21) -> Workload:
     """fp16 H=1, D=576 rows (1152 B) into 1280-byte slots."""
     return make_copy("odd", T=65536, H=1, D=576, n_slots=n_slots, seed=0x5EED0005,
@@ -356,6 +380,8 @@ WORKLOADS = {
     "odd": odd,
     "paged": paged,
     "fp8_dynamic": fp8_dynamic,
+    "fp8_dynamic_token": fp8_dynamic_token,
+    "fp8_e5m2": fp8_e5m2,
     "gather_decode": gather_decode,
     "gather_prefill": gather_prefill,
     "gather_fp8": gather_fp8,
