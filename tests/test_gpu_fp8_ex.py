@@ -30,17 +30,20 @@ def _lib():
     yield
 
 
-def run_store(p, fmt, mode, sstride=None):
-    """kv_store_fp8_ex on the GPU and the oracle; compare caches, scales, errors."""
+def run_store(p, fmt, mode, sstride=None, host=False):
+    """kv_store_fp8_ex on the GPU and the oracle; compare caches, scales, errors.
+    host: K, V and the slot ids in pinned host memory, read in place."""
     import torch
     import fp8_quant_gb300 as kv
     dev = torch.device("cuda")
     G = p.H if mode == "token_head" else 1
     sstride = sstride or G
     n = p.size_limit
-    k = torch.from_numpy(p.k_src).to(dev)
-    v = torch.from_numpy(p.v_src).to(dev)
-    idx = torch.from_numpy(p.indices).to(dev)
+    put = (lambda a: torch.from_numpy(a).pin_memory()) if host else (
+        lambda a: torch.from_numpy(a).to(dev))
+    k = put(p.k_src)
+    v = put(p.v_src)
+    idx = put(p.indices)
     kc = torch.from_numpy(filled(p.cache_bytes, SENT8)).to(dev)
     vc = kc.clone()
     ks = torch.full((n * sstride,), -1.0, dtype=torch.float32, device=dev)
@@ -107,6 +110,15 @@ def test_store_fp8_ex_dynamic_oob_and_scale_stride(mode):
     p = fp8_problem(T=300, H=4, D=64, n_slots=1000, seed=71, page_size=8)
     p.indices[[2, 150]] = [-1, 1000]
     run_store(p, "e4m3fn", mode, sstride=p.H + 3)
+
+
+@pytest.mark.parametrize("mode", ["tensor", "token", "token_head"])
+@pytest.mark.parametrize("tokens", [300, 3000])
+def test_store_fp8_ex_pinned_host_inputs(mode, tokens):
+    """K, V and the slot ids in pinned host memory (no L2 prefetch of host
+    memory), one side per warp and paired."""
+    p = fp8_problem(T=tokens, H=8, D=128, n_slots=8192, seed=79, page_size=16)
+    run_store(p, "e4m3fn", mode, host=True)
 
 
 @pytest.mark.parametrize("fmt", sorted(FMTS))
