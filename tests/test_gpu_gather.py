@@ -91,8 +91,9 @@ def make(kind, T, H, D, n, seed, elem=2, idx_dtype=np.int64, index_stride=1, slo
 SENT = bytes([0xC0, 0x7F])
 
 
-def run_both(g: G, host_out=False):
-    """host_out: the gathered rows are written straight into pinned host memory."""
+def run_both(g: G, host_out=False, host_idx=False):
+    """host_out: the gathered rows are written straight into pinned host memory;
+    host_idx: the slot ids are read from pinned host memory."""
     import torch
     import fp8_quant_gb300 as kv
     dev = torch.device("cuda")
@@ -105,7 +106,7 @@ def run_both(g: G, host_out=False):
     else:
         ko = torch.from_numpy(filled).to(dev)
         vo = ko.clone()
-    idx = torch.from_numpy(g.idx).to(dev)
+    idx = torch.from_numpy(g.idx).pin_memory() if host_idx else torch.from_numpy(g.idx).to(dev)
     err = torch.zeros(2, dtype=torch.int64, device=dev)
     sc = torch.tensor([g.scale, g.scale], dtype=torch.float32, device=dev)
     s = torch.cuda.current_stream().cuda_stream
@@ -277,3 +278,16 @@ def test_gather_into_pinned_host_memory(kind):
         g = make("fp8", T=900, H=8, D=128, n=4096, seed=802, page_size=16, page_pad=64,
                  scale=0.05)
     run_both(g, host_out=True)
+
+
+@pytest.mark.parametrize("kind", ["copy", "fp8"])
+@pytest.mark.parametrize("tokens", [300, 3000])
+def test_gather_offload_from_pinned_slots(kind, tokens):
+    """Slot ids read from pinned host memory and rows written into pinned host
+    memory (the zero-copy offload), one side per warp and paired."""
+    if kind == "copy":
+        g = make("copy", T=tokens, H=8, D=128, n=8192, seed=803, bad=((1, -1),))
+    else:
+        g = make("fp8", T=tokens, H=8, D=128, n=8192, seed=804, page_size=16, scale=0.1,
+                 bad=((2, 8192),))
+    run_both(g, host_out=True, host_idx=True)
