@@ -1,14 +1,15 @@
 """GB300 KV-cache write path: Python binding of ``libkvstore.so``.
 
-The library (``csrc/kvstore.cu``, C ABI in ``include/kvstore.h``) does all the
-work; this module only marshals arguments. It exposes the C entry points under
+The library (the kernels in ``csrc/*.cu``, C ABI in ``include/kvstore.h``) does
+all the work; this module only marshals arguments. It exposes the C entry points under
 the same names:
 
 * :func:`kv_store`      -- plain byte-exact scatter of K/V rows into cache slots
   (sglang ``kvcache.cuh``, ``store_kvcache``).
 * :func:`kv_store_fp8`  -- fused fp32 scale + FP8 e4m3fn conversion + paged
   scatter (sglang ``trtllm_fp8_kv_kernel.py``, ``fused_fp8_set_kv_buffer``).
-* :func:`kv_store_paged`, :func:`kv_store_fp8_ex` (e5m2, per-token scales),
+* :func:`kv_store_paged`, :func:`kv_store_fp8_ex` (e5m2; scales per tensor, or
+  per token row / per (token, head) computed in the kernel),
   :func:`kv_gather`, :func:`kv_gather_fp8` (the inverse), :func:`kv_inv_scale`,
   :func:`kv_absmax_inv` (scale preparation).
 * :func:`kv_error_poll`, :func:`kv_error_reset`, :func:`kv_status_str`.
