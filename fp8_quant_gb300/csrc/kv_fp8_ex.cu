@@ -10,8 +10,8 @@
 // scale cache.  fmax is 448 for e4m3fn and 57344 for e5m2.
 //
 // One warp owns one group.  The group's elements are loaded once into
-// registers (up to 4 chunks per lane; longer groups are re-read from L2 in a
-// second pass), the warp reduces amax with shuffles, then converts and stores
+// registers (up to 4 chunks per lane, 2 for 16-byte chunks; longer groups
+// are re-read from L2 in a second pass), the warp reduces amax with shuffles, then converts and stores
 // the codes and lane 0 stores the group's scale.  As in the other write
 // kernels, the group's source bytes are prefetched into L2 before the
 // programmatic-launch wait.
@@ -91,7 +91,7 @@ __device__ __forceinline__ Chunk<CH> chunk_quant(const Chunk<2 * CH>& c, float i
 
 template <int CH, typename IdxT, bool kBF16, int FMT>
 __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_rows(const __grid_constant__ DynParams p) {
-  constexpr int kMaxJ = 4;  // chunks per lane held in registers
+  constexpr int kMaxJ = CH >= 8 ? 2 : 4;  // chunks per lane held in registers (16-byte chunks: 2, no spill)
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
   uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + (threadIdx.x >> 5);

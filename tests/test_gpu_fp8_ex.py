@@ -86,6 +86,8 @@ CASES = {
     "rows_1024": dict(T=700, H=8, D=128, n_slots=2048, page_size=32),
     "pages_padded": dict(T=500, H=8, D=128, n_slots=2048, page_size=16, page_pad=256),
     "segmented_heads": dict(T=400, H=8, D=64, n_slots=1024, head_pad_src=64, head_pad_dst=32),
+    "segmented_long_heads": dict(T=300, H=8, D=128, n_slots=1024, head_pad_src=64,
+                                 head_pad_dst=32),
     "two_pass_2048": dict(T=200, H=16, D=128, n_slots=512),
     "odd_d_narrow": dict(T=300, H=3, D=45, n_slots=1024, src_dtype="f16"),
     "d24_i32": dict(T=300, H=2, D=24, n_slots=1024, idx_dtype=np.int32, index_stride=2),
