@@ -3,8 +3,10 @@
  * It allocates device memory with the CUDA runtime, writes a small batch
  * with kv_store and kv_store_fp8, reads the caches back and checks them
  * against the definitions (copy: the row lands at its slot byte for byte;
- * FP8: a few values with known e4m3fn codes), and checks that an
- * out-of-range slot is reported by kv_error_poll and not written.
+ * FP8: a few values with known e4m3fn codes), checks that an out-of-range
+ * slot is reported by kv_error_poll and not written, gathers the copied
+ * rows back with kv_gather, and writes one row with a per-token scale
+ * computed in the kernel (kv_store_fp8_ex), checking the scale and codes.
  * Exit status 0 on success.
  */
 #include <stdint.h>
@@ -105,6 +107,63 @@ int main(void)
         for (int e = 0; e < H * D; ++e)
             if (q[ok_slots[t] * H * D + e] != want[(t * H * D + e) % 5])
                 return fail("fp8 code differs");
+
+    /* kv_gather: the rows of the in-range tokens come back byte for byte */
+    uint16_t *dout;
+    if (cudaMalloc((void **)&dout, 2 * sizeof k))
+        return fail("cudaMalloc gather");
+    cudaMemcpy(didx, slots, sizeof slots, cudaMemcpyHostToDevice);
+    cudaMemset(dout, 0, 2 * sizeof k);
+    st = kv_gather(dkc, dvc, dout, dout + T * H * D, didx, KV_INDEX_I64, 1, T, H, D, 2, &s,
+                   SLOTS, (kv_error_record *)derr, NULL);
+    if (st != KV_OK)
+        return fail(kv_status_str(st));
+    if (kv_error_poll((kv_error_record *)derr, NULL, &nbad, &first) != KV_ERR_INDEX_OOB ||
+        nbad != 1 || first != 2)
+        return fail("gather: out-of-range slot not reported");
+    uint16_t back[2 * T * H * D];
+    cudaMemcpy(back, dout, sizeof back, cudaMemcpyDeviceToHost);
+    for (int t = 0; t < T; ++t) {
+        if (t == 2)
+            continue;
+        if (memcmp(back + t * H * D, k + t * H * D, row) ||
+            memcmp(back + T * H * D + t * H * D, v + t * H * D, row))
+            return fail("gathered row differs");
+    }
+
+    /* kv_store_fp8_ex, one scale per token row: a row of 2.0 and -1.0 has
+       amax 2, inv = 448/2 = 224, scale = 2/448, codes 0x7E and 0xF6 */
+    uint16_t kd[T * H * D];
+    for (int i = 0; i < T * H * D; ++i)
+        kd[i] = (i % 2) ? 0xBF80 : 0x4000;          /* bf16 -1.0, 2.0 */
+    cudaMemcpy(dk, kd, sizeof kd, cudaMemcpyHostToDevice);
+    cudaMemcpy(didx, ok_slots, sizeof ok_slots, cudaMemcpyHostToDevice);
+    float *dsc;
+    if (cudaMalloc((void **)&dsc, 2 * SLOTS * sizeof(float)))
+        return fail("cudaMalloc scales");
+    cudaMemset(dq, 0x7F, 2 * SLOTS * H * D);
+    st = kv_store_fp8_ex(dk, dk, dq, dq + SLOTS * H * D, didx, KV_INDEX_I64, 1, T, H, D,
+                         KV_SRC_BF16, &s8, 4, 4 * H * D, 4 * H * D, SLOTS, KV_FP8_E4M3FN,
+                         KV_SCALE_TOKEN, NULL, NULL, dsc, dsc + SLOTS, 1,
+                         (kv_error_record *)derr, NULL);
+    if (st != KV_OK)
+        return fail(kv_status_str(st));
+    if (kv_error_poll((kv_error_record *)derr, NULL, NULL, NULL) != KV_OK)
+        return fail("fp8_ex: unexpected error report");
+    float sc[2 * SLOTS];
+    cudaMemcpy(q, dq, sizeof q, cudaMemcpyDeviceToHost);
+    cudaMemcpy(sc, dsc, sizeof sc, cudaMemcpyDeviceToHost);
+    const float want_scale = 2.0f / 448.0f;
+    for (int t = 0; t < T; ++t) {
+        if (sc[ok_slots[t]] != want_scale || sc[SLOTS + ok_slots[t]] != want_scale)
+            return fail("fp8_ex: per-token scale differs");
+        for (int e = 0; e < H * D; ++e)
+            if (q[ok_slots[t] * H * D + e] != ((e % 2) ? 0xF6 : 0x7E))
+                return fail("fp8_ex code differs");
+    }
+    cudaFree(dout);
+    cudaFree(dsc);
+
     if (kv_abi_version() != KV_ABI_VERSION)
         return fail("ABI version");
     cudaFree(dk); cudaFree(dv); cudaFree(dkc); cudaFree(dvc); cudaFree(didx); cudaFree(derr);
