@@ -3,34 +3,41 @@
 
 One step = one call of the write path over one batch of the workload (the
 batch's K rows and V rows scattered into the caches at its slot indices).
-Default workload: the decode batch (T=256 tokens, 8 KV heads, head_dim 128,
-bf16, int64 slots into a 1,048,576-slot cache). Other workloads with
-``--workload``: tiny, prefill, fp8, fp8_noscale, strided, odd.
+Default workload (the headline): the strided copy, the largest single-GPU
+configuration -- fp16 K and V as column views of a fused QKV tensor
+[65536, 6144] (token stride 12,288 B), int32 slots into a 2,097,152-slot
+cache, 537 MB moved per call.  Other workloads with ``--workload``.
 
 Protocol (``--impl ours``):
   * inputs already in HBM; every step uses the next batch of a pool of
     distinct batches (K/V rows and slot sets) whose total size exceeds 4x the
-    L2 cache, so consecutive steps never hit L2 for their inputs;
-  * the steps run back to back from CUDA graphs of recorded calls (calls
-    are launch-bound at decode size, so the graph removes host overhead but
-    not the per-kernel device cost);
-  * W warm-up steps, then exactly K timed steps bracketed by barrier +
-    synchronise, CUDA events on the launching stream, max over ranks;
+    L2 cache, or one batch larger than twice the L2, so consecutive steps
+    never hit L2 for their inputs;
+  * the steps run back to back from CUDA graphs of recorded calls;
+  * W warm-up steps and one untimed replay that uploads the timed graphs,
+    then exactly K timed steps bracketed by barrier + synchronise; a short
+    device-side delay before the opening CUDA event keeps the host's
+    submission out of the bracket; events on the launching stream; max over
+    ranks;
   * clocks sampled with nvidia-smi during the timed region;
-  * ``e2e``: the same steps with each step's inputs copied host->device from
-    pinned memory and the error record read back device->host, all inside
-    the timed region;
-  * ``cpu_baseline``: the CPU oracle, single thread, on a bounded sample of
-    the same workload (rank 0, N=1 only).
+  * ``per_config``: every configuration (and, with ``--suite all``, the
+    further rows) timed the same way, with the command's K and W, plus the
+    same calls over a region of at least ``--long-ms``;
+  * ``e2e``: the same steps with each step's inputs coming from pinned host
+    memory and the step's status read back into host memory, inside the
+    timed region;
+  * ``cpu_baseline``: the CPU oracle on a bounded sample of the same
+    workload, on one thread and on all host threads (rank 0, N=1 only).
 
 ``--impl reference`` times the CPU oracle as the reference arm on the same
-metric and prints its own JSON line.
+metric and configuration and prints its own JSON line.
 """
 
 from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -403,12 +410,21 @@ def run_graphs(graphs):
             g.replay()
 
 
+# Device-side delay enqueued before the opening event of a timed region, in
+# GPU clock cycles (about 0.1 ms): the host submits the region's work while
+# the GPU is still busy with it, so the events bracket device time only and
+# not the host's submission latency.
+_HOLD_CYCLES = 200_000
+
+
 def time_region(torch, dist, fn, device):
+    """Device time of fn()'s work on the current stream, in ms (max over ranks)."""
     dist.barrier()
     torch.cuda.synchronize()
     st = torch.cuda.current_stream()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(_HOLD_CYCLES)
     e0.record(st)
     fn()
     e1.record(st)
@@ -416,6 +432,43 @@ def time_region(torch, dist, fn, device):
     dist.barrier()
     ms = e0.elapsed_time(e1)
     return dist.max(ms, device=device)
+
+
+def measure_calls(torch, dist, device, step, steps, warmup, chunk, long_ms=0.0):
+    """Per-call device time of `step` (one call of the path) run back to back
+    from CUDA graphs: `warmup` untimed calls, one untimed replay that uploads
+    the timed graphs, then exactly `steps` timed calls.  With long_ms > 0 the
+    same calls are also timed over a region of at least long_ms (graphs of up
+    to `chunk` calls replayed), which resolves calls of a microsecond or two
+    better than a short region can."""
+    graphs = capture_graphs(torch, step, steps, min(steps, chunk))
+    warm = capture_graphs(torch, step, warmup, min(warmup, chunk))
+    run_graphs(warm)
+    run_graphs(graphs)
+    torch.cuda.synchronize()
+    del warm
+    ms = time_region(torch, dist, lambda: run_graphs(graphs), device)
+    out = {"us_per_call": ms * 1e3 / steps, "calls": steps}
+    del graphs
+    if long_ms > 0:
+        per_ms = max(ms / steps, 1e-6)
+        want = max(steps, int(math.ceil(long_ms / per_ms)))
+        size = min(want, chunk)
+        reps = -(-want // size)
+        lg = capture_graphs(torch, step, size, size)
+        run_graphs(lg)
+        torch.cuda.synchronize()
+        g = lg[0][0]
+
+        def replay():
+            for _ in range(reps):
+                g.replay()
+
+        ms_l = time_region(torch, dist, replay, device)
+        out["us_per_call_long"] = ms_l * 1e3 / (reps * size)
+        out["calls_long"] = reps * size
+        del lg
+    return out
 
 
 def single_call_cold_us(torch, pool, stream_handle, reps=30):
@@ -429,7 +482,7 @@ def single_call_cold_us(torch, pool, stream_handle, reps=30):
     st = torch.cuda.current_stream()
     for r in range(reps):
         flush.fill_(float(r))
-        torch.cuda._sleep(200_000)          # ~0.1 ms of GPU clock cycles
+        torch.cuda._sleep(_HOLD_CYCLES)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(st)
@@ -446,12 +499,6 @@ def single_call_cold_us(torch, pool, stream_handle, reps=30):
 # CPU oracle timing
 # ---------------------------------------------------------------------------
 
-# Workload kinds whose oracle call takes a token range, so that host threads
-# can split a batch (ctypes releases the GIL during the call); the padded-page
-# copy has no token-range form and runs on one thread.
-_ORACLE_SPLITS = ("copy", "fp8")
-
-
 def host_threads() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -459,74 +506,80 @@ def host_threads() -> int:
         return os.cpu_count() or 1
 
 
-def oracle_batch_runner(name, w, threads, tokens=None):
-    """fn() that pushes the first `tokens` tokens of the workload's batch
-    (default: all) through the CPU oracle, split over `threads` host threads
-    by token range when the kind allows, and the thread count it uses."""
-    tokens = w.T if tokens is None else tokens
-    oracle_step(name, w, 1)       # loads the oracle and its host caches in this thread
-    if threads <= 1 or w.kind not in _ORACLE_SPLITS or w.paged or "fmt" in w.notes:
-        return (lambda: oracle_step(name, w, tokens)), 1
-    from concurrent.futures import ThreadPoolExecutor
-    threads = min(threads, tokens)
-    cuts = [tokens * i // threads for i in range(threads + 1)]
-    ranges = list(zip(cuts[:-1], cuts[1:]))
-    ex = ThreadPoolExecutor(threads)
-    return (lambda: list(ex.map(lambda r: oracle_step(name, w, r[1], t_begin=r[0]), ranges))), threads
+_ORACLE_CACHE = {}
+
+
+def oracle_buffers(name, w):
+    """Host caches (full size; only written pages are ever touched), the
+    source rows and the strides of workload `name` for the CPU oracle."""
+    import oracle
+    if name not in _ORACLE_CACHE:
+        cache_bytes = 1 if w.kind == "absmax" else w.cache_bytes
+        if w.kind == "fp8_dyn":
+            _ORACLE_CACHE[name + "/scales"] = (np.empty(w.n_slots * w.H, dtype=np.float32),
+                                               np.empty(w.n_slots * w.H, dtype=np.float32))
+        k = np.ascontiguousarray(w.k).view(np.uint8).reshape(-1).copy()
+        v = k if w.notes.get("shared_source") else \
+            np.ascontiguousarray(w.v).view(np.uint8).reshape(-1).copy()
+        _ORACLE_CACHE[name] = (np.empty(cache_bytes, dtype=np.uint8),
+                               np.empty(cache_bytes, dtype=np.uint8), k, v,
+                               oracle.Strides(k_token=w.k_view[1], k_head=w.k_view[2],
+                                              k_dim=w.k_view[3], v_token=w.v_view[1],
+                                              v_head=w.v_view[2], v_dim=w.v_view[3],
+                                              kc_slot=w.slot_stride, kc_head=w.cache_head_stride,
+                                              kc_dim=w.cache_elem, vc_slot=w.slot_stride,
+                                              vc_head=w.cache_head_stride, vc_dim=w.cache_elem))
+    return _ORACLE_CACHE[name]
+
+
+def oracle_job(name, w):
+    """The oracle's write loop for workload `name` as a job that runs on POSIX
+    threads over token ranges (kinds whose oracle call takes a token range:
+    the flat and paged copies and the per-tensor FP8 write), else None."""
+    import oracle
+    if w.kind not in ("copy", "fp8") or "fmt" in w.notes:
+        return None
+    kc, vc, k, v, st = oracle_buffers(name, w)
+    if w.kind == "copy":
+        return oracle.ThreadedJob("copy_paged" if w.paged else "copy", k, v, kc, vc, w.indices,
+                                  st, w.H, w.D, w.n_slots, elem_bytes=2, page_size=w.page_size,
+                                  kc_page_stride=w.page_stride, vc_page_stride=w.page_stride,
+                                  k_off=w.k_view[0], v_off=w.v_view[0])
+    return oracle.ThreadedJob("fp8", k, v, kc, vc, w.indices, st, w.H, w.D, w.n_slots,
+                              src_dtype=w.src_dtype, page_size=w.page_size,
+                              kc_page_stride=w.page_stride, vc_page_stride=w.page_stride,
+                              inv_k=w.inv_k, inv_v=w.inv_v, use_scale=w.use_scale,
+                              k_off=w.k_view[0], v_off=w.v_view[0])
 
 
 def oracle_tokens_per_s(name: str, seconds: float, threads: int = 1):
     """Time the CPU oracle (as it stands) on a bounded sample of the workload:
-    its whole batch, repeated until `seconds` elapse (at least three times),
-    on `threads` host threads (token ranges) where the kind allows.
-    Returns (tokens/s, description of the sample, threads used)."""
+    its batch, repeated for about `seconds`.  Kinds with a token-range oracle
+    call run on `threads` POSIX threads, thread i repeating its own token
+    range of the batch (no interpreter lock, no hand-off between threads);
+    the others run on one thread.  Returns (tokens/s, sample, threads used)."""
     w = load_workload(name)
-    run, used = oracle_batch_runner(name, w, threads)
-    run()                                       # first touch of the written pages
-    if used == 1:
-        n = 0
-        t0 = time.perf_counter()
-        while True:
-            run()
-            n += 1
-            el = time.perf_counter() - t0
-            if el >= seconds and n >= 3:
-                break
-        sample = (f"{n} repetitions of the workload's batch of {w.T} tokens "
-                  f"({el:.1f} s, one thread, full-size host caches)")
-        return n * w.T / el, sample, 1
-    # each thread repeats its own token range until the deadline (no per-batch
-    # hand-off between threads); throughput = all tokens / the longest thread
-    import threading
-    cuts = [w.T * i // used for i in range(used + 1)]
-    counts = [0] * used
-    ends = [0.0] * used
-    start = threading.Barrier(used + 1)
-    t0 = [0.0]
-
-    def worker(i):
-        start.wait()
-        deadline = t0[0] + seconds
-        while True:
-            oracle_step(name, w, cuts[i + 1], t_begin=cuts[i])
-            counts[i] += 1
-            now = time.perf_counter()
-            if now >= deadline and counts[i] >= 3:
-                ends[i] = now
-                return
-
-    ts = [threading.Thread(target=worker, args=(i,)) for i in range(used)]
-    for t in ts:
-        t.start()
-    t0[0] = time.perf_counter()
-    start.wait()
-    for t in ts:
-        t.join()
-    el = max(ends) - t0[0]
-    tokens = sum(c * (cuts[i + 1] - cuts[i]) for i, c in enumerate(counts))
-    sample = (f"{tokens} tokens of the workload's batch of {w.T} ({el:.1f} s, {used} threads, "
-              f"each repeating its own token range, full-size host caches)")
-    return tokens / el, sample, used
+    job = oracle_job(name, w)
+    if job is not None:
+        used = max(1, min(threads, w.T))
+        job.run(used)                        # first touch of the written pages
+        done, el, _ = job.run(used, seconds, 3)
+        sample = (f"{done} tokens: {used} POSIX thread{'s' if used > 1 else ''}, each "
+                  f"repeating its own token range of the workload's batch of {w.T} tokens for "
+                  f"{el:.1f} s (full-size host caches)")
+        return done / el, sample, used
+    oracle_step(name, w, w.T)                # loads the oracle and touches the written pages
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle_step(name, w, w.T)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds and n >= 3:
+            break
+    sample = (f"{n} repetitions of the workload's batch of {w.T} tokens ({el:.1f} s, one "
+              f"thread, full-size host caches)")
+    return n * w.T / el, sample, 1
 
 
 def cpu_model():
@@ -540,48 +593,91 @@ def cpu_model():
     return "unknown"
 
 
+def pool_batches(w, pool_bytes: int) -> int:
+    """Distinct input batches a Pool of `pool_bytes` rotates through (one when
+    a single batch already exceeds twice the L2)."""
+    shared = bool(w.notes.get("shared_source"))
+    src_batch_bytes = w.k.nbytes if shared else 2 * w.k.nbytes
+    if src_batch_bytes >= 2 * L2_BYTES:
+        return 1
+    return max(1, min(256, -(-pool_bytes // max(1, src_batch_bytes))))
+
+
+def line_config(name, w, world, pool_bytes, slots=None):
+    """The `config` object of the JSON line: what the workload is, identical
+    for both arms."""
+    nb = pool_batches(w, pool_bytes)
+    in_bytes = 2 * w.row_bytes * w.T + w.indices.itemsize * w.T
+    return {
+        "workload": DESCRIPTIONS[name] + ("" if slots is None
+                                          else f" [cache reduced to {slots} slots]"),
+        "tokens_per_step": w.T,
+        "bytes_per_step": w.algorithmic_bytes(),
+        "parallelism": f"replicas x{world}",
+        "l2": (f"inputs rotate over {nb} batches ({nb * in_bytes / 1e6:.0f} MB read per cycle) "
+               + ("> L2 (129 MB)" if nb * in_bytes > L2_BYTES else
+                  "< L2 (129 MB): L2-resident, parity-only size")
+               if nb > 1 else
+               f"one batch: {in_bytes / 1e6:.0f} MB read and {(w.algorithmic_bytes() - in_bytes) / 1e6:.0f}"
+               f" MB written per step, each larger than L2 (129 MB)"),
+    }
+
+
 # ---------------------------------------------------------------------------
 # Arms
 # ---------------------------------------------------------------------------
 
 def run_reference(args, dist):
-    """The CPU oracle as the reference arm (rank 0 only)."""
+    """The CPU oracle as the reference arm (rank 0 only): each step writes the
+    workload's batch (or, if that would not fit the time budget, its first
+    tokens) through the oracle on all host threads."""
     if dist.rank != 0:
         return
     name = args.workload
     w = load_workload(name)
-    # calibrate on one whole batch (after a first pass that touches the pages),
-    # then size each step's sample so that the whole run takes about two minutes
-    run, used = oracle_batch_runner(name, w, host_threads())
-    run()
-    t0 = time.perf_counter()
-    run()
-    rate = w.T / (time.perf_counter() - t0)
-    per_step_s = 120.0 / max(1, args.steps + args.warmup)
+    threads = host_threads()
+    job = oracle_job(name, w)
+    if job is not None:
+        used = max(1, min(threads, w.T))
+        job.run(used)                                # first touch
+        t0 = time.perf_counter()
+        job.run(used)
+        rate = w.T / (time.perf_counter() - t0)
+        run = lambda n: job.run(used, 0.0, 1, num_tokens=n)
+    else:
+        used = 1
+        oracle_step(name, w, w.T)
+        t0 = time.perf_counter()
+        oracle_step(name, w, w.T)
+        rate = w.T / (time.perf_counter() - t0)
+        run = lambda n: oracle_step(name, w, n)
+    per_step_s = 150.0 / max(1, args.steps + args.warmup)
     tokens = max(1, min(w.T, int(rate * per_step_s)))
-    if tokens < w.T:
-        run, used = oracle_batch_runner(name, w, host_threads(), tokens)
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        run()
+        run(tokens)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     total = sum(times)
     value = args.steps * tokens / total
+    config = line_config(name, w, args.gpus, args.pool_mb << 20)
+    if tokens < w.T:
+        config["tokens_per_step"] = tokens
+        config["bytes_per_step"] = w.algorithmic_bytes() * tokens // w.T
+    how = ("one thread" if used == 1 else
+           f"{used} POSIX threads, one token range each")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype_of(w), "data": "synthetic",
-        "config": {"workload": DESCRIPTIONS[name], "tokens_per_step": tokens,
-                   "achieved_gbs": value * w.algorithmic_bytes() / w.T / 1e9},
+        "config": config,
+        "achieved_gbs": value * w.algorithmic_bytes() / w.T / 1e9,
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
-                         "sample": f"each step: the first {tokens} of the workload's {w.T} "
-                                   f"tokens through the CPU oracle, "
-                                   + ("one thread" if used == 1 else
-                                      f"{used} threads, one token range each")
-                                   + f" ({cpu_model()})"},
+                         "sample": f"each step: {'the' if tokens == w.T else 'the first'} "
+                                   f"{tokens} of the workload's {w.T} tokens through the CPU "
+                                   f"oracle, {how} ({cpu_model()})"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -596,29 +692,12 @@ def load_workload(name, n_slots=None):
     return wl.WORKLOADS[name](**kw)
 
 
-_ORACLE_CACHE = {}
-
-
 def oracle_step(name, w, tokens, t_begin=0):
-    """Tokens [t_begin, tokens) of the workload through the CPU oracle
-    (t_begin > 0 only for the kinds in _ORACLE_SPLITS)."""
+    """Tokens [t_begin, tokens) of the workload through the CPU oracle, from
+    this thread."""
     import oracle
     key = name
-    if key not in _ORACLE_CACHE:
-        cache_bytes = 1 if w.kind == "absmax" else w.cache_bytes
-        if w.kind == "fp8_dyn":
-            _ORACLE_CACHE[key + "/scales"] = (np.empty(w.n_slots * w.H, dtype=np.float32),
-                                              np.empty(w.n_slots * w.H, dtype=np.float32))
-        _ORACLE_CACHE[key] = (np.empty(cache_bytes, dtype=np.uint8),
-                              np.empty(cache_bytes, dtype=np.uint8),
-                              np.ascontiguousarray(w.k).view(np.uint8).reshape(-1).copy(),
-                              np.ascontiguousarray(w.v).view(np.uint8).reshape(-1).copy(),
-                              oracle.Strides(k_token=w.k_view[1], k_head=w.k_view[2],
-                                             k_dim=w.k_view[3], v_token=w.v_view[1],
-                                             v_head=w.v_view[2], v_dim=w.v_view[3],
-                                             kc_slot=w.slot_stride, kc_head=w.cache_head_stride,
-                                             kc_dim=w.cache_elem, vc_slot=w.slot_stride,
-                                             vc_head=w.cache_head_stride, vc_dim=w.cache_elem))
+    oracle_buffers(name, w)
     kc, vc, k, v, st = _ORACLE_CACHE[key]
     if w.kind == "absmax":
         oracle.absmax_inv(k, v, st, tokens, w.H, w.D, w.src_dtype)
@@ -662,6 +741,112 @@ def dtype_of(w):
     return w.src_dtype
 
 
+# The configurations the write path is measured on (decode with its row
+# splits, prefill, the fused FP8 write with and without the scale, the
+# strided QKV views, the odd row size), then the further rows: paged pages,
+# e5m2, dynamic scales, the gathers and the per-tensor scale pass.
+SUITE_CONFIGS = ("decode", "prefill", "fp8", "fp8_noscale", "strided", "odd")
+SUITE_MORE = ("paged", "fp8_e5m2", "fp8_dynamic", "fp8_dynamic_token", "gather_decode",
+              "gather_prefill", "gather_fp8", "absmax")
+HEADLINE = "strided"
+
+
+def pool_step(kv, pool):
+    """step(i): one call of the path on batch i (mod the pool's batches)."""
+    import torch
+
+    def step(i):
+        rc = pool.call(i % pool.num_batches, torch.cuda.current_stream().cuda_stream)
+        if rc != 0:
+            raise RuntimeError(f"launch failed: {kv.kv_status_str(rc)}")
+    return step
+
+
+def fractions(entry, bytes_per_call, tokens, peak):
+    """GB/s, tokens/s and roofline fraction of an entry's per-call times."""
+    for key, tag in (("us_per_call", ""), ("us_per_call_long", "_long")):
+        if key in entry:
+            us = entry[key]
+            entry["gbs" + tag] = bytes_per_call / (us * 1e-6) / 1e9
+            entry["frac" + tag] = entry["gbs" + tag] / peak
+            entry["tokens_per_s" + tag] = tokens / (us * 1e-6)
+    return entry
+
+
+def suite_entry(args, dist, torch, kv, device, name, peak, pool=None):
+    """Per-call time of workload `name` in the headline's protocol: the
+    command's steps and warm-up (else the workload's defaults), plus a long
+    region of at least --long-ms; decode adds its row splits and the
+    launch floor."""
+    own = pool is None
+    if own:
+        pool = Pool(name, device, pool_bytes=args.pool_mb << 20, seed=1234 + dist.rank)
+    steps = args.steps if args.steps_given else DEFAULT_STEPS[name]
+    warm = args.warmup if args.warmup_given else max(3, steps // 20)
+    w = pool.w
+    e = measure_calls(torch, dist, device, pool_step(kv, pool), steps, warm, args.graph_chunk,
+                      args.long_ms)
+    e["launches_per_call"] = pool.launches_per_call
+    fractions(e, pool.algorithmic_bytes(), w.T, peak)
+    if name == "decode":
+        e["by_num_split"] = {}
+        saved = w.num_split
+        try:
+            for split in (1, 2, 4):
+                if split > 1 and w.row_bytes % (split * 128):
+                    continue
+                w.num_split = split
+                sub = measure_calls(torch, dist, device, pool_step(kv, pool), steps, warm,
+                                    args.graph_chunk, args.long_ms)
+                e["by_num_split"][str(split)] = fractions(sub, pool.algorithmic_bytes(), w.T,
+                                                          peak)
+        finally:
+            w.num_split = saved
+        # an empty kernel with the decode launch's shape and hand-over: the
+        # per-launch floor under a decode call
+        warps = floor_warps(pool)
+
+        def floor_step(i):
+            rc = kv.raw.kv_launch_floor(warps, torch.cuda.current_stream().cuda_stream)
+            if rc != 0:
+                raise RuntimeError(kv.kv_status_str(rc))
+
+        f = measure_calls(torch, dist, device, floor_step, steps, warm, args.graph_chunk,
+                          args.long_ms)
+        f["warps"] = warps
+        e["launch_floor"] = f
+    e["single_call_cold_us"] = single_call_cold_us(torch, pool,
+                                                   torch.cuda.current_stream().cuda_stream)
+    st, nbad, _ = kv.kv_error_poll(pool.err)
+    if st != kv.KVStatus.OK:
+        raise RuntimeError(f"{nbad} out-of-range slots in the benchmark data")
+    if own:
+        del pool
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return e
+
+
+def floor_warps(pool):
+    """Warps of work in one call of the pool's copy workload (its launch shape)."""
+    w = pool.w
+    parts = w.num_split
+    if parts == 0:      # the automatic split of the library for these row sizes
+        sms = 152
+        try:
+            import torch
+            sms = torch.cuda.get_device_properties(pool.dev).multi_processor_count
+        except Exception:
+            pass
+        parts = 1
+        chunks = w.row_bytes // 32
+        units = 2 * w.T
+        while (units * parts < sms * 16 and chunks % (2 * parts) == 0
+               and chunks // (2 * parts) >= 32 and parts < 8):
+            parts *= 2
+    return 2 * w.T * parts
+
+
 def run_ours(args, dist):
     import torch
     import fp8_quant_gb300 as kv
@@ -671,25 +856,19 @@ def run_ours(args, dist):
     device = torch.device("cuda", dist.local_rank)
     kv.load_library()
     name = args.workload
+    peak, peak_src = hbm_peak()
     pool = Pool(name, device, pool_bytes=args.pool_mb << 20, seed=1234 + dist.rank,
                 n_slots=args.slots)
     w = pool.w
     T = w.T
-    stream_handle = lambda: torch.cuda.current_stream().cuda_stream
-    nb = pool.num_batches
+    step = pool_step(kv, pool)
 
-    # --- device-resident steps -------------------------------------------
-    def step(i):
-        rc = pool.call(i % nb, stream_handle())
-        if rc != 0:
-            raise RuntimeError(f"launch failed: {kv.kv_status_str(rc)}")
-
-    chunk = min(args.steps, args.graph_chunk)
-    graphs = capture_graphs(torch, step, args.steps, chunk)
-    warm = max(args.warmup, 1)
-    warm_graphs = capture_graphs(torch, step, warm, min(warm, args.graph_chunk))
+    # --- headline: exactly --steps timed calls ------------------------------
+    graphs = capture_graphs(torch, step, args.steps, min(args.steps, args.graph_chunk))
+    warm_graphs = capture_graphs(torch, step, args.warmup, min(args.warmup, args.graph_chunk))
     run_graphs(warm_graphs)
-    run_graphs(graphs)                      # first replay uploads the graph
+    del warm_graphs
+    run_graphs(graphs)                      # untimed replay: uploads the timed graphs
     torch.cuda.synchronize()
 
     visible = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
@@ -701,6 +880,7 @@ def run_ours(args, dist):
     ms = time_region(torch, dist, lambda: run_graphs(graphs), device)
     clocks.mark()
     clock_summary = clocks.stop()
+    del graphs
 
     st, nbad, _ = kv.kv_error_poll(pool.err)
     if st != kv.KVStatus.OK:
@@ -710,16 +890,40 @@ def run_ours(args, dist):
     sec_per_step = ms / 1e3 / args.steps
     value = dist.world * T / sec_per_step
     achieved_gbs = bytes_per_step / sec_per_step / 1e9
-    peak, peak_src = hbm_peak()
 
-    # row splits under the headline's conditions, right after it
-    splits = (split_timings(torch, kv, pool, steps=args.steps, chunk=args.graph_chunk)
-              if not args.no_split_timings else {})
+    # --- the same calls over a long region, and cold single calls ------------
+    head = {"us_per_call": ms * 1e3 / args.steps, "calls": args.steps}
+    if args.long_ms > 0:
+        longer = measure_calls(torch, dist, device, step, args.steps, args.warmup,
+                               args.graph_chunk, args.long_ms)
+        head["us_per_call_long"] = longer["us_per_call_long"]
+        head["calls_long"] = longer["calls_long"]
+    head["launches_per_call"] = pool.launches_per_call
+    fractions(head, bytes_per_step, T, peak)
+    head["single_call_cold_us"] = single_call_cold_us(torch, pool,
+                                                      torch.cuda.current_stream().cuda_stream)
 
-    # --- end to end: pinned host -> device inputs, error record back --------
+    # --- end to end: pinned host inputs, result back to the host ------------
     e2e = run_e2e(args, dist, torch, kv, pool, device)
 
-    cold_us = single_call_cold_us(torch, pool, stream_handle())
+    # --- every configuration in the same protocol ----------------------------
+    per_config = {}
+    if args.suite != "none" and args.slots is None:
+        names = SUITE_CONFIGS + (SUITE_MORE if args.suite == "all" else ())
+        del pool
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        pool = None
+        for other in names:
+            if other == name:
+                per_config[other] = head
+                continue
+            try:
+                per_config[other] = suite_entry(args, dist, torch, kv, device, other, peak)
+            except Exception as exc:     # recorded, not fatal: the headline stands
+                per_config[other] = {"error": f"{type(exc).__name__}: {exc}"}
+                torch.cuda.synchronize()
+                torch.cuda.empty_cache()
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -732,28 +936,26 @@ def run_ours(args, dist):
     traffic = load_traffic(name)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
-        "steps": args.steps, "warmup": warm + args.steps,
+        "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype_of(w), "data": "synthetic",
-        "config": {
-            "workload": DESCRIPTIONS[name] + ("" if args.slots is None
-                                              else f" [cache reduced to {args.slots} slots]"),
-            "tokens_per_step": T,
-            "bytes_per_step": bytes_per_step, "parallelism": f"replicas x{dist.world}",
-            "l2": f"inputs rotate over {nb} batches ({nb * pool.in_bytes_per_batch / 1e6:.0f} MB"
-                  f" read per cycle) > L2 (129 MB)" if nb > 1 else
-                  "one batch, inputs and writes each larger than L2",
-            "timing": "CUDA graphs of back-to-back calls, CUDA events on the launching stream",
-            "achieved_gbs": achieved_gbs, "single_call_cold_us": cold_us,
-            "single_call_cold_gbs": bytes_per_step / (cold_us * 1e-6) / 1e9,
-            "us_per_call_by_num_split": splits,
+        "config": line_config(name, w, dist.world, args.pool_mb << 20, args.slots),
+        "timing": {
+            "protocol": "CUDA graphs of back-to-back calls; a device-side delay before the "
+                        "opening CUDA event so that the events bracket device time only; "
+                        "events on the launching stream",
+            "upload_replays": 1,
+            "headline": head,
         },
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "traffic": traffic,
-                     "peak_source": peak_src},
+                     "peak_source": peak_src,
+                     "kernel": "kv_copy_rows" if w.kind == "copy" else w.kind},
+        "per_config": per_config,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * pool.launches_per_call,
+        "gpu_launches": args.steps * (pool.launches_per_call if pool is not None
+                                      else head["launches_per_call"]),
         "clocks": clock_summary,
     }
     if dist.rank == 0:
@@ -867,13 +1069,17 @@ def run_e2e(args, dist, torch, kv, pool, device):
         out[name] = dist.world * w.T / (ms / 1e3 / steps)
         del graphs
     best = max(out, key=out.get)
+    # zero-copy moves only what the kernel reads over the link: the K and V
+    # rows (not the Q columns of a fused QKV batch) and the slot ids
+    h2d = {"staged": total,
+           "zero_copy": 2 * w.row_bytes * w.T + (0 if w.kind == "absmax" else ibytes)}
     how = {"staged": "every step: one pinned host -> device copy of the batch (K, V, slot ids "
                      "packed) into a device buffer, the call on the staged inputs, and a "
                      "device -> host read of the error record; back-to-back from CUDA graphs",
            "zero_copy": "every step: the call reads the batch (K, V, slot ids) directly from "
                         "pinned host memory over NVLink-C2C, then kv_error_snapshot writes the "
                         "error record into pinned host memory; back-to-back from CUDA graphs"}
-    return {"value": out[best], "unit": "tokens/s", "h2d_bytes_per_step": total,
+    return {"value": out[best], "unit": "tokens/s", "h2d_bytes_per_step": h2d[best],
             "d2h_bytes_per_step": d2h, "steps": steps, "mode": best, "how": how[best],
             "by_mode": out}
 
@@ -938,56 +1144,31 @@ def run_e2e_gather(args, dist, torch, kv, pool, device):
             "by_mode": out}
 
 
-def split_timings(torch, kv, pool, steps, chunk):
-    """Per-call time of the copy workload with each legal row split (1, 2, 4),
-    timed like the headline: the same number of steps from CUDA graphs of
-    `chunk` calls, after one untimed replay."""
-    w = pool.w
-    out = {}
-    if w.kind != "copy":
-        return out
-    saved = w.num_split
-    try:
-        for split in (1, 2, 4):
-            if split > 1 and w.row_bytes % (split * 128):
-                continue
-            w.num_split = split
-
-            def step(i):
-                assert pool.call(i % pool.num_batches, torch.cuda.current_stream().cuda_stream) == 0
-
-            graphs = capture_graphs(torch, step, steps, min(steps, chunk))
-            run_graphs(graphs)
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
-            run_graphs(graphs)
-            e1.record()
-            torch.cuda.synchronize()
-            out[str(split)] = e0.elapsed_time(e1) * 1e3 / steps
-    finally:
-        w.num_split = saved
-    return out
-
-
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--workload", default="decode", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(DESCRIPTIONS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--suite", default="all", choices=["all", "configs", "none"],
+                    help="after the headline, time every configuration (configs) and the "
+                         "further rows (all) in the same protocol")
+    ap.add_argument("--long-ms", type=float, default=10.0,
+                    help="also time each workload's calls over a region of at least this "
+                         "many ms (0: off)")
     ap.add_argument("--pool-mb", type=int, default=512)
     ap.add_argument("--graph-chunk", type=int, default=1000)
     ap.add_argument("--e2e-steps", type=int, default=20000)
     ap.add_argument("--cpu-seconds", type=float, default=20.0,
                     help="CPU oracle timing: half on one thread, half on all host threads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-split-timings", action="store_true")
     ap.add_argument("--slots", type=int, default=None,
-                    help="override the cache size in slots (small profiler captures)")
+                    help="override the cache size in slots (small profiler captures; "
+                         "no suite)")
     a = ap.parse_args(argv)
+    a.steps_given = a.steps is not None
+    a.warmup_given = a.warmup is not None
     if a.steps is None:
         a.steps = DEFAULT_STEPS[a.workload] if a.impl == "ours" else 20
     if a.warmup is None:

@@ -117,6 +117,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kv_error_poll.restype = I32
         lib.kv_error_snapshot.argtypes = [P, P, P]
         lib.kv_error_snapshot.restype = I32
+        lib.kv_launch_floor.argtypes = [I64, P]
+        lib.kv_launch_floor.restype = I32
         lib.kv_error_reset.argtypes = [P, P]
         lib.kv_error_reset.restype = I32
         lib.kv_status_str.argtypes = [I32]
@@ -277,6 +279,10 @@ class raw:
     @staticmethod
     def kv_error_reset(d_err, stream) -> int:
         return load_library().kv_error_reset(d_err, stream)
+
+    @staticmethod
+    def kv_launch_floor(num_warps, stream) -> int:
+        return load_library().kv_launch_floor(num_warps, stream)
 
 
 # ---------------------------------------------------------------------------

@@ -26,6 +26,8 @@
 //  * Every kernel waits on the previous grid (griddepcontrol.wait) before its
 //    first global access and is launched with programmatic stream
 //    serialisation, so its launch overlaps the previous kernel's tail.
+#include <cuda.h>  // context types of the driver entry points fetched at run time
+
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
@@ -845,6 +847,28 @@ extern "C" kv_status kv_error_snapshot(const kv_error_record* d_err, kv_error_re
                 reinterpret_cast<cudaStream_t>(stream_));
 }
 
+namespace kvimpl {
+namespace {
+
+struct FloorParams {
+  int unused;
+};
+
+// No memory access: the grid-dependency hand-over of the row kernels and
+// nothing else.
+__global__ void __launch_bounds__(kThreads) kv_launch_floor_kernel(const __grid_constant__ FloorParams) {
+  grid_handover();
+}
+
+}  // namespace
+}  // namespace kvimpl
+
+extern "C" kv_status kv_launch_floor(int64_t num_warps, kv_stream_t stream_) {
+  if (num_warps < 1 || num_warps > (int64_t{1} << 40)) return KV_ERR_INVALID_ARG;
+  return launch(kv_launch_floor_kernel, static_cast<uint64_t>(num_warps), FloorParams{0},
+                reinterpret_cast<cudaStream_t>(stream_));
+}
+
 extern "C" kv_status kv_error_reset(kv_error_record* d_err, kv_stream_t stream_) {
   if (!d_err || (u64(d_err) & 7u) != 0) return KV_ERR_INVALID_ARG;
   const cudaError_t e =
@@ -878,22 +902,65 @@ namespace kvimpl {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KV_NOALLOC_SCRATCH_BYTES];
 static_assert(sizeof(kv_error_record) <= KV_NOALLOC_SCRATCH_BYTES, "record must fit the array");
 
-// Device address of g_noalloc_scratch, looked up once per device with that
-// device current.  In host code the array's name is only a host-side stand-in.
-std::atomic<void*> g_noalloc_addr[kMaxDevices];
+// Unique id of the calling thread's current CUDA context, or 0 when there is
+// none yet (or the driver cannot tell).  The driver functions are fetched
+// through the runtime, so the library does not link the driver library.
+unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(f);
+    f = nullptr;
+    q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(f);
+    (void)cudaGetLastError();
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch for each device, looked up with that
+// device current and kept together with the id of the context it belongs to.
+// In host code the array's name is only a host-side stand-in.  A context
+// that is not the one of the cached address (after cudaDeviceReset the
+// runtime makes a new one, and the module, with the array, may then load
+// elsewhere) or an unknown context leads to a fresh lookup.
+struct NoallocAddr {
+  unsigned long long ctx_id;
+  void* addr;
+};
+std::mutex g_noalloc_mutex;
+NoallocAddr g_noalloc_addr[kMaxDevices];
 
 kv_status noalloc_record(kv_error_record** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return KV_ERR_UNSUPPORTED;
-  void* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
+  const unsigned long long ctx = current_context_id();
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  NoallocAddr& slot = g_noalloc_addr[dev];
+  if (ctx == 0 || slot.addr == nullptr || slot.ctx_id != ctx) {
+    void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e);
-    g_noalloc_addr[dev].store(p, std::memory_order_release);
+    slot.addr = p;
+    slot.ctx_id = current_context_id();  // the lookup has made the context current
   }
-  *out = static_cast<kv_error_record*>(p);
+  *out = static_cast<kv_error_record*>(slot.addr);
   return KV_OK;
 }
 

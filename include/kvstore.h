@@ -350,26 +350,31 @@ kv_status kv_absmax_inv(const void *k, const void *v, kv_src_dtype src_dtype,
  * users only.
  *
  * Some callers cannot call cudaMalloc at the point where they write the KV
- * cache: code running inside an allocator hook or a host callback (where
- * allocating would re-enter the allocator or deadlock), a plugin that is handed
- * the tensors but owns no memory pool, or a process whose device memory is
- * entirely reserved by a pool it does not control.  kv_store needs one more
- * device buffer besides the tensors, its error record, so those callers could
- * not use it.  kv_store_noalloc takes the same arguments as kv_store except
- * d_err and allocates nothing: the record lives in a 256-byte static device
- * array inside this library (KV_NOALLOC_SCRATCH_BYTES), which every GPU that
- * loads the library holds until the process exits.  The record needs 16 bytes
- * whatever the batch size, so no batch exceeds the array; a build whose record
- * did not fit would return KV_ERR_UNSUPPORTED.
+ * cache: code running inside an allocator hook (where allocating would
+ * re-enter the allocator), a plugin that is handed the tensors but owns no
+ * memory pool, or a process whose device memory is entirely reserved by a pool
+ * it does not control.  kv_store needs one more device buffer besides the
+ * tensors, its error record, so those callers could not use it.
+ * kv_store_noalloc takes the same arguments as kv_store except d_err and
+ * allocates nothing: the record lives in a 256-byte static device array inside
+ * this library (KV_NOALLOC_SCRATCH_BYTES), which every GPU that loads the
+ * library holds until the process exits.  The record needs 16 bytes whatever
+ * the batch size, so no batch exceeds the array; a build whose record did not
+ * fit would return KV_ERR_UNSUPPORTED.
  *
  * Behaviour:
  *  - The first call on a device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress); make that first call
- *    before any stream capture on the device.
+ *    before any stream capture on the device.  The address is kept with the
+ *    id of the CUDA context it was found in; a call from another context (for
+ *    instance after cudaDeviceReset) looks it up again.
  *  - Each call clears the record on `stream`, runs kv_store with it, then
  *    synchronises `stream` and copies the record to *oob_count and
  *    *first_bad_token (host, nullable; -1 when no token was skipped).  It
  *    therefore blocks the host until the write has finished.
+ *  - It makes CUDA API calls, so it must not be called from a stream callback
+ *    or a host function enqueued with cudaLaunchHostFunc, where CUDA forbids
+ *    them.
  *  - Every call shares the one array: calls that overlap on the GPU (from
  *    other host threads or on other streams) race on it and may report each
  *    other's counts.  The cache writes themselves are not affected.
@@ -411,6 +416,16 @@ kv_status kv_error_snapshot(const kv_error_record *d_err, kv_error_record *dst,
 
 /* kv_error_reset -- zero the record asynchronously on `stream` (capturable). */
 kv_status kv_error_reset(kv_error_record *d_err, kv_stream_t stream);
+
+/* kv_launch_floor -- a measurement aid with no counterpart on the pages.
+ * Launches an empty kernel sized for num_warps warps of work, with the CTA
+ * size, grid and programmatic-launch attributes the write kernels use for
+ * that much work, and the same wait for the preceding grid.  It touches no
+ * memory.  Timed back to back on a stream, it gives the fixed cost that every
+ * launch of this library pays, the floor under a small call such as a decode
+ * step (256 tokens of 2048-byte rows run as 1,024 warps).  num_warps in
+ * [1, 2^40], else KV_ERR_INVALID_ARG. */
+kv_status kv_launch_floor(int64_t num_warps, kv_stream_t stream);
 
 /* Static, NUL-terminated name of a status code. */
 const char *kv_status_str(kv_status status);

@@ -24,21 +24,23 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kv_oracle.c")
+_SRC_THREADS = os.path.join(_HERE, "kv_oracle_threads.c")
 _LIBDIR = os.path.join(_HERE, "lib")
 _LIB = os.path.join(_LIBDIR, "libkvoracle.so")
 _lock = threading.Lock()
 _lib = None
 
-CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread"]
 
 
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc into ``oracle/lib/libkvoracle.so``."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+    if (not force and os.path.exists(_LIB)
+            and all(os.path.getmtime(_LIB) >= os.path.getmtime(s) for s in (_SRC, _SRC_THREADS))):
         return _LIB
     os.makedirs(_LIBDIR, exist_ok=True)
     tmp = _LIB + f".tmp{os.getpid()}"
-    subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
+    subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, _SRC_THREADS, "-lm"])
     os.replace(tmp, _LIB)
     return _LIB
 
@@ -91,6 +93,8 @@ def _load():
         lib.kvo_gather_copy_paged.restype = I32
         lib.kvo_gather_fp8.argtypes = lib.kvo_store_fp8.argtypes
         lib.kvo_gather_fp8.restype = I32
+        lib.kvo_run_threads.argtypes = [P, I64, I32, ctypes.c_double, I64, P, P, P]
+        lib.kvo_run_threads.restype = I32
         lib.kvo_f32_to_bf16_array.argtypes = [P, P, I64]
         lib.kvo_f32_to_f16_array.argtypes = [P, P, I64]
         _lib = lib
@@ -397,3 +401,73 @@ def gather_fp8_ex(k_cache, v_cache, k_out, v_out, indices, strides: Strides, num
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return int(bad[0]), int(first[0])
+
+
+# -- host-thread runner (CPU baseline timing) ---------------------------------
+
+class _Job(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("index_is_i64", ctypes.c_int32),
+                ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("indices", ctypes.c_void_p), ("index_stride", ctypes.c_int64),
+                ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("use_scale", ctypes.c_int32),
+                ("strides", ctypes.c_void_p), ("page_size", ctypes.c_int64),
+                ("kc_page_stride", ctypes.c_int64), ("vc_page_stride", ctypes.c_int64),
+                ("size_limit", ctypes.c_int64), ("inv_k", ctypes.c_float),
+                ("inv_v", ctypes.c_float)]
+
+
+JOB_KINDS = {"copy": 0, "copy_paged": 1, "fp8": 2}
+
+
+class ThreadedJob:
+    """One write problem for ``kvo_run_threads``: the unchanged oracle loop
+    (``store_copy``, ``store_copy_paged`` or ``store_fp8``) run over token
+    ranges on POSIX threads, outside the interpreter lock.
+
+    ``kind`` is ``"copy"``, ``"copy_paged"`` or ``"fp8"``; the keyword
+    arguments are those of the matching function above (``elem_bytes`` or
+    ``src_dtype``, page geometry, inverse scales)."""
+
+    def __init__(self, kind, k, v, k_cache, v_cache, indices, strides: Strides, num_heads,
+                 head_dim, size_limit, elem_bytes=2, src_dtype="bf16", page_size=1,
+                 kc_page_stride=0, vc_page_stride=0, inv_k=1.0, inv_v=1.0, use_scale=0,
+                 k_off=0, v_off=0, index_stride=1):
+        for a, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+            _check_buf(a, n)
+        self.idx = np.ascontiguousarray(indices)
+        if self.idx.dtype not in (np.int32, np.int64):
+            raise TypeError("indices must be int32 or int64")
+        self.num_tokens = self.idx.size // index_stride
+        self._keep = (k, v, k_cache, v_cache, strides)
+        j = _Job()
+        j.kind = JOB_KINDS[kind]
+        j.index_is_i64 = int(self.idx.dtype == np.int64)
+        j.k, j.v = _ptr(k) + k_off, _ptr(v) + v_off
+        j.k_cache, j.v_cache = _ptr(k_cache), _ptr(v_cache)
+        j.indices = _ptr(self.idx)
+        j.index_stride = index_stride
+        j.num_heads, j.head_dim = num_heads, head_dim
+        j.dtype = int(src_dtype == "bf16") if kind == "fp8" else elem_bytes
+        j.use_scale = int(use_scale)
+        j.strides = _ptr(strides.values)
+        j.page_size = page_size
+        j.kc_page_stride, j.vc_page_stride = kc_page_stride, vc_page_stride
+        j.size_limit = size_limit
+        j.inv_k, j.inv_v = float(np.float32(inv_k)), float(np.float32(inv_v))
+        self.job = j
+
+    def run(self, threads: int, seconds: float = 0.0, min_reps: int = 1, num_tokens=None):
+        """Thread i repeats tokens [T*i/n, T*(i+1)/n) until ``seconds`` have
+        passed and it has made ``min_reps`` passes. Returns (tokens processed,
+        elapsed seconds, out-of-range tokens met)."""
+        T = self.num_tokens if num_tokens is None else num_tokens
+        done = np.zeros(1, np.int64)
+        el = np.zeros(1, np.float64)
+        bad = np.zeros(1, np.int64)
+        rc = _load().kvo_run_threads(ctypes.addressof(self.job), T, threads, seconds, min_reps,
+                                     _ptr(done), _ptr(el), _ptr(bad))
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments")
+        return int(done[0]), float(el[0]), int(bad[0])

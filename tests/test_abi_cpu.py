@@ -131,6 +131,9 @@ def test_valid_calls_need_a_gpu(lib):
     assert kv.raw.kv_error_poll(A, None)[0] == CUDA
     assert kv.raw.kv_error_poll(None, None)[0] == INVALID
     assert kv.raw.kv_error_reset(A + 1, None) == INVALID
+    assert kv.raw.kv_launch_floor(1024, None) == CUDA
+    assert kv.raw.kv_launch_floor(0, None) == INVALID
+    assert kv.raw.kv_launch_floor(-3, None) == INVALID
 
 
 def test_missing_library_fails_loudly(tmp_path):

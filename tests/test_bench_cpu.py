@@ -12,26 +12,50 @@ import numpy as np
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def test_split_oracle_run_writes_the_same_caches():
-    """Token ranges on several threads write exactly what one whole-batch
-    call writes."""
+def test_threaded_oracle_run_writes_the_same_caches():
+    """Token ranges on several POSIX threads write exactly what one
+    whole-batch oracle call writes (copy and FP8 kinds)."""
     sys.path.insert(0, ROOT)
     import bench
-    for name in ("tiny",):
-        w = bench.load_workload(name)
-        run1, used1 = bench.oracle_batch_runner(name, w, 1)
+    import workloads as wl
+    for name in ("tiny", "fp8_small"):
+        w = (bench.load_workload(name) if name == "tiny" else
+             wl.make_fp8(name, T=512, H=8, D=128, n_slots=4096, seed=3, page_size=32))
+        bench._ORACLE_CACHE.pop(name, None)
+        job = bench.oracle_job(name, w)
         kc, vc = bench._ORACLE_CACHE[name][:2]
         kc[:] = 0
         vc[:] = 0
-        run1()
+        bench.oracle_step(name, w, w.T)
         want = kc.copy(), vc.copy()
-        run4, used4 = bench.oracle_batch_runner(name, w, 4)
-        assert (used1, used4) == (1, 4)
         kc[:] = 0
         vc[:] = 0
-        run4()
+        done, el, bad = job.run(4)
+        assert done == w.T and bad == 0 and el >= 0
         assert np.array_equal(kc, want[0]) and np.array_equal(vc, want[1])
         assert np.count_nonzero(want[0]) > 0
+        bench._ORACLE_CACHE.pop(name, None)
+
+
+def test_threaded_runner_counts_tokens_and_bad_slots():
+    """The runner's bookkeeping: every thread's passes are counted, and
+    out-of-range slots met by the oracle are summed over threads."""
+    sys.path.insert(0, ROOT)
+    import oracle
+    T, H, D = 40, 1, 8
+    k = np.arange(T * H * D, dtype=np.uint16)
+    v = k[::-1].copy()
+    kc = np.zeros(64 * H * D, np.uint16)
+    vc = kc.copy()
+    idx = np.arange(T, dtype=np.int32)
+    idx[[3, 17, 39]] = [-1, 64, 1000]
+    R = H * D * 2
+    st = oracle.Strides(k_token=R, k_head=D * 2, k_dim=2, v_token=R, v_head=D * 2, v_dim=2,
+                        kc_slot=R, kc_head=D * 2, kc_dim=2, vc_slot=R, vc_head=D * 2, vc_dim=2)
+    job = oracle.ThreadedJob("copy", k, v, kc, vc, idx, st, H, D, 64, elem_bytes=2)
+    done, el, bad = job.run(3, 0.0, 2)
+    assert done % T == 0 and done >= 2 * T and bad == 3 * (done // T)
+    assert np.array_equal(kc.reshape(64, D)[:T][idx >= 0][: 3], k.reshape(T, D)[:3])
 
 
 def test_oracle_rates_are_positive():
@@ -40,7 +64,7 @@ def test_oracle_rates_are_positive():
     r1, s1, c1 = bench.oracle_tokens_per_s("tiny", 0.2)
     r4, s4, c4 = bench.oracle_tokens_per_s("tiny", 0.2, threads=4)
     assert r1 > 0 and r4 > 0 and c1 == 1 and c4 == 4
-    assert "one thread" in s1 and "4 threads" in s4
+    assert "1 POSIX thread," in s1 and "4 POSIX threads" in s4
 
 
 def test_reference_arm_line():
@@ -52,6 +76,12 @@ def test_reference_arm_line():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    # the same config object as the GPU arm's line
+    sys.path.insert(0, ROOT)
+    import bench
+    w = bench.load_workload("tiny")
+    assert line["config"] == bench.line_config("tiny", w, 1, 512 << 20)
+    assert line["steps"] == 3 and line["warmup"] == 3
 
 
 def test_workload_sizes():

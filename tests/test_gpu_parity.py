@@ -503,3 +503,27 @@ def test_tensor_wrappers_round_trips():
     inv = kv.kv_inv_scale(torch.tensor([2.0, 8.0], device=dev))
     assert inv.tolist() == [0.5, 0.125]
     assert kv.kv_error_poll()[1] == 0
+
+
+@pytest.mark.gpu
+def test_launch_floor_runs_in_stream_order_and_in_a_graph():
+    """kv_launch_floor (the measurement aid) launches, keeps stream order
+    after a torch producer and replays from a CUDA graph; it writes nothing."""
+    import torch
+    import fp8_quant_gb300 as kv
+    dev = torch.device("cuda", 0)
+    x = torch.zeros(1 << 20, device=dev)
+    st = torch.cuda.current_stream().cuda_stream
+    x.fill_(3.0)
+    assert kv.raw.kv_launch_floor(1024, st) == 0
+    assert kv.raw.kv_launch_floor(1, st) == 0
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(8):
+            assert kv.raw.kv_launch_floor(32768, s.cuda_stream) == 0
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert bool((x == 3.0).all())

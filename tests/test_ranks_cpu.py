@@ -66,7 +66,7 @@ def test_single_rank_defaults(monkeypatch):
 def test_bench_arguments():
     import bench
     a = bench.parse_args([])
-    assert a.workload == "decode" and a.impl == "ours" and a.warmup >= 3
+    assert a.workload == "strided" and a.impl == "ours" and a.warmup >= 3 and a.suite == "all"
     a = bench.parse_args(["--impl", "reference", "--steps", "7", "--warmup", "4"])
     assert (a.steps, a.warmup) == (7, 4)
     with pytest.raises(SystemExit):
