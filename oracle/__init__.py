@@ -331,7 +331,7 @@ def absmax_inv(k, v, strides: Strides, num_tokens, num_heads, head_dim, src_dtyp
 # -- e5m2 and the extended FP8 write / gather -------------------------------------
 
 FMT = {"e4m3fn": 0, "e5m2": 1}
-SCALE_MODE = {"none": 0, "tensor": 1, "token": 2, "token_head": 3}
+SCALE_MODE = {"none": 0, "tensor": 1, "token": 2, "token_head": 3, "page": 4}
 
 
 def e5m2_encode(x) -> np.ndarray:
@@ -357,6 +357,8 @@ def store_fp8_ex(k, v, k_cache, v_cache, indices, strides: Strides, num_heads, h
                  scale_mode="none", inv_k=1.0, inv_v=1.0, k_scales=None, v_scales=None,
                  scales_slot_stride=1, k_off=0, v_off=0, index_stride=1, t_end=None):
     """Extended FP8 write (format, scale mode, per-slot scale caches); in place.
+    With ``scale_mode="page"``, ``k_scales`` / ``v_scales`` hold one fp32
+    INVERSE scale per cache page (index slot // page_size), read only.
     Returns (bad_count, first_bad)."""
     for a, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
         _check_buf(a, n)
@@ -384,6 +386,9 @@ def gather_fp8_ex(k_cache, v_cache, k_out, v_out, indices, strides: Strides, num
                   out_dtype, page_size, kc_page_stride, vc_page_stride, size_limit,
                   fmt="e4m3fn", scale_mode="none", scale_k=1.0, scale_v=1.0, k_scales=None,
                   v_scales=None, scales_slot_stride=1, index_stride=1, t_end=None):
+    """Extended dequantising gather. With ``scale_mode="page"``, ``k_scales`` /
+    ``v_scales`` hold one fp32 (forward) scale per cache page. Returns
+    (bad_count, first_bad)."""
     for a, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_out, "k_out"), (v_out, "v_out")):
         _check_buf(a, n)
     idx = np.ascontiguousarray(indices)

@@ -584,7 +584,10 @@ void kvo_e5m2_decode_array(const uint8_t *codes, double *out, int64_t n)
 
 /* Extended FP8 write.  fmt: 0 e4m3fn, 1 e5m2.  scale_mode: 0 none, 1 one fp32
  * inverse scale per tensor (inv_k / inv_v), 2 dynamic per token row, 3
- * dynamic per (token, head).  Dynamic: over the group's elements x (the whole
+ * dynamic per (token, head), 4 one fp32 inverse scale per cache page, read
+ * from k_scales[page_id] / v_scales[page_id] (page_id = slot / page_size, the
+ * page of the fused FP8 write's `_process_kv_tensor`): the codes are
+ * enc(fl32(x * inv[page_id])).  Dynamic: over the group's elements x (the whole
  * K row of the token, or one head of it), amax = max |x| (NaN ignored); when
  * amax > 0, inv = fl32(fmax / amax) and scale = fl32(amax / fmax), else both
  * are 1; the codes are enc(fl32(x * inv)) and `scale` is stored at
@@ -604,7 +607,7 @@ int kvo_store_fp8_ex(const uint8_t *k, const uint8_t *v, uint8_t *k_cache, uint8
 {
     if (num_heads <= 0 || head_dim <= 0 || page_size <= 0 || t_begin > t_end)
         return KVO_ERR_ARG;
-    if (fmt < 0 || fmt > 1 || scale_mode < 0 || scale_mode > 3)
+    if (fmt < 0 || fmt > 1 || scale_mode < 0 || scale_mode > 4)
         return KVO_ERR_ARG;
     const double fmax = fmt ? 57344.0 : 448.0;
     *bad_count = 0;
@@ -630,6 +633,8 @@ int kvo_store_fp8_ex(const uint8_t *k, const uint8_t *v, uint8_t *k_cache, uint8
                 float inv = 1.0f;
                 if (scale_mode == 1) {
                     inv = kv ? inv_v : inv_k;
+                } else if (scale_mode == 4) {
+                    inv = scales[page_id];
                 } else if (scale_mode >= 2) {
                     double amax = 0.0;
                     for (int32_t hh = 0; hh < heads_per_group; ++hh)
@@ -667,7 +672,8 @@ int kvo_store_fp8_ex(const uint8_t *k, const uint8_t *v, uint8_t *k_cache, uint8
 /* Extended dequantising gather: codes of format fmt decoded exactly, times
  * the scale (mode 0: none; 1: scale_k / scale_v per tensor; 2/3: the per-slot
  * scale k_scales[slot * scales_slot_stride + g] written by the extended
- * write), rounded to bf16 / fp16. */
+ * write; 4: the per-page scale k_scales[slot / page_size]), rounded to
+ * bf16 / fp16. */
 int kvo_gather_fp8_ex(const uint8_t *k_cache, const uint8_t *v_cache, uint8_t *k_out,
                       uint8_t *v_out, const void *indices, int index_is_i64,
                       int64_t index_stride, int64_t t_begin, int64_t t_end, int32_t num_heads,
@@ -679,7 +685,7 @@ int kvo_gather_fp8_ex(const uint8_t *k_cache, const uint8_t *v_cache, uint8_t *k
 {
     if (num_heads <= 0 || head_dim <= 0 || page_size <= 0 || t_begin > t_end)
         return KVO_ERR_ARG;
-    if (fmt < 0 || fmt > 1 || scale_mode < 0 || scale_mode > 3)
+    if (fmt < 0 || fmt > 1 || scale_mode < 0 || scale_mode > 4)
         return KVO_ERR_ARG;
     *bad_count = 0;
     *first_bad = -1;
@@ -702,6 +708,8 @@ int kvo_gather_fp8_ex(const uint8_t *k_cache, const uint8_t *v_cache, uint8_t *k
                 float scale = 1.0f;
                 if (scale_mode == 1)
                     scale = kv ? scale_v : scale_k;
+                else if (scale_mode == 4)
+                    scale = scales[page_id];
                 else if (scale_mode >= 2)
                     scale = scales[slot * scales_slot_stride + (scale_mode == 3 ? h : 0)];
                 for (int32_t d = 0; d < head_dim; ++d) {

@@ -728,3 +728,131 @@ def test_paged_gather_round_trip():
     keep = np.arange(T) != 5
     assert np.array_equal(ko[keep], k[keep]) and np.array_equal(vo[keep], v[keep])
     assert np.all(ko[5] == 0)
+
+
+# ---------------------------------------------------------------------------
+# Per-page scales (one fp32 scale per cache page, page = slot // page_size)
+# ---------------------------------------------------------------------------
+
+def _page_scales(n_pages, seed):
+    """Positive fp32 inverse scales of assorted magnitudes, one per page: some
+    pages scale into saturation, some far down, one is exactly 1."""
+    u = wl.uniform01(seed, n_pages)
+    inv = (2.0 ** (np.floor(u * 24) - 12) * (1.0 + wl.uniform01(seed + 1, n_pages)))
+    inv = inv.astype(np.float32)
+    inv[0] = 1.0
+    return inv
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("src", ["bf16", "f16"])
+def test_store_fp8_ex_per_page_scales(fmt, src):
+    """Every code is the brute-force code of numpy's fp32 product x * inv[page]
+    of its slot's page; rows land at page * page_stride + offset * slot_stride
+    of padded 4-D pages; every other byte keeps the pre-fill."""
+    T, H, D, ps, n_pages = 96, 4, 32, 8, 32
+    n = ps * n_pages
+    w = wl.make_fp8("t", T, H, D, n, seed=121, dtype=src, page_size=ps)
+    R8 = H * D
+    page_stride = ps * R8 + 64                      # 64 bytes of pad per page
+    st = _fp8_strides(H, D, 2, R8)
+    inv_k = _page_scales(n_pages, 122)
+    inv_v = _page_scales(n_pages, 124)
+    kc = np.full(n_pages * page_stride, 0x7F, np.uint8)
+    vc = kc.copy()
+    assert oracle.store_fp8_ex(w.k, w.v, kc, vc, w.indices, st, H, D, src, ps, page_stride,
+                               page_stride, n, fmt=fmt, scale_mode="page", k_scales=inv_k,
+                               v_scales=inv_v) == (0, -1)
+    enc = brute_encode if fmt == "e4m3fn" else brute_encode_e5m2
+    page, off = w.indices // ps, w.indices % ps
+    for bits, cache, inv in ((w.k, kc, inv_k), (w.v, vc, inv_v)):
+        x = _widen(bits.reshape(T, H * D), src)
+        y = (x * inv[page][:, None]).astype(np.float32)
+        want = enc(y).reshape(T, R8)
+        rows = cache.reshape(n_pages, page_stride)[:, :ps * R8].reshape(n_pages, ps, R8)
+        assert np.array_equal(rows[page, off], want)
+        touched = np.zeros((n_pages, ps), bool)
+        touched[page, off] = True
+        assert np.all(rows[~touched] == 0x7F)
+        assert np.all(cache.reshape(n_pages, page_stride)[:, ps * R8:] == 0x7F)
+
+
+def test_store_fp8_ex_page_constant_equals_tensor_mode():
+    """With the same inverse scale on every page, the per-page write equals the
+    per-tensor write byte for byte (flat and padded pages)."""
+    T, H, D, ps, n_pages = 64, 2, 64, 16, 16
+    n = ps * n_pages
+    w, st = _ex_problem(T, H, D, n, seed=126, ps=ps)
+    for page_stride in (ps * H * D, ps * H * D + 128):
+        a = [np.full(n_pages * page_stride, 0x7F, np.uint8) for _ in range(4)]
+        oracle.store_fp8_ex(w.k, w.v, a[0], a[1], w.indices, st, H, D, "bf16", ps, page_stride,
+                            page_stride, n, scale_mode="tensor", inv_k=w.inv_k, inv_v=w.inv_v)
+        oracle.store_fp8_ex(w.k, w.v, a[2], a[3], w.indices, st, H, D, "bf16", ps, page_stride,
+                            page_stride, n, scale_mode="page",
+                            k_scales=np.full(n_pages, w.inv_k, np.float32),
+                            v_scales=np.full(n_pages, w.inv_v, np.float32))
+        assert np.array_equal(a[0], a[2]) and np.array_equal(a[1], a[3])
+
+
+@pytest.mark.parametrize("out", ["bf16", "f16"])
+def test_gather_fp8_ex_per_page_scales(out):
+    """Each output element is torch's e4m3fn decode of its code times the
+    scale of its slot's page in fp32, rounded by torch (bf16) / numpy (fp16);
+    an out-of-range slot leaves its row alone."""
+    T, H, D, ps, n_pages = 40, 2, 64, 4, 64
+    n = ps * n_pages
+    R8 = H * D
+    idx = wl.distinct_slots(127, n, T)
+    codes = (wl.splitmix64(128, 0, T * R8) % np.uint64(256)).astype(np.uint8).reshape(T, R8)
+    kc = np.full(n * R8, 0x7F, np.uint8)
+    kc.reshape(n, R8)[idx] = codes
+    vc = kc.copy()
+    sk = _page_scales(n_pages, 129)
+    sv = (sk * np.float32(0.5)).astype(np.float32)
+    st = oracle.Strides(k_token=R8 * 2, k_head=D * 2, k_dim=2, v_token=R8 * 2, v_head=D * 2,
+                        v_dim=2, kc_slot=R8, kc_head=D, kc_dim=1, vc_slot=R8, vc_head=D,
+                        vc_dim=1)
+    ko = np.full(T * R8, 0x1234, np.uint16)
+    vo = ko.copy()
+    bad = idx.copy()
+    bad[9] = n
+    assert oracle.gather_fp8_ex(kc, vc, ko, vo, bad, st, H, D, out, ps, ps * R8, ps * R8, n,
+                                scale_mode="page", k_scales=sk, v_scales=sv) == (1, 9)
+    keep = np.arange(T) != 9
+    for o, s in ((ko, sk), (vo, sv)):
+        rows = o.reshape(T, R8)
+        for t in np.nonzero(keep)[0]:
+            assert np.array_equal(rows[t], _lib_dequant(codes[t], s[idx[t] // ps], out))
+        assert np.all(rows[9] == 0x1234)
+
+
+def test_per_page_store_then_gather_within_half_step():
+    """Writing with inv[page] and reading back with 1/inv[page] lands within
+    half an e4m3 step of the scaled value, mapped back by the page's scale."""
+    T, H, D, ps, n_pages = 64, 4, 32, 8, 64
+    n = ps * n_pages
+    w, st = _ex_problem(T, H, D, n, seed=131, ps=ps)
+    amax = np.float32(np.max(np.abs(_widen(w.k.reshape(-1), "bf16"))))
+    inv = (np.float32(448.0) / amax * _page_scales(n_pages, 132) /
+           np.float32(2.0)).astype(np.float32)
+    inv = np.minimum(inv, np.float32(448.0) / amax).astype(np.float32)  # no saturation
+    scale = (np.float32(1.0) / inv).astype(np.float32)
+    kc = np.full(n * H * D, 0x7F, np.uint8)
+    vc = kc.copy()
+    oracle.store_fp8_ex(w.k, w.v, kc, vc, w.indices, st, H, D, "bf16", ps, ps * H * D,
+                        ps * H * D, n, scale_mode="page", k_scales=inv, v_scales=inv)
+    ko = np.zeros(T * H * D, np.uint16)
+    vo = ko.copy()
+    ost = oracle.Strides(k_token=H * D * 2, k_head=D * 2, k_dim=2, v_token=H * D * 2,
+                         v_head=D * 2, v_dim=2, kc_slot=H * D, kc_head=D, kc_dim=1,
+                         vc_slot=H * D, vc_head=D, vc_dim=1)
+    oracle.gather_fp8_ex(kc, vc, ko, vo, w.indices, ost, H, D, "bf16", ps, ps * H * D,
+                         ps * H * D, n, scale_mode="page", k_scales=scale, v_scales=scale)
+    x = _widen(w.k.reshape(T, -1), "bf16").astype(np.float64)
+    back = (ko.astype(np.uint32) << 16).view(np.float32).reshape(T, -1).astype(np.float64)
+    pinv = inv[w.indices // ps].astype(np.float64)[:, None]
+    psc = scale[w.indices // ps].astype(np.float64)[:, None]
+    y = x * pinv
+    e = np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -6)))
+    bound = 2.0 ** (e - 4) * psc * (1 + 2 ** -7) + np.abs(back) * 2.0 ** -8 + np.abs(y) * psc * 2 ** -22
+    assert np.all(np.abs(back - y * psc) <= bound + 1e-30)
