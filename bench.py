@@ -71,6 +71,8 @@ DESCRIPTIONS = {
                          "(amax over the 1024 elements of the K or V row)",
     "fp8_e5m2": "FP8 write into an e5m2 cache: the fp8 batch, per-tensor inv_scale=57344/amax, "
                 "kv_store_fp8_ex",
+    "fp8_page": "FP8 write with per-page scales: the fp8 batch, one fp32 inverse scale per "
+                "32-slot page (32,768 pages, inv_k * 2^-3..2^0), kv_store_fp8_ex",
     "paged": "paged copy: the prefill batch into 4-D pages [65536, 64, 8, 128] padded by one "
              "slot per page (page stride 133,120 B), int32",
     "strided": "strided copy: fp16 K/V views into QKV [65536, 6144] (token stride 12,288 B), "
@@ -90,7 +92,7 @@ DESCRIPTIONS = {
 DEFAULT_STEPS = {"tiny": 200000, "decode": 200000, "prefill": 10000, "fp8": 50000,
                  "fp8_noscale": 50000, "strided": 5000, "odd": 10000, "gather_decode": 200000,
                  "gather_fp8": 50000, "absmax": 50000, "fp8_dynamic": 50000, "paged": 10000,
-                 "fp8_dynamic_token": 50000, "fp8_e5m2": 50000,
+                 "fp8_dynamic_token": 50000, "fp8_e5m2": 50000, "fp8_page": 50000,
                  "gather_prefill": 10000}
 
 
@@ -290,13 +292,17 @@ class Pool:
             self.ks = torch.full((w.n_slots * self.groups,), -1.0, dtype=torch.float32,
                                  device=device)
             self.vs = torch.full_like(self.ks, -1.0)
+        if w.notes.get("scale_mode") == "page":     # one inverse scale per cache page
+            self.page_inv = [torch.from_numpy(w.notes["page_inv_k"]).to(device),
+                             torch.from_numpy(w.notes["page_inv_v"]).to(device)]
         self.inv = torch.tensor([w.inv_k, w.inv_v], dtype=torch.float32, device=device)
         self.scale = torch.ones(2, dtype=torch.float32, device=device) / self.inv
         self.amax_inv = torch.zeros(4, dtype=torch.float32, device=device)
+        self.absmax_work = torch.zeros(4, dtype=torch.int32, device=device)
         self.err = torch.zeros(2, dtype=torch.int64, device=device)
         self.i64 = idx_dtype == torch.int64
-        # kernels one call launches: kv_absmax_inv zeroes, reduces and finishes
-        self.launches_per_call = 3 if w.kind == "absmax" else 1
+        # kernels one call launches: kv_absmax_inv with a workspace reduces and finishes
+        self.launches_per_call = 2 if w.kind == "absmax" else 1
 
     def _slots(self, g, idx_dtype):
         import torch
@@ -348,6 +354,13 @@ class Pool:
                                           3 if self.groups > 1 else 2, None, None,
                                           self.ks.data_ptr(), self.vs.data_ptr(), self.groups,
                                           self.err.data_ptr(), stream_handle)
+        if w.notes.get("scale_mode") == "page":
+            return kv.raw.kv_store_fp8_ex(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(),
+                                          idx_ptr, idt, 1, w.T, w.H, w.D,
+                                          1 if w.src_dtype == "bf16" else 0, strides, w.page_size,
+                                          w.page_stride, w.page_stride, w.n_slots, 0, 4,
+                                          self.page_inv[0].data_ptr(), self.page_inv[1].data_ptr(),
+                                          None, None, 0, self.err.data_ptr(), stream_handle)
         if w.notes.get("fmt") == "e5m2":
             return kv.raw.kv_store_fp8_ex(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(),
                                           idx_ptr, idt, 1, w.T, w.H, w.D,
@@ -358,7 +371,8 @@ class Pool:
         if w.kind == "absmax":
             return kv.raw.kv_absmax_inv(k_ptr, v_ptr, 1 if w.src_dtype == "bf16" else 0, w.T, w.H,
                                         w.D, strides, 448.0, self.amax_inv.data_ptr(),
-                                        self.amax_inv.data_ptr() + 8, stream_handle)
+                                        self.amax_inv.data_ptr() + 8,
+                                        self.absmax_work.data_ptr(), stream_handle)
         if w.kind == "gather":
             return kv.raw.kv_gather(self.kc.data_ptr(), self.vc.data_ptr(), k_ptr, v_ptr, idx_ptr,
                                     idt, 1, w.T, w.H, w.D, 2, strides, w.n_slots,
@@ -537,7 +551,7 @@ def oracle_job(name, w):
     threads over token ranges (kinds whose oracle call takes a token range:
     the flat and paged copies and the per-tensor FP8 write), else None."""
     import oracle
-    if w.kind not in ("copy", "fp8") or "fmt" in w.notes:
+    if w.kind not in ("copy", "fp8") or "fmt" in w.notes or "scale_mode" in w.notes:
         return None
     kc, vc, k, v, st = oracle_buffers(name, w)
     if w.kind == "copy":
@@ -721,6 +735,11 @@ def oracle_step(name, w, tokens, t_begin=0):
                             w.page_stride, w.page_stride, w.n_slots, fmt="e4m3fn",
                             scale_mode=mode, k_scales=ks, v_scales=vs,
                             scales_slot_stride=w.H if mode == "token_head" else 1, t_end=tokens)
+    elif w.notes.get("scale_mode") == "page":
+        oracle.store_fp8_ex(k, v, kc, vc, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
+                            w.page_stride, w.page_stride, w.n_slots, fmt="e4m3fn",
+                            scale_mode="page", k_scales=w.notes["page_inv_k"],
+                            v_scales=w.notes["page_inv_v"], t_end=tokens)
     elif w.notes.get("fmt") == "e5m2":
         oracle.store_fp8_ex(k, v, kc, vc, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
                             w.page_stride, w.page_stride, w.n_slots, fmt="e5m2",
@@ -746,7 +765,7 @@ def dtype_of(w):
 # strided QKV views, the odd row size), then the further rows: paged pages,
 # e5m2, dynamic scales, the gathers and the per-tensor scale pass.
 SUITE_CONFIGS = ("decode", "prefill", "fp8", "fp8_noscale", "strided", "odd")
-SUITE_MORE = ("paged", "fp8_e5m2", "fp8_dynamic", "fp8_dynamic_token", "gather_decode",
+SUITE_MORE = ("paged", "fp8_e5m2", "fp8_page", "fp8_dynamic", "fp8_dynamic_token", "gather_decode",
               "gather_prefill", "gather_fp8", "absmax")
 HEADLINE = "strided"
 

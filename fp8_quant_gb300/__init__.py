@@ -107,7 +107,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kv_inv_scale.argtypes = [P, P, I64, P]
         lib.kv_inv_scale.restype = I32
         lib.kv_absmax_inv.argtypes = [P, P, I32, I64, I32, I32, ctypes.POINTER(_Strides),
-                                      ctypes.c_float, P, P, P]
+                                      ctypes.c_float, P, P, P, P]
         lib.kv_absmax_inv.restype = I32
         lib.kv_store_noalloc.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
                                          ctypes.POINTER(_Strides), I64, I32,
@@ -244,10 +244,11 @@ class raw:
 
     @staticmethod
     def kv_absmax_inv(k, v, src_dtype, num_tokens, num_heads, head_dim, strides: Sequence[int],
-                      fp8_max, amax, inv, stream) -> int:
+                      fp8_max, amax, inv, work, stream) -> int:
         st = _Strides(*[int(x) for x in strides])
         return load_library().kv_absmax_inv(k, v, src_dtype, num_tokens, num_heads, head_dim,
-                                            ctypes.byref(st), float(fp8_max), amax, inv, stream)
+                                            ctypes.byref(st), float(fp8_max), amax, inv, work,
+                                            stream)
 
     @staticmethod
     def kv_store_noalloc(k, v, k_cache, v_cache, indices, index_dtype, index_stride,
@@ -463,7 +464,7 @@ def kv_error_reset(err=None, stream=None, device=None) -> None:
 # ---------------------------------------------------------------------------
 
 FP8_FORMATS = {"e4m3fn": 0, "e5m2": 1}
-SCALE_MODES = {"none": 0, "tensor": 1, "token": 2, "token_head": 3}
+SCALE_MODES = {"none": 0, "tensor": 1, "token": 2, "token_head": 3, "page": 4}
 
 
 def _paged_cache(cache, page_size, H, D):
@@ -586,9 +587,11 @@ def kv_inv_scale(scale, out=None, stream=None):
 
 
 def kv_absmax_inv(k, v, *, fp8_max: float = 448.0, num_heads=None, head_dim=None, out=None,
-                  stream=None):
+                  work=None, stream=None):
     """Per-tensor max |K|, max |V| and fp8_max / amax on the device: returns a
-    4-float tensor [amax_k, amax_v, inv_k, inv_v]."""
+    4-float tensor [amax_k, amax_v, inv_k, inv_v]. ``work``: an optional
+    device workspace of at least 8 bytes, zero before first use, kept zero by
+    the calls (two kernels per call instead of three)."""
     import torch
     if k.dim() == 3:
         H, D = k.shape[1], k.shape[2]
@@ -599,6 +602,8 @@ def kv_absmax_inv(k, v, *, fp8_max: float = 448.0, num_heads=None, head_dim=None
     out = torch.empty(4, dtype=torch.float32, device=k.device) if out is None else out
     _check(raw.kv_absmax_inv(k.data_ptr(), v.data_ptr(), 1 if k.dtype == torch.bfloat16 else 0,
                              k.shape[0], H, D, (kt, kh, kd, vt, vh, vd, 0, 0, 0, 0, 0, 0), fp8_max,
-                             out.data_ptr(), out.data_ptr() + 8, _stream_handle(stream, k.device)),
+                             out.data_ptr(), out.data_ptr() + 8,
+                             None if work is None else work.data_ptr(),
+                             _stream_handle(stream, k.device)),
            "kv_absmax_inv")
     return out

@@ -351,14 +351,16 @@ extern "C" kv_status kv_store_fp8_ex(const void* k, const void* v, void* k_cache
                                      kv_error_record* d_err, kv_stream_t stream_) {
   if (format != KV_FP8_E4M3FN && format != KV_FP8_E5M2) return KV_ERR_INVALID_ARG;
   if (scale_mode != KV_SCALE_NONE && scale_mode != KV_SCALE_TENSOR && scale_mode != KV_SCALE_TOKEN &&
-      scale_mode != KV_SCALE_TOKEN_HEAD)
+      scale_mode != KV_SCALE_TOKEN_HEAD && scale_mode != KV_SCALE_PAGE)
     return KV_ERR_INVALID_ARG;
   const int fmt = format == KV_FP8_E5M2 ? kFmtE5M2 : kFmtE4M3;
-  if (scale_mode == KV_SCALE_NONE || scale_mode == KV_SCALE_TENSOR)
+  if (scale_mode == KV_SCALE_PAGE && page_size < 1) return KV_ERR_INVALID_ARG;
+  if (scale_mode == KV_SCALE_NONE || scale_mode == KV_SCALE_TENSOR || scale_mode == KV_SCALE_PAGE)
     return store_fp8_static(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_tokens,
                             num_heads, head_dim, src_dtype, s, page_size, kc_page_stride,
                             vc_page_stride, size_limit, inv_k_scale, inv_v_scale,
-                            scale_mode == KV_SCALE_TENSOR ? 1 : 0, fmt, d_err, stream_);
+                            scale_mode == KV_SCALE_NONE ? 0 : 1,
+                            scale_mode == KV_SCALE_PAGE ? page_size : 0, fmt, d_err, stream_);
 
   // dynamic scales
   if (num_tokens < 0) return KV_ERR_INVALID_ARG;

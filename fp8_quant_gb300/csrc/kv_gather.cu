@@ -25,7 +25,7 @@ struct GatherSide {
   uint8_t* out;          // element (0, 0, 0) of the token-major output
   int64_t cache_slot, cache_seg, cache_page;
   int64_t out_token, out_seg;
-  const float* scale;    // fp8, per-tensor mode: device scalar
+  const float* scale;    // fp8, per-tensor mode: device scalar; per-page mode: one per page
   const float* scales;   // fp8, per-token / per-head modes: per-slot scale cache
 };
 
@@ -38,7 +38,7 @@ struct GatherParams {
   int vec;          // cache bytes per chunk
   int prefetch;     // cache rows are 16-byte aligned: speculative L2 prefetch allowed
   int scale_mode;   // fp8: kv_scale_mode (per-head mode: one head per unit segment)
-  int64_t scales_stride;
+  int64_t scales_stride;  // per-slot modes: floats per slot; per-page mode: the page size
   uint64_t ahead;   // > 0: also prefetch the cache rows of unit u + ahead (set by launch_rows)
 };
 
@@ -49,6 +49,7 @@ __device__ __forceinline__ float unit_scale(const GatherParams& p, const GatherS
     case KV_SCALE_TENSOR: return __ldg(sd.scale);
     case KV_SCALE_TOKEN: return __ldg(sd.scales + slot * p.scales_stride);
     case KV_SCALE_TOKEN_HEAD: return __ldg(sd.scales + slot * p.scales_stride + seg);
+    case KV_SCALE_PAGE: return __ldg(sd.scale + slot / p.scales_stride);
     default: return 1.0f;
   }
 }
@@ -355,6 +356,8 @@ __global__ void __launch_bounds__(kThreads) kv_gather_elements(const __grid_cons
       else if (p.scale_mode == KV_SCALE_TOKEN) scale = __ldg(p.scales[kv] + slot * p.scales_stride);
       else if (p.scale_mode == KV_SCALE_TOKEN_HEAD)
         scale = __ldg(p.scales[kv] + slot * p.scales_stride + h);
+      else if (p.scale_mode == KV_SCALE_PAGE)
+        scale = __ldg(p.scale[kv] + slot / p.scales_stride);
     }
     for (int64_t d = lane; d < p.head_dim; d += 32) {
       const uint8_t* s = src + d * p.cache_dim[kv];
@@ -599,9 +602,10 @@ kv_status gather_fp8(const void* k_cache, const void* v_cache, void* k_out, void
     return KV_ERR_INVALID_ARG;
   if (out_dtype != KV_SRC_F16 && out_dtype != KV_SRC_BF16) return KV_ERR_INVALID_ARG;
   if (page_size < 1) return KV_ERR_INVALID_ARG;
-  if (scale_mode == KV_SCALE_TENSOR &&
+  if ((scale_mode == KV_SCALE_TENSOR || scale_mode == KV_SCALE_PAGE) &&
       (!k_scale || !v_scale || ((u64(k_scale) | u64(v_scale)) & 3u) != 0))
     return KV_ERR_INVALID_ARG;
+  if (scale_mode == KV_SCALE_PAGE) scales_stride = page_size;  // the scale index is slot / page_size
   const bool per_slot = scale_mode == KV_SCALE_TOKEN || scale_mode == KV_SCALE_TOKEN_HEAD;
   if (per_slot && (!k_scales || !v_scales || ((u64(k_scales) | u64(v_scales)) & 3u) != 0 ||
                    scales_stride < (scale_mode == KV_SCALE_TOKEN_HEAD ? num_heads : 1)))
@@ -619,8 +623,9 @@ kv_status gather_fp8(const void* k_cache, const void* v_cache, void* k_out, void
     const kv_status cs = classify_inputs(in, 5, &on_device);
     if (cs != KV_OK) return cs;
   }
-  const float* sk = scale_mode == KV_SCALE_TENSOR ? k_scale : nullptr;
-  const float* sv = scale_mode == KV_SCALE_TENSOR ? v_scale : nullptr;
+  const bool one_scale_ptr = scale_mode == KV_SCALE_TENSOR || scale_mode == KV_SCALE_PAGE;
+  const float* sk = one_scale_ptr ? k_scale : nullptr;
+  const float* sv = one_scale_ptr ? v_scale : nullptr;
   const bool flat = kc_page_stride == page_size * s->kc_slot && vc_page_stride == page_size * s->vc_slot;
   const bool contiguous = s->k_dim == 2 && s->v_dim == 2 && s->kc_dim == 1 && s->vc_dim == 1;
 
@@ -724,7 +729,7 @@ extern "C" kv_status kv_gather_fp8_ex(const void* k_cache, const void* v_cache, 
                                       kv_error_record* d_err, kv_stream_t stream) {
   if (format != KV_FP8_E4M3FN && format != KV_FP8_E5M2) return KV_ERR_INVALID_ARG;
   if (scale_mode != KV_SCALE_NONE && scale_mode != KV_SCALE_TENSOR && scale_mode != KV_SCALE_TOKEN &&
-      scale_mode != KV_SCALE_TOKEN_HEAD)
+      scale_mode != KV_SCALE_TOKEN_HEAD && scale_mode != KV_SCALE_PAGE)
     return KV_ERR_INVALID_ARG;
   return gather_fp8(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
                     num_tokens, num_heads, head_dim, out_dtype, s, page_size, kc_page_stride,

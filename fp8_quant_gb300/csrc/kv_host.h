@@ -22,7 +22,8 @@ kv_status cuda_fail(cudaError_t e);
 // kernels may prefetch inputs into L2 with bulk copies.
 kv_status classify_inputs(const void* const* ptrs, int n, bool* all_device);
 
-// The FP8 write with a per-tensor inverse scale (or none) in format fmt
+// The FP8 write with a per-tensor inverse scale (or none), or one inverse
+// scale per page of scale_page slots (scale_page > 0), in format fmt
 // (kFmtE4M3 / kFmtE5M2): kv_store_fp8 and the static modes of kv_store_fp8_ex.
 kv_status store_fp8_static(const void* k, const void* v, void* k_cache, void* v_cache,
                            const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
@@ -30,7 +31,8 @@ kv_status store_fp8_static(const void* k, const void* v, void* k_cache, void* v_
                            kv_src_dtype src_dtype, const kv_strides* s, int64_t page_size,
                            int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
                            const float* inv_k_scale, const float* inv_v_scale, int32_t use_scale,
-                           int fmt, kv_error_record* d_err, kv_stream_t stream);
+                           int64_t scale_page, int fmt, kv_error_record* d_err,
+                           kv_stream_t stream);
 kv_status current_sm_count(int* out);
 kv_status blocks_per_sm(const void* fn, int threads, int* out);
 
@@ -42,11 +44,12 @@ inline int launch_threads(uint64_t num_units) {
 }
 
 // Grid: enough CTAs for every unit to have a warp, capped at the resident
-// capacity (a whole number of CTAs per SM); warps loop over the rest.
+// capacity (a whole number of CTAs per SM) and at max_ctas; warps loop over
+// the rest.  threads_override > 0 fixes the CTA size.
 template <typename Params>
 kv_status launch(void (*kernel)(Params), uint64_t num_units, const Params& params,
-                 cudaStream_t stream, uint64_t max_ctas = 0) {
-  const int threads = launch_threads(num_units);
+                 cudaStream_t stream, uint64_t max_ctas = 0, int threads_override = 0) {
+  const int threads = threads_override > 0 ? threads_override : launch_threads(num_units);
   const uint64_t warps = static_cast<uint64_t>(threads / 32);
   int sms = 0, per_sm = 0;
   kv_status st = current_sm_count(&sms);

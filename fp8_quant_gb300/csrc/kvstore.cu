@@ -240,6 +240,7 @@ struct Fp8Params {
   Fp8Side side[2];
   const void* indices;
   int64_t index_stride, size_limit, page_size;
+  int64_t scale_page;  // 0: side.inv is one scalar; > 0: one inverse scale per page of this size
   UnitShape shape;
   kv_error_record* err;
   int prefetch;  // sources are 16-byte aligned: prefetch them into L2 before the grid wait
@@ -267,7 +268,7 @@ __device__ __forceinline__ void fp8_unit(const Fp8Params& p, const Unit& w, uint
   for (int i = 0; i < NS; ++i) {
     const Fp8Side& sd = p.side[NS == 2 ? i : w.kv];
     src[i] = fp8_src(p, sd, w);
-    inv[i] = sd.inv != nullptr ? __ldg(sd.inv) : 1.0f;
+    inv[i] = sd.inv != nullptr && p.scale_page == 0 ? __ldg(sd.inv) : 1.0f;
   }
   Fp8Chunk<OUT> buf[NS][U];
 #pragma unroll
@@ -280,6 +281,11 @@ __device__ __forceinline__ void fp8_unit(const Fp8Params& p, const Unit& w, uint
   if (slot < 0 || slot >= p.size_limit) {
     if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
     return;
+  }
+  if (p.scale_page != 0) {  // per-page inverse scales: the slot's page picks the scale
+    const int64_t page = slot / p.scale_page;
+#pragma unroll
+    for (int i = 0; i < NS; ++i) inv[i] = __ldg(p.side[NS == 2 ? i : w.kv].inv + page);
   }
   uint8_t* dst[NS];
 #pragma unroll
@@ -349,6 +355,7 @@ struct GenericFp8Params {
   const float* inv[2];
   const void* indices;
   int64_t index_stride, size_limit, page_size;
+  int64_t scale_page;  // as Fp8Params::scale_page
   uint64_t num_units;
   int32_t num_heads, head_dim;
   kv_error_record* err;
@@ -371,7 +378,9 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_elements(const __grid_constan
       if (r == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(t));
       continue;
     }
-    const float inv = p.inv[kv] != nullptr ? __ldg(p.inv[kv]) : 1.0f;
+    const float inv = p.inv[kv] == nullptr ? 1.0f
+                      : p.scale_page != 0 ? __ldg(p.inv[kv] + slot / p.scale_page)
+                                          : __ldg(p.inv[kv]);
     const uint8_t* src = p.src[kv] + t * p.src_token[kv] + h * p.src_head[kv];
     uint8_t* dst = p.dst[kv] + paged_offset(slot, p.page_size, p.dst_page[kv], p.dst_slot[kv]) +
                    h * p.dst_head[kv];
@@ -667,7 +676,9 @@ extern "C" kv_status kv_store_paged(const void* k, const void* v, void* k_cache,
 }
 
 // kv_store_fp8, and the static scale modes of kv_store_fp8_ex: one inverse
-// scale per tensor (or none), output format fmt (kFmtE4M3 / kFmtE5M2).
+// scale per tensor (or none), or with scale_page > 0 one inverse scale per
+// cache page (index slot / scale_page); output format fmt (kFmtE4M3 /
+// kFmtE5M2).
 kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, void* v_cache,
                                    const void* indices, kv_index_dtype index_dtype,
                                    int64_t index_stride, int64_t num_tokens, int32_t num_heads,
@@ -675,8 +686,8 @@ kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, 
                                    int64_t page_size, int64_t kc_page_stride,
                                    int64_t vc_page_stride, int64_t size_limit,
                                    const float* inv_k_scale, const float* inv_v_scale,
-                                   int32_t use_scale, int fmt, kv_error_record* d_err,
-                                   kv_stream_t stream_) {
+                                   int32_t use_scale, int64_t scale_page, int fmt,
+                                   kv_error_record* d_err, kv_stream_t stream_) {
   if (num_tokens < 0) return KV_ERR_INVALID_ARG;
   if (num_tokens == 0) return KV_OK;
   if (!common_args_ok(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_heads,
@@ -686,6 +697,7 @@ kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, 
   if (page_size < 1) return KV_ERR_INVALID_ARG;
   if (use_scale && (!inv_k_scale || !inv_v_scale)) return KV_ERR_INVALID_ARG;
   if (use_scale && ((u64(inv_k_scale) | u64(inv_v_scale)) & 3u) != 0) return KV_ERR_INVALID_ARG;
+  if (scale_page < 0 || (scale_page != 0 && !use_scale)) return KV_ERR_INVALID_ARG;
   const uint64_t src_bits = u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token) | u64(s->k_head) |
                             u64(s->v_head) | u64(s->k_dim) | u64(s->v_dim);
   if ((src_bits & 1u) != 0) return KV_ERR_INVALID_ARG;
@@ -740,6 +752,7 @@ kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, 
     g.page_size = flat ? 1 : page_size;
     g.inv[0] = inv_k;
     g.inv[1] = inv_v;
+    g.scale_page = scale_page;
     g.indices = indices;
     g.index_stride = index_stride;
     g.size_limit = size_limit;
@@ -767,6 +780,7 @@ kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, 
   p.index_stride = index_stride;
   p.size_limit = size_limit;
   p.page_size = flat ? 1 : page_size;
+  p.scale_page = scale_page;
   p.shape.parts = parts;
   p.shape.units_per_side = sg.count * parts;
   p.shape.units_per_token = 2u * p.shape.units_per_side;
@@ -789,7 +803,7 @@ extern "C" kv_status kv_store_fp8(const void* k, const void* v, void* k_cache, v
                                   kv_error_record* d_err, kv_stream_t stream) {
   return store_fp8_static(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_tokens,
                           num_heads, head_dim, src_dtype, s, page_size, kc_page_stride,
-                          vc_page_stride, size_limit, inv_k_scale, inv_v_scale, use_scale,
+                          vc_page_stride, size_limit, inv_k_scale, inv_v_scale, use_scale, 0,
                           kFmtE4M3, d_err, stream);
 }
 

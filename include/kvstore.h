@@ -252,7 +252,8 @@ typedef enum kv_scale_mode {
     KV_SCALE_NONE = 0,        /* values converted unscaled */
     KV_SCALE_TENSOR = 1,      /* one fp32 scale per tensor, a device scalar */
     KV_SCALE_TOKEN = 2,       /* one scale per token row (all heads), computed per call */
-    KV_SCALE_TOKEN_HEAD = 3   /* one scale per (token, head), computed per call */
+    KV_SCALE_TOKEN_HEAD = 3,  /* one scale per (token, head), computed per call */
+    KV_SCALE_PAGE = 4         /* one fp32 scale per cache page, supplied by the caller */
 } kv_scale_mode;
 
 /*
@@ -279,6 +280,14 @@ typedef enum kv_scale_mode {
  *                multiplier) at k_scales[slot * scales_slot_stride + g],
  *                g = head (TOKEN_HEAD) or 0 (TOKEN); likewise V.  The scale
  *                caches are device float arrays indexed by slot, not by page.
+ *                KV_SCALE_PAGE: inv_k_scale / inv_v_scale point to device
+ *                arrays of fp32 INVERSE scales, one per cache page; the
+ *                token written to slot s uses inv[s / page_size] in place of
+ *                the per-tensor scalar (codes of fl32(x * inv[s / page_size])).
+ *                The arrays must hold ceil(size_limit / page_size) floats.
+ *                The fused FP8 write's module docstring names per-page scales
+ *                and its kernel has none; the page is the one its kernel
+ *                computes, slot // page_size.  Any layout kv_store_fp8 takes.
  *   k_scales,
  *   v_scales,
  *   scales_slot_stride   used by the dynamic modes only: non-NULL, 4-byte
@@ -302,8 +311,9 @@ kv_status kv_store_fp8_ex(const void *k, const void *v, void *k_cache, void *v_c
  * codes of `format` decoded exactly, multiplied by the scale of `scale_mode`
  * (NONE: none; TENSOR: *k_scale / *v_scale, the forward scales; TOKEN /
  * TOKEN_HEAD: k_scales[slot * scales_slot_stride + g] as written by
- * kv_store_fp8_ex), rounded to bf16 / fp16.  kv_gather_fp8 is this call
- * with KV_FP8_E4M3FN and NONE / TENSOR.
+ * kv_store_fp8_ex; PAGE: k_scale[slot / page_size] / v_scale[...], device
+ * arrays of forward scales, one per cache page), rounded to bf16 / fp16.
+ * kv_gather_fp8 is this call with KV_FP8_E4M3FN and NONE / TENSOR.
  */
 kv_status kv_gather_fp8_ex(const void *k_cache, const void *v_cache, void *k_out, void *v_out,
                            const void *indices, kv_index_dtype index_dtype, int64_t index_stride,
@@ -335,14 +345,22 @@ kv_status kv_inv_scale(const float *scale, float *inv, int64_t n, kv_stream_t st
  *   k, v       bf16 / fp16 rows (src_dtype); strides->k_* and v_* are used
  *              (dims must be contiguous: k_dim = v_dim = 2; else
  *              KV_ERR_UNSUPPORTED).
- *   amax, inv  device pointers to two floats each, written by the call
- *              (cleared first by a kernel on `stream`).
+ *   amax, inv  device pointers to two floats each, written by the call.
+ *   work       NULL, or a device workspace of KV_ABSMAX_WORK_BYTES (4-byte
+ *              aligned) owned by the caller: zero before its first use (e.g.
+ *              cudaMemsetAsync), and left zero by every call that completes.
+ *              With it a call is two kernels (reduce, finish); without it,
+ *              three (amax is cleared by a kernel first and serves as the
+ *              accumulator).  Calls that share one workspace must not
+ *              overlap on the GPU (their maxima would mix); calls on one
+ *              stream never do.
  * fp8_max must be positive and finite.
  */
+#define KV_ABSMAX_WORK_BYTES 8
 kv_status kv_absmax_inv(const void *k, const void *v, kv_src_dtype src_dtype,
                         int64_t num_tokens, int32_t num_heads, int32_t head_dim,
                         const kv_strides *strides, float fp8_max, float *amax, float *inv,
-                        kv_stream_t stream);
+                        uint32_t *work, kv_stream_t stream);
 
 /*
  * kv_store_noalloc -- kv_store for callers that cannot allocate device memory.

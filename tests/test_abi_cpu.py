@@ -139,3 +139,39 @@ def test_valid_calls_need_a_gpu(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         kv.load_library(str(tmp_path / "nope.so"))
+
+
+def store8ex(**over):
+    a = dict(k=A, v=A, k_cache=A, v_cache=A, indices=A, index_dtype=1, index_stride=1,
+             num_tokens=16, num_heads=8, head_dim=128, src_dtype=1, strides=S8, page_size=16,
+             kc_page_stride=16 * 2048, vc_page_stride=16 * 2048, size_limit=100, fmt=0,
+             scale_mode=4, inv_k_scale=A, inv_v_scale=A, k_scales=None, v_scales=None,
+             scales_slot_stride=0, d_err=A, stream=None)
+    a.update(over)
+    return kv.raw.kv_store_fp8_ex(**a)
+
+
+def gather8ex(**over):
+    a = dict(k_cache=A, v_cache=A, k_out=A, v_out=A, indices=A, index_dtype=1, index_stride=1,
+             num_tokens=16, num_heads=8, head_dim=128, out_dtype=1, strides=S8, page_size=16,
+             kc_page_stride=16 * 2048, vc_page_stride=16 * 2048, size_limit=100, fmt=0,
+             scale_mode=4, k_scale=A, v_scale=A, k_scales=None, v_scales=None,
+             scales_slot_stride=0, d_err=A, stream=None)
+    a.update(over)
+    return kv.raw.kv_gather_fp8_ex(**a)
+
+
+@pytest.mark.parametrize("over", [
+    dict(inv_k_scale=None), dict(inv_v_scale=None), dict(inv_k_scale=A + 2), dict(page_size=0),
+    dict(scale_mode=5), dict(scale_mode=-1), dict(fmt=2),
+])
+def test_per_page_scale_mode_rejects_bad_arguments(lib, over):
+    assert store8ex(**over) == INVALID
+    g = {("k_scale" if k == "inv_k_scale" else "v_scale" if k == "inv_v_scale" else k): x
+         for k, x in over.items()}
+    assert gather8ex(**g) == INVALID
+
+
+def test_per_page_scale_mode_valid_calls_need_a_gpu(lib):
+    assert store8ex() == CUDA
+    assert gather8ex() == CUDA

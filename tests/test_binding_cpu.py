@@ -161,3 +161,7 @@ def test_scale_wrappers(monkeypatch):
     kv.kv_absmax_inv(k, k)
     name, a = cap.calls[-1]
     assert name == "kv_absmax_inv" and a[2:6] == (1, 7, 2, 16) and a[7] == 448.0
+    assert a[10] is None
+    w = torch.zeros(2, dtype=torch.int32)
+    kv.kv_absmax_inv(k, k, work=w)
+    assert cap.calls[-1][1][10] == w.data_ptr()

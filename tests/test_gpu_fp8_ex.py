@@ -1,7 +1,8 @@
 """GPU parity of the extended FP8 write and gather (kv_store_fp8_ex,
 kv_gather_fp8_ex) against the CPU oracle: e4m3fn and e5m2 caches; no scale,
 per-tensor scales, and scales computed per token row or per (token, head),
-whose per-slot scale caches are compared too. Layouts: contiguous rows (the
+whose per-slot scale caches are compared too, and caller-supplied scales
+per cache page. Layouts: contiguous rows (the
 row-layout kernel, one side or K and V paired per warp), head-segmented
 rows, padded 4-D pages, odd head dims (narrow chunks), groups longer than a
 warp holds in registers (two-pass), both index types and out-of-range
@@ -19,7 +20,19 @@ from kvcheck import SENT8, filled, fp8_problem
 
 pytestmark = pytest.mark.gpu
 
-MODES = {"none": 0, "tensor": 1, "token": 2, "token_head": 3}
+MODES = {"none": 0, "tensor": 1, "token": 2, "token_head": 3, "page": 4}
+
+
+def page_inverse_scales(p, seed):
+    """Per-page inverse scales around the problem's per-tensor ones: from a
+    quarter of it (codes well inside the range) to 16 times it (outliers and
+    large values saturate)."""
+    n_pages = -(-p.size_limit // p.page_size)
+    out = []
+    for j, inv in enumerate((p.inv_k, p.inv_v)):
+        u = wl.uniform01(seed + j, n_pages)
+        out.append((np.float32(inv) * (2.0 ** np.floor(u * 7 - 2))).astype(np.float32))
+    return out
 FMTS = {"e4m3fn": 0, "e5m2": 1}
 
 
@@ -49,13 +62,19 @@ def run_store(p, fmt, mode, sstride=None, host=False):
     ks = torch.full((n * sstride,), -1.0, dtype=torch.float32, device=dev)
     vs = ks.clone()
     inv = torch.tensor([p.inv_k, p.inv_v], dtype=torch.float32, device=dev)
+    pages = page_inverse_scales(p, zlib.crc32(fmt.encode()) % 997) if mode == "page" else None
+    if pages is not None:
+        pk, pv = (torch.from_numpy(a).to(dev) for a in pages)
+        inv_k_ptr, inv_v_ptr = pk.data_ptr(), pv.data_ptr()
+    else:
+        inv_k_ptr, inv_v_ptr = inv.data_ptr(), inv.data_ptr() + 4
     err = torch.zeros(2, dtype=torch.int64, device=dev)
     s = torch.cuda.current_stream().cuda_stream
     rc = kv.raw.kv_store_fp8_ex(
         k.data_ptr() + p.k_view.offset, v.data_ptr() + p.v_view.offset, kc.data_ptr(),
         vc.data_ptr(), idx.data_ptr(), 1 if p.indices.dtype == np.int64 else 0, p.index_stride,
         p.T, p.H, p.D, 1 if p.src_dtype == "bf16" else 0, p.strides(), p.page_size, p.kc_page,
-        p.vc_page, n, FMTS[fmt], MODES[mode], inv.data_ptr(), inv.data_ptr() + 4,
+        p.vc_page, n, FMTS[fmt], MODES[mode], inv_k_ptr, inv_v_ptr,
         ks.data_ptr(), vs.data_ptr(), sstride, err.data_ptr(), s)
     assert rc == 0, kv.kv_status_str(rc)
     prc, pn, pfirst = kv.raw.kv_error_poll(err.data_ptr(), s)
@@ -67,7 +86,9 @@ def run_store(p, fmt, mode, sstride=None, host=False):
     st = oracle.Strides(**dict(zip(oracle.Strides.FIELDS, p.strides())))
     res = oracle.store_fp8_ex(p.k_src, p.v_src, okc, ovc, p.indices, st, p.H, p.D, p.src_dtype,
                               p.page_size, p.kc_page, p.vc_page, n, fmt=fmt, scale_mode=mode,
-                              inv_k=p.inv_k, inv_v=p.inv_v, k_scales=oks, v_scales=ovs,
+                              inv_k=p.inv_k, inv_v=p.inv_v,
+                              k_scales=oks if pages is None else pages[0],
+                              v_scales=ovs if pages is None else pages[1],
                               scales_slot_stride=sstride, k_off=p.k_view.offset,
                               v_off=p.v_view.offset, index_stride=p.index_stride, t_end=p.T)
     for got, want, what in ((kc, okc, "K"), (vc, ovc, "V")):
@@ -79,7 +100,7 @@ def run_store(p, fmt, mode, sstride=None, host=False):
     assert np.array_equal(ks.cpu().numpy().view(np.uint32), oks.view(np.uint32))
     assert np.array_equal(vs.cpu().numpy().view(np.uint32), ovs.view(np.uint32))
     assert (pn, pfirst) == res and prc == (4 if res[0] else 0)
-    return kc, vc, ks, vs
+    return kc, vc, ks, vs, pages
 
 
 CASES = {
@@ -158,7 +179,10 @@ def test_dynamic_exhaustive_input_patterns(src, fmt, mode, tokens):
     run_store(p, fmt, mode)
 
 
-def _gather(kc, vc, p, fmt, mode, ks=None, vs=None, sstride=1, out="bf16", scale=(1.0, 1.0)):
+def _gather(kc, vc, p, fmt, mode, ks=None, vs=None, sstride=1, out="bf16", scale=(1.0, 1.0),
+            pages=None):
+    """kv_gather_fp8_ex on the GPU against the oracle.  pages: per-page forward
+    scales (K, V) for the per-page mode."""
     import torch
     import fp8_quant_gb300 as kv
     dev = torch.device("cuda")
@@ -167,6 +191,11 @@ def _gather(kc, vc, p, fmt, mode, ks=None, vs=None, sstride=1, out="bf16", scale
     ko = torch.zeros(T * R, dtype=torch.uint8, device=dev)
     vo = torch.zeros_like(ko)
     sc = torch.tensor(scale, dtype=torch.float32, device=dev)
+    if pages is not None:
+        gk, gv = (torch.from_numpy(a).to(dev) for a in pages)
+        sk_ptr, sv_ptr = gk.data_ptr(), gv.data_ptr()
+    else:
+        sk_ptr, sv_ptr = sc.data_ptr(), sc.data_ptr() + 4
     err = torch.zeros(2, dtype=torch.int64, device=dev)
     strides = (R, D * 2, 2, R, D * 2, 2) + p.strides()[6:]
     s = torch.cuda.current_stream().cuda_stream
@@ -174,7 +203,7 @@ def _gather(kc, vc, p, fmt, mode, ks=None, vs=None, sstride=1, out="bf16", scale
         kc.data_ptr(), vc.data_ptr(), ko.data_ptr(), vo.data_ptr(),
         torch.from_numpy(p.indices).to(dev).data_ptr(), 1 if p.indices.dtype == np.int64 else 0,
         p.index_stride, T, H, D, 1 if out == "bf16" else 0, strides, p.page_size, p.kc_page,
-        p.vc_page, p.size_limit, FMTS[fmt], MODES[mode], sc.data_ptr(), sc.data_ptr() + 4,
+        p.vc_page, p.size_limit, FMTS[fmt], MODES[mode], sk_ptr, sv_ptr,
         None if ks is None else ks.data_ptr(), None if vs is None else vs.data_ptr(), sstride,
         err.data_ptr(), s)
     assert rc == 0, kv.kv_status_str(rc)
@@ -185,8 +214,10 @@ def _gather(kc, vc, p, fmt, mode, ks=None, vs=None, sstride=1, out="bf16", scale
     oracle.gather_fp8_ex(kc.cpu().numpy(), vc.cpu().numpy(), ok, ov, p.indices, st, H, D, out,
                          p.page_size, p.kc_page, p.vc_page, p.size_limit, fmt=fmt,
                          scale_mode=mode, scale_k=scale[0], scale_v=scale[1],
-                         k_scales=None if ks is None else ks.cpu().numpy(),
-                         v_scales=None if vs is None else vs.cpu().numpy(),
+                         k_scales=pages[0] if pages is not None else
+                         None if ks is None else ks.cpu().numpy(),
+                         v_scales=pages[1] if pages is not None else
+                         None if vs is None else vs.cpu().numpy(),
                          scales_slot_stride=sstride, index_stride=p.index_stride, t_end=T)
     assert np.array_equal(ko.cpu().numpy(), ok) and np.array_equal(vo.cpu().numpy(), ov)
 
@@ -196,11 +227,12 @@ def _gather(kc, vc, p, fmt, mode, ks=None, vs=None, sstride=1, out="bf16", scale
 @pytest.mark.parametrize("out", ["bf16", "f16"])
 def test_store_then_gather_fp8_ex(fmt, mode, out):
     p = fp8_problem(T=600, H=8, D=128, n_slots=2048, seed=73, page_size=16, page_pad=128)
-    kc, vc, ks, vs = run_store(p, fmt, mode)
+    kc, vc, ks, vs, pages = run_store(p, fmt, mode)
     G = p.H if mode == "token_head" else 1
     scale = (1.0 / p.inv_k, 1.0 / p.inv_v)
+    fwd = None if pages is None else [(np.float32(1.0) / a).astype(np.float32) for a in pages]
     _gather(kc, vc, p, fmt, mode, ks if mode in ("token", "token_head") else None,
-            vs if mode in ("token", "token_head") else None, G, out, scale)
+            vs if mode in ("token", "token_head") else None, G, out, scale, pages=fwd)
 
 
 @pytest.mark.parametrize("fmt", sorted(FMTS))
@@ -219,3 +251,33 @@ def test_gather_fp8_ex_every_code(fmt):
     vs = torch.from_numpy(sc[::-1].copy()).to(dev)
     _gather(kc, vc, p, fmt, "token_head", ks, vs, H, "bf16")
     _gather(kc, vc, p, fmt, "token_head", ks, vs, H, "f16")
+
+
+@pytest.mark.parametrize("tokens", [300, 3000])
+def test_store_fp8_ex_per_page_oob_and_host_inputs(tokens):
+    """Per-page scales with out-of-range slots (skipped before the scale load:
+    no read past the scale arrays) and with K, V and slot ids in pinned host
+    memory; one side per warp and paired."""
+    p = fp8_problem(T=tokens, H=8, D=128, n_slots=8192, seed=81, page_size=16)
+    p.indices[[1, tokens // 2, tokens - 1]] = [-1, 8192, 2 ** 40]
+    run_store(p, "e4m3fn", "page")
+    q = fp8_problem(T=tokens, H=8, D=128, n_slots=8192, seed=82, page_size=16)
+    run_store(q, "e5m2", "page", host=True)
+
+
+@pytest.mark.parametrize("fmt", sorted(FMTS))
+def test_gather_fp8_ex_per_page_every_code(fmt):
+    """Random caches (every code) through the dequantising gather with one
+    random forward scale per page, paged layout with padding, both outputs."""
+    import torch
+    T, H, D, n = 3000, 8, 128, 8192
+    p = fp8_problem(T=T, H=H, D=D, n_slots=n, seed=83, page_size=32, page_pad=512)
+    dev = torch.device("cuda")
+    raw = wl.splitmix64(84, 0, p.cache_bytes // 8 + 1).view(np.uint8)[:p.cache_bytes].copy()
+    kc = torch.from_numpy(raw).to(dev)
+    vc = torch.from_numpy(raw[::-1].copy()).to(dev)
+    n_pages = -(-n // p.page_size)
+    fk = (wl.uniform01(85, n_pages) * 4 + 0.01).astype(np.float32)
+    fv = (wl.uniform01(86, n_pages) * 8 + 0.5).astype(np.float32)
+    _gather(kc, vc, p, fmt, "page", out="bf16", pages=(fk, fv))
+    _gather(kc, vc, p, fmt, "page", out="f16", pages=(fk, fv))

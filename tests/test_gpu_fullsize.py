@@ -237,3 +237,43 @@ def test_full_size_dynamic_fp8(name):
         assert int((scales != -1.0).sum().item()) == T * H
     del pool
     torch.cuda.empty_cache()
+
+
+def test_full_size_per_page_scales():
+    """The fp8 batch with one inverse scale per 32-slot page (32,768 pages):
+    every written row equals the oracle's, nothing else changed.  The oracle
+    runs on a compact cache (slot j for token j, pages of one slot) whose
+    scale j is the scale of token j's real page, which leaves every code
+    unchanged."""
+    import torch
+    import bench
+    import fp8_quant_gb300 as kv
+    dev = torch.device("cuda", 0)
+    pool = bench.Pool("fp8_page", dev, pool_bytes=0)
+    w = pool.w
+    assert pool.num_batches == 1 and w.page_stride == w.page_size * w.slot_stride
+    assert pool.call(0, torch.cuda.current_stream().cuda_stream) == 0
+    assert kv.kv_error_poll(pool.err) == (kv.KVStatus.OK, 0, -1)
+    T, sb = w.T, w.slot_stride
+    idx = np.arange(T, dtype=w.indices.dtype)
+    page = w.indices.astype(np.int64) // w.page_size
+    ck = w.notes["page_inv_k"][page].copy()
+    cv = w.notes["page_inv_v"][page].copy()
+    okc = np.full(T * sb, w.sentinel, np.uint8)
+    ovc = okc.copy()
+    st = oracle.Strides(k_token=w.k_view[1], k_head=w.k_view[2], k_dim=w.k_view[3],
+                        v_token=w.v_view[1], v_head=w.v_view[2], v_dim=w.v_view[3],
+                        kc_slot=sb, kc_head=w.cache_head_stride, kc_dim=1,
+                        vc_slot=sb, vc_head=w.cache_head_stride, vc_dim=1)
+    k = np.ascontiguousarray(w.k).view(np.uint8).reshape(-1)
+    v = np.ascontiguousarray(w.v).view(np.uint8).reshape(-1)
+    assert oracle.store_fp8_ex(k, v, okc, ovc, idx, st, w.H, w.D, w.src_dtype, 1, sb, sb, T,
+                               fmt="e4m3fn", scale_mode="page", k_scales=ck,
+                               v_scales=cv) == (0, -1)
+    slots = torch.from_numpy(w.indices.astype(np.int64)).to(dev)
+    for cache, want, what in ((pool.kc, okc, "K"), (pool.vc, ovc, "V")):
+        rows = cache.view(w.n_slots, sb).index_select(0, slots).cpu().numpy().reshape(-1)
+        assert np.array_equal(rows, want), f"{what} cache rows differ"
+        assert _rows_changed(torch, cache, w.n_slots, sb, bytes([w.sentinel])) == T
+    del pool
+    torch.cuda.empty_cache()

@@ -67,14 +67,21 @@ def _absmax_case(T, H, D, src, seed, head_pad=0, nan_at=(), inf_at=(), zero=Fals
     want_amax, want_inv = oracle.absmax_inv(buf[0].copy(), buf[1].copy(), st, T, H, D, src,
                                             fp8_max)
     dbuf = torch.from_numpy(buf).pin_memory() if host else torch.from_numpy(buf).cuda()
-    out = torch.full((4,), 123.0, dtype=torch.float32, device="cuda")
-    rc = kv.raw.kv_absmax_inv(dbuf[0].data_ptr(), dbuf[1].data_ptr(), 1 if src == "bf16" else 0,
-                              T, H, D, tuple(int(x) for x in st.values), fp8_max,
-                              out.data_ptr(), out.data_ptr() + 8, _stream())
-    assert rc == 0, kv.kv_status_str(rc)
-    got = out.cpu().numpy()
-    assert np.array_equal(got[:2].view(np.uint32), want_amax.view(np.uint32)), (got, want_amax)
-    assert np.array_equal(got[2:].view(np.uint32), want_inv.view(np.uint32)), (got, want_inv)
+    # without a workspace (three kernels) and with one (two kernels; the
+    # workspace is zero before the call and zero again after it)
+    work = torch.zeros(2, dtype=torch.int32, device="cuda")
+    for use_work in (False, True):
+        out = torch.full((4,), 123.0, dtype=torch.float32, device="cuda")
+        rc = kv.raw.kv_absmax_inv(dbuf[0].data_ptr(), dbuf[1].data_ptr(),
+                                  1 if src == "bf16" else 0, T, H, D,
+                                  tuple(int(x) for x in st.values), fp8_max, out.data_ptr(),
+                                  out.data_ptr() + 8, work.data_ptr() if use_work else None,
+                                  _stream())
+        assert rc == 0, kv.kv_status_str(rc)
+        got = out.cpu().numpy()
+        assert np.array_equal(got[:2].view(np.uint32), want_amax.view(np.uint32)), (got, want_amax)
+        assert np.array_equal(got[2:].view(np.uint32), want_inv.view(np.uint32)), (got, want_inv)
+        assert work.cpu().tolist() == [0, 0]
     return w, got
 
 
@@ -105,7 +112,7 @@ def test_absmax_inv_host_rows():
     out = torch.full((4,), 123.0, dtype=torch.float32, device="cuda")
     st = (256, 128, 2, 256, 128, 2) + (0,) * 6
     rc = kv.raw.kv_absmax_inv(rows.ctypes.data, rows.ctypes.data + 64 * 256, 1, 64, 2, 64, st,
-                              448.0, out.data_ptr(), out.data_ptr() + 8, _stream())
+                              448.0, out.data_ptr(), out.data_ptr() + 8, None, _stream())
     assert rc == kv.KVStatus.ERR_INVALID_ARG
     assert out.cpu().tolist() == [123.0] * 4
 
@@ -132,8 +139,10 @@ def test_two_pass_dynamic_per_tensor_write():
     scal = torch.empty(4, dtype=torch.float32, device=dev)
     R = H * D * 2
     strides = (R, D * 2, 2, R, D * 2, 2, H * D, D, 1, H * D, D, 1)
+    work = torch.zeros(2, dtype=torch.int32, device=dev)
     assert kv.raw.kv_absmax_inv(k.data_ptr(), v.data_ptr(), 1, T, H, D, strides, 448.0,
-                                scal.data_ptr(), scal.data_ptr() + 8, _stream()) == 0
+                                scal.data_ptr(), scal.data_ptr() + 8, work.data_ptr(),
+                                _stream()) == 0
     kv.kv_store_fp8(k, v, kc, vc, idx, page_size=ps, inv_k_scale=scal[2:3],
                     inv_v_scale=scal[3:4])
     st = oracle.Strides(k_token=R, k_head=D * 2, k_dim=2, v_token=R, v_head=D * 2, v_dim=2,
@@ -154,9 +163,47 @@ def test_scale_argument_errors():
     assert kv.raw.kv_inv_scale(None, None, -1, s) == kv.KVStatus.ERR_INVALID_ARG
     assert kv.raw.kv_inv_scale(0x1002, 0x2000, 4, s) == kv.KVStatus.ERR_INVALID_ARG
     st = (256, 128, 2, 256, 128, 2) + (0,) * 6
-    assert kv.raw.kv_absmax_inv(0x1000, 0x1000, 1, 4, 2, 64, st, 0.0, 0x3000, 0x3008,
+    assert kv.raw.kv_absmax_inv(0x1000, 0x1000, 1, 4, 2, 64, st, 0.0, 0x3000, 0x3008, None,
                                 s) == kv.KVStatus.ERR_INVALID_ARG
     assert kv.raw.kv_absmax_inv(0x1000, 0x1000, 1, 4, 2, 64, st[:2] + (4,) + st[3:], 448.0,
-                                0x3000, 0x3008, s) == kv.KVStatus.ERR_UNSUPPORTED
-    assert kv.raw.kv_absmax_inv(0x1000, 0x1000, 5, 4, 2, 64, z, 448.0, 0x3000, 0x3008,
+                                0x3000, 0x3008, None, s) == kv.KVStatus.ERR_UNSUPPORTED
+    assert kv.raw.kv_absmax_inv(0x1000, 0x1000, 5, 4, 2, 64, z, 448.0, 0x3000, 0x3008, None,
                                 s) == kv.KVStatus.ERR_INVALID_ARG
+    assert kv.raw.kv_absmax_inv(0x1000, 0x1000, 1, 4, 2, 64, st, 448.0, 0x3000, 0x3008, 0x4002,
+                                s) == kv.KVStatus.ERR_INVALID_ARG
+
+
+def test_absmax_workspace_back_to_back_calls():
+    """Calls sharing one workspace on a stream, back to back and from a CUDA
+    graph: each call's result is its own tensors' (no maximum carried over from
+    the previous call, whose values are larger), and the workspace ends zero."""
+    import torch
+    import fp8_quant_gb300 as kv
+    dev = torch.device("cuda")
+    T, H, D = 3000, 8, 128
+    xs = [torch.randn(T, H, D, device=dev).to(torch.bfloat16) * (8.0 / (i + 1)) for i in range(4)]
+    work = torch.zeros(2, dtype=torch.int32, device=dev)
+    outs = [torch.zeros(4, dtype=torch.float32, device=dev) for _ in range(4)]
+    R = H * D * 2
+    strides = (R, D * 2, 2, R, D * 2, 2) + (0,) * 6
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(4):
+            assert kv.raw.kv_absmax_inv(xs[i].data_ptr(), xs[3 - i].data_ptr(), 1, T, H, D,
+                                        strides, 448.0, outs[i].data_ptr(),
+                                        outs[i].data_ptr() + 8, work.data_ptr(),
+                                        s.cuda_stream) == 0
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        for o in outs:
+            o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for i in range(4):
+            a = np.array([xs[i].float().abs().max().item(), xs[3 - i].float().abs().max().item()],
+                         np.float32)
+            got = outs[i].cpu().numpy()
+            assert np.array_equal(got[:2], a) and np.array_equal(got[2:], np.float32(448.0) / a)
+        assert work.cpu().tolist() == [0, 0]

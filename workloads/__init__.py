@@ -32,6 +32,7 @@ measured on; ``T`` tokens, ``H`` KV heads, ``D`` head dim):
                kernel and stored per slot (``fp8_dynamic_token``: one scale
                per token row).
 * ``fp8_e5m2`` the fp8 batch into an e5m2 cache, per-tensor scales 57344/amax.
+* ``fp8_page`` the fp8 batch with one inverse scale per 32-slot cache page.
 
 The gather workloads read these caches back (``gather_decode``,
 ``gather_prefill``, ``gather_fp8``), and ``absmax`` reads the fp8 batch once.
@@ -183,6 +184,8 @@ class Workload:
         out_row = self.H * self.D * self.cache_elem
         groups = self.H if self.notes.get("scale_mode", "token_head") == "token_head" else 1
         scales = 2 * groups * 4 if self.kind == "fp8_dyn" else 0
+        if self.notes.get("scale_mode") == "page":
+            scales = 2 * 4          # the page's inverse scale, K and V
         return self.T * (2 * self.row_bytes + 2 * out_row + self.indices.itemsize + scales)
 
 
@@ -336,6 +339,21 @@ def fp8_e5m2(n_slots: int = 1 << 20) -> Workload:
     return w
 
 
+def fp8_page(n_slots: int = 1 << 20) -> Workload:
+    """The ``fp8`` batch written with one inverse scale per 32-slot cache page
+    (scale mode "page"): page p of the K cache has inv_k * 2**e_p with e_p
+    drawn from {-3, -2, -1, 0} (likewise V), so every page's scale keeps the
+    batch's values within the e4m3fn range except the saturating outliers."""
+    w = fp8(n_slots=n_slots)
+    w.name = "fp8_page"
+    w.notes["scale_mode"] = "page"
+    n_pages = -(-n_slots // w.page_size)
+    for j, inv in ((0, w.inv_k), (1, w.inv_v)):
+        e = np.floor(uniform01(0x5EED0006 + j, n_pages) * 4) - 3
+        w.notes["page_inv_" + "kv"[j]] = (np.float32(inv) * (2.0 ** e)).astype(np.float32)
+    return w
+
+
 def odd(n_slots: int = 1 << 21) -> Workload:
     """fp16 H=1, D=576 rows (1152 B) into 1280-byte slots."""
     return make_copy("odd", T=65536, H=1, D=576, n_slots=n_slots, seed=0x5EED0005,
@@ -382,6 +400,7 @@ WORKLOADS = {
     "fp8_dynamic": fp8_dynamic,
     "fp8_dynamic_token": fp8_dynamic_token,
     "fp8_e5m2": fp8_e5m2,
+    "fp8_page": fp8_page,
     "gather_decode": gather_decode,
     "gather_prefill": gather_prefill,
     "gather_fp8": gather_fp8,
