@@ -193,6 +193,75 @@ __device__ __forceinline__ void record_oob(kv_error_record* err, uint64_t t) {
             static_cast<unsigned long long>(~t));
 }
 
+// Bit 63 of oob_count: a kernel stopped waiting on its own asynchronous
+// copies after its iteration limit (never expected; the call's output is then
+// undefined).  kv_error_poll reports it as KV_ERR_DEVICE_TIMEOUT.
+constexpr unsigned long long kTimeoutBit = 1ull << 63;
+
+__device__ __forceinline__ void record_timeout(kv_error_record* err) {
+  atomicOr(reinterpret_cast<unsigned long long*>(&err->oob_count), kTimeoutBit);
+}
+
+// ---------------------------------------------------------------------------
+// Bulk asynchronous copies into shared memory, completed on mbarriers.
+// ---------------------------------------------------------------------------
+
+// Polls of an mbarrier before a wait gives up (each poll may suspend the
+// thread for a while); far beyond any copy's latency.
+constexpr uint32_t kWaitPolls = 1u << 24;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// One arrival that also announces `bytes` of copies completing on the barrier.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Waits until the phase of parity `parity` has completed; false after
+// kWaitPolls polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kWaitPolls; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// `bytes` (a multiple of 16, both addresses 16-byte aligned) from global to
+// shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void lds16(uint32_t (&w)[4], uint32_t addr) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "r"(addr));
+}
+
 // Unit u -> (token, K|V, segment, part).
 struct UnitShape {
   uint64_t num_units;        // num_tokens * units_per_token

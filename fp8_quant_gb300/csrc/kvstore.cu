@@ -820,10 +820,13 @@ extern "C" kv_status kv_error_poll(kv_error_record* d_err, kv_stream_t stream_, 
   if (e != cudaSuccess) return cuda_fail(e);
   e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (oob_count) *oob_count = static_cast<int64_t>(h.oob_count);
+  const bool timed_out = (h.oob_count & kTimeoutBit) != 0;
+  const uint64_t skipped = h.oob_count & ~kTimeoutBit;
+  if (oob_count) *oob_count = static_cast<int64_t>(skipped);
   if (first_bad_token)
-    *first_bad_token = h.oob_count ? static_cast<int64_t>(~h.first_bad_key) : int64_t{-1};
-  return h.oob_count ? KV_ERR_INDEX_OOB : KV_OK;
+    *first_bad_token = skipped ? static_cast<int64_t>(~h.first_bad_key) : int64_t{-1};
+  if (timed_out) return KV_ERR_DEVICE_TIMEOUT;
+  return skipped ? KV_ERR_INDEX_OOB : KV_OK;
 }
 
 namespace kvimpl {
@@ -898,6 +901,7 @@ extern "C" const char* kv_status_str(kv_status status) {
     case KV_ERR_UNSUPPORTED: return "KV_ERR_UNSUPPORTED";
     case KV_ERR_CUDA: return "KV_ERR_CUDA";
     case KV_ERR_INDEX_OOB: return "KV_ERR_INDEX_OOB";
+    case KV_ERR_DEVICE_TIMEOUT: return "KV_ERR_DEVICE_TIMEOUT";
   }
   return "KV_STATUS_UNKNOWN";
 }
@@ -1006,7 +1010,9 @@ extern "C" kv_status kv_store_noalloc(const void* k, const void* v, void* k_cach
   if (e != cudaSuccess) return cuda_fail(e);
   e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (oob_count) *oob_count = static_cast<int64_t>(h.oob_count);
-  if (first_bad_token && h.oob_count) *first_bad_token = static_cast<int64_t>(~h.first_bad_key);
-  return h.oob_count ? KV_ERR_INDEX_OOB : KV_OK;
+  const uint64_t skipped = h.oob_count & ~kTimeoutBit;
+  if (oob_count) *oob_count = static_cast<int64_t>(skipped);
+  if (first_bad_token && skipped) *first_bad_token = static_cast<int64_t>(~h.first_bad_key);
+  if (h.oob_count & kTimeoutBit) return KV_ERR_DEVICE_TIMEOUT;
+  return skipped ? KV_ERR_INDEX_OOB : KV_OK;
 }
