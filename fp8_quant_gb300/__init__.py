@@ -44,7 +44,6 @@ class KVStatus(enum.IntEnum):
     ERR_UNSUPPORTED = 2
     ERR_CUDA = 3
     ERR_INDEX_OOB = 4
-    ERR_DEVICE_TIMEOUT = 5
 
 
 class KVError(RuntimeError):

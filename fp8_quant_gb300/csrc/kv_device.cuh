@@ -50,6 +50,9 @@
 #ifndef KV_PREFETCH
 #define KV_PREFETCH 1           // L2 prefetch of the unit's source bytes before the grid wait
 #endif
+#ifndef KV_PACKED_MATH
+#define KV_PACKED_MATH 1        // packed sm_100 arithmetic: f32x2 products, bf16x2/f16x2 maxima
+#endif
 
 namespace kvimpl {
 
@@ -185,81 +188,30 @@ __device__ __forceinline__ int64_t load_slot(const void* indices, int64_t stride
   return static_cast<int64_t>(__ldg(static_cast<const IdxT*>(indices) + t * stride));
 }
 
+// Slot id read before the programmatic-launch wait, at L2 only (no L1 line
+// is filled, so the authoritative load after the wait cannot hit a stale
+// copy).  The previous grid may still be writing it: the value is used only
+// to aim an L2 prefetch, never to address a load or a store.
+template <typename IdxT>
+__device__ __forceinline__ int64_t speculative_slot(const void* indices, int64_t stride, int64_t t) {
+  const IdxT* p = static_cast<const IdxT*>(indices) + t * stride;
+  if constexpr (sizeof(IdxT) == 8) {
+    long long v;
+    asm volatile("ld.global.cg.s64 %0, [%1];" : "=l"(v) : "l"(p));
+    return static_cast<int64_t>(v);
+  } else {
+    int v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return static_cast<int64_t>(v);
+  }
+}
+
 // One record per skipped token: a count and the lowest skipped token (kept as
 // its bitwise NOT so that a zeroed record means "none").
 __device__ __forceinline__ void record_oob(kv_error_record* err, uint64_t t) {
   atomicAdd(reinterpret_cast<unsigned long long*>(&err->oob_count), 1ull);
   atomicMax(reinterpret_cast<unsigned long long*>(&err->first_bad_key),
             static_cast<unsigned long long>(~t));
-}
-
-// Bit 63 of oob_count: a kernel stopped waiting on its own asynchronous
-// copies after its iteration limit (never expected; the call's output is then
-// undefined).  kv_error_poll reports it as KV_ERR_DEVICE_TIMEOUT.
-constexpr unsigned long long kTimeoutBit = 1ull << 63;
-
-__device__ __forceinline__ void record_timeout(kv_error_record* err) {
-  atomicOr(reinterpret_cast<unsigned long long*>(&err->oob_count), kTimeoutBit);
-}
-
-// ---------------------------------------------------------------------------
-// Bulk asynchronous copies into shared memory, completed on mbarriers.
-// ---------------------------------------------------------------------------
-
-// Polls of an mbarrier before a wait gives up (each poll may suspend the
-// thread for a while); far beyond any copy's latency.
-constexpr uint32_t kWaitPolls = 1u << 24;
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-// One arrival that also announces `bytes` of copies completing on the barrier.
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Waits until the phase of parity `parity` has completed; false after
-// kWaitPolls polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kWaitPolls; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred q;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-// `bytes` (a multiple of 16, both addresses 16-byte aligned) from global to
-// shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void lds16(uint32_t (&w)[4], uint32_t addr) {
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-               : "r"(addr));
 }
 
 // Unit u -> (token, K|V, segment, part).
@@ -324,10 +276,52 @@ __device__ __forceinline__ float2 widen2(uint32_t w) {
   }
 }
 
+// x * s for both lanes of x: two IEEE fp32 products, round to nearest,
+// subnormals kept -- with KV_PACKED_MATH one packed sm_100 instruction
+// (mul.rn.f32x2) instead of two.
+__device__ __forceinline__ float2 mul2_rn(float2 x, float s) {
+#if KV_PACKED_MATH
+  float2 r;
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %4};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(x.x), "f"(x.y), "f"(s));
+  return r;
+#else
+  return make_float2(__fmul_rn(x.x, s), __fmul_rn(x.y, s));
+#endif
+}
+
 template <bool kBF16, int FMT = kFmtE4M3>
 __device__ __forceinline__ uint32_t quant2(uint32_t w, float inv) {
-  const float2 x = widen2<kBF16>(w);
-  return fp8x2<FMT>(__fmul_rn(x.x, inv), __fmul_rn(x.y, inv));
+  const float2 y = mul2_rn(widen2<kBF16>(w), inv);
+  return fp8x2<FMT>(y.x, y.y);
+}
+
+// Running maximum of |x| over packed pairs of 2-byte floats, lane by lane,
+// in one instruction per pair: max.xorsign.abs keeps the larger magnitude
+// (the sign bit is the XOR of the operands' signs, cleared when the value is
+// read), and a NaN operand yields the other one, so NaN elements never win.
+// Start from m = 0.
+template <bool kBF16>
+__device__ __forceinline__ uint32_t absmax_pair(uint32_t m, uint32_t w) {
+  uint32_t r;
+  if constexpr (kBF16) {
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(w));
+  } else {
+    asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(w));
+  }
+  return r;
+}
+
+// The larger magnitude of a running pair maximum, as fp32 (exact).
+template <bool kBF16>
+__device__ __forceinline__ float absmax_pair_value(uint32_t m) {
+  const float2 x = widen2<kBF16>(m);
+  return fmaxf(fabsf(x.x), fabsf(x.y));
 }
 
 // One lane's chunk: OUT output bytes from OUT 2-byte inputs.

@@ -17,23 +17,12 @@
 // programmatic-launch wait.
 #include "kv_host.h"
 
-#ifndef KV_DYN_STAGED
-#define KV_DYN_STAGED 1              // staged (shared-memory ring) form of the row-layout write
-#endif
-#ifndef KV_DYN_CONSUMERS
-#define KV_DYN_CONSUMERS 8           // consumer warps per CTA of the staged form
-#endif
-#ifndef KV_DYN_CTAS_PER_SM
-#define KV_DYN_CTAS_PER_SM 2
-#endif
-#ifndef KV_DYN_STAGE_BYTES
-#define KV_DYN_STAGE_BYTES (96 * 1024)  // shared memory for the stages of one CTA
+#ifndef KV_DYN_LOOKAHEAD
+#define KV_DYN_LOOKAHEAD 1   // multi-wave row launches: prefetch the unit one resident wave ahead
 #endif
 
 namespace kvimpl {
 namespace {
-
-constexpr uint32_t kDynMaxStages = 64;
 
 struct DynSide {
   const uint8_t* src;
@@ -76,11 +65,18 @@ __device__ __forceinline__ DynUnit dyn_unit(const DynParams& p, uint64_t u) {
 template <int CH, bool kBF16>
 __device__ __forceinline__ float chunk_absmax(float m, const Chunk<2 * CH>& c) {
   if constexpr (CH >= 2) {
+#if KV_PACKED_MATH
+    uint32_t pm = 0;
+#pragma unroll
+    for (int i = 0; i < CH / 2; ++i) pm = absmax_pair<kBF16>(pm, c.w[i]);
+    m = fmaxf(m, absmax_pair_value<kBF16>(pm));
+#else
 #pragma unroll
     for (int i = 0; i < CH / 2; ++i) {
       const float2 x = widen2<kBF16>(c.w[i]);
       m = fmaxf(m, fmaxf(fabsf(x.x), fabsf(x.y)));
     }
+#endif
   } else {
     const float2 x = widen2<kBF16>(static_cast<uint32_t>(c.h));
     m = fmaxf(m, fabsf(x.x));
@@ -204,6 +200,7 @@ struct DynRowParams {
   float fmax;
   kv_error_record* err;
   int prefetch;             // rows in device memory: bulk L2 prefetch allowed
+  uint64_t ahead;           // > 0: also prefetch the rows of unit u + ahead (set by launch_rows)
 };
 
 template <int J, int NS, typename IdxT, bool kBF16, int FMT>
@@ -237,6 +234,17 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant
         const uint32_t c = lane + 32u * j;
         if (c < n) ld_stream(buf[i][j], src + static_cast<size_t>(c) * 32u);
       }
+    }
+    // the unit that takes this warp's place one resident wave later: its rows
+    // go to L2 while this unit's reduction waits on its loads
+    if (KV_DYN_LOOKAHEAD && p.ahead != 0 && lane == 0 && u + p.ahead < p.shape.num_units) {
+      const Unit nx = decode_unit(p.shape, u + p.ahead);
+#pragma unroll
+      for (int i = 0; i < NS; ++i) {
+        const DynSide& sd = p.side[NS == 2 ? i : nx.kv];
+        prefetch_l2_bulk(sd.src + nx.token * sd.src_token, n * 32u);
+      }
+      prefetch_l2_line(static_cast<const IdxT*>(p.indices) + nx.token * p.index_stride);
     }
     float a[NS][J];
 #pragma unroll
@@ -307,11 +315,11 @@ kv_status launch_dyn_row_j(bool bf16, const DynRowParams& p, cudaStream_t stream
     q.shape.units_per_token = 1;
     q.shape.units_per_side = 1;
     q.shape.num_units /= 2;
-    if (bf16) return launch(kv_fp8_dyn_row<J, 2, IdxT, true, FMT>, q.shape.num_units, q, stream);
-    return launch(kv_fp8_dyn_row<J, 2, IdxT, false, FMT>, q.shape.num_units, q, stream);
+    if (bf16) return launch_rows(kv_fp8_dyn_row<J, 2, IdxT, true, FMT>, q.shape.num_units, q, stream);
+    return launch_rows(kv_fp8_dyn_row<J, 2, IdxT, false, FMT>, q.shape.num_units, q, stream);
   }
-  if (bf16) return launch(kv_fp8_dyn_row<J, 1, IdxT, true, FMT>, p.shape.num_units, p, stream);
-  return launch(kv_fp8_dyn_row<J, 1, IdxT, false, FMT>, p.shape.num_units, p, stream);
+  if (bf16) return launch_rows(kv_fp8_dyn_row<J, 1, IdxT, true, FMT>, p.shape.num_units, p, stream);
+  return launch_rows(kv_fp8_dyn_row<J, 1, IdxT, false, FMT>, p.shape.num_units, p, stream);
 }
 
 template <typename IdxT, int FMT>
@@ -325,242 +333,6 @@ template <typename IdxT>
 kv_status launch_dyn_row(int j, int fmt, bool bf16, const DynRowParams& p, cudaStream_t stream) {
   if (fmt == kFmtE5M2) return launch_dyn_row_fmt<IdxT, kFmtE5M2>(j, bf16, p, stream);
   return launch_dyn_row_fmt<IdxT, kFmtE4M3>(j, bf16, p, stream);
-}
-
-// ---------------------------------------------------------------------------
-// Staged form of the row-layout dynamic write (device-resident inputs, rows a
-// multiple of 512 bytes).  The whole row must be in hand before any code can
-// be formed, and a warp that holds its rows in registers has nothing to do
-// while they arrive.  Here one producer thread per CTA streams the K and V
-// rows of the CTA's tokens into a ring of shared-memory stages with bulk
-// asynchronous copies (one mbarrier per stage carries the byte count), so the
-// loads of later tokens are in flight while consumer warps reduce, convert
-// and store earlier ones; a consumer frees its stage by arriving on the
-// stage's second mbarrier.  Lane l of a consumer takes the 16-byte pieces l,
-// l+32, ... of each row: a scale group (a head of D elements: D/8 pieces, or
-// the whole row) is an aligned run of lanes in one 32-piece slab, or whole
-// slabs.  Every wait is bounded; a wait that gives up sets the timeout bit of
-// the error record, and the CTA then waits (bounded) for the copies it
-// issued before it exits.
-// ---------------------------------------------------------------------------
-struct StagedParams {
-  DynSide side[2];
-  const void* indices;
-  int64_t index_stride, size_limit, page_size, scales_stride;
-  int64_t num_tokens;
-  uint32_t row_bytes;     // R: a multiple of 512
-  uint32_t group_pieces;  // 16-byte pieces per scale group: D / 8, or R / 16 (whole row)
-  uint32_t stages;        // ring depth (each stage holds one token's K and V rows)
-  float fmax;
-  kv_error_record* err;
-  int prefetch;           // L2 prefetch of the first tokens before the grid wait
-};
-
-template <int P, typename IdxT, bool kBF16, int FMT>  // P: pieces per lane and row (R / 512)
-__global__ void __launch_bounds__(32 * (KV_DYN_CONSUMERS + 1))
-    kv_fp8_dyn_staged(const __grid_constant__ StagedParams p) {
-  extern __shared__ __align__(128) uint8_t stage_mem[];
-  __shared__ uint32_t issued[kDynMaxStages];  // copies issued per stage
-  __shared__ int aborted;
-  const uint32_t S = p.stages;
-  const uint32_t R = p.row_bytes;
-  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
-  const uint64_t G = gridDim.x;
-  const int64_t nk = p.num_tokens > static_cast<int64_t>(blockIdx.x)
-                         ? (p.num_tokens - 1 - static_cast<int64_t>(blockIdx.x)) / static_cast<int64_t>(G) + 1
-                         : 0;  // tokens of this CTA: blockIdx.x + k * G
-  const uint32_t data0 = smem_addr(stage_mem);
-  const uint32_t full0 = data0 + S * 2u * R;  // full[s]: the stage's rows have landed
-  const uint32_t empty0 = full0 + 8u * S;     // empty[s]: its consumer is done with it
-  if (threadIdx.x == 0) {
-    for (uint32_t s = 0; s < S; ++s) {
-      mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, 1);
-      issued[s] = 0;
-    }
-    aborted = 0;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // inits seen by the copy engine
-  }
-  if (KV_PREFETCH && p.prefetch && warp == 0) {
-    for (int64_t k = lane; k < nk && k < static_cast<int64_t>(S); k += 32) {
-      const int64_t t = static_cast<int64_t>(blockIdx.x) + k * static_cast<int64_t>(G);
-      prefetch_l2_bulk(p.side[0].src + t * p.side[0].src_token, R);
-      prefetch_l2_bulk(p.side[1].src + t * p.side[1].src_token, R);
-    }
-  }
-  __syncthreads();
-  grid_handover();
-
-  if (warp == 0) {
-    if (lane == 0) {  // producer
-      for (int64_t k = 0; k < nk; ++k) {
-        const uint32_t s = static_cast<uint32_t>(k % S);
-        const uint32_t n = static_cast<uint32_t>(k / S);
-        if (n > 0 && !mbar_wait(empty0 + 8u * s, (n - 1u) & 1u)) {
-          record_timeout(p.err);
-          atomicExch(&aborted, 1);
-          break;
-        }
-        if (*reinterpret_cast<volatile int*>(&aborted)) break;
-        const int64_t t = static_cast<int64_t>(blockIdx.x) + k * static_cast<int64_t>(G);
-        const uint32_t buf = data0 + s * 2u * R;
-        mbar_expect_tx(full0 + 8u * s, 2u * R);
-        bulk_load(buf, p.side[0].src + t * p.side[0].src_token, R, full0 + 8u * s);
-        bulk_load(buf + R, p.side[1].src + t * p.side[1].src_token, R, full0 + 8u * s);
-        issued[s] = n + 1u;
-      }
-    }
-  } else {  // consumers
-    const uint32_t gp = p.group_pieces;
-    const uint32_t gpr = 32u * P / gp;        // scale groups per row
-    const uint32_t my_g = lane < 2u * gpr ? lane : 0u;  // the group this lane divides for
-    const uint32_t my_i = my_g / gpr;                   // its side
-    const uint32_t my_q0 = (my_g - my_i * gpr) * gp;    // its first piece
-    for (int64_t k = warp - 1; k < nk; k += KV_DYN_CONSUMERS) {
-      const uint32_t s = static_cast<uint32_t>(k % S);
-      const uint32_t n = static_cast<uint32_t>(k / S);
-      const int64_t t = static_cast<int64_t>(blockIdx.x) + k * static_cast<int64_t>(G);
-      const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, t);
-      if (!mbar_wait(full0 + 8u * s, n & 1u)) {
-        if (lane == 0) {
-          record_timeout(p.err);
-          atomicExch(&aborted, 1);
-        }
-        break;
-      }
-      const uint32_t buf = data0 + s * 2u * R;
-      uint32_t x[2][P][4];
-      float a[2][P];
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-          lds16(x[i][j], buf + static_cast<uint32_t>(i) * R + (lane + 32u * j) * 16u);
-          float m = 0.0f;
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const float2 v = widen2<kBF16>(x[i][j][w]);
-            m = fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
-          }
-          a[i][j] = m;
-        }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8u * s);  // the rows are in registers: free the stage
-      // group maxima: a run of gp lanes inside a slab, or whole slabs
-      if (gp < 32u) {
-        for (uint32_t o = 1; o < gp; o <<= 1)
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < P; ++j) a[i][j] = fmaxf(a[i][j], __shfl_xor_sync(0xFFFFFFFFu, a[i][j], o));
-      } else {
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-          for (int j = 0; j < P; ++j)
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) a[i][j] = fmaxf(a[i][j], __shfl_xor_sync(0xFFFFFFFFu, a[i][j], o));
-        const uint32_t slabs = gp / 32u;  // slabs per group (a power of two dividing P)
-#pragma unroll
-        for (int e = 1; e < P; e <<= 1) {  // xor steps stay inside aligned blocks of `slabs`
-          if (static_cast<uint32_t>(e) >= slabs) break;
-          float b[2][P];
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < P; ++j) b[i][j] = fmaxf(a[i][j], a[i][j ^ e]);
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < P; ++j) a[i][j] = b[i][j];
-        }
-      }
-      // lane g divides for group g: its maximum sits in slab my_q0 / 32 at lane my_q0 % 32
-      float amax_g = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-          const float v = __shfl_sync(0xFFFFFFFFu, a[i][j], my_q0 % 32u);
-          if (my_i == static_cast<uint32_t>(i) && my_q0 / 32u == static_cast<uint32_t>(j)) amax_g = v;
-        }
-      const bool pos = amax_g > 0.0f;
-      const float inv_g = pos ? __fdiv_rn(p.fmax, amax_g) : 1.0f;
-      if (slot < 0 || slot >= p.size_limit) {
-        if (lane == 0) record_oob(p.err, static_cast<uint64_t>(t));
-        continue;
-      }
-      if (lane < 2u * gpr)
-        p.side[my_i].scales[slot * p.scales_stride + (my_g - my_i * gpr)] =
-            pos ? __fdiv_rn(amax_g, p.fmax) : 1.0f;
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const DynSide& sd = p.side[i];
-        uint8_t* dst = sd.dst + paged_offset(slot, p.page_size, sd.dst_page, sd.dst_slot);
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-          const uint32_t q = lane + 32u * j;
-          const float inv = __shfl_sync(0xFFFFFFFFu, inv_g, static_cast<uint32_t>(i) * gpr + q / gp);
-          Chunk<8> o;
-          o.w[0] = quant2<kBF16, FMT>(x[i][j][0], inv) | (quant2<kBF16, FMT>(x[i][j][1], inv) << 16);
-          o.w[1] = quant2<kBF16, FMT>(x[i][j][2], inv) | (quant2<kBF16, FMT>(x[i][j][3], inv) << 16);
-          st_stream(dst + static_cast<size_t>(q) * 8u, o);
-        }
-      }
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && aborted) {
-    // a wait gave up: do not exit while a copy into this CTA's shared memory
-    // may still be in flight (bounded as well)
-    for (uint32_t s = 0; s < S; ++s)
-      if (issued[s] > 0) (void)mbar_wait(full0 + 8u * s, (issued[s] - 1u) & 1u);
-  }
-  if (!KV_EARLY_TRIGGER) grid_dependents_launch();
-}
-
-template <int P, typename IdxT, int FMT>
-kv_status launch_dyn_staged_p(bool bf16, const StagedParams& p, cudaStream_t stream) {
-  void (*kernel)(StagedParams) = bf16 ? kv_fp8_dyn_staged<P, IdxT, true, FMT>
-                                      : kv_fp8_dyn_staged<P, IdxT, false, FMT>;
-  const size_t smem = static_cast<size_t>(p.stages) * 2u * p.row_bytes + 16u * p.stages;
-  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel),
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return cuda_fail(e);
-  int sms = 0;
-  kv_status st = current_sm_count(&sms);
-  if (st != KV_OK) return st;
-  int64_t grid = static_cast<int64_t>(sms) * KV_DYN_CTAS_PER_SM;
-  if (grid > p.num_tokens) grid = p.num_tokens;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(32u * (KV_DYN_CONSUMERS + 1), 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kernel, p);
-  if (e != cudaSuccess) return cuda_fail(e);
-  return KV_OK;
-}
-
-template <typename IdxT, int FMT>
-kv_status launch_dyn_staged_fmt(int pieces, bool bf16, const StagedParams& p, cudaStream_t stream) {
-  switch (pieces) {
-    case 1: return launch_dyn_staged_p<1, IdxT, FMT>(bf16, p, stream);
-    case 2: return launch_dyn_staged_p<2, IdxT, FMT>(bf16, p, stream);
-    default: return launch_dyn_staged_p<4, IdxT, FMT>(bf16, p, stream);
-  }
-}
-
-template <typename IdxT>
-kv_status launch_dyn_staged(int pieces, int fmt, bool bf16, const StagedParams& p, cudaStream_t stream) {
-  if (fmt == kFmtE5M2) return launch_dyn_staged_fmt<IdxT, kFmtE5M2>(pieces, bf16, p, stream);
-  return launch_dyn_staged_fmt<IdxT, kFmtE4M3>(pieces, bf16, p, stream);
 }
 
 template <int CH, typename IdxT, int FMT>
@@ -654,43 +426,6 @@ extern "C" kv_status kv_store_fp8_ex(const void* k, const void* v, void* k_cache
     const bool groups_ok = !per_head || (head_dim % 16 == 0 && gch <= 32 && (gch & (gch - 1)) == 0 &&
                                          2 * num_heads <= 32);
     const int64_t chunks = row / 16;
-    // staged form: input rows of 512, 1024 or 2048 bytes in device memory,
-    // 16-byte aligned; groups of a power-of-two number of pieces that split a
-    // row into at most 16 groups
-    const int64_t rb = 2 * row;  // input row bytes
-    const int64_t gpieces = per_head ? head_dim / 8 : rb / 16;
-    const bool staged_ok = KV_DYN_STAGED && on_device && contiguous &&
-                           (rb == 512 || rb == 1024 || rb == 2048) &&
-                           (in_bits & 15u) == 0 && (out_bits & 7u) == 0 &&
-                           (!per_head || (head_dim % 8 == 0 && (gpieces & (gpieces - 1)) == 0 &&
-                                          rb / 16 / gpieces <= 16));
-    if (staged_ok) {
-      StagedParams q = {};
-      q.side[0] = DynSide{static_cast<const uint8_t*>(k), static_cast<uint8_t*>(k_cache),
-                          s->k_token, s->k_head, s->kc_slot, s->kc_head,
-                          flat ? s->kc_slot : kc_page_stride, k_scales};
-      q.side[1] = DynSide{static_cast<const uint8_t*>(v), static_cast<uint8_t*>(v_cache),
-                          s->v_token, s->v_head, s->vc_slot, s->vc_head,
-                          flat ? s->vc_slot : vc_page_stride, v_scales};
-      q.indices = indices;
-      q.index_stride = index_stride;
-      q.size_limit = size_limit;
-      q.page_size = flat ? 1 : page_size;
-      q.scales_stride = scales_slot_stride;
-      q.num_tokens = num_tokens;
-      q.row_bytes = static_cast<uint32_t>(rb);
-      q.group_pieces = static_cast<uint32_t>(gpieces);
-      int64_t stages = KV_DYN_STAGE_BYTES / (2 * rb);
-      if (stages > static_cast<int64_t>(kDynMaxStages)) stages = kDynMaxStages;
-      if (stages < 2) stages = 2;
-      q.stages = static_cast<uint32_t>(stages);
-      q.fmax = fmt == kFmtE5M2 ? 57344.0f : 448.0f;
-      q.err = d_err;
-      q.prefetch = 1;
-      const int pieces = static_cast<int>(rb / 512);
-      return index_dtype == KV_INDEX_I64 ? launch_dyn_staged<int64_t>(pieces, fmt, bf16, q, stream)
-                                         : launch_dyn_staged<int32_t>(pieces, fmt, bf16, q, stream);
-    }
     if (contiguous && row % 16 == 0 && chunks <= 128 && (in_bits & 31u) == 0 &&
         (out_bits & 15u) == 0 && groups_ok) {
       DynRowParams p = {};

@@ -55,24 +55,6 @@ __device__ __forceinline__ float unit_scale(const GatherParams& p, const GatherS
 }
 
 
-// Slot id read before the programmatic-launch wait, at L2 only (no L1 line
-// is filled, so the authoritative load after the wait cannot hit a stale
-// copy).  The previous grid may still be writing it: the value is used only
-// to aim an L2 prefetch, never to address a load or a store.
-template <typename IdxT>
-__device__ __forceinline__ int64_t speculative_slot(const void* indices, int64_t stride, int64_t t) {
-  const IdxT* p = static_cast<const IdxT*>(indices) + t * stride;
-  if constexpr (sizeof(IdxT) == 8) {
-    long long v;
-    asm volatile("ld.global.cg.s64 %0, [%1];" : "=l"(v) : "l"(p));
-    return static_cast<int64_t>(v);
-  } else {
-    int v;
-    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
-    return static_cast<int64_t>(v);
-  }
-}
-
 __device__ __forceinline__ int64_t gather_slot_offset(const GatherParams& p, const GatherSide& sd,
                                                       int64_t slot) {
   if (p.page_size == 1) return slot * sd.cache_page;
@@ -222,8 +204,10 @@ template <bool kBF16, int FMT>
 __device__ __forceinline__ void dequant4(uint32_t codes, float scale, uint32_t& o0, uint32_t& o1) {
   const float2 a = fp8x2_to_f32x2<FMT>(codes & 0xFFFFu);
   const float2 b = fp8x2_to_f32x2<FMT>(codes >> 16);
-  o0 = narrow2<kBF16>(__fmul_rn(a.x, scale), __fmul_rn(a.y, scale));
-  o1 = narrow2<kBF16>(__fmul_rn(b.x, scale), __fmul_rn(b.y, scale));
+  const float2 ya = mul2_rn(a, scale);
+  const float2 yb = mul2_rn(b, scale);
+  o0 = narrow2<kBF16>(ya.x, ya.y);
+  o1 = narrow2<kBF16>(yb.x, yb.y);
 }
 
 // IN cache bytes (codes) per lane chunk -> 2*IN output bytes; NS as in

@@ -146,8 +146,15 @@ __global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant
           const uint32_t c = c0 + lane + 32u * j;
           if (src[i] == nullptr || c >= nchunks) continue;
           if constexpr (VEC >= 4) {
+#if KV_PACKED_MATH
+            uint32_t pm = 0;
+#pragma unroll
+            for (int q = 0; q < VEC / 4; ++q) pm = absmax_pair<kBF16>(pm, ch[i][j].w[q]);
+            acc[i] = fmaxf(acc[i], absmax_pair_value<kBF16>(pm));
+#else
 #pragma unroll
             for (int q = 0; q < VEC / 4; ++q) acc[i] = absmax2<kBF16>(acc[i], ch[i][j].w[q]);
+#endif
           } else {
             acc[i] = absmax2<kBF16>(acc[i], static_cast<uint32_t>(ch[i][j].h));  // upper element is 0
           }

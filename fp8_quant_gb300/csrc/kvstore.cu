@@ -241,6 +241,7 @@ struct Fp8Params {
   const void* indices;
   int64_t index_stride, size_limit, page_size;
   int64_t scale_page;  // 0: side.inv is one scalar; > 0: one inverse scale per page of this size
+  int scale_page_shift;  // log2(scale_page) when it is a power of two, else -1
   UnitShape shape;
   kv_error_record* err;
   int prefetch;  // sources are 16-byte aligned: prefetch them into L2 before the grid wait
@@ -283,7 +284,7 @@ __device__ __forceinline__ void fp8_unit(const Fp8Params& p, const Unit& w, uint
     return;
   }
   if (p.scale_page != 0) {  // per-page inverse scales: the slot's page picks the scale
-    const int64_t page = slot / p.scale_page;
+    const int64_t page = p.scale_page_shift >= 0 ? slot >> p.scale_page_shift : slot / p.scale_page;
 #pragma unroll
     for (int i = 0; i < NS; ++i) inv[i] = __ldg(p.side[NS == 2 ? i : w.kv].inv + page);
   }
@@ -332,7 +333,19 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_rows(const __grid_constant__ 
     for (int i = 0; i < NS; ++i)
       prefetch_l2_bulk(fp8_src(p, p.side[NS == 2 ? i : w.kv], w),
                        p.shape.part_chunks * 2u * static_cast<uint32_t>(OUT));
-    prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
+    if (p.scale_page != 0) {
+      // per-page scales: the slot read speculatively (the previous grid may
+      // still write it; the guess only aims a prefetch) brings the page's
+      // scale into L2, shortening the slot -> scale -> codes chain
+      const int64_t g = speculative_slot<IdxT>(p.indices, p.index_stride, w.token);
+      if (g >= 0 && g < p.size_limit) {
+        const int64_t page = p.scale_page_shift >= 0 ? g >> p.scale_page_shift : g / p.scale_page;
+#pragma unroll
+        for (int i = 0; i < NS; ++i) prefetch_l2_line(p.side[NS == 2 ? i : w.kv].inv + page);
+      }
+    } else {
+      prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
+    }
   }
   grid_handover();
 
@@ -781,6 +794,11 @@ kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, 
   p.size_limit = size_limit;
   p.page_size = flat ? 1 : page_size;
   p.scale_page = scale_page;
+  p.scale_page_shift = -1;
+  if (scale_page > 0 && (scale_page & (scale_page - 1)) == 0) {
+    p.scale_page_shift = 0;
+    while ((int64_t{1} << p.scale_page_shift) < scale_page) ++p.scale_page_shift;
+  }
   p.shape.parts = parts;
   p.shape.units_per_side = sg.count * parts;
   p.shape.units_per_token = 2u * p.shape.units_per_side;
@@ -820,13 +838,10 @@ extern "C" kv_status kv_error_poll(kv_error_record* d_err, kv_stream_t stream_, 
   if (e != cudaSuccess) return cuda_fail(e);
   e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e);
-  const bool timed_out = (h.oob_count & kTimeoutBit) != 0;
-  const uint64_t skipped = h.oob_count & ~kTimeoutBit;
-  if (oob_count) *oob_count = static_cast<int64_t>(skipped);
+  if (oob_count) *oob_count = static_cast<int64_t>(h.oob_count);
   if (first_bad_token)
-    *first_bad_token = skipped ? static_cast<int64_t>(~h.first_bad_key) : int64_t{-1};
-  if (timed_out) return KV_ERR_DEVICE_TIMEOUT;
-  return skipped ? KV_ERR_INDEX_OOB : KV_OK;
+    *first_bad_token = h.oob_count ? static_cast<int64_t>(~h.first_bad_key) : int64_t{-1};
+  return h.oob_count ? KV_ERR_INDEX_OOB : KV_OK;
 }
 
 namespace kvimpl {
@@ -901,7 +916,6 @@ extern "C" const char* kv_status_str(kv_status status) {
     case KV_ERR_UNSUPPORTED: return "KV_ERR_UNSUPPORTED";
     case KV_ERR_CUDA: return "KV_ERR_CUDA";
     case KV_ERR_INDEX_OOB: return "KV_ERR_INDEX_OOB";
-    case KV_ERR_DEVICE_TIMEOUT: return "KV_ERR_DEVICE_TIMEOUT";
   }
   return "KV_STATUS_UNKNOWN";
 }
@@ -1010,9 +1024,7 @@ extern "C" kv_status kv_store_noalloc(const void* k, const void* v, void* k_cach
   if (e != cudaSuccess) return cuda_fail(e);
   e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e);
-  const uint64_t skipped = h.oob_count & ~kTimeoutBit;
-  if (oob_count) *oob_count = static_cast<int64_t>(skipped);
-  if (first_bad_token && skipped) *first_bad_token = static_cast<int64_t>(~h.first_bad_key);
-  if (h.oob_count & kTimeoutBit) return KV_ERR_DEVICE_TIMEOUT;
-  return skipped ? KV_ERR_INDEX_OOB : KV_OK;
+  if (oob_count) *oob_count = static_cast<int64_t>(h.oob_count);
+  if (first_bad_token && h.oob_count) *first_bad_token = static_cast<int64_t>(~h.first_bad_key);
+  return h.oob_count ? KV_ERR_INDEX_OOB : KV_OK;
 }

@@ -69,8 +69,7 @@ typedef enum kv_status {
     KV_ERR_INVALID_ARG = 1,  /* bad argument found on the host; nothing was launched */
     KV_ERR_UNSUPPORTED = 2,  /* legal request this library does not implement; nothing launched */
     KV_ERR_CUDA = 3,         /* a CUDA runtime call failed; see kv_last_cuda_error() */
-    KV_ERR_INDEX_OOB = 4,    /* kv_error_poll: at least one token had an out-of-range slot */
-    KV_ERR_DEVICE_TIMEOUT = 5  /* kv_error_poll: a kernel gave up waiting on its own copies */
+    KV_ERR_INDEX_OOB = 4     /* kv_error_poll: at least one token had an out-of-range slot */
 } kv_status;
 
 typedef enum kv_index_dtype { KV_INDEX_I32 = 0, KV_INDEX_I64 = 1 } kv_index_dtype;
@@ -94,9 +93,7 @@ typedef struct kv_strides {
  * kv_error_reset).  Kernels only add to it; kv_error_poll reads and clears it.
  * Calls that share one record on different streams share its counts. */
 typedef struct kv_error_record {
-    uint64_t oob_count;      /* tokens skipped because their slot was out of range; bit 63
-                                is set instead when a kernel stopped waiting on its own
-                                asynchronous copies after its iteration limit */
+    uint64_t oob_count;      /* tokens skipped because their slot was out of range */
     uint64_t first_bad_key;  /* bitwise NOT of the lowest skipped token; 0 if none */
 } kv_error_record;
 
@@ -417,12 +414,9 @@ kv_status kv_store_noalloc(const void *k, const void *v, void *k_cache, void *v_
  * (The pages trap inside the kernel on a bad slot; this library reports it
  * here instead.)  Writes the number of skipped tokens and the lowest skipped
  * token (-1 if none) to the optional host outputs.  Returns KV_OK when no
- * token was skipped, KV_ERR_INDEX_OOB when one was, KV_ERR_DEVICE_TIMEOUT when
- * a kernel gave up waiting on its own asynchronous copies (bit 63 of the
- * record's count; never expected, and the output of that call is undefined),
- * KV_ERR_INVALID_ARG for a NULL or misaligned record, KV_ERR_CUDA if a CUDA
- * call failed (including an earlier asynchronous error surfaced by the
- * synchronisation).
+ * token was skipped, KV_ERR_INDEX_OOB when one was, KV_ERR_INVALID_ARG for a
+ * NULL or misaligned record, KV_ERR_CUDA if a CUDA call failed (including an
+ * earlier asynchronous error surfaced by the synchronisation).
  * Not capturable in a CUDA graph (it synchronises).
  */
 kv_status kv_error_poll(kv_error_record *d_err, kv_stream_t stream, int64_t *oob_count,

@@ -58,8 +58,7 @@ def test_abi_version_and_status_strings(lib):
     m = re.search(r"#define\s+KV_ABI_VERSION\s+(\d+)", open(HEADER).read())
     assert lib.kv_abi_version() == int(m.group(1))
     for code, name in [(0, "KV_OK"), (1, "KV_ERR_INVALID_ARG"), (2, "KV_ERR_UNSUPPORTED"),
-                       (3, "KV_ERR_CUDA"), (4, "KV_ERR_INDEX_OOB"),
-                       (5, "KV_ERR_DEVICE_TIMEOUT")]:
+                       (3, "KV_ERR_CUDA"), (4, "KV_ERR_INDEX_OOB")]:
         assert kv.kv_status_str(code) == name
         assert kv.KVStatus(code).value == code
     assert kv.kv_status_str(99) == "KV_STATUS_UNKNOWN"

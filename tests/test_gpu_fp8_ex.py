@@ -116,8 +116,8 @@ CASES = {
     # at least 4096 rows: one warp converts the K and the V row of a token
     "paired_rows_pages": dict(T=2500, H=8, D=128, n_slots=8192, page_size=16, page_pad=256),
     "paired_long_rows_i32": dict(T=2100, H=16, D=128, n_slots=4096, idx_dtype=np.int32),
-    # the staged (shared-memory ring) form: 512 / 1024 / 2048-byte rows, heads
-    # of 2 / 4 / 8 / 16 pieces, and heads of one, two and four 32-piece slabs
+    # row-layout kernel: 512 / 1024 / 2048-byte rows, heads of 16 to 1024
+    # elements (per-head groups from 2 lanes to whole multi-slab rows)
     "staged_d64_pages": dict(T=1000, H=8, D=64, n_slots=4096, page_size=16, page_pad=256),
     "staged_d32_i32": dict(T=777, H=8, D=32, n_slots=4096, idx_dtype=np.int32),
     "staged_d16": dict(T=333, H=16, D=16, n_slots=1024),

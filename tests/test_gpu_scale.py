@@ -208,16 +208,3 @@ def test_absmax_workspace_back_to_back_calls():
             assert np.array_equal(got[:2], a) and np.array_equal(got[2:], np.float32(448.0) / a)
         assert work.cpu().tolist() == [0, 0]
 
-
-def test_error_poll_reports_a_device_timeout():
-    """Bit 63 of the record's count (set by a kernel that gave up waiting on
-    its own copies) reads back as KV_ERR_DEVICE_TIMEOUT, the rest of the count
-    as the skipped tokens; the poll clears the record."""
-    import torch
-    import fp8_quant_gb300 as kv
-    err = torch.zeros(2, dtype=torch.int64, device="cuda")
-    err[0] = -(2 ** 63) + 3          # bit 63 and three skipped tokens
-    err[1] = ~5                       # lowest skipped token 5
-    rc, n, first = kv.raw.kv_error_poll(err.data_ptr(), _stream())
-    assert (rc, n, first) == (kv.KVStatus.ERR_DEVICE_TIMEOUT, 3, 5)
-    assert err.cpu().tolist() == [0, 0]
