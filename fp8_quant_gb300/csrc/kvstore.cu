@@ -333,19 +333,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_rows(const __grid_constant__ 
     for (int i = 0; i < NS; ++i)
       prefetch_l2_bulk(fp8_src(p, p.side[NS == 2 ? i : w.kv], w),
                        p.shape.part_chunks * 2u * static_cast<uint32_t>(OUT));
-    if (p.scale_page != 0) {
-      // per-page scales: the slot read speculatively (the previous grid may
-      // still write it; the guess only aims a prefetch) brings the page's
-      // scale into L2, shortening the slot -> scale -> codes chain
-      const int64_t g = speculative_slot<IdxT>(p.indices, p.index_stride, w.token);
-      if (g >= 0 && g < p.size_limit) {
-        const int64_t page = p.scale_page_shift >= 0 ? g >> p.scale_page_shift : g / p.scale_page;
-#pragma unroll
-        for (int i = 0; i < NS; ++i) prefetch_l2_line(p.side[NS == 2 ? i : w.kv].inv + page);
-      }
-    } else {
-      prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
-    }
+    prefetch_l2_line(static_cast<const IdxT*>(p.indices) + w.token * p.index_stride);
   }
   grid_handover();
 
