@@ -47,6 +47,9 @@
 #ifndef KV_LOOKAHEAD
 #define KV_LOOKAHEAD 1          // multi-wave gathers: each warp prefetches the unit one resident wave ahead
 #endif
+#ifndef KV_LOOKAHEAD_MAX_BYTES
+#define KV_LOOKAHEAD_MAX_BYTES (64ull << 20)  // ... only when a launch moves at most this many bytes
+#endif
 #ifndef KV_PREFETCH
 #define KV_PREFETCH 1           // L2 prefetch of the unit's source bytes before the grid wait
 #endif

@@ -310,16 +310,18 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant
 
 template <int J, typename IdxT, int FMT>
 kv_status launch_dyn_row_j(bool bf16, const DynRowParams& p, cudaStream_t stream) {
+  // bytes moved: each row's 32-byte input chunks read, 16-byte codes written
+  const uint64_t bytes = p.shape.num_units * p.chunks * 48u;
   if (p.shape.num_units >= KV_LARGE_LAUNCH_WARPS) {
     DynRowParams q = p;   // one warp per token: K and V rows together
     q.shape.units_per_token = 1;
     q.shape.units_per_side = 1;
     q.shape.num_units /= 2;
-    if (bf16) return launch_rows(kv_fp8_dyn_row<J, 2, IdxT, true, FMT>, q.shape.num_units, q, stream);
-    return launch_rows(kv_fp8_dyn_row<J, 2, IdxT, false, FMT>, q.shape.num_units, q, stream);
+    if (bf16) return launch_rows(kv_fp8_dyn_row<J, 2, IdxT, true, FMT>, q.shape.num_units, q, stream, bytes);
+    return launch_rows(kv_fp8_dyn_row<J, 2, IdxT, false, FMT>, q.shape.num_units, q, stream, bytes);
   }
-  if (bf16) return launch_rows(kv_fp8_dyn_row<J, 1, IdxT, true, FMT>, p.shape.num_units, p, stream);
-  return launch_rows(kv_fp8_dyn_row<J, 1, IdxT, false, FMT>, p.shape.num_units, p, stream);
+  if (bf16) return launch_rows(kv_fp8_dyn_row<J, 1, IdxT, true, FMT>, p.shape.num_units, p, stream, bytes);
+  return launch_rows(kv_fp8_dyn_row<J, 1, IdxT, false, FMT>, p.shape.num_units, p, stream, bytes);
 }
 
 template <typename IdxT, int FMT>

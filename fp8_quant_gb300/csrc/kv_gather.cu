@@ -372,11 +372,19 @@ inline int gather_sides(GatherParams& p) {
   return 2;
 }
 
+// Bytes a gather launch moves: every unit's part read from the cache and
+// written out (an FP8 unit writes out_per_in bytes per code).
+inline uint64_t gather_bytes(const GatherParams& p, uint64_t out_per_in) {
+  return p.shape.num_units * p.shape.part_chunks * static_cast<uint64_t>(p.vec) * (1 + out_per_in);
+}
+
 template <int VEC, typename IdxT>
 kv_status launch_gather_vec(GatherParams p, cudaStream_t stream) {
   constexpr int U = VEC == 32 ? (KV_COPY_UNROLL + 1) / 2 : KV_COPY_UNROLL;
-  if (gather_sides(p) == 2) return launch_rows(kv_gather_rows<VEC, U, 2, IdxT>, p.shape.num_units, p, stream);
-  return launch_rows(kv_gather_rows<VEC, U, 1, IdxT>, p.shape.num_units, p, stream);
+  const uint64_t bytes = gather_bytes(p, 1);
+  if (gather_sides(p) == 2)
+    return launch_rows(kv_gather_rows<VEC, U, 2, IdxT>, p.shape.num_units, p, stream, bytes);
+  return launch_rows(kv_gather_rows<VEC, U, 1, IdxT>, p.shape.num_units, p, stream, bytes);
 }
 
 template <typename IdxT>
@@ -396,13 +404,16 @@ kv_status launch_gather(int vec, const GatherParams& p, cudaStream_t stream) {
 template <int IN, typename IdxT, int FMT>
 kv_status launch_gather_fp8_fmt(bool bf16, const GatherParams& p, cudaStream_t stream) {
   constexpr int U = IN == 16 ? 2 : 4;
+  const uint64_t bytes = gather_bytes(p, 2);
   GatherParams q = p;
   if (gather_sides(q) == 2) {
-    if (bf16) return launch_rows(kv_gather_fp8_rows<IN, U, 2, IdxT, true, FMT>, q.shape.num_units, q, stream);
-    return launch_rows(kv_gather_fp8_rows<IN, U, 2, IdxT, false, FMT>, q.shape.num_units, q, stream);
+    if (bf16)
+      return launch_rows(kv_gather_fp8_rows<IN, U, 2, IdxT, true, FMT>, q.shape.num_units, q, stream, bytes);
+    return launch_rows(kv_gather_fp8_rows<IN, U, 2, IdxT, false, FMT>, q.shape.num_units, q, stream, bytes);
   }
-  if (bf16) return launch_rows(kv_gather_fp8_rows<IN, U, 1, IdxT, true, FMT>, p.shape.num_units, p, stream);
-  return launch_rows(kv_gather_fp8_rows<IN, U, 1, IdxT, false, FMT>, p.shape.num_units, p, stream);
+  if (bf16)
+    return launch_rows(kv_gather_fp8_rows<IN, U, 1, IdxT, true, FMT>, p.shape.num_units, p, stream, bytes);
+  return launch_rows(kv_gather_fp8_rows<IN, U, 1, IdxT, false, FMT>, p.shape.num_units, p, stream, bytes);
 }
 
 template <int IN, typename IdxT>

@@ -83,19 +83,24 @@ kv_status launch(void (*kernel)(Params), uint64_t num_units, const Params& param
   return KV_OK;
 }
 
-// launch() for the row gathers, which prefetch ahead: when the launch runs
-// in more than one wave of resident CTAs, params.ahead is set to the
-// resident warps, and each warp prefetches into L2 what the warp that will
-// take its place one wave later is going to read.  In a gather that hides
-// the slot -> row dependency of the later waves (measured: gather_fp8
-// 8.67 -> 8.38 us).  The writes, whose row loads do not wait on the slot,
+// launch() for the row gathers and the dynamic-scale write, which prefetch
+// ahead: when the launch runs in more than one wave of resident CTAs and
+// moves at most KV_LOOKAHEAD_MAX_BYTES (launch_bytes: read + written),
+// params.ahead is set to the resident warps, and each warp prefetches into L2
+// what the warp that will take its place one wave later is going to read.
+// In a gather that hides the slot -> row dependency of the later waves
+// (gather_fp8 8.84 -> 8.65 us), and in the dynamic write the row's arrival
+// before its scale can be formed (fp8_dynamic 9.58 -> 9.2 us).  A launch
+// whose traffic exceeds L2 by far loses more to prefetched rows evicted
+// before use than it gains (gather_prefill, 268 MB: 39.2 us without, 41.2
+// with).  The static writes, whose row loads do not wait on the slot,
 // measured slower with it (fp8 7.68 -> 7.88 us, strided 78.6 -> 81.6 us) and
 // do not use it.
 template <typename Params>
 kv_status launch_rows(void (*kernel)(Params), uint64_t num_units, Params params,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, uint64_t launch_bytes) {
   params.ahead = 0;
-  if (KV_LOOKAHEAD && params.prefetch) {
+  if (KV_LOOKAHEAD && params.prefetch && launch_bytes <= KV_LOOKAHEAD_MAX_BYTES) {
     const int threads = launch_threads(num_units);
     int sms = 0, per_sm = 0;
     kv_status st = current_sm_count(&sms);
