@@ -17,9 +17,6 @@
 // programmatic-launch wait.
 #include "kv_host.h"
 
-#ifndef KV_DYN_PAIR
-#define KV_DYN_PAIR 1        // large row launches: one warp converts the K and the V row of a token
-#endif
 #ifndef KV_DYN_LOOKAHEAD
 #define KV_DYN_LOOKAHEAD 1   // multi-wave row launches: prefetch the unit one resident wave ahead
 #endif
@@ -315,7 +312,7 @@ template <int J, typename IdxT, int FMT>
 kv_status launch_dyn_row_j(bool bf16, const DynRowParams& p, cudaStream_t stream) {
   // bytes moved: each row's 32-byte input chunks read, 16-byte codes written
   const uint64_t bytes = p.shape.num_units * p.chunks * 48u;
-  if (KV_DYN_PAIR && p.shape.num_units >= KV_LARGE_LAUNCH_WARPS) {
+  if (p.shape.num_units >= KV_LARGE_LAUNCH_WARPS) {
     DynRowParams q = p;   // one warp per token: K and V rows together
     q.shape.units_per_token = 1;
     q.shape.units_per_side = 1;
