@@ -1,7 +1,6 @@
 """kv_store_noalloc: the entry point for callers that cannot allocate device
-memory (code inside allocator hooks or host callbacks, plugins without a
-memory pool, processes whose device memory is all reserved by a pool they do
-not own).
+memory (code inside allocator hooks, plugins without a memory pool, processes
+whose device memory is all reserved by a pool they do not own).
 
 It must write exactly what kv_store writes, and report out-of-range slots
 through its own static record, which every call clears first. Two calls in a
