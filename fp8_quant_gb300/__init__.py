@@ -35,6 +35,7 @@ __all__ = [
     "KVStatus", "KVError", "kv_store", "kv_store_fp8", "kv_store_paged", "kv_store_fp8_ex",
     "kv_gather", "kv_gather_fp8", "kv_inv_scale", "kv_absmax_inv", "kv_error_poll",
     "kv_error_reset", "kv_status_str", "error_record", "load_library", "raw", "STRIDE_FIELDS",
+    "fused_fp8_set_kv_buffer",
 ]
 
 
@@ -584,6 +585,43 @@ def kv_inv_scale(scale, out=None, stream=None):
     _check(raw.kv_inv_scale(scale.data_ptr(), out.data_ptr(), scale.numel(),
                             _stream_handle(stream, scale.device)), "kv_inv_scale")
     return out
+
+
+def fused_fp8_set_kv_buffer(k, v, k_cache, v_cache, cache_loc, k_scale=None, v_scale=None,
+                            page_size: int = 16, *, err=None, stream=None) -> None:
+    """The fused FP8 write with the argument list of sglang trtllm_fp8_kv_kernel.py
+    (`fused_fp8_set_kv_buffer`, its wrapper): K and V rows ([T, H, D] or
+    [T, H*D], bf16 or fp16) go to slots ``cache_loc`` of e4m3fn caches,
+    [slots, H, D] (``slots`` a multiple of ``page_size``) or
+    [pages, page_size, H, D].  ``k_scale`` / ``v_scale`` are the forward
+    (dequantisation) scales, Python floats or fp32 tensors, used only when both
+    are given; as in that wrapper, ``1 / scale`` is formed on the device
+    (``kv_inv_scale``), so tensor scales cost no host synchronisation.  The
+    write itself is ``kv_store_fp8``; there is no second, unfused path.  The
+    scale staging runs on ``stream`` (torch's current stream when None)."""
+    import contextlib
+    import torch
+    if k_cache.dim() == 3 and k_cache.shape[0] % page_size:
+        raise ValueError("cache slots must be a multiple of page_size")
+    inv = None
+    if k_scale is not None and v_scale is not None:
+        ctx = (torch.cuda.stream(stream) if isinstance(stream, torch.cuda.Stream)
+               else contextlib.nullcontext())
+        if stream is not None and not isinstance(stream, torch.cuda.Stream):
+            raise TypeError("with scales, stream must be a torch.cuda.Stream or None")
+        with ctx:
+            sc = torch.empty(2, dtype=torch.float32, device=k.device)
+            for i, x in enumerate((k_scale, v_scale)):
+                if isinstance(x, torch.Tensor):
+                    if x.numel() != 1:
+                        raise ValueError("a scale tensor holds one value")
+                    sc[i:i + 1].copy_(x.reshape(1))
+                else:
+                    sc[i:i + 1].fill_(float(x))
+            inv = kv_inv_scale(sc, stream=stream)
+    kv_store_fp8(k, v, k_cache, v_cache, cache_loc, page_size=page_size,
+                 inv_k_scale=None if inv is None else inv[0:1],
+                 inv_v_scale=None if inv is None else inv[1:2], err=err, stream=stream)
 
 
 def kv_absmax_inv(k, v, *, fp8_max: float = 448.0, num_heads=None, head_dim=None, out=None,

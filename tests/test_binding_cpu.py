@@ -165,3 +165,34 @@ def test_scale_wrappers(monkeypatch):
     w = torch.zeros(2, dtype=torch.int32)
     kv.kv_absmax_inv(k, k, work=w)
     assert cap.calls[-1][1][10] == w.data_ptr()
+
+
+def test_fused_fp8_set_kv_buffer_argument_list(monkeypatch):
+    """The wrapper with the argument list of the fused FP8 write's page: the
+    unscaled call passes use_scale 0 and the page layout on; a 3-D cache whose
+    slot count is not a multiple of page_size, or a page_size that differs
+    from a 4-D cache's, is rejected; given both scales, their reciprocals are
+    formed by kv_inv_scale (two values) before the write."""
+    cap = CaptureAll(monkeypatch)
+    T, H, D, ps, pages = 5, 4, 64, 16, 8
+    k = torch.zeros(T, H * D, dtype=torch.bfloat16)
+    idx = torch.arange(T, dtype=torch.int32)
+    c3 = torch.zeros(ps * pages, H, D, dtype=torch.uint8)
+    kv.fused_fp8_set_kv_buffer(k, k, c3, c3, idx)              # page_size defaults to 16
+    name, a = cap.calls[-1]
+    assert name == "kv_store_fp8"
+    assert (a[12], a[13], a[14], a[15]) == (ps, ps * 256, ps * 256, ps * pages)
+    assert (a[16], a[17], a[18]) == (None, None, 0)
+    with pytest.raises(ValueError):
+        kv.fused_fp8_set_kv_buffer(k, k, c3[:ps * pages - 1], c3[:ps * pages - 1], idx)
+    c4 = torch.zeros(pages, ps, H, D, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        kv.fused_fp8_set_kv_buffer(k, k, c4, c4, idx, page_size=8)
+    n = len(cap.calls)
+    with pytest.raises(TypeError):          # host-side scales reach kv_store_fp8's device check
+        kv.fused_fp8_set_kv_buffer(k, k, c4, c4, idx, 2.0, torch.tensor(0.5))
+    assert cap.calls[n][0] == "kv_inv_scale" and cap.calls[n][1][2] == 2
+    kv.fused_fp8_set_kv_buffer(k, k, c4, c4, idx, 2.0, None)   # one scale alone: unscaled
+    assert cap.calls[-1][0] == "kv_store_fp8" and cap.calls[-1][1][18] == 0
+    with pytest.raises(ValueError):
+        kv.fused_fp8_set_kv_buffer(k, k, c4, c4, idx, torch.ones(2), 1.0)

@@ -505,6 +505,52 @@ def test_tensor_wrappers_round_trips():
     assert kv.kv_error_poll()[1] == 0
 
 
+
+@pytest.mark.parametrize("layout", ["3d_float_scales", "4d_tensor_scales", "4d_no_scale"])
+def test_fused_fp8_set_kv_buffer_matches_oracle(layout):
+    """The wrapper with the argument list of the fused FP8 write's page: float
+    or device-tensor forward scales (reciprocal formed on the device) or none,
+    [T, H*D] or [T, H, D] rows, 3-D or 4-D caches; every cache byte equals the
+    oracle's write with fl32(1 / scale)."""
+    import torch
+    import fp8_quant_gb300 as kv
+    import oracle
+    dev = torch.device("cuda")
+    T, H, D, ps, pages = 777, 8, 128, 16, 96
+    seed = zlib.crc32(layout.encode()) % 10000
+    kb = wl.f32_to_bf16_bits(wl.normal(seed, T * H * D) * 3.0).reshape(T, H, D)
+    vb = wl.f32_to_bf16_bits(wl.normal(seed + 1, T * H * D) * 0.25).reshape(T, H, D)
+    slots = wl.distinct_slots(seed, ps * pages, T).astype(np.int32)
+    k = torch.from_numpy(kb.view(np.int16)).to(dev).view(torch.bfloat16)
+    v = torch.from_numpy(vb.view(np.int16)).to(dev).view(torch.bfloat16)
+    scales = (0.0234375, 0.00390625) if layout != "4d_no_scale" else (None, None)
+    if layout == "3d_float_scales":
+        shape = (ps * pages, H, D)
+        k, v = k.reshape(T, H * D), v.reshape(T, H * D)
+        ks, vs = scales
+    else:
+        shape = (pages, ps, H, D)
+        ks, vs = (None, None) if scales[0] is None else (
+            torch.tensor(scales[0], device=dev), torch.tensor(scales[1], device=dev))
+    kc = torch.full(shape, 0x5A, dtype=torch.uint8, device=dev)
+    vc = torch.full(shape, 0xA5, dtype=torch.uint8, device=dev)
+    kv.fused_fp8_set_kv_buffer(k, v, kc, vc, torch.from_numpy(slots).to(dev), ks, vs,
+                               page_size=ps)
+    assert kv.kv_error_poll()[1] == 0
+    R = H * D
+    okc = np.full(ps * pages * R, 0x5A, np.uint8)
+    ovc = np.full(ps * pages * R, 0xA5, np.uint8)
+    st = oracle.Strides(k_token=2 * R, k_head=2 * D, k_dim=2, v_token=2 * R, v_head=2 * D,
+                        v_dim=2, kc_slot=R, kc_head=D, kc_dim=1, vc_slot=R, vc_head=D, vc_dim=1)
+    use = scales[0] is not None
+    inv = oracle.inv_scale(scales) if use else (1.0, 1.0)
+    bad, _ = oracle.store_fp8(kb, vb, okc, ovc, slots, st, H, D, "bf16", ps, ps * R, ps * R,
+                              ps * pages, inv_k=inv[0], inv_v=inv[1], use_scale=int(use))
+    assert bad == 0
+    assert np.array_equal(kc.cpu().numpy().ravel(), okc)
+    assert np.array_equal(vc.cpu().numpy().ravel(), ovc)
+
+
 @pytest.mark.gpu
 def test_launch_floor_runs_in_stream_order_and_in_a_graph():
     """kv_launch_floor (the measurement aid) launches, keeps stream order
