@@ -327,6 +327,15 @@ __device__ __forceinline__ float absmax_pair_value(uint32_t m) {
   return fmaxf(fabsf(x.x), fabsf(x.y));
 }
 
+// max |x| over the 32 lanes of a warp (all of them execute it): one
+// redux.sync on fp32, which ignores NaN inputs (only NaN everywhere gives
+// NaN).
+__device__ __forceinline__ float warp_absmax(float x) {
+  float r;
+  asm volatile("redux.sync.max.abs.f32 %0, %1, %2;" : "=f"(r) : "f"(x), "r"(0xFFFFFFFFu));
+  return r;
+}
+
 // One lane's chunk: OUT output bytes from OUT 2-byte inputs.
 // Byte offset of cache row `slot`: (slot / page_size) * page_stride +
 // (slot % page_size) * slot_stride.  page_size == 1 means a flat cache whose

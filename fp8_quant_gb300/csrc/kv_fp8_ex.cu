@@ -100,6 +100,27 @@ __device__ __forceinline__ Chunk<CH> chunk_quant(const Chunk<2 * CH>& c, float i
   return o;
 }
 
+// Maxima of |x| over the even and over the odd elements of a 32-byte chunk
+// (16 elements), as the two 16-bit halves of one word: a tree of packed
+// max.xorsign.abs steps.  The maximum of 16-bit inputs is one of them, so
+// the values are exact; their sign bits are arbitrary (cleared by the
+// reduction below).  A NaN element never wins over a number.
+template <bool kBF16>
+__device__ __forceinline__ uint32_t chunk_pairmax(const Chunk<32>& c) {
+  const uint32_t a0 = absmax_pair<kBF16>(c.w[0], c.w[1]);
+  const uint32_t a1 = absmax_pair<kBF16>(c.w[2], c.w[3]);
+  const uint32_t a2 = absmax_pair<kBF16>(c.w[4], c.w[5]);
+  const uint32_t a3 = absmax_pair<kBF16>(c.w[6], c.w[7]);
+  return absmax_pair<kBF16>(absmax_pair<kBF16>(a0, a1), absmax_pair<kBF16>(a2, a3));
+}
+
+// Two pair maxima a, b folded into one word: max over a's halves in the low
+// half, over b's in the high half.
+template <bool kBF16>
+__device__ __forceinline__ uint32_t fold_pairs(uint32_t a, uint32_t b) {
+  return absmax_pair<kBF16>(__byte_perm(a, b, 0x5410), __byte_perm(a, b, 0x7632));
+}
+
 template <int CH, typename IdxT, bool kBF16, int FMT>
 __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_rows(const __grid_constant__ DynParams p) {
   constexpr int kMaxJ = CH >= 8 ? 2 : 4;  // chunks per lane held in registers (16-byte chunks: 2, no spill)
@@ -149,8 +170,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_rows(const __grid_constan
         amax = chunk_absmax<CH, kBF16>(amax, t);
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    amax = warp_absmax(amax);
     if (slot < 0 || slot >= p.size_limit) {
       if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
       continue;
@@ -187,9 +207,11 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_rows(const __grid_constan
 // a row: 32 input bytes, 16 output bytes each), with each group's amax
 // reduced over the lanes that hold it.  A head of D elements is D/16
 // consecutive chunks, so in every 32-chunk slab of the row it sits on an
-// aligned run of D/16 lanes; a shuffle over those lanes gives its amax.  In
+// aligned run of D/16 lanes; xor shuffles over those lanes give its amax.  In
 // the per-token mode the group is the whole row.  Large launches pair the K
-// and the V row of a token in one warp (NS == 2).
+// and the V row of a token in one warp (NS == 2).  The per-head and the
+// per-token forms are separate instantiations (kHead), so each carries only
+// its own reduction.
 struct DynRowParams {
   DynSide side[2];
   const void* indices;
@@ -203,7 +225,7 @@ struct DynRowParams {
   uint64_t ahead;           // > 0: also prefetch the rows of unit u + ahead (set by launch_rows)
 };
 
-template <int J, int NS, typename IdxT, bool kBF16, int FMT>
+template <int J, int NS, bool kHead, typename IdxT, bool kBF16, int FMT>
 __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant__ DynRowParams p) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
@@ -237,7 +259,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant
     }
     // the unit that takes this warp's place one resident wave later: its rows
     // go to L2 while this unit's reduction waits on its loads
-    if (KV_DYN_LOOKAHEAD && p.ahead != 0 && lane == 0 && u + p.ahead < p.shape.num_units) {
+    if (KV_DYN_LOOKAHEAD && kHead && p.ahead != 0 && lane == 0 && u + p.ahead < p.shape.num_units) {
       const Unit nx = decode_unit(p.shape, u + p.ahead);
 #pragma unroll
       for (int i = 0; i < NS; ++i) {
@@ -246,51 +268,148 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant
       }
       prefetch_l2_line(static_cast<const IdxT*>(p.indices) + nx.token * p.index_stride);
     }
-    float a[NS][J];
+    // Group maxima.  Value t = i * J + j of a lane is side i's lane chunk j;
+    // per head its group is the head of that chunk (g lanes hold it), per
+    // token the side's row.  Each chunk's exact 16-bit maximum is packed two
+    // to a word (value t in half t % 2 of word t / 2).
+    //  - Per head, with at least 2V lanes to a group: a reduce-scatter over
+    //    the group's lanes.  Each of the first log2(W) xor rounds hands the
+    //    partner the half of the live words this lane does not keep, so one
+    //    word (values 2b, 2b + 1) is left, and the remaining rounds reduce
+    //    it over the lanes that kept the same word.
+    //  - Per head with fewer lanes: every word is reduced over the group.
+    //  - Per token: the sides' maxima in one word, reduced over the warp by
+    //    redux.sync on fp32 copies (redux.sync over 8-lane masks measured
+    //    slower than the shuffles; over the whole warp it is faster).
+    constexpr int V = NS * J;
+    constexpr int W = (V + 1) / 2;
+    constexpr int S = W == 4 ? 2 : W == 2 ? 1 : 0;  // log2(W)
+    const bool scatter = kHead && 2u * V <= g;
+    float gm[V];       // per token: side t (t < NS); per head without scatter: the group of value t
+    uint32_t word = 0u, wb = 0u;  // per head with scatter: the lane's word and its index
+    {
+      uint32_t b[V];
 #pragma unroll
-    for (int i = 0; i < NS; ++i) {
+      for (int t = 0; t < V; ++t)
+        b[t] = lane + 32u * (t % J) < n ? chunk_pairmax<kBF16>(buf[t / J][t % J]) : 0u;
+      if constexpr (kHead) {
+        uint32_t pk[W];
 #pragma unroll
-      for (int j = 0; j < J; ++j)
-        a[i][j] = lane + 32u * j < n ? chunk_absmax<16, kBF16>(0.0f, buf[i][j]) : 0.0f;
-      if (g != 0) {             // per head: the aligned run of g lanes
-        for (uint32_t o = 1; o < g; o <<= 1)
+        for (int s = 0; s < W; ++s) pk[s] = 0u;
 #pragma unroll
-          for (int j = 0; j < J; ++j) a[i][j] = fmaxf(a[i][j], __shfl_xor_sync(0xFFFFFFFFu, a[i][j], o));
-      } else {                  // per token: the whole row
-        float m = 0.0f;
+        for (int t = 0; t < V; ++t) {   // the chunk's maximum in both halves, kept in half t % 2
+          const uint32_t m = absmax_pair<kBF16>(b[t], __byte_perm(b[t], 0u, 0x1032));
+          pk[t / 2] |= m & ((t & 1) ? 0xFFFF0000u : 0x0000FFFFu);
+        }
+        if (scatter) {
 #pragma unroll
-        for (int j = 0; j < J; ++j) m = fmaxf(m, a[i][j]);
+          for (int k = 0; k < S; ++k) {
+            const uint32_t o = g >> (k + 1);
+            const bool up = (lane & o) != 0u;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            for (int x = 0; x < (W >> (k + 1)); ++x) {
+              const uint32_t send = up ? pk[x] : pk[(W >> (k + 1)) + x];
+              const uint32_t keep = up ? pk[(W >> (k + 1)) + x] : pk[x];
+              pk[x] = absmax_pair<kBF16>(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
+            }
+            if (up) wb += static_cast<uint32_t>(W >> (k + 1));
+          }
+          for (uint32_t o = g >> (S + 1); o > 0u; o >>= 1)
+            pk[0] = absmax_pair<kBF16>(pk[0], __shfl_xor_sync(0xFFFFFFFFu, pk[0], o));
+          word = pk[0];
+        } else {
+          for (uint32_t o = 1; o < g; o <<= 1)
 #pragma unroll
-        for (int j = 0; j < J; ++j) a[i][j] = m;
+            for (int s = 0; s < W; ++s) pk[s] = absmax_pair<kBF16>(pk[s], __shfl_xor_sync(0xFFFFFFFFu, pk[s], o));
+#pragma unroll
+          for (int s = 0; s < W; ++s) {
+            const float2 x = widen2<kBF16>(pk[s]);
+            gm[2 * s] = fabsf(x.x);
+            if (2 * s + 1 < V) gm[2 * s + 1] = fabsf(x.y);
+          }
+        }
+      } else {
+        uint32_t side[NS];
+#pragma unroll
+        for (int i = 0; i < NS; ++i) {
+          side[i] = b[i * J];
+#pragma unroll
+          for (int j = 1; j < J; ++j) side[i] = absmax_pair<kBF16>(side[i], b[i * J + j]);
+        }
+        const float2 x = widen2<kBF16>(fold_pairs<kBF16>(side[0], NS == 2 ? side[NS - 1] : 0u));
+        gm[0] = warp_absmax(x.x);
+        if (NS == 2) gm[NS - 1] = warp_absmax(x.y);
       }
     }
     if (slot < 0 || slot >= p.size_limit) {
       if (w.rank == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(w.token));
       continue;
     }
-    // The warp holds NS * gps groups (gps per row).  Lane k computes the
-    // two divisions of group k, once: its amax comes from the lane holding
-    // the group's first chunk, and every lane then takes the inverse scale
-    // of its chunks' groups from lane k.
-    const uint32_t gps = g != 0 ? n / g : 1u;
-    const uint32_t gk = lane % gps;                       // lane's group within its side
-    const uint32_t c0 = g != 0 ? gk * g : 0u;             // first chunk of that group
-    float amax_k = 0.0f;
+    // Scales.  A group's two divisions (fmax / amax, its inverse scale, and
+    // amax / fmax, its stored scale) go to two lanes that hold the group's
+    // maximum, so the warp runs one division; every lane then takes its
+    // chunks' inverse scales from the inverse-scale lanes.
+    float inv[V];
+    if constexpr (!kHead) {
+      // lanes i and NS + i serve side i
+      const float a = lane == 1u || lane == NS + 1u ? gm[NS - 1] : gm[0];
+      const bool inv_role = lane < NS;
+      const float res = a > 0.0f ? __fdiv_rn(inv_role ? p.fmax : a, inv_role ? a : p.fmax) : 1.0f;
+      if (!inv_role && lane < 2u * NS) p.side[NS == 2 ? lane - NS : w.kv].scales[slot * p.scales_stride] = res;
 #pragma unroll
-    for (int i = 0; i < NS; ++i)
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const float v = __shfl_sync(0xFFFFFFFFu, a[i][j], c0 % 32u);
-        if (lane / gps == static_cast<uint32_t>(i) && c0 / 32u == static_cast<uint32_t>(j)) amax_k = v;
+      for (int t = 0; t < V; ++t) inv[t] = __shfl_sync(0xFFFFFFFFu, res, static_cast<uint32_t>(t / J));
+    } else if (scatter) {
+      // In the g lanes of a group block, lane r holds word wb: for V >= 2 it
+      // serves value 2 wb + (r & 1), bit 1 of r picks the division; the lanes
+      // with the same word and r below 4 (below 2 for V = 1) store scales.
+      const uint32_t r = lane & (g - 1u);
+      const uint32_t sub = r & ((g >> S) - 1u);
+      const uint32_t t = V >= 2 ? 2u * wb + (r & 1u) : 0u;
+      const bool scale_role = V >= 2 ? ((r >> 1) & 1u) != 0u : (r & 1u) != 0u;
+      const float2 x = widen2<kBF16>(word);
+      const float a = fabsf(V >= 2 && (r & 1u) ? x.y : x.x);
+      const float res = a > 0.0f ? __fdiv_rn(scale_role ? a : p.fmax, scale_role ? p.fmax : a) : 1.0f;
+      if (scale_role && sub < (V >= 2 ? 4u : 2u)) {
+        const uint32_t j = t % J;
+        const uint32_t first = 32u * j + (lane & ~(g - 1u));  // the group's first chunk
+        if (first < n) p.side[NS == 2 ? t / J : w.kv].scales[slot * p.scales_stride + first / g] = res;
       }
-    const bool pos_k = amax_k > 0.0f;
-    const bool owner = lane < NS * gps;
-    const float inv_k = owner && pos_k ? __fdiv_rn(p.fmax, amax_k) : 1.0f;
-    if (owner) {
-      const DynSide& sd = p.side[NS == 2 ? lane / gps : w.kv];
-      sd.scales[slot * p.scales_stride + gk] = pos_k ? __fdiv_rn(amax_k, p.fmax) : 1.0f;
+      const uint32_t base = lane & ~(g - 1u);
+#pragma unroll
+      for (int u2 = 0; u2 < V; ++u2) {
+        // the inverse-scale lane of value u2: its word's scatter bits, and bit 0 = u2 & 1
+        uint32_t rl = V >= 2 ? static_cast<uint32_t>(u2 & 1) : 0u;
+#pragma unroll
+        for (int k = 0; k < S; ++k)
+          if ((u2 >> 1) & (W >> (k + 1))) rl += g >> (k + 1);
+        inv[u2] = __shfl_sync(0xFFFFFFFFu, res, base + rl);
+      }
+    } else {
+      // Small heads (fewer than 2V lanes to a group): the warp holds NS * gps
+      // groups (gps per side); lane k forms both divisions of group k, its
+      // maximum taken from the lane holding the group's first chunk, and
+      // every lane takes its chunks' inverse scales from the owners.
+      const uint32_t gps = n / g;
+      const uint32_t gk = lane % gps;          // lane's group within its side
+      const uint32_t c0 = gk * g;              // first chunk of that group
+      float amax_k = 0.0f;
+#pragma unroll
+      for (int t = 0; t < V; ++t) {
+        const float v = __shfl_sync(0xFFFFFFFFu, gm[t], c0 % 32u);
+        if (lane / gps == static_cast<uint32_t>(t / J) && c0 / 32u == static_cast<uint32_t>(t % J)) amax_k = v;
+      }
+      const bool pos_k = amax_k > 0.0f;
+      const bool owner = lane < NS * gps;
+      const float inv_k = owner && pos_k ? __fdiv_rn(p.fmax, amax_k) : 1.0f;
+      if (owner) {
+        const DynSide& sd = p.side[NS == 2 ? lane / gps : w.kv];
+        sd.scales[slot * p.scales_stride + gk] = pos_k ? __fdiv_rn(amax_k, p.fmax) : 1.0f;
+      }
+#pragma unroll
+      for (int t = 0; t < V; ++t) {
+        const uint32_t k = static_cast<uint32_t>(t / J) * gps + (lane + 32u * (t % J)) / g;
+        inv[t] = __shfl_sync(0xFFFFFFFFu, inv_k, k < 32u ? k : 0u);
+      }
     }
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
@@ -299,29 +418,42 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const uint32_t c = lane + 32u * j;
-        const uint32_t k = static_cast<uint32_t>(i) * gps + (g != 0 ? c / g : 0u);
-        const float inv = __shfl_sync(0xFFFFFFFFu, inv_k, k < 32u ? k : 0u);
-        if (c < n) st_stream(dst + static_cast<size_t>(c) * 16u, chunk_quant<16, kBF16, FMT>(buf[i][j], inv));
+        if (c < n) st_stream(dst + static_cast<size_t>(c) * 16u, chunk_quant<16, kBF16, FMT>(buf[i][j], inv[i * J + j]));
       }
     }
   }
   if (!KV_EARLY_TRIGGER) grid_dependents_launch();
 }
 
+// Per head, the warps of a multi-wave launch prefetch the rows one resident
+// wave ahead (launch_rows sets params.ahead); per token the look-ahead
+// measured slower and is compiled out.
+template <int J, int NS, bool kHead, typename IdxT, int FMT>
+kv_status launch_dyn_row_k(bool bf16, const DynRowParams& p, cudaStream_t stream, uint64_t bytes) {
+  if constexpr (kHead) {
+    if (bf16) return launch_rows(kv_fp8_dyn_row<J, NS, true, IdxT, true, FMT>, p.shape.num_units, p, stream, bytes);
+    return launch_rows(kv_fp8_dyn_row<J, NS, true, IdxT, false, FMT>, p.shape.num_units, p, stream, bytes);
+  } else {
+    if (bf16) return launch(kv_fp8_dyn_row<J, NS, false, IdxT, true, FMT>, p.shape.num_units, p, stream);
+    return launch(kv_fp8_dyn_row<J, NS, false, IdxT, false, FMT>, p.shape.num_units, p, stream);
+  }
+}
+
 template <int J, typename IdxT, int FMT>
 kv_status launch_dyn_row_j(bool bf16, const DynRowParams& p, cudaStream_t stream) {
   // bytes moved: each row's 32-byte input chunks read, 16-byte codes written
   const uint64_t bytes = p.shape.num_units * p.chunks * 48u;
+  const bool head = p.group_chunks != 0;
   if (p.shape.num_units >= KV_LARGE_LAUNCH_WARPS) {
     DynRowParams q = p;   // one warp per token: K and V rows together
     q.shape.units_per_token = 1;
     q.shape.units_per_side = 1;
     q.shape.num_units /= 2;
-    if (bf16) return launch_rows(kv_fp8_dyn_row<J, 2, IdxT, true, FMT>, q.shape.num_units, q, stream, bytes);
-    return launch_rows(kv_fp8_dyn_row<J, 2, IdxT, false, FMT>, q.shape.num_units, q, stream, bytes);
+    return head ? launch_dyn_row_k<J, 2, true, IdxT, FMT>(bf16, q, stream, bytes)
+                : launch_dyn_row_k<J, 2, false, IdxT, FMT>(bf16, q, stream, bytes);
   }
-  if (bf16) return launch_rows(kv_fp8_dyn_row<J, 1, IdxT, true, FMT>, p.shape.num_units, p, stream, bytes);
-  return launch_rows(kv_fp8_dyn_row<J, 1, IdxT, false, FMT>, p.shape.num_units, p, stream, bytes);
+  return head ? launch_dyn_row_k<J, 1, true, IdxT, FMT>(bf16, p, stream, bytes)
+              : launch_dyn_row_k<J, 1, false, IdxT, FMT>(bf16, p, stream, bytes);
 }
 
 template <typename IdxT, int FMT>

@@ -169,8 +169,7 @@ __global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant
   float m[2] = {m0, m1};
 #pragma unroll
   for (int kv = 0; kv < 2; ++kv) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m[kv] = fmaxf(m[kv], __shfl_xor_sync(0xFFFFFFFFu, m[kv], o));
+    m[kv] = warp_absmax(m[kv]);
     if (lane == 0) part[kv][warp] = m[kv];
   }
   __syncthreads();

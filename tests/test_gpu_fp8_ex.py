@@ -125,6 +125,13 @@ CASES = {
     "staged_h2_d512": dict(T=700, H=2, D=512, n_slots=2048),
     "staged_h1_d1024_f16": dict(T=650, H=1, D=1024, n_slots=2048, src_dtype="f16"),
     "staged_many_tokens": dict(T=20000, H=8, D=128, n_slots=65536, page_size=32),
+    # paired rows of one chunk per lane: per head the two divisions of a
+    # group fit its 4 lanes (D=64), or not (D=32: the owner-lane form)
+    "paired_h4_d64": dict(T=2500, H=4, D=64, n_slots=8192, page_size=16),
+    "paired_h8_d32_i32": dict(T=2200, H=8, D=32, n_slots=8192, idx_dtype=np.int32),
+    # paired rows of 2 and 4 chunks per lane with 16-lane heads (D=256)
+    "paired_h4_d256": dict(T=2100, H=4, D=256, n_slots=4096, page_size=8),
+    "paired_h8_d256_i32": dict(T=2100, H=8, D=256, n_slots=4096, idx_dtype=np.int32),
 }
 
 
