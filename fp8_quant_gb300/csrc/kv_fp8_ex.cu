@@ -218,7 +218,7 @@ struct DynRowParams {
   int64_t index_stride, size_limit, page_size, scales_stride;
   UnitShape shape;          // units: (token, K|V) rows, or tokens when paired
   uint32_t chunks;          // 16-element chunks per row
-  uint32_t group_chunks;    // chunks per scale group (D / 16), or 0: the whole row
+  uint32_t group_chunks;    // chunks per scale group (D / 16, a power of two), or 0: the whole row
   float fmax;
   kv_error_record* err;
   int prefetch;             // rows in device memory: bulk L2 prefetch allowed
@@ -226,12 +226,14 @@ struct DynRowParams {
 };
 
 template <int J, int NS, bool kHead, typename IdxT, bool kBF16, int FMT>
-__global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant__ DynRowParams p) {
+__global__ void __launch_bounds__(kThreads, 65536 / (kThreads * (J * NS <= 4 ? 64 : 128)))
+    kv_fp8_dyn_row(const __grid_constant__ DynRowParams p) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
   uint64_t u = static_cast<uint64_t>(blockIdx.x) * warps_per_cta() + (threadIdx.x >> 5);
   const uint32_t n = p.chunks;
   const uint32_t g = p.group_chunks;
+  const uint32_t gsh = g != 0u ? static_cast<uint32_t>(__ffs(g) - 1) : 0u;  // log2(g)
   if (KV_PREFETCH && p.prefetch && lane == 0 && u < p.shape.num_units) {
     const Unit w = decode_unit(p.shape, u);
 #pragma unroll
@@ -372,7 +374,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant
       if (scale_role && sub < (V >= 2 ? 4u : 2u)) {
         const uint32_t j = t % J;
         const uint32_t first = 32u * j + (lane & ~(g - 1u));  // the group's first chunk
-        if (first < n) p.side[NS == 2 ? t / J : w.kv].scales[slot * p.scales_stride + first / g] = res;
+        if (first < n) p.side[NS == 2 ? t / J : w.kv].scales[slot * p.scales_stride + (first >> gsh)] = res;
       }
       const uint32_t base = lane & ~(g - 1u);
 #pragma unroll
@@ -389,7 +391,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant
       // groups (gps per side); lane k forms both divisions of group k, its
       // maximum taken from the lane holding the group's first chunk, and
       // every lane takes its chunks' inverse scales from the owners.
-      const uint32_t gps = n / g;
+      const uint32_t gps = n >> gsh;
       const uint32_t gk = lane % gps;          // lane's group within its side
       const uint32_t c0 = gk * g;              // first chunk of that group
       float amax_k = 0.0f;
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dyn_row(const __grid_constant
       }
 #pragma unroll
       for (int t = 0; t < V; ++t) {
-        const uint32_t k = static_cast<uint32_t>(t / J) * gps + (lane + 32u * (t % J)) / g;
+        const uint32_t k = static_cast<uint32_t>(t / J) * gps + ((lane + 32u * (t % J)) >> gsh);
         inv[t] = __shfl_sync(0xFFFFFFFFu, inv_k, k < 32u ? k : 0u);
       }
     }
