@@ -9,12 +9,15 @@
 // amax is 0); codes = fp8(x * inv); `scale` goes to the caller's per-slot
 // scale cache.  fmax is 448 for e4m3fn and 57344 for e5m2.
 //
-// One warp owns one group.  The group's elements are loaded once into
-// registers (up to 4 chunks per lane, 2 for 16-byte chunks; longer groups
-// are re-read from L2 in a second pass), the warp reduces amax with shuffles, then converts and stores
-// the codes and lane 0 stores the group's scale.  As in the other write
-// kernels, the group's source bytes are prefetched into L2 before the
-// programmatic-launch wait.
+// Two kernels.  kv_fp8_dyn_row takes rows whose heads are contiguous (the
+// common layout): the static write's lane layout, each group's amax reduced
+// over the lanes that hold it, one division per warp (see there).  The
+// general kernel kv_fp8_dyn_rows takes every other layout: one warp owns one
+// group, whose elements are loaded once into registers (up to 4 chunks per
+// lane, 2 for 16-byte chunks; longer groups are re-read from L2 in a second
+// pass); the warp reduces amax, then converts and stores the codes, and lane
+// 0 stores the group's scale.  As in the other write kernels, the source
+// bytes are prefetched into L2 before the programmatic-launch wait.
 #include "kv_host.h"
 
 #ifndef KV_DYN_LOOKAHEAD
