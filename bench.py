@@ -87,13 +87,16 @@ DESCRIPTIONS = {
                   "1,048,576-slot cache, page_size 32, int64",
     "absmax": "per-tensor scale pass: max |x| of the fp8 batch's K and V (8192 x 8 x 128 bf16 "
               "each) and inv = 448/amax on the device",
+    "fp8_tensor_dynamic": "fused dynamic per-tensor FP8 write: the fp8 batch, amax of K and of V "
+                          "over the batch, inv = 448/amax and the e4m3fn write in one call "
+                          "(kv_store_fp8_dynamic_tensor, two launches)",
 }
 
 DEFAULT_STEPS = {"tiny": 200000, "decode": 200000, "prefill": 10000, "fp8": 50000,
                  "fp8_noscale": 50000, "strided": 5000, "odd": 10000, "gather_decode": 200000,
                  "gather_fp8": 50000, "absmax": 50000, "fp8_dynamic": 50000, "paged": 10000,
                  "fp8_dynamic_token": 50000, "fp8_e5m2": 50000, "fp8_page": 50000,
-                 "gather_prefill": 10000}
+                 "gather_prefill": 10000, "fp8_tensor_dynamic": 50000}
 
 
 # ---------------------------------------------------------------------------
@@ -299,10 +302,14 @@ class Pool:
         self.scale = torch.ones(2, dtype=torch.float32, device=device) / self.inv
         self.amax_inv = torch.zeros(4, dtype=torch.float32, device=device)
         self.absmax_work = torch.zeros(4, dtype=torch.int32, device=device)
+        self.dyn_work = torch.zeros(3, dtype=torch.int64, device=device)   # fused dynamic write
+        self.dyn_scale = torch.zeros(2, dtype=torch.float32, device=device)
         self.err = torch.zeros(2, dtype=torch.int64, device=device)
         self.i64 = idx_dtype == torch.int64
-        # kernels one call launches: kv_absmax_inv with a workspace reduces and finishes
-        self.launches_per_call = 2 if w.kind == "absmax" else 1
+        # kernels one call launches: kv_absmax_inv with a workspace reduces and
+        # finishes; the fused dynamic write reduces and writes
+        dyn = w.notes.get("scale_mode") == "tensor_dynamic"
+        self.launches_per_call = 2 if w.kind == "absmax" or dyn else 1
 
     def _slots(self, g, idx_dtype):
         import torch
@@ -354,6 +361,13 @@ class Pool:
                                           3 if self.groups > 1 else 2, None, None,
                                           self.ks.data_ptr(), self.vs.data_ptr(), self.groups,
                                           self.err.data_ptr(), stream_handle)
+        if w.notes.get("scale_mode") == "tensor_dynamic":
+            return kv.raw.kv_store_fp8_dynamic_tensor(
+                k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(), idx_ptr, idt, 1, w.T, w.H,
+                w.D, 1 if w.src_dtype == "bf16" else 0, strides, w.page_size, w.page_stride,
+                w.page_stride, w.n_slots, 0, self.dyn_scale.data_ptr(),
+                self.dyn_scale.data_ptr() + 4, self.dyn_work.data_ptr(), self.err.data_ptr(),
+                stream_handle)
         if w.notes.get("scale_mode") == "page":
             return kv.raw.kv_store_fp8_ex(k_ptr, v_ptr, self.kc.data_ptr(), self.vc.data_ptr(),
                                           idx_ptr, idt, 1, w.T, w.H, w.D,
@@ -735,6 +749,13 @@ def oracle_step(name, w, tokens, t_begin=0):
                             w.page_stride, w.page_stride, w.n_slots, fmt="e4m3fn",
                             scale_mode=mode, k_scales=ks, v_scales=vs,
                             scales_slot_stride=w.H if mode == "token_head" else 1, t_end=tokens)
+    elif w.notes.get("scale_mode") == "tensor_dynamic":
+        _, inv = oracle.absmax_inv(k, v, st, tokens, w.H, w.D, w.src_dtype, 448.0,
+                                   k_off=w.k_view[0], v_off=w.v_view[0])
+        oracle.store_fp8_ex(k, v, kc, vc, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
+                            w.page_stride, w.page_stride, w.n_slots, fmt="e4m3fn",
+                            scale_mode="tensor", inv_k=float(inv[0]), inv_v=float(inv[1]),
+                            t_end=tokens)
     elif w.notes.get("scale_mode") == "page":
         oracle.store_fp8_ex(k, v, kc, vc, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
                             w.page_stride, w.page_stride, w.n_slots, fmt="e4m3fn",
@@ -766,7 +787,7 @@ def dtype_of(w):
 # e5m2, dynamic scales, the gathers and the per-tensor scale pass.
 SUITE_CONFIGS = ("decode", "prefill", "fp8", "fp8_noscale", "strided", "odd")
 SUITE_MORE = ("paged", "fp8_e5m2", "fp8_page", "fp8_dynamic", "fp8_dynamic_token", "gather_decode",
-              "gather_prefill", "gather_fp8", "absmax")
+              "gather_prefill", "gather_fp8", "absmax", "fp8_tensor_dynamic")
 HEADLINE = "strided"
 
 

@@ -11,7 +11,8 @@ the same names:
 * :func:`kv_store_paged`, :func:`kv_store_fp8_ex` (e5m2; scales per tensor, or
   per token row / per (token, head) computed in the kernel),
   :func:`kv_gather`, :func:`kv_gather_fp8` (the inverse), :func:`kv_inv_scale`,
-  :func:`kv_absmax_inv` (scale preparation).
+  :func:`kv_absmax_inv` (scale preparation), :func:`kv_store_fp8_dynamic_tensor`
+  (per-tensor scales formed from the batch and the write, in one call).
 * :func:`kv_error_poll`, :func:`kv_error_reset`, :func:`kv_status_str`.
 
 The tensor-level functions take torch tensors (device memory and streams come
@@ -35,7 +36,7 @@ __all__ = [
     "KVStatus", "KVError", "kv_store", "kv_store_fp8", "kv_store_paged", "kv_store_fp8_ex",
     "kv_gather", "kv_gather_fp8", "kv_inv_scale", "kv_absmax_inv", "kv_error_poll",
     "kv_error_reset", "kv_status_str", "error_record", "load_library", "raw", "STRIDE_FIELDS",
-    "fused_fp8_set_kv_buffer",
+    "fused_fp8_set_kv_buffer", "kv_store_fp8_dynamic_tensor", "DYNAMIC_TENSOR_WORK_BYTES",
 ]
 
 
@@ -110,6 +111,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.kv_absmax_inv.argtypes = [P, P, I32, I64, I32, I32, ctypes.POINTER(_Strides),
                                       ctypes.c_float, P, P, P, P]
         lib.kv_absmax_inv.restype = I32
+        lib.kv_store_fp8_dynamic_tensor.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
+                                                    ctypes.POINTER(_Strides), I64, I64, I64, I64,
+                                                    I32, P, P, P, P, P]
+        lib.kv_store_fp8_dynamic_tensor.restype = I32
         lib.kv_store_noalloc.argtypes = [P, P, P, P, P, I32, I64, I64, I32, I32, I32,
                                          ctypes.POINTER(_Strides), I64, I32,
                                          ctypes.POINTER(I64), ctypes.POINTER(I64), P]
@@ -224,6 +229,18 @@ class raw:
                                               kc_page_stride, vc_page_stride, size_limit, fmt,
                                               scale_mode, inv_k_scale, inv_v_scale, k_scales,
                                               v_scales, scales_slot_stride, d_err, stream)
+
+    @staticmethod
+    def kv_store_fp8_dynamic_tensor(k, v, k_cache, v_cache, indices, index_dtype, index_stride,
+                                    num_tokens, num_heads, head_dim, src_dtype,
+                                    strides: Sequence[int], page_size, kc_page_stride,
+                                    vc_page_stride, size_limit, fmt, k_scale, v_scale, work,
+                                    d_err, stream) -> int:
+        st = _Strides(*[int(x) for x in strides])
+        return load_library().kv_store_fp8_dynamic_tensor(
+            k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_tokens, num_heads,
+            head_dim, src_dtype, ctypes.byref(st), page_size, kc_page_stride, vc_page_stride,
+            size_limit, fmt, k_scale, v_scale, work, d_err, stream)
 
     @staticmethod
     def kv_gather_fp8_ex(k_cache, v_cache, k_out, v_out, indices, index_dtype, index_stride,
@@ -530,6 +547,46 @@ def kv_store_fp8_ex(k, v, k_cache, v_cache, indices, *, page_size: int = 1,
         _device_ptr_or_none(inv_k_scale), _device_ptr_or_none(inv_v_scale),
         _device_ptr_or_none(k_scales), _device_ptr_or_none(v_scales), sstride, rec.data_ptr(),
         _stream_handle(stream, k.device)), "kv_store_fp8_ex")
+
+
+DYNAMIC_TENSOR_WORK_BYTES = 24  # KV_DYNAMIC_TENSOR_WORK_BYTES of the C header
+
+
+def kv_store_fp8_dynamic_tensor(k, v, k_cache, v_cache, indices, *, page_size: int = 1,
+                                fmt: str = "e4m3fn", scales=None, work=None, size_limit=None,
+                                err=None, stream=None):
+    """FP8 write with per-tensor scales formed from the batch, in one call:
+    amax over all K (V) rows, inv = fmax / amax, codes fp8(x * inv).  Returns
+    ``scales``: a 2-element fp32 device tensor receiving the forward scales
+    amax / fmax (K, V).  ``work``: a device tensor of at least
+    DYNAMIC_TENSOR_WORK_BYTES bytes, zero before its first use and reused
+    across calls on one stream (a fresh zeroed one when None)."""
+    import torch
+    slots, H, D = _cache_shape(k_cache)
+    kt, kh, kd = _rows3(k, H, D)
+    vt, vh, vd = _rows3(v, H, D)
+    ks, khc, kdc, kp = _paged_cache(k_cache, page_size, H, D)
+    vs, vhc, vdc, vp = _paged_cache(v_cache, page_size, H, D)
+    idt, istride = _index_args(indices)
+    if k.dtype not in (torch.bfloat16, torch.float16) or v.dtype != k.dtype:
+        raise TypeError("K and V must both be bf16 or both fp16")
+    if scales is None:
+        scales = torch.empty(2, dtype=torch.float32, device=k.device)
+    if scales.dtype != torch.float32 or scales.numel() < 2 or not scales.is_contiguous():
+        raise TypeError("scales must be a contiguous fp32 tensor of 2 elements")
+    if work is None:
+        work = torch.zeros(DYNAMIC_TENSOR_WORK_BYTES // 8, dtype=torch.int64, device=k.device)
+    if work.numel() * work.element_size() < DYNAMIC_TENSOR_WORK_BYTES:
+        raise ValueError(f"work holds fewer than {DYNAMIC_TENSOR_WORK_BYTES} bytes")
+    rec = err if err is not None else _default_record(k.device)
+    _check(raw.kv_store_fp8_dynamic_tensor(
+        k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), indices.data_ptr(),
+        idt, istride, indices.shape[0], H, D, 1 if k.dtype == torch.bfloat16 else 0,
+        (kt, kh, kd, vt, vh, vd, ks, khc, kdc, vs, vhc, vdc), page_size, kp, vp,
+        slots if size_limit is None else size_limit, FP8_FORMATS[fmt], scales.data_ptr(),
+        scales.data_ptr() + 4, work.data_ptr(), rec.data_ptr(), _stream_handle(stream, k.device)),
+        "kv_store_fp8_dynamic_tensor")
+    return scales
 
 
 def kv_gather(k_cache, v_cache, k_out, v_out, indices, *, page_size: int = 1, size_limit=None,

@@ -22,9 +22,21 @@ kv_status cuda_fail(cudaError_t e);
 // kernels may prefetch inputs into L2 with bulk copies.
 kv_status classify_inputs(const void* const* ptrs, int n, bool* all_device);
 
+// The fused dynamic per-tensor write's state (kv_store_fp8_dynamic_tensor):
+// work = {generation, tagged K maximum, tagged V maximum}, each tagged word
+// (generation << 16) | the 16-bit pattern of max |x|; scale_out receives the
+// forward scales amax / fmax.
+struct DynTensor {
+  uint64_t* work;
+  float* scale_out[2];
+  float fmax;
+};
+
 // The FP8 write with a per-tensor inverse scale (or none), or one inverse
 // scale per page of scale_page slots (scale_page > 0), in format fmt
 // (kFmtE4M3 / kFmtE5M2): kv_store_fp8 and the static modes of kv_store_fp8_ex.
+// dyn non-null: the inverse scales come from the tagged maxima instead (the
+// fused dynamic per-tensor write; inv pointers unused, use_scale 1).
 kv_status store_fp8_static(const void* k, const void* v, void* k_cache, void* v_cache,
                            const void* indices, kv_index_dtype index_dtype, int64_t index_stride,
                            int64_t num_tokens, int32_t num_heads, int32_t head_dim,
@@ -32,7 +44,14 @@ kv_status store_fp8_static(const void* k, const void* v, void* k_cache, void* v_
                            int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit,
                            const float* inv_k_scale, const float* inv_v_scale, int32_t use_scale,
                            int64_t scale_page, int fmt, kv_error_record* d_err,
-                           kv_stream_t stream);
+                           kv_stream_t stream, const DynTensor* dyn = nullptr);
+
+// The absmax reduction (kv_scale.cu) into acc (two 32-bit float-bit
+// accumulators) or, when tagged is non-null, into the fused write's tagged
+// workspace.  The callers check the arguments; num_tokens > 0.
+kv_status absmax_reduce(const void* k, const void* v, kv_src_dtype src_dtype, int64_t num_tokens,
+                        int32_t num_heads, int32_t head_dim, const kv_strides* s,
+                        unsigned int* acc, uint64_t* tagged, bool on_device, cudaStream_t stream);
 kv_status current_sm_count(int* out);
 kv_status blocks_per_sm(const void* fn, int threads, int* out);
 

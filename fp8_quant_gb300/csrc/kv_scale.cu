@@ -64,6 +64,7 @@ struct AbsmaxParams {
   int64_t token[2], seg[2];  // byte strides of the rows and of their segments
   UnitShape shape;           // units: (token, K|V, segment); parts = 1
   unsigned int* amax_bits;   // two accumulator words: K, V
+  uint64_t* tagged;          // non-null: the tagged accumulators of the fused dynamic write instead
   int vec;                   // bytes per chunk
   int prefetch;              // rows are device memory with 16-byte aligned segments
 };
@@ -177,7 +178,18 @@ __global__ void __launch_bounds__(kThreads) kv_absmax_rows(const __grid_constant
     float v = 0.0f;
 #pragma unroll
     for (uint32_t i = 0; i < warps_per_cta(); ++i) v = fmaxf(v, part[threadIdx.x][i]);
-    if (v > 0.0f) atomicMax(p.amax_bits + threadIdx.x, __float_as_uint(v));
+    if (p.tagged != nullptr) {
+      // (generation << 16) | the maximum's 16-bit pattern (exact: a maximum of
+      // 16-bit inputs is one of them; non-negative patterns order like their
+      // values), so a later call's words always win: nothing is cleared
+      const uint64_t gen = p.tagged[0];
+      const uint32_t bits = kBF16 ? (__float_as_uint(v) >> 16)
+                                  : static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v)));
+      atomicMax(reinterpret_cast<unsigned long long*>(p.tagged + 1 + threadIdx.x),
+                static_cast<unsigned long long>((gen << 16) | bits));
+    } else if (v > 0.0f) {
+      atomicMax(p.amax_bits + threadIdx.x, __float_as_uint(v));
+    }
   }
 }
 
@@ -230,6 +242,54 @@ extern "C" kv_status kv_inv_scale(const float* scale, float* inv, int64_t n, kv_
                 reinterpret_cast<cudaStream_t>(stream_));
 }
 
+// The reduction launch shared by kv_absmax_inv and the fused dynamic
+// per-tensor write: acc (two 32-bit words, float bits) or tagged (the fused
+// write's workspace).  Arguments are checked by the callers; num_tokens > 0.
+kv_status kvimpl::absmax_reduce(const void* k, const void* v, kv_src_dtype src_dtype,
+                                int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                                const kv_strides* s, unsigned int* acc, uint64_t* tagged,
+                                bool on_device, cudaStream_t stream) {
+  const int64_t head_bytes = 2 * static_cast<int64_t>(head_dim);
+  const bool merged = num_heads == 1 || (s->k_head == head_bytes && s->v_head == head_bytes);
+  const uint32_t nseg = merged ? 1u : static_cast<uint32_t>(num_heads);
+  const int64_t seg_bytes = merged ? head_bytes * num_heads : head_bytes;
+  uint64_t bits = u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token) | u64(seg_bytes);
+  if (!merged) bits |= u64(s->k_head) | u64(s->v_head);
+  const int vec = pow2_align(bits);
+  AbsmaxParams p = {};
+  p.src[0] = static_cast<const uint8_t*>(k);
+  p.src[1] = static_cast<const uint8_t*>(v);
+  p.token[0] = s->k_token;
+  p.token[1] = s->v_token;
+  p.seg[0] = s->k_head;
+  p.seg[1] = s->v_head;
+  p.shape.parts = 1;
+  p.shape.units_per_side = nseg;
+  p.shape.units_per_token = 2u * nseg;
+  p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
+  p.shape.part_chunks = static_cast<uint32_t>(seg_bytes / vec);
+  p.amax_bits = acc;
+  p.tagged = tagged;
+  p.vec = vec;
+  p.prefetch = vec >= 16 && on_device ? 1 : 0;
+  // a resident grid of a few CTAs per SM loops over the rows, so only a few
+  // hundred same-address atomics land at the end
+  int sms = 0;
+  const kv_status st = current_sm_count(&sms);
+  if (st != KV_OK) return st;
+  const uint64_t max_ctas = static_cast<uint64_t>(sms) * KV_ABSMAX_CTAS_PER_SM;
+  const bool bf16 = src_dtype == KV_SRC_BF16;
+  switch (vec) {
+#if KV_MAX_VEC >= 32
+    case 32: return launch_absmax<32>(bf16, p, stream, max_ctas);
+#endif
+    case 16: return launch_absmax<16>(bf16, p, stream, max_ctas);
+    case 8: return launch_absmax<8>(bf16, p, stream, max_ctas);
+    case 4: return launch_absmax<4>(bf16, p, stream, max_ctas);
+    default: return launch_absmax<2>(bf16, p, stream, max_ctas);
+  }
+}
+
 extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype src_dtype,
                                    int64_t num_tokens, int32_t num_heads, int32_t head_dim,
                                    const kv_strides* s, float fp8_max, float* amax, float* inv,
@@ -263,44 +323,8 @@ extern "C" kv_status kv_absmax_inv(const void* k, const void* v, kv_src_dtype sr
     if (st != KV_OK) return st;
   }
   if (num_tokens > 0) {
-    const int64_t head_bytes = 2 * static_cast<int64_t>(head_dim);
-    const bool merged = num_heads == 1 || (s->k_head == head_bytes && s->v_head == head_bytes);
-    const uint32_t nseg = merged ? 1u : static_cast<uint32_t>(num_heads);
-    const int64_t seg_bytes = merged ? head_bytes * num_heads : head_bytes;
-    uint64_t bits = u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token) | u64(seg_bytes);
-    if (!merged) bits |= u64(s->k_head) | u64(s->v_head);
-    const int vec = pow2_align(bits);
-    AbsmaxParams p = {};
-    p.src[0] = static_cast<const uint8_t*>(k);
-    p.src[1] = static_cast<const uint8_t*>(v);
-    p.token[0] = s->k_token;
-    p.token[1] = s->v_token;
-    p.seg[0] = s->k_head;
-    p.seg[1] = s->v_head;
-    p.shape.parts = 1;
-    p.shape.units_per_side = nseg;
-    p.shape.units_per_token = 2u * nseg;
-    p.shape.num_units = static_cast<uint64_t>(num_tokens) * p.shape.units_per_token;
-    p.shape.part_chunks = static_cast<uint32_t>(seg_bytes / vec);
-    p.amax_bits = acc;
-    p.vec = vec;
-    p.prefetch = vec >= 16 && on_device ? 1 : 0;
-    // a resident grid of a few CTAs per SM loops over the rows, so only a few
-    // hundred same-address atomics land at the end
-    int sms = 0;
-    st = current_sm_count(&sms);
-    if (st != KV_OK) return st;
-    const uint64_t max_ctas = static_cast<uint64_t>(sms) * KV_ABSMAX_CTAS_PER_SM;
-    const bool bf16 = src_dtype == KV_SRC_BF16;
-    switch (vec) {
-#if KV_MAX_VEC >= 32
-      case 32: st = launch_absmax<32>(bf16, p, stream, max_ctas); break;
-#endif
-      case 16: st = launch_absmax<16>(bf16, p, stream, max_ctas); break;
-      case 8: st = launch_absmax<8>(bf16, p, stream, max_ctas); break;
-      case 4: st = launch_absmax<4>(bf16, p, stream, max_ctas); break;
-      default: st = launch_absmax<2>(bf16, p, stream, max_ctas); break;
-    }
+    st = absmax_reduce(k, v, src_dtype, num_tokens, num_heads, head_dim, s, acc, nullptr, on_device,
+                       stream);
     if (st != KV_OK) return st;
   }
   return launch(kv_absmax_finish, 1, FinishParams{acc, amax, inv, fp8_max, work != nullptr ? 1 : 0},

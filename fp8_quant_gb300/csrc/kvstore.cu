@@ -246,7 +246,30 @@ struct Fp8Params {
   kv_error_record* err;
   int prefetch;  // sources are 16-byte aligned: prefetch them into L2 before the grid wait
   int vec;       // bytes per chunk (the kernel's VEC / OUT)
+  DynTensor dyn; // dyn.work non-null: the fused dynamic per-tensor write
 };
+
+// The fused dynamic per-tensor write, after the grid wait: both sides'
+// inverse scales fmax / amax from the tagged maxima the reduction left in
+// the workspace (1 when amax is 0).  One thread of the grid also writes the
+// forward scales amax / fmax and moves the workspace to the next generation;
+// the other threads read only the tagged words, which that store leaves alone.
+template <bool kBF16>
+__device__ __forceinline__ void dyn_tensor_inv(const DynTensor& d, float* inv) {
+  float amax[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t bits = static_cast<uint32_t>(d.work[1 + i]) & 0xFFFFu;
+    amax[i] = kBF16 ? __uint_as_float(bits << 16)
+                    : __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+    inv[i] = amax[i] > 0.0f ? __fdiv_rn(d.fmax, amax[i]) : 1.0f;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) d.scale_out[i][0] = amax[i] > 0.0f ? __fdiv_rn(amax[i], d.fmax) : 1.0f;
+    d.work[0] = d.work[0] + 1u;
+  }
+}
 
 
 __device__ __forceinline__ const uint8_t* fp8_src(const Fp8Params& p, const Fp8Side& sd, const Unit& w) {
@@ -257,9 +280,11 @@ __device__ __forceinline__ const uint8_t* fp8_src(const Fp8Params& p, const Fp8S
 // One unit: loads (issued before the slot is known), bounds check, scale,
 // conversion and stores.  NS == 2 moves the K and the V part of the unit
 // (one slot load for both, twice the bytes in flight per warp), NS == 1 the
-// side w.kv.
-template <int OUT, int U, int NS, typename IdxT, bool kBF16, int FMT>
-__device__ __forceinline__ void fp8_unit(const Fp8Params& p, const Unit& w, uint32_t lane) {
+// side w.kv.  kDyn: the inverse scales are dyn_inv (K, V), from the fused
+// dynamic per-tensor write's prologue.
+template <int OUT, int U, int NS, typename IdxT, bool kBF16, int FMT, bool kDyn = false>
+__device__ __forceinline__ void fp8_unit(const Fp8Params& p, const Unit& w, uint32_t lane,
+                                         const float* dyn_inv = nullptr) {
   const uint32_t nchunks = p.shape.part_chunks;
   const int64_t part_out = static_cast<int64_t>(nchunks) * OUT;  // bytes out per part
   const int64_t slot = load_slot<IdxT>(p.indices, p.index_stride, w.token);
@@ -269,7 +294,8 @@ __device__ __forceinline__ void fp8_unit(const Fp8Params& p, const Unit& w, uint
   for (int i = 0; i < NS; ++i) {
     const Fp8Side& sd = p.side[NS == 2 ? i : w.kv];
     src[i] = fp8_src(p, sd, w);
-    inv[i] = sd.inv != nullptr && p.scale_page == 0 ? __ldg(sd.inv) : 1.0f;
+    if constexpr (kDyn) inv[i] = (NS == 2 ? i : static_cast<int>(w.kv)) != 0 ? dyn_inv[1] : dyn_inv[0];
+    else inv[i] = sd.inv != nullptr && p.scale_page == 0 ? __ldg(sd.inv) : 1.0f;
   }
   Fp8Chunk<OUT> buf[NS][U];
 #pragma unroll
@@ -320,7 +346,7 @@ __device__ __forceinline__ void fp8_unit(const Fp8Params& p, const Unit& w, uint
   }
 }
 
-template <int OUT, int U, int NS, typename IdxT, bool kBF16, int FMT>
+template <int OUT, int U, int NS, typename IdxT, bool kBF16, int FMT, bool kDyn>
 __global__ void __launch_bounds__(kThreads) kv_fp8_rows(const __grid_constant__ Fp8Params p) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
@@ -337,8 +363,10 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_rows(const __grid_constant__ 
   }
   grid_handover();
 
+  float dyn_inv[2] = {1.0f, 1.0f};
+  if constexpr (kDyn) dyn_tensor_inv<kBF16>(p.dyn, dyn_inv);
   while (u < p.shape.num_units) {
-    fp8_unit<OUT, U, NS, IdxT, kBF16, FMT>(p, w, lane);
+    fp8_unit<OUT, U, NS, IdxT, kBF16, FMT, kDyn>(p, w, lane, dyn_inv);
     u += nwarps;
     if (u >= p.shape.num_units) break;
     w = decode_unit(p.shape, u);
@@ -360,11 +388,14 @@ struct GenericFp8Params {
   uint64_t num_units;
   int32_t num_heads, head_dim;
   kv_error_record* err;
+  DynTensor dyn;       // as Fp8Params::dyn
 };
 
 template <typename IdxT, bool kBF16, int FMT>
 __global__ void __launch_bounds__(kThreads) kv_fp8_elements(const __grid_constant__ GenericFp8Params p) {
   grid_handover();
+  float dyn_inv[2] = {1.0f, 1.0f};
+  if (p.dyn.work != nullptr) dyn_tensor_inv<kBF16>(p.dyn, dyn_inv);
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * warps_per_cta();
   const uint64_t per_token = 2ull * static_cast<uint64_t>(p.num_heads);
@@ -379,7 +410,8 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_elements(const __grid_constan
       if (r == 0 && lane == 0) record_oob(p.err, static_cast<uint64_t>(t));
       continue;
     }
-    const float inv = p.inv[kv] == nullptr ? 1.0f
+    const float inv = p.dyn.work != nullptr ? (kv != 0 ? dyn_inv[1] : dyn_inv[0])
+                      : p.inv[kv] == nullptr ? 1.0f
                       : p.scale_page != 0 ? __ldg(p.inv[kv] + slot / p.scale_page)
                                           : __ldg(p.inv[kv]);
     const uint8_t* src = p.src[kv] + t * p.src_token[kv] + h * p.src_head[kv];
@@ -500,11 +532,19 @@ kv_status launch_fp8_fmt(bool bf16, const Fp8Params& p, cudaStream_t stream) {
     Fp8Params q = p;   // one warp per (token, segment, part): K and V together
     q.shape.units_per_token = q.shape.units_per_side;
     q.shape.num_units /= 2;
-    if (bf16) return launch(kv_fp8_rows<OUT, U, 2, IdxT, true, FMT>, q.shape.num_units, q, stream);
-    return launch(kv_fp8_rows<OUT, U, 2, IdxT, false, FMT>, q.shape.num_units, q, stream);
+    if (q.dyn.work != nullptr) {
+      if (bf16) return launch(kv_fp8_rows<OUT, U, 2, IdxT, true, FMT, true>, q.shape.num_units, q, stream);
+      return launch(kv_fp8_rows<OUT, U, 2, IdxT, false, FMT, true>, q.shape.num_units, q, stream);
+    }
+    if (bf16) return launch(kv_fp8_rows<OUT, U, 2, IdxT, true, FMT, false>, q.shape.num_units, q, stream);
+    return launch(kv_fp8_rows<OUT, U, 2, IdxT, false, FMT, false>, q.shape.num_units, q, stream);
   }
-  if (bf16) return launch(kv_fp8_rows<OUT, U, 1, IdxT, true, FMT>, p.shape.num_units, p, stream);
-  return launch(kv_fp8_rows<OUT, U, 1, IdxT, false, FMT>, p.shape.num_units, p, stream);
+  if (p.dyn.work != nullptr) {
+    if (bf16) return launch(kv_fp8_rows<OUT, U, 1, IdxT, true, FMT, true>, p.shape.num_units, p, stream);
+    return launch(kv_fp8_rows<OUT, U, 1, IdxT, false, FMT, true>, p.shape.num_units, p, stream);
+  }
+  if (bf16) return launch(kv_fp8_rows<OUT, U, 1, IdxT, true, FMT, false>, p.shape.num_units, p, stream);
+  return launch(kv_fp8_rows<OUT, U, 1, IdxT, false, FMT, false>, p.shape.num_units, p, stream);
 }
 
 template <int OUT, typename IdxT>
@@ -688,7 +728,8 @@ kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, 
                                    int64_t vc_page_stride, int64_t size_limit,
                                    const float* inv_k_scale, const float* inv_v_scale,
                                    int32_t use_scale, int64_t scale_page, int fmt,
-                                   kv_error_record* d_err, kv_stream_t stream_) {
+                                   kv_error_record* d_err, kv_stream_t stream_,
+                                   const DynTensor* dyn) {
   if (num_tokens < 0) return KV_ERR_INVALID_ARG;
   if (num_tokens == 0) return KV_OK;
   if (!common_args_ok(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_heads,
@@ -696,7 +737,7 @@ kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, 
     return KV_ERR_INVALID_ARG;
   if (src_dtype != KV_SRC_F16 && src_dtype != KV_SRC_BF16) return KV_ERR_INVALID_ARG;
   if (page_size < 1) return KV_ERR_INVALID_ARG;
-  if (use_scale && (!inv_k_scale || !inv_v_scale)) return KV_ERR_INVALID_ARG;
+  if (dyn == nullptr && use_scale && (!inv_k_scale || !inv_v_scale)) return KV_ERR_INVALID_ARG;
   if (use_scale && ((u64(inv_k_scale) | u64(inv_v_scale)) & 3u) != 0) return KV_ERR_INVALID_ARG;
   if (scale_page < 0 || (scale_page != 0 && !use_scale)) return KV_ERR_INVALID_ARG;
   const uint64_t src_bits = u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token) | u64(s->k_head) |
@@ -761,6 +802,7 @@ kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, 
     g.num_heads = num_heads;
     g.head_dim = head_dim;
     g.err = d_err;
+    if (dyn != nullptr) g.dyn = *dyn;
     return i64 ? launch_fp8_elements<int64_t>(fmt, bf16, g, stream)
                : launch_fp8_elements<int32_t>(fmt, bf16, g, stream);
   }
@@ -795,6 +837,7 @@ kv_status kvimpl::store_fp8_static(const void* k, const void* v, void* k_cache, 
   p.err = d_err;
   p.prefetch = out >= 8 && on_device ? 1 : 0;  // 2*OUT input bytes per chunk, 16-byte aligned
   p.vec = out;
+  if (dyn != nullptr) p.dyn = *dyn;
   return i64 ? launch_fp8<int64_t>(out, fmt, bf16, p, stream)
              : launch_fp8<int32_t>(out, fmt, bf16, p, stream);
 }
@@ -811,6 +854,58 @@ extern "C" kv_status kv_store_fp8(const void* k, const void* v, void* k_cache, v
                           num_heads, head_dim, src_dtype, s, page_size, kc_page_stride,
                           vc_page_stride, size_limit, inv_k_scale, inv_v_scale, use_scale, 0,
                           kFmtE4M3, d_err, stream);
+}
+
+extern "C" kv_status kv_store_fp8_dynamic_tensor(
+    const void* k, const void* v, void* k_cache, void* v_cache, const void* indices,
+    kv_index_dtype index_dtype, int64_t index_stride, int64_t num_tokens, int32_t num_heads,
+    int32_t head_dim, kv_src_dtype src_dtype, const kv_strides* s, int64_t page_size,
+    int64_t kc_page_stride, int64_t vc_page_stride, int64_t size_limit, kv_fp8_format format,
+    float* k_scale, float* v_scale, uint64_t* work, kv_error_record* d_err, kv_stream_t stream_) {
+  // Every check the two launches make comes first: once the reduction has
+  // run, the write must follow, or the workspace is left mid-call.
+  if (format != KV_FP8_E4M3FN && format != KV_FP8_E5M2) return KV_ERR_INVALID_ARG;
+  if (num_tokens < 0) return KV_ERR_INVALID_ARG;
+  if (!k_scale || !v_scale || !work || ((u64(k_scale) | u64(v_scale)) & 3u) != 0 ||
+      (u64(work) & 7u) != 0)
+    return KV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KV_OK;
+  if (!common_args_ok(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_heads,
+                      head_dim, s, size_limit, d_err))
+    return KV_ERR_INVALID_ARG;
+  if (src_dtype != KV_SRC_F16 && src_dtype != KV_SRC_BF16) return KV_ERR_INVALID_ARG;
+  if (page_size < 1) return KV_ERR_INVALID_ARG;
+  if (((u64(k) | u64(v) | u64(s->k_token) | u64(s->v_token) | u64(s->k_head) | u64(s->v_head)) &
+       1u) != 0)
+    return KV_ERR_INVALID_ARG;
+  if (s->k_dim != 2 || s->v_dim != 2) return KV_ERR_UNSUPPORTED;
+  if (num_tokens > (int64_t{1} << 40)) return KV_ERR_UNSUPPORTED;
+  // the workspace (64-bit atomics) and the scale outputs live in device memory
+  const void* dev_only[3] = {work, k_scale, v_scale};
+  for (const void* q : dev_only) {
+    cudaPointerAttributes a;
+    const cudaError_t e = cudaPointerGetAttributes(&a, q);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return cuda_fail(e);
+    }
+    if (a.type != cudaMemoryTypeDevice) return KV_ERR_INVALID_ARG;
+  }
+  bool on_device = true;
+  {
+    const void* in[3] = {k, v, indices};
+    const kv_status cs = classify_inputs(in, 3, &on_device);
+    if (cs != KV_OK) return cs;
+  }
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  kv_status st = absmax_reduce(k, v, src_dtype, num_tokens, num_heads, head_dim, s, nullptr, work,
+                               on_device, stream);
+  if (st != KV_OK) return st;
+  const DynTensor dyn{work, {k_scale, v_scale}, format == KV_FP8_E5M2 ? 57344.0f : 448.0f};
+  return store_fp8_static(k, v, k_cache, v_cache, indices, index_dtype, index_stride, num_tokens,
+                          num_heads, head_dim, src_dtype, s, page_size, kc_page_stride,
+                          vc_page_stride, size_limit, nullptr, nullptr, 1, 0,
+                          format == KV_FP8_E5M2 ? kFmtE5M2 : kFmtE4M3, d_err, stream_, &dyn);
 }
 
 extern "C" kv_status kv_error_poll(kv_error_record* d_err, kv_stream_t stream_, int64_t* oob_count,

@@ -363,6 +363,44 @@ kv_status kv_absmax_inv(const void *k, const void *v, kv_src_dtype src_dtype,
                         uint32_t *work, kv_stream_t stream);
 
 /*
+ * kv_store_fp8_dynamic_tensor -- the FP8 write with per-tensor scales formed
+ * from the batch itself, in one call: the fused form of kv_absmax_inv
+ * followed by kv_store_fp8_ex in KV_SCALE_TENSOR mode (the trtllm page's
+ * docstring names "scale computation" but its kernel takes a given scale;
+ * the recipe is the per-tensor one, inv = fmax / amax).
+ *   amax_k = max |K| and amax_v = max |V| over all num_tokens rows (NaN
+ *   elements ignored; out-of-range slots do not exclude their rows), then
+ *   inv = fmax / amax in fp32 round-to-nearest (1.0 when amax is 0) and the
+ *   codes fp8(fl32(x * inv)) as kv_store_fp8_ex writes them; fmax is 448
+ *   (e4m3fn) or 57344 (e5m2).  *k_scale / *v_scale receive the forward
+ *   (dequantisation) scales amax / fmax (1.0 when amax is 0), what
+ *   kv_gather_fp8_ex takes in KV_SCALE_TENSOR mode.
+ * Arguments as kv_store_fp8_ex, plus:
+ *   k_scale, v_scale  device pointers to one float each (4-byte aligned).
+ *   work   device workspace of KV_DYNAMIC_TENSOR_WORK_BYTES (8-byte aligned),
+ *          owned by the caller, zero before its first use.  It holds a
+ *          generation counter and the two maxima tagged with it, so a call
+ *          needs no clearing pass: two kernels (the reduction, then the
+ *          write, which forms the inverse scales in its prologue).  Calls
+ *          sharing one workspace must not overlap on the GPU; calls on one
+ *          stream never do.  After a KV_ERR_CUDA return its contents are
+ *          undefined: zero it again before the next call.
+ * Dims must be contiguous on the input side (k_dim = v_dim = 2; else
+ * KV_ERR_UNSUPPORTED); the cache side may use any layout kv_store_fp8_ex
+ * takes.  num_tokens == 0: KV_OK, nothing launched, nothing written.
+ */
+#define KV_DYNAMIC_TENSOR_WORK_BYTES 24
+kv_status kv_store_fp8_dynamic_tensor(const void *k, const void *v, void *k_cache,
+                                      void *v_cache, const void *indices,
+                                      kv_index_dtype index_dtype, int64_t index_stride,
+                                      int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                                      kv_src_dtype src_dtype, const kv_strides *strides,
+                                      int64_t page_size, int64_t kc_page_stride,
+                                      int64_t vc_page_stride, int64_t size_limit,
+                                      kv_fp8_format format, float *k_scale, float *v_scale,
+                                      uint64_t *work, kv_error_record *d_err, kv_stream_t stream);
+
+/*
  * kv_store_noalloc -- kv_store for callers that cannot allocate device memory.
  * The pages have no counterpart; this entry point exists for this library's
  * users only.

@@ -175,3 +175,30 @@ def test_per_page_scale_mode_rejects_bad_arguments(lib, over):
 def test_per_page_scale_mode_valid_calls_need_a_gpu(lib):
     assert store8ex() == CUDA
     assert gather8ex() == CUDA
+
+
+def store8dyn(**over):
+    a = dict(k=A, v=A, k_cache=A, v_cache=A, indices=A, index_dtype=1, index_stride=1,
+             num_tokens=16, num_heads=8, head_dim=128, src_dtype=1, strides=S8, page_size=16,
+             kc_page_stride=16 * 2048, vc_page_stride=16 * 2048, size_limit=100, fmt=0,
+             k_scale=A, v_scale=A + 4, work=A, d_err=A, stream=None)
+    a.update(over)
+    return kv.raw.kv_store_fp8_dynamic_tensor(**a)
+
+
+@pytest.mark.parametrize("over", [
+    dict(k_scale=None), dict(v_scale=None), dict(work=None), dict(work=A + 4),
+    dict(k_scale=A + 2), dict(fmt=2), dict(num_tokens=-1), dict(d_err=None), dict(page_size=0),
+    dict(src_dtype=2), dict(k=A + 1), dict(strides=(4097,) + S8[1:]),
+])
+def test_dynamic_tensor_write_rejects_bad_arguments(lib, over):
+    """Every argument error is found before anything is launched (a reduction
+    that ran without its write would leave the workspace mid-call)."""
+    assert store8dyn(**over) == INVALID
+
+
+def test_dynamic_tensor_write_dims_and_empty_batch(lib):
+    assert store8dyn(strides=(4096, 256, 4) + S8[3:]) == kv.KVStatus.ERR_UNSUPPORTED
+    assert store8dyn(num_tokens=0, k=None, v=None, k_cache=None, v_cache=None, indices=None,
+                     d_err=None) == 0
+    assert store8dyn() == CUDA          # valid arguments: the device checks need a GPU

@@ -277,3 +277,45 @@ def test_full_size_per_page_scales():
         assert _rows_changed(torch, cache, w.n_slots, sb, bytes([w.sentinel])) == T
     del pool
     torch.cuda.empty_cache()
+
+
+def test_full_size_fused_dynamic_tensor_write():
+    """The fused dynamic per-tensor write on the fp8 batch at full size,
+    through bench.Pool.call (the launch the bench times), twice in a row on
+    the pool's one workspace: every written row equals the oracle's (absmax,
+    inverse scale, per-tensor write), the forward scales are amax / 448 bit
+    for bit, nothing else changed."""
+    import torch
+    import bench
+    import fp8_quant_gb300 as kv
+    dev = torch.device("cuda", 0)
+    pool = bench.Pool("fp8_tensor_dynamic", dev, pool_bytes=0)
+    w = pool.w
+    assert pool.num_batches == 1
+    s = torch.cuda.current_stream().cuda_stream
+    for _ in range(2):
+        assert pool.call(0, s) == 0
+    assert kv.kv_error_poll(pool.err) == (kv.KVStatus.OK, 0, -1)
+    assert int(pool.dyn_work.cpu()[0]) == 2
+    T, sb = w.T, w.slot_stride
+    st = oracle.Strides(k_token=w.k_view[1], k_head=w.k_view[2], k_dim=w.k_view[3],
+                        v_token=w.v_view[1], v_head=w.v_view[2], v_dim=w.v_view[3],
+                        kc_slot=sb, kc_head=w.cache_head_stride, kc_dim=1,
+                        vc_slot=sb, vc_head=w.cache_head_stride, vc_dim=1)
+    k = np.ascontiguousarray(w.k).view(np.uint8).reshape(-1)
+    v = np.ascontiguousarray(w.v).view(np.uint8).reshape(-1)
+    amax, inv = oracle.absmax_inv(k, v, st, T, w.H, w.D, w.src_dtype, 448.0)
+    idx = np.arange(T, dtype=w.indices.dtype)          # compact oracle cache: slot j for token j
+    okc = np.full(T * sb, w.sentinel, np.uint8)
+    ovc = okc.copy()
+    assert oracle.store_fp8_ex(k, v, okc, ovc, idx, st, w.H, w.D, w.src_dtype, 1, sb, sb, T,
+                               fmt="e4m3fn", scale_mode="tensor", inv_k=float(inv[0]),
+                               inv_v=float(inv[1])) == (0, -1)
+    slots = torch.from_numpy(w.indices.astype(np.int64)).to(dev)
+    for cache, want, what in ((pool.kc, okc, "K"), (pool.vc, ovc, "V")):
+        rows = cache.view(w.n_slots, sb).index_select(0, slots).cpu().numpy().reshape(-1)
+        assert np.array_equal(rows, want), f"{what} cache rows differ"
+        assert _rows_changed(torch, cache, w.n_slots, sb, bytes([w.sentinel])) == T
+    assert np.array_equal(pool.dyn_scale.cpu().numpy(), (amax / np.float32(448.0)).astype(np.float32))
+    del pool
+    torch.cuda.empty_cache()

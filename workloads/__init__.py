@@ -178,7 +178,8 @@ class Workload:
     def algorithmic_bytes(self) -> int:
         """Bytes a call must move: K and V rows read, cache rows written, indices read
         (for the absmax pass: K and V rows read, four floats written; for the
-        dynamic FP8 write also one fp32 scale per token and head, K and V)."""
+        dynamic FP8 write also one fp32 scale per token and head, K and V; for
+        the fused per-tensor dynamic write the rows once and two scales)."""
         if self.kind == "absmax":
             return self.T * 2 * self.row_bytes + 16
         out_row = self.H * self.D * self.cache_elem
@@ -186,6 +187,10 @@ class Workload:
         scales = 2 * groups * 4 if self.kind == "fp8_dyn" else 0
         if self.notes.get("scale_mode") == "page":
             scales = 2 * 4          # the page's inverse scale, K and V
+        if self.notes.get("scale_mode") == "tensor_dynamic":
+            # K and V counted once (the scale pass's read; the write's second
+            # read of the same rows is served from L2), plus the two scales
+            return self.T * (2 * self.row_bytes + 2 * out_row + self.indices.itemsize) + 8
         return self.T * (2 * self.row_bytes + 2 * out_row + self.indices.itemsize + scales)
 
 
@@ -382,6 +387,16 @@ def gather_fp8(n_slots: int = 1 << 20) -> Workload:
     return w
 
 
+def fp8_tensor_dynamic(n_slots: int = 1 << 20) -> Workload:
+    """The ``fp8`` batch written with per-tensor scales formed from the batch
+    in the same call (amax over K and over V, inv = 448 / amax, then the
+    write): the fused dynamic per-tensor write."""
+    w = fp8(n_slots=n_slots)
+    w.name = "fp8_tensor_dynamic"
+    w.notes["scale_mode"] = "tensor_dynamic"
+    return w
+
+
 def absmax(n_slots: int = 1 << 20) -> Workload:
     """Per-tensor scale pass over the ``fp8`` batch (K and V read once)."""
     w = fp8(n_slots=n_slots)
@@ -405,4 +420,5 @@ WORKLOADS = {
     "gather_prefill": gather_prefill,
     "gather_fp8": gather_fp8,
     "absmax": absmax,
+    "fp8_tensor_dynamic": fp8_tensor_dynamic,
 }
