@@ -108,6 +108,10 @@ CASES = {
     "strided_cache_dims": dict(T=300, H=4, D=32, n_slots=1024, dst_dim_mult=2),
     "odd_d_narrow_i32": dict(T=300, H=3, D=45, n_slots=1024, idx_dtype=np.int32, index_stride=2),
     "single_head_576": dict(T=256, H=1, D=576, n_slots=1024),
+    # 32-byte rows, many of them
+    "tiny_rows_many": dict(T=100000, H=1, D=16, n_slots=200000),
+    # a batch beyond L2 (82 MB): the write's second read comes from HBM
+    "large_batch": dict(T=20000, H=8, D=128, n_slots=32768, page_size=16),
 }
 
 
