@@ -273,3 +273,23 @@ def test_dynamic_tensor_tensor_wrapper():
     assert np.array_equal(kc.cpu().numpy().ravel(), okc)
     assert np.array_equal(vc.cpu().numpy().ravel(), ovc)
     assert np.array_equal(sc.cpu().numpy(), (amax / np.float32(448.0)).astype(np.float32))
+
+
+def test_dynamic_tensor_concurrent_streams_separate_workspaces():
+    """Two streams, each with its own workspace and batch, write at the same
+    time (no synchronisation between them): both results equal their oracle
+    results, and each workspace advances by its own calls only."""
+    import torch
+    ps = _batches(2)
+    ds = [Dev(p) for p in ps]
+    works = [new_work(), new_work()]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for d, w, s in zip(ds, works, streams):
+            with torch.cuda.stream(s):
+                assert d.call("e4m3fn", w, stream=s.cuda_stream) == 0
+    torch.cuda.synchronize()
+    for d in ds:
+        d.check("e4m3fn")
+    assert [int(w.cpu()[0]) for w in works] == [3, 3]

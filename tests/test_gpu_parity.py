@@ -551,6 +551,34 @@ def test_fused_fp8_set_kv_buffer_matches_oracle(layout):
     assert np.array_equal(vc.cpu().numpy().ravel(), ovc)
 
 
+
+def test_fused_fp8_set_kv_buffer_on_a_side_stream():
+    """Scales computed on a side stream and the wrapper called on that stream
+    (the inverse scales are staged there too): the result equals the same
+    call on the default stream, byte for byte."""
+    import torch
+    import fp8_quant_gb300 as kv
+    dev = torch.device("cuda")
+    T, H, D, ps, pages = 640, 8, 128, 16, 64
+    kb = wl.f32_to_bf16_bits(wl.normal(901, T * H * D) * 2.0).reshape(T, H, D)
+    k = torch.from_numpy(kb.view(np.int16)).to(dev).view(torch.bfloat16)
+    v = (k.float() * 0.5).to(torch.bfloat16)
+    idx = torch.from_numpy(wl.distinct_slots(902, ps * pages, T).astype(np.int64)).to(dev)
+    caches = [torch.zeros(pages, ps, H, D, dtype=torch.uint8, device=dev) for _ in range(4)]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ks = k.float().abs().max() / 448.0          # produced on the side stream
+        vs = v.float().abs().max() / 448.0
+        kv.fused_fp8_set_kv_buffer(k, v, caches[0], caches[1], idx, ks, vs, page_size=ps,
+                                   stream=s)
+    torch.cuda.synchronize()
+    kv.fused_fp8_set_kv_buffer(k, v, caches[2], caches[3], idx, ks, vs, page_size=ps)
+    torch.cuda.synchronize()
+    assert torch.equal(caches[0], caches[2]) and torch.equal(caches[1], caches[3])
+    assert int((caches[0] != 0).sum()) > 0
+    assert kv.kv_error_poll()[1] == 0
+
 @pytest.mark.gpu
 def test_launch_floor_runs_in_stream_order_and_in_a_graph():
     """kv_launch_floor (the measurement aid) launches, keeps stream order
