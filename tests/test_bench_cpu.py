@@ -106,3 +106,32 @@ def test_workload_sizes():
     assert gp.kind == "gather" and gp.algorithmic_bytes() == 32768 * (4 * 2048 + 4)
     o = wl.odd()
     assert o.slot_stride == 1280 and o.algorithmic_bytes() == 65536 * (4 * 1152 + 4)
+
+
+def test_fused_dynamic_workload_and_oracle_step():
+    """The fused per-tensor dynamic write's workload counts K and V once plus
+    the two scales, and the reference arm's oracle step for it equals the
+    oracle's absmax followed by the per-tensor write on the same tokens."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    import workloads as wl
+    w = wl.fp8_tensor_dynamic(n_slots=1 << 14)
+    assert w.algorithmic_bytes() == wl.fp8(n_slots=1 << 14).algorithmic_bytes() + 8
+    name = "fp8_tensor_dynamic_cpu_test"
+    bench._ORACLE_CACHE.pop(name, None)
+    tokens = 48
+    kc, vc, k, v, st = bench.oracle_buffers(name, w)
+    kc[:] = 0x7F
+    vc[:] = 0x7F
+    bench.oracle_step(name, w, tokens)
+    amax, inv = oracle.absmax_inv(k, v, st, tokens, w.H, w.D, w.src_dtype, 448.0)
+    okc = np.full_like(kc, 0x7F)
+    ovc = okc.copy()
+    oracle.store_fp8_ex(k, v, okc, ovc, w.indices, st, w.H, w.D, w.src_dtype, w.page_size,
+                        w.page_stride, w.page_stride, w.n_slots, fmt="e4m3fn",
+                        scale_mode="tensor", inv_k=float(inv[0]), inv_v=float(inv[1]),
+                        t_end=tokens)
+    assert np.array_equal(kc, okc) and np.array_equal(vc, ovc)
+    assert (kc != 0x7F).sum() > 0
+    bench._ORACLE_CACHE.pop(name, None)
