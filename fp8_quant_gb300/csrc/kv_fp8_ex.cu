@@ -2,8 +2,8 @@
 // the kernel per token row or per (token, head).
 //
 // The fused FP8 write's module docstring (sglang trtllm_fp8_kv_kernel.py)
-// names "per-token or per-page scale computation" but its kernel only takes
-// a per-tensor scale; this file supplies the per-token form.  For each group
+// advertises scales computed per token or per page, but its kernel only
+// takes a per-tensor scale; this file supplies the per-token form.  For each group
 // (the K or V row of a token, or one head of it): amax = max |x| (NaN
 // ignored); inv = fmax / amax and scale = amax / fmax in fp32 (both 1 when
 // amax is 0); codes = fp8(x * inv); `scale` goes to the caller's per-slot

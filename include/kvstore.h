@@ -366,7 +366,7 @@ kv_status kv_absmax_inv(const void *k, const void *v, kv_src_dtype src_dtype,
  * kv_store_fp8_dynamic_tensor -- the FP8 write with per-tensor scales formed
  * from the batch itself, in one call: the fused form of kv_absmax_inv
  * followed by kv_store_fp8_ex in KV_SCALE_TENSOR mode (the trtllm page's
- * docstring names "scale computation" but its kernel takes a given scale;
+ * docstring advertises computed scales while its kernel takes a given one;
  * the recipe is the per-tensor one, inv = fmax / amax).
  *   amax_k = max |K| and amax_v = max |V| over all num_tokens rows (NaN
  *   elements ignored; out-of-range slots do not exclude their rows), then
